@@ -1,0 +1,690 @@
+/*
+ * gs2d oracle: a plain, slow, single-threaded CPU statement of the tile-based
+ * 2D Gaussian-splatting rasterizer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path calls, links or
+ * loads this file; only the test suite, the package's smoke check and the
+ * benchmark's CPU-baseline leg do.  It shares no code, header, table or
+ * helper with the CUDA library: the configuration struct below is declared
+ * here on its own.
+ *
+ * What it computes, and where that comes from:
+ *   - Each Gaussian has 8 parameters: position (2), covariance (3) and colour
+ *     (3).  Images are rendered by an accumulated (order-independent) sum of
+ *     the Gaussians' colours weighted by exp(-q/2)
+ *     (GaussianImage project page, Overview).
+ *   - The covariance is given by a lower-triangular Cholesky factor L,
+ *     Sigma = L L^T (DrawingWithGaussians README, MLX-specific notes;
+ *     GaussianImage project page, "Representation" scripts for the Cholesky
+ *     variant).
+ *   - In the sum form there is no opacity: the gate is folded into the colour,
+ *     and colours add (FlashImgs README, Python API and Web viewer sections).
+ *   - The optional variant alpha-composites depth-ordered Gaussians front to
+ *     back over a trainable background (DrawingWithGaussians README,
+ *     Overview, "2D fitting").
+ *   - Gaussians are binned to 16x16 pixel tiles (fVDB radiance_fields API,
+ *     GaussianSplatReconstructionConfig.tile_size).
+ *   - The loss is the L2 (mean squared) image error (FlashImgs README,
+ *     Configuration: l2_loss_ratio).
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - pixel (row i, column j) has its centre at (j + 0.5, i + 0.5) in pixel
+ *     units, x to the right and y down;
+ *   - a Gaussian touches a pixel when the pixel lies inside its 3-sigma
+ *     axis-aligned box AND q = d^T Sigma^-1 d <= k^2 at the pixel centre
+ *     (k = cutoff_sigma, 3 by default).  That decision is an integer outcome
+ *     taken from floating point, so it is taken here in the same FP32
+ *     operation sequence as the GPU kernel (see ref_mask_data); every value
+ *     (weights, colours, gradients) is computed in double;
+ *   - sum-mode tile lists are in ascending Gaussian index; composite lists in
+ *     ascending depth with ties broken by ascending index;
+ *   - composite: a masked Gaussian contributes only while the transmittance
+ *     before it is >= t_min; the background is added with weight T_final;
+ *   - Gaussians with non-finite parameters, a zero diagonal entry of L, a
+ *     non-finite FP32 inverse covariance, an empty box, or (composite) an
+ *     opacity outside [0, 1) are culled: they touch no pixel and get a zero
+ *     gradient.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (oracle/build.py).
+ * -ffp-contract=off keeps every FP32 product and sum separately rounded, so
+ * that only the explicit fmaf calls fuse.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+  int32_t width;
+  int32_t height;
+  int32_t tile;          /* 16 */
+  int32_t mode;          /* 0: accumulated sum, 1: alpha composite */
+  float cutoff_sigma;    /* k: the mask is q <= k*k */
+  float t_min;           /* composite early-termination threshold */
+} ref_cfg;
+
+#define REF_MODE_SUM 0
+#define REF_MODE_COMPOSITE 1
+
+static int32_t ref_tiles_x(const ref_cfg* cfg) { return (cfg->width + cfg->tile - 1) / cfg->tile; }
+static int32_t ref_tiles_y(const ref_cfg* cfg) { return (cfg->height + cfg->tile - 1) / cfg->tile; }
+
+int32_t gs2dref_num_tiles(const ref_cfg* cfg) { return ref_tiles_x(cfg) * ref_tiles_y(cfg); }
+
+/* ------------------------------------------------------------------------- */
+/* Projection: validity, FP32 inverse covariance, pixel box, tile rectangle.  */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Mask data of one Gaussian in FP32, the precision in which the kernel takes
+ * the touch/no-touch decision.
+ *
+ * With L = [[a, 0], [b, c]], Sigma = L L^T = [[a^2, ab], [ab, b^2 + c^2]] and
+ * Sigma^-1 = [[A, B], [B, C]] with A = (b^2 + c^2)/(a^2 c^2), B = -b/(a c^2),
+ * C = 1/c^2.  The FP32 evaluation order is fixed (each product rounded, one
+ * explicit fused multiply-add):
+ *     ia = 1/a, ic = 1/c, C = ic*ic, t = b*ia, B = -(t*C), A = fma(t*t, C, ia*ia).
+ * The box is the tight axis-aligned box of the ellipse q <= k^2, whose half
+ * widths are k*sqrt(Sigma_xx) = k|a| and k*sqrt(Sigma_yy) = k*sqrt(b^2 + c^2),
+ * clipped to the image; pixel column j is inside when its centre j + 0.5 lies
+ * within [mu_x - r_x, mu_x + r_x].
+ * Returns 1 and fills conic/aabb, or 0 when the Gaussian is culled.
+ */
+static int ref_mask_data(const ref_cfg* cfg, float mx, float my, float a, float b, float c,
+                         float conic[3], int32_t aabb[4]) {
+  if (a == 0.0f || c == 0.0f) return 0;
+  const float ia = 1.0f / a;
+  const float ic = 1.0f / c;
+  const float C = ic * ic;
+  const float t = b * ia;
+  const float B = -(t * C);
+  const float A = fmaf(t * t, C, ia * ia);
+  if (!isfinite(A) || !isfinite(B) || !isfinite(C)) return 0;
+
+  const float k = cfg->cutoff_sigma;
+  const float rx = k * fabsf(a);
+  const float ry = k * sqrtf(fmaf(b, b, c * c));
+  const float fx0 = ceilf((mx - rx) - 0.5f);
+  const float fx1 = floorf((mx + rx) - 0.5f);
+  const float fy0 = ceilf((my - ry) - 0.5f);
+  const float fy1 = floorf((my + ry) - 0.5f);
+  const float wmax = (float)(cfg->width - 1);
+  const float hmax = (float)(cfg->height - 1);
+  if (!(fx0 <= fx1) || !(fy0 <= fy1)) return 0;
+  if (fx0 > wmax || fx1 < 0.0f || fy0 > hmax || fy1 < 0.0f) return 0;
+  conic[0] = A;
+  conic[1] = B;
+  conic[2] = C;
+  aabb[0] = (int32_t)fmaxf(fx0, 0.0f);
+  aabb[1] = (int32_t)fmaxf(fy0, 0.0f);
+  aabb[2] = (int32_t)fminf(fx1, wmax);
+  aabb[3] = (int32_t)fminf(fy1, hmax);
+  return 1;
+}
+
+/*
+ * Per-Gaussian projection for n Gaussians.
+ *   conic[n,3]  FP32 (A, B, C) of Sigma^-1, zero when culled
+ *   aabb[n,4]   pixel box (x0, y0, x1, y1) inclusive, (0, 0, -1, -1) when culled
+ *   rect[n,4]   tile rectangle (tx0, ty0, tx1, ty1) inclusive, same when culled
+ *   count[n]    number of tiles in rect, 0 when culled
+ * depth/opacity are read only in composite mode (may be NULL in sum mode).
+ * Returns the number of valid Gaussians.
+ */
+int32_t gs2dref_project(const ref_cfg* cfg, int32_t n, const float* xy, const float* chol,
+                        const float* rgb, const float* depth, const float* opacity, float* conic,
+                        int32_t* aabb, int32_t* rect, int32_t* count) {
+  int32_t valid = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    float* cn = conic + 3 * (int64_t)i;
+    int32_t* bb = aabb + 4 * (int64_t)i;
+    int32_t* rc = rect + 4 * (int64_t)i;
+    cn[0] = cn[1] = cn[2] = 0.0f;
+    bb[0] = bb[1] = 0;
+    bb[2] = bb[3] = -1;
+    rc[0] = rc[1] = 0;
+    rc[2] = rc[3] = -1;
+    count[i] = 0;
+
+    int ok = 1;
+    for (int d = 0; d < 2; ++d) ok &= isfinite(xy[2 * (int64_t)i + d]) != 0;
+    for (int d = 0; d < 3; ++d) ok &= isfinite(chol[3 * (int64_t)i + d]) != 0;
+    for (int d = 0; d < 3; ++d) ok &= isfinite(rgb[3 * (int64_t)i + d]) != 0;
+    if (cfg->mode == REF_MODE_COMPOSITE) {
+      ok &= isfinite(depth[i]) != 0;
+      ok &= isfinite(opacity[i]) != 0;
+      ok &= (opacity[i] >= 0.0f && opacity[i] < 1.0f);
+    }
+    if (!ok) continue;
+
+    float cf[3];
+    int32_t b4[4];
+    if (!ref_mask_data(cfg, xy[2 * (int64_t)i], xy[2 * (int64_t)i + 1], chol[3 * (int64_t)i],
+                       chol[3 * (int64_t)i + 1], chol[3 * (int64_t)i + 2], cf, b4))
+      continue;
+    memcpy(cn, cf, sizeof cf);
+    memcpy(bb, b4, sizeof b4);
+    rc[0] = b4[0] / cfg->tile;
+    rc[1] = b4[1] / cfg->tile;
+    rc[2] = b4[2] / cfg->tile;
+    rc[3] = b4[3] / cfg->tile;
+    count[i] = (rc[2] - rc[0] + 1) * (rc[3] - rc[1] + 1);
+    ++valid;
+  }
+  return valid;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Tile lists.                                                                */
+/* ------------------------------------------------------------------------- */
+
+static const float* g_sort_depth; /* qsort has no context argument */
+
+static int ref_cmp_depth_gid(const void* pa, const void* pb) {
+  const int32_t a = *(const int32_t*)pa, b = *(const int32_t*)pb;
+  const float da = g_sort_depth[a], db = g_sort_depth[b];
+  if (da < db) return -1;
+  if (db < da) return 1;
+  return (a > b) - (a < b);
+}
+
+/*
+ * The list of tile t holds every Gaussian whose tile rectangle contains t:
+ * in ascending index (sum) or ascending (depth, index) (composite).
+ *   ranges[T,2]     [start, end) of tile t in sorted_gid (may be NULL)
+ *   sorted_gid[P]   concatenated lists, tiles in row-major order (may be NULL)
+ * Returns P, the total number of (tile, Gaussian) pairs.
+ */
+int64_t gs2dref_bin(const ref_cfg* cfg, int32_t n, const int32_t* rect, const int32_t* count,
+                    const float* depth, int32_t* ranges, int32_t* sorted_gid) {
+  const int32_t tx = ref_tiles_x(cfg), T = gs2dref_num_tiles(cfg);
+  int64_t P = 0;
+  for (int32_t i = 0; i < n; ++i) P += count[i];
+  if (!ranges && !sorted_gid) return P;
+
+  int64_t* start = (int64_t*)calloc((size_t)T + 1, sizeof(int64_t));
+  for (int32_t i = 0; i < n; ++i) {
+    if (count[i] == 0) continue;
+    const int32_t* r = rect + 4 * (int64_t)i;
+    for (int32_t y = r[1]; y <= r[3]; ++y)
+      for (int32_t x = r[0]; x <= r[2]; ++x) start[(int64_t)y * tx + x + 1] += 1;
+  }
+  for (int32_t t = 0; t < T; ++t) start[t + 1] += start[t];
+  if (ranges)
+    for (int32_t t = 0; t < T; ++t) {
+      ranges[2 * (int64_t)t] = (int32_t)start[t];
+      ranges[2 * (int64_t)t + 1] = (int32_t)start[t + 1];
+    }
+  if (sorted_gid) {
+    int64_t* fill = (int64_t*)malloc(sizeof(int64_t) * (size_t)T);
+    memcpy(fill, start, sizeof(int64_t) * (size_t)T);
+    for (int32_t i = 0; i < n; ++i) { /* ascending i: each list comes out ascending */
+      if (count[i] == 0) continue;
+      const int32_t* r = rect + 4 * (int64_t)i;
+      for (int32_t y = r[1]; y <= r[3]; ++y)
+        for (int32_t x = r[0]; x <= r[2]; ++x) sorted_gid[fill[(int64_t)y * tx + x]++] = i;
+    }
+    if (cfg->mode == REF_MODE_COMPOSITE) {
+      g_sort_depth = depth;
+      for (int32_t t = 0; t < T; ++t)
+        qsort(sorted_gid + start[t], (size_t)(start[t + 1] - start[t]), sizeof(int32_t),
+              ref_cmp_depth_gid);
+    }
+    free(fill);
+  }
+  free(start);
+  return P;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Per-pair evaluation.                                                       */
+/* ------------------------------------------------------------------------- */
+
+/* The touch decision for pixel (row i, column j), FP32 as in the kernel:
+ * the pixel lies in the box and q <= k^2 with
+ * q = fma(dx, fma(A, dx, (2B)*dy), (C*dy)*dy),  dx = (j+0.5) - mu_x, dy = (i+0.5) - mu_y. */
+static int ref_touches(const ref_cfg* cfg, const float* xy, const float* conic, const int32_t* bb,
+                       int32_t i, int32_t j) {
+  if (j < bb[0] || j > bb[2] || i < bb[1] || i > bb[3]) return 0;
+  const float kk = cfg->cutoff_sigma * cfg->cutoff_sigma;
+  const float dx = ((float)j + 0.5f) - xy[0];
+  const float dy = ((float)i + 0.5f) - xy[1];
+  const float q = fmaf(dx, fmaf(conic[0], dx, (2.0f * conic[1]) * dy), (conic[2] * dy) * dy);
+  return q <= kk;
+}
+
+/* Sigma^-1 of L = [[a,0],[b,c]] in double: adj(Sigma)/det(Sigma). */
+static void ref_inverse_cov(const double* L, double* A, double* B, double* C) {
+  const double a = L[0], b = L[1], c = L[2];
+  const double sxx = a * a, sxy = a * b, syy = b * b + c * c;
+  const double det = sxx * syy - sxy * sxy;
+  *A = syy / det;
+  *B = -sxy / det;
+  *C = sxx / det;
+}
+
+/* One Gaussian at one pixel centre, in double: w = exp(-q/2), plus dx, dy. */
+static double ref_weight(const double* xy, const double* L, int32_t i, int32_t j, double* dx,
+                         double* dy) {
+  double A, B, C;
+  ref_inverse_cov(L, &A, &B, &C);
+  *dx = ((double)j + 0.5) - xy[0];
+  *dy = ((double)i + 0.5) - xy[1];
+  const double q = A * (*dx) * (*dx) + 2.0 * B * (*dx) * (*dy) + C * (*dy) * (*dy);
+  return exp(-0.5 * q);
+}
+
+/* Double-precision parameters, FP32 mask data and tile lists, bundled. */
+typedef struct {
+  const ref_cfg* cfg;
+  const double* xy;
+  const double* chol;
+  const double* rgb;
+  const double* opacity; /* composite only */
+  const double* bg;      /* composite only, [3] */
+  const float* xy_f;     /* FP32 positions for the mask decision */
+  const float* conic_f;
+  const int32_t* aabb;
+  const int32_t* ranges;
+  const int32_t* sorted_gid;
+} ref_scene;
+
+typedef struct {
+  int32_t gid;
+  double w, alpha, T; /* T is the transmittance in front of this Gaussian */
+  double dx, dy;
+} ref_contrib;
+
+/*
+ * Forward at pixel (i, j) over a list of Gaussian indices.  Fills out[3];
+ * for composite also *tfin, *last (1 + list position of the last Gaussian
+ * that contributed, 0 if none) and *margin = min over the termination checks
+ * of |ln(T / t_min)|, the distance of the early-termination decision from its
+ * threshold (HUGE_VAL when no check was made).  When contrib is non-NULL the
+ * contributing Gaussians are recorded in order and *ncontrib set.
+ */
+static void ref_pixel_fwd(const ref_scene* s, const int32_t* list, int64_t len, int32_t i,
+                          int32_t j, double out[3], double* tfin, int32_t* last, double* margin,
+                          int64_t* masked, ref_contrib* contrib, int64_t* ncontrib) {
+  const ref_cfg* cfg = s->cfg;
+  double C[3] = {0.0, 0.0, 0.0};
+  double T = 1.0, mg = HUGE_VAL;
+  int32_t lst = 0;
+  int64_t nm = 0, nc = 0;
+  for (int64_t k = 0; k < len; ++k) {
+    const int32_t g = list[k];
+    if (!ref_touches(cfg, s->xy_f + 2 * (int64_t)g, s->conic_f + 3 * (int64_t)g,
+                     s->aabb + 4 * (int64_t)g, i, j))
+      continue;
+    ++nm;
+    double dx, dy;
+    const double w = ref_weight(s->xy + 2 * (int64_t)g, s->chol + 3 * (int64_t)g, i, j, &dx, &dy);
+    const double* c = s->rgb + 3 * (int64_t)g;
+    if (cfg->mode == REF_MODE_SUM) {
+      for (int d = 0; d < 3; ++d) C[d] += c[d] * w;
+      if (contrib) contrib[nc] = (ref_contrib){g, w, 0.0, 1.0, dx, dy};
+      ++nc;
+    } else {
+      const double m = fabs(log(T / (double)cfg->t_min));
+      if (m < mg) mg = m;
+      if (T < (double)cfg->t_min) break;
+      const double alpha = s->opacity[g] * w;
+      for (int d = 0; d < 3; ++d) C[d] += c[d] * alpha * T;
+      if (contrib) contrib[nc] = (ref_contrib){g, w, alpha, T, dx, dy};
+      ++nc;
+      T *= (1.0 - alpha);
+      lst = (int32_t)(k + 1);
+    }
+  }
+  if (cfg->mode == REF_MODE_COMPOSITE)
+    for (int d = 0; d < 3; ++d) C[d] += T * s->bg[d];
+  for (int d = 0; d < 3; ++d) out[d] = C[d];
+  if (tfin) *tfin = (cfg->mode == REF_MODE_COMPOSITE) ? T : 1.0;
+  if (last) *last = lst;
+  if (margin) *margin = mg;
+  if (masked) *masked += nm;
+  if (ncontrib) *ncontrib = nc;
+}
+
+static void ref_scene_init(ref_scene* s, const ref_cfg* cfg, const double* xy, const double* chol,
+                           const double* rgb, const double* opacity, const double* bg,
+                           const float* xy_f, const float* conic_f, const int32_t* aabb,
+                           const int32_t* ranges, const int32_t* sorted_gid) {
+  s->cfg = cfg;
+  s->xy = xy;
+  s->chol = chol;
+  s->rgb = rgb;
+  s->opacity = opacity;
+  s->bg = bg;
+  s->xy_f = xy_f;
+  s->conic_f = conic_f;
+  s->aabb = aabb;
+  s->ranges = ranges;
+  s->sorted_gid = sorted_gid;
+}
+
+/*
+ * Full-image forward, pixel by pixel over the pixel's tile list.
+ *   image[3,H,W] (planar), t_final[H,W], last[H,W], margin[H,W]: outputs,
+ *   the last three may be NULL.  Returns the number of (pixel, Gaussian)
+ *   pairs that pass the touch test.
+ */
+int64_t gs2dref_render_fwd(const ref_cfg* cfg, const double* xy, const double* chol,
+                           const double* rgb, const double* opacity, const double* bg,
+                           const float* xy_f, const float* conic_f, const int32_t* aabb,
+                           const int32_t* ranges, const int32_t* sorted_gid, double* image,
+                           double* t_final, int32_t* last, double* margin) {
+  ref_scene s;
+  ref_scene_init(&s, cfg, xy, chol, rgb, opacity, bg, xy_f, conic_f, aabb, ranges, sorted_gid);
+  const int64_t H = cfg->height, W = cfg->width, HW = H * W;
+  const int32_t tx = ref_tiles_x(cfg);
+  int64_t masked = 0;
+  for (int32_t i = 0; i < cfg->height; ++i)
+    for (int32_t j = 0; j < cfg->width; ++j) {
+      const int64_t t = (int64_t)(i / cfg->tile) * tx + j / cfg->tile;
+      const int32_t* list = sorted_gid + ranges[2 * t];
+      const int64_t len = ranges[2 * t + 1] - ranges[2 * t];
+      double out[3], tf, mg;
+      int32_t ls;
+      ref_pixel_fwd(&s, list, len, i, j, out, &tf, &ls, &mg, &masked, NULL, NULL);
+      const int64_t p = (int64_t)i * W + j;
+      for (int d = 0; d < 3; ++d) image[d * HW + p] = out[d];
+      if (t_final) t_final[p] = tf;
+      if (last) last[p] = ls;
+      if (margin) margin[p] = mg;
+    }
+  return masked;
+}
+
+/* Forward at m sampled pixels (linear index i*W + j); out[m,3]. */
+void gs2dref_render_pixels(const ref_cfg* cfg, const double* xy, const double* chol,
+                           const double* rgb, const double* opacity, const double* bg,
+                           const float* xy_f, const float* conic_f, const int32_t* aabb,
+                           const int32_t* ranges, const int32_t* sorted_gid, const int64_t* pix,
+                           int64_t m, double* out, double* t_final, int32_t* last,
+                           double* margin) {
+  ref_scene s;
+  ref_scene_init(&s, cfg, xy, chol, rgb, opacity, bg, xy_f, conic_f, aabb, ranges, sorted_gid);
+  const int32_t tx = ref_tiles_x(cfg);
+  for (int64_t k = 0; k < m; ++k) {
+    const int32_t i = (int32_t)(pix[k] / cfg->width), j = (int32_t)(pix[k] % cfg->width);
+    const int64_t t = (int64_t)(i / cfg->tile) * tx + j / cfg->tile;
+    double tf, mg;
+    int32_t ls;
+    ref_pixel_fwd(&s, sorted_gid + ranges[2 * t], ranges[2 * t + 1] - ranges[2 * t], i, j,
+                  out + 3 * k, &tf, &ls, &mg, NULL, NULL, NULL);
+    if (t_final) t_final[k] = tf;
+    if (last) last[k] = ls;
+    if (margin) margin[k] = mg;
+  }
+}
+
+/*
+ * Brute force: every pixel against every valid Gaussian, no tiles.  Sum mode
+ * visits Gaussians in index order; composite in (depth, index) order.
+ * valid[n] is the projection's count > 0.
+ */
+void gs2dref_render_brute(const ref_cfg* cfg, int32_t n, const double* xy, const double* chol,
+                          const double* rgb, const double* opacity, const double* bg,
+                          const float* xy_f, const float* conic_f, const int32_t* aabb,
+                          const int32_t* count, const float* depth, double* image,
+                          double* t_final) {
+  ref_scene s;
+  ref_scene_init(&s, cfg, xy, chol, rgb, opacity, bg, xy_f, conic_f, aabb, NULL, NULL);
+  int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+  int64_t len = 0;
+  for (int32_t g = 0; g < n; ++g)
+    if (count[g] > 0) order[len++] = g;
+  if (cfg->mode == REF_MODE_COMPOSITE) {
+    g_sort_depth = depth;
+    qsort(order, (size_t)len, sizeof(int32_t), ref_cmp_depth_gid);
+  }
+  const int64_t HW = (int64_t)cfg->height * cfg->width;
+  for (int32_t i = 0; i < cfg->height; ++i)
+    for (int32_t j = 0; j < cfg->width; ++j) {
+      double out[3], tf;
+      ref_pixel_fwd(&s, order, len, i, j, out, &tf, NULL, NULL, NULL, NULL, NULL);
+      const int64_t p = (int64_t)i * cfg->width + j;
+      for (int d = 0; d < 3; ++d) image[d * HW + p] = out[d];
+      if (t_final) t_final[p] = tf;
+    }
+  free(order);
+}
+
+/* ------------------------------------------------------------------------- */
+/* L2 loss.                                                                   */
+/* ------------------------------------------------------------------------- */
+
+/* loss = (1/(3HW)) sum (C - target)^2 and d_image = 2 (C - target) / (3HW). */
+double gs2dref_loss_l2(int32_t h, int32_t w, const double* image, const double* target,
+                       double* d_image) {
+  const int64_t m = 3 * (int64_t)h * w;
+  double acc = 0.0;
+  for (int64_t k = 0; k < m; ++k) {
+    const double e = image[k] - target[k];
+    acc += e * e;
+    if (d_image) d_image[k] = 2.0 * e / (double)m;
+  }
+  return m > 0 ? acc / (double)m : 0.0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Backward.                                                                  */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Gradient accumulators of one Gaussian, in the variables the image depends
+ * on directly: mean, inverse-covariance entries (A, B, C), colour, opacity.
+ */
+typedef struct {
+  double dmu[2], dconic[3], drgb[3], dopac;
+} ref_grad;
+
+/*
+ * Chain rule through one touching pair, given dL/dw (how the loss moves with
+ * the weight w of this Gaussian at this pixel).  With
+ * q = A dx^2 + 2B dx dy + C dy^2, dx = px - mu_x, dy = py - mu_y and
+ * w = exp(-q/2):  dw/dq = -w/2,  dq/dmu_x = -2(A dx + B dy),
+ * dq/dmu_y = -2(B dx + C dy),  dq/dA = dx^2, dq/dB = 2 dx dy, dq/dC = dy^2.
+ */
+static void ref_accumulate_w(ref_grad* g, const double* L, double w, double dLdw, double dx,
+                             double dy) {
+  double A, B, C;
+  ref_inverse_cov(L, &A, &B, &C);
+  const double dq = dLdw * (-0.5 * w);
+  g->dmu[0] += dq * (-2.0) * (A * dx + B * dy);
+  g->dmu[1] += dq * (-2.0) * (B * dx + C * dy);
+  g->dconic[0] += dq * dx * dx;
+  g->dconic[1] += dq * 2.0 * dx * dy;
+  g->dconic[2] += dq * dy * dy;
+}
+
+/*
+ * Backward at pixel (i, j): adds this pixel's share of dL/d(params) to
+ * grads[] (indexed by Gaussian) or, when only_gid >= 0, only to grads[0] for
+ * that Gaussian.  dimg3 is dL/dC at the pixel; dbg (composite, may be NULL)
+ * receives T_final * dL/dC.
+ *   sum:        C = sum_i c_i w_i;  dC/dc_i = w_i,  dC/dw_i = c_i.
+ *   composite:  C = sum_i c_i a_i T_i + T_N bg, a_i = o_i w_i,
+ *               T_i = prod_{l<i} (1 - a_l);
+ *               dC/dc_i = a_i T_i,
+ *               dC/da_i = c_i T_i - S_i / (1 - a_i),
+ *               S_i = sum_{j>i} c_j a_j T_j + T_N bg,
+ *               da_i/do_i = w_i, da_i/dw_i = o_i, dC/dbg = T_N.
+ * The touch decision and the early-termination decision are held fixed (the
+ * mask is piecewise constant, its derivative is zero almost everywhere).
+ */
+static void ref_pixel_bwd(const ref_scene* s, const int32_t* list, int64_t len, int32_t i,
+                          int32_t j, const double dimg3[3], ref_grad* grads, int32_t only_gid,
+                          double* dbg, ref_contrib* scratch) {
+  const ref_cfg* cfg = s->cfg;
+  double out[3], T;
+  int64_t nc = 0;
+  ref_pixel_fwd(s, list, len, i, j, out, &T, NULL, NULL, NULL, scratch, &nc);
+  if (cfg->mode == REF_MODE_SUM) {
+    for (int64_t k = 0; k < nc; ++k) {
+      const ref_contrib* e = &scratch[k];
+      if (only_gid >= 0 && e->gid != only_gid) continue;
+      ref_grad* g = only_gid >= 0 ? &grads[0] : &grads[e->gid];
+      const double* c = s->rgb + 3 * (int64_t)e->gid;
+      double dLdw = 0.0;
+      for (int d = 0; d < 3; ++d) {
+        g->drgb[d] += dimg3[d] * e->w;
+        dLdw += dimg3[d] * c[d];
+      }
+      ref_accumulate_w(g, s->chol + 3 * (int64_t)e->gid, e->w, dLdw, e->dx, e->dy);
+    }
+    return;
+  }
+  /* composite: suffix sums S_i walked from the back */
+  double S[3];
+  for (int d = 0; d < 3; ++d) S[d] = T * s->bg[d];
+  if (dbg)
+    for (int d = 0; d < 3; ++d) dbg[d] += T * dimg3[d];
+  for (int64_t k = nc - 1; k >= 0; --k) {
+    const ref_contrib* e = &scratch[k];
+    const double* c = s->rgb + 3 * (int64_t)e->gid;
+    if (!(only_gid >= 0 && e->gid != only_gid)) {
+      ref_grad* g = only_gid >= 0 ? &grads[0] : &grads[e->gid];
+      double dLda = 0.0;
+      for (int d = 0; d < 3; ++d) {
+        g->drgb[d] += dimg3[d] * e->alpha * e->T;
+        dLda += dimg3[d] * (c[d] * e->T - S[d] / (1.0 - e->alpha));
+      }
+      const double o = s->opacity[e->gid];
+      g->dopac += dLda * e->w;
+      ref_accumulate_w(g, s->chol + 3 * (int64_t)e->gid, e->w, dLda * o, e->dx, e->dy);
+    }
+    for (int d = 0; d < 3; ++d) S[d] += c[d] * e->alpha * e->T;
+  }
+}
+
+/*
+ * From the inverse-covariance gradient to the Cholesky factor.  With
+ * A = b^2/(a^2 c^2) + 1/a^2, B = -b/(a c^2), C = 1/c^2:
+ *   dA/da = -2A/a,            dA/db = 2b/(a^2 c^2),  dA/dc = -2b^2/(a^2 c^3),
+ *   dB/da = b/(a^2 c^2),      dB/db = -1/(a c^2),    dB/dc = 2b/(a c^3),
+ *   dC/dc = -2/c^3.
+ * The position gradient is the mean gradient (xy is the mean).
+ */
+static void ref_finish(const double* L, const ref_grad* g, double* dxy, double* dchol,
+                       double* drgb, double* dopac) {
+  const double a = L[0], b = L[1], c = L[2];
+  double A, B, C;
+  ref_inverse_cov(L, &A, &B, &C);
+  (void)B;
+  (void)C;
+  const double dA = g->dconic[0], dB = g->dconic[1], dC = g->dconic[2];
+  dchol[0] = dA * (-2.0 * A / a) + dB * (b / (a * a * c * c));
+  dchol[1] = dA * (2.0 * b / (a * a * c * c)) + dB * (-1.0 / (a * c * c));
+  dchol[2] = dA * (-2.0 * b * b / (a * a * c * c * c)) + dB * (2.0 * b / (a * c * c * c)) +
+             dC * (-2.0 / (c * c * c));
+  dxy[0] = g->dmu[0];
+  dxy[1] = g->dmu[1];
+  for (int d = 0; d < 3; ++d) drgb[d] = g->drgb[d];
+  if (dopac) *dopac = g->dopac;
+}
+
+static int64_t ref_max_list(const ref_cfg* cfg, const int32_t* ranges) {
+  int64_t mx = 1;
+  for (int64_t t = 0; t < gs2dref_num_tiles(cfg); ++t)
+    if (ranges[2 * t + 1] - ranges[2 * t] > mx) mx = ranges[2 * t + 1] - ranges[2 * t];
+  return mx;
+}
+
+/*
+ * Full backward: gradients of the loss for all n Gaussians, given
+ * d_image[3,H,W] = dL/dC.  Outputs d_xy[n,2], d_chol[n,3], d_rgb[n,3],
+ * d_opacity[n] (composite, may be NULL), d_bg[3] (composite, may be NULL),
+ * d_conic[n,3] (may be NULL).  count[n] marks valid Gaussians.
+ */
+void gs2dref_render_bwd(const ref_cfg* cfg, int32_t n, const double* xy, const double* chol,
+                        const double* rgb, const double* opacity, const double* bg,
+                        const float* xy_f, const float* conic_f, const int32_t* aabb,
+                        const int32_t* count, const int32_t* ranges, const int32_t* sorted_gid,
+                        const double* d_image, double* d_xy, double* d_chol, double* d_rgb,
+                        double* d_opacity, double* d_bg, double* d_conic) {
+  ref_scene s;
+  ref_scene_init(&s, cfg, xy, chol, rgb, opacity, bg, xy_f, conic_f, aabb, ranges, sorted_gid);
+  ref_grad* grads = (ref_grad*)calloc((size_t)(n > 0 ? n : 1), sizeof(ref_grad));
+  ref_contrib* scratch = (ref_contrib*)malloc(sizeof(ref_contrib) * (size_t)ref_max_list(cfg, ranges));
+  double dbg[3] = {0.0, 0.0, 0.0};
+  const int64_t HW = (int64_t)cfg->height * cfg->width;
+  const int32_t tx = ref_tiles_x(cfg);
+  for (int32_t i = 0; i < cfg->height; ++i)
+    for (int32_t j = 0; j < cfg->width; ++j) {
+      const int64_t p = (int64_t)i * cfg->width + j;
+      const int64_t t = (int64_t)(i / cfg->tile) * tx + j / cfg->tile;
+      const double g3[3] = {d_image[p], d_image[HW + p], d_image[2 * HW + p]};
+      ref_pixel_bwd(&s, sorted_gid + ranges[2 * t], ranges[2 * t + 1] - ranges[2 * t], i, j, g3,
+                    grads, -1, dbg, scratch);
+    }
+  for (int32_t g = 0; g < n; ++g) {
+    double dummy = 0.0;
+    if (count[g] == 0) {
+      memset(d_xy + 2 * (int64_t)g, 0, 2 * sizeof(double));
+      memset(d_chol + 3 * (int64_t)g, 0, 3 * sizeof(double));
+      memset(d_rgb + 3 * (int64_t)g, 0, 3 * sizeof(double));
+      if (d_opacity) d_opacity[g] = 0.0;
+      if (d_conic) memset(d_conic + 3 * (int64_t)g, 0, 3 * sizeof(double));
+      continue;
+    }
+    ref_finish(chol + 3 * (int64_t)g, &grads[g], d_xy + 2 * (int64_t)g, d_chol + 3 * (int64_t)g,
+               d_rgb + 3 * (int64_t)g, d_opacity ? d_opacity + g : &dummy);
+    if (d_conic)
+      for (int d = 0; d < 3; ++d) d_conic[3 * (int64_t)g + d] = grads[g].dconic[d];
+  }
+  if (d_bg)
+    for (int d = 0; d < 3; ++d) d_bg[d] = (cfg->mode == REF_MODE_COMPOSITE) ? dbg[d] : 0.0;
+  free(scratch);
+  free(grads);
+}
+
+/*
+ * Backward for m sampled Gaussians, visiting each one's own pixel box (a
+ * different traversal from gs2dref_render_bwd, which walks pixels).  For
+ * every pixel of the box it replays that pixel's tile list, so composite
+ * gradients see the Gaussians in front and behind.  Outputs are [m, ...].
+ */
+void gs2dref_render_bwd_gaussians(const ref_cfg* cfg, int32_t n, const double* xy,
+                                  const double* chol, const double* rgb, const double* opacity,
+                                  const double* bg, const float* xy_f, const float* conic_f,
+                                  const int32_t* aabb, const int32_t* count,
+                                  const int32_t* ranges, const int32_t* sorted_gid,
+                                  const double* d_image, const int32_t* gids, int32_t m,
+                                  double* d_xy, double* d_chol, double* d_rgb,
+                                  double* d_opacity) {
+  (void)n;
+  ref_scene s;
+  ref_scene_init(&s, cfg, xy, chol, rgb, opacity, bg, xy_f, conic_f, aabb, ranges, sorted_gid);
+  ref_contrib* scratch = (ref_contrib*)malloc(sizeof(ref_contrib) * (size_t)ref_max_list(cfg, ranges));
+  const int64_t HW = (int64_t)cfg->height * cfg->width;
+  const int32_t tx = ref_tiles_x(cfg);
+  for (int32_t k = 0; k < m; ++k) {
+    const int32_t g = gids[k];
+    ref_grad acc;
+    memset(&acc, 0, sizeof acc);
+    double dummy = 0.0;
+    if (count[g] > 0) {
+      const int32_t* bb = aabb + 4 * (int64_t)g;
+      for (int32_t i = bb[1]; i <= bb[3]; ++i)
+        for (int32_t j = bb[0]; j <= bb[2]; ++j) {
+          if (!ref_touches(cfg, xy_f + 2 * (int64_t)g, conic_f + 3 * (int64_t)g, bb, i, j))
+            continue;
+          const int64_t p = (int64_t)i * cfg->width + j;
+          const int64_t t = (int64_t)(i / cfg->tile) * tx + j / cfg->tile;
+          const double g3[3] = {d_image[p], d_image[HW + p], d_image[2 * HW + p]};
+          ref_pixel_bwd(&s, sorted_gid + ranges[2 * t], ranges[2 * t + 1] - ranges[2 * t], i, j,
+                        g3, &acc, g, NULL, scratch);
+        }
+      ref_finish(chol + 3 * (int64_t)g, &acc, d_xy + 2 * (int64_t)k, d_chol + 3 * (int64_t)k,
+                 d_rgb + 3 * (int64_t)k, d_opacity ? d_opacity + k : &dummy);
+    } else {
+      memset(d_xy + 2 * (int64_t)k, 0, 2 * sizeof(double));
+      memset(d_chol + 3 * (int64_t)k, 0, 3 * sizeof(double));
+      memset(d_rgb + 3 * (int64_t)k, 0, 3 * sizeof(double));
+      if (d_opacity) d_opacity[k] = 0.0;
+    }
+  }
+  free(scratch);
+}

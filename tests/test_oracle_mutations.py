@@ -1,0 +1,76 @@
+"""The oracle's pins bite: plant one plausible mistake at a time in a copy of
+the oracle source (on the CPU, in a temporary directory), rebuild it, and
+check that at least one pin fails for every planted mistake.
+"""
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import build as obuild
+
+import test_oracle_pins as pins
+
+# (name, text in the oracle source, replacement)
+MUTATIONS = [
+    ("fp32 off-diagonal sign", "const float B = -(t * C);", "const float B = (t * C);"),
+    ("double off-diagonal sign", "*B = -sxy / det;", "*B = sxy / det;"),
+    ("dropped one half in the weight", "return exp(-0.5 * q);", "return exp(-q);"),
+    ("transposed Cholesky (b<->c in Syy)", "syy = b * b + c * c;", "syy = a * a + c * c;"),
+    ("box radius from the wrong factor", "const float rx = k * fabsf(a);",
+     "const float rx = k * fabsf(c);"),
+    ("tile rectangle end from the start", "rc[2] = b4[2] / cfg->tile;", "rc[2] = b4[0] / cfg->tile;"),
+    ("mean gradient uses C for B", "g->dmu[0] += dq * (-2.0) * (A * dx + B * dy);",
+     "g->dmu[0] += dq * (-2.0) * (A * dx + C * dy);"),
+    ("chain rule dA/da halved", "dchol[0] = dA * (-2.0 * A / a)", "dchol[0] = dA * (-1.0 * A / a)"),
+    ("chain rule dC/dc sign", "dC * (-2.0 / (c * c * c));", "dC * (2.0 / (c * c * c));"),
+    ("composite: no division by 1-alpha", "S[d] / (1.0 - e->alpha)", "S[d]"),
+    ("composite: background dropped", "C[d] += T * s->bg[d];", "C[d] += 0.0 * s->bg[d];"),
+    ("composite: transmittance from opacity", "T *= (1.0 - alpha);", "T *= (1.0 - s->opacity[g]);"),
+    ("composite: no early termination", "if (T < (double)cfg->t_min) break;", "if (T < 0.0) break;"),
+    ("loss gradient without the 2", "d_image[k] = 2.0 * e / (double)m;", "d_image[k] = e / (double)m;"),
+    ("composite lists not depth sorted", "if (cfg->mode == REF_MODE_COMPOSITE) {\n      g_sort_depth = depth;\n      for",
+     "if (0) {\n      g_sort_depth = depth;\n      for"),
+]
+
+PINS = [
+    pins.test_golden_single_gaussian_values,
+    pins.test_golden_composite_values,
+    pins.test_single_gaussian_matches_library_density,
+    pins.test_pixel_box_formula,
+    lambda: pins.test_tile_lists_by_brute_force(oracle.SUM),
+    lambda: pins.test_tile_lists_by_brute_force(oracle.COMPOSITE),
+    lambda: pins.test_tiled_equals_brute_force(40, 33, 64, oracle.SUM),
+    lambda: pins.test_tiled_equals_brute_force(40, 33, 64, oracle.COMPOSITE),
+    pins.test_composite_early_termination,
+    pins.test_composite_depends_on_depth_order,
+    pins.test_sum_gradients_by_central_differences,
+    pins.test_composite_gradients_by_central_differences,
+    pins.test_loss_gradient_by_central_differences,
+]
+
+
+@pytest.fixture(scope="module")
+def source():
+    return open(obuild.SRC).read()
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(source, name, old, new, tmp_path):
+    assert source.count(old) == 1, f"mutation anchor not found once: {old!r}"
+    src = tmp_path / "mutant.c"
+    src.write_text(source.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o",
+                    str(lib), str(src), "-lm"], check=True)
+    caught = []
+    with oracle.use_library(str(lib)):
+        for pin in PINS:
+            try:
+                pin()
+            except (AssertionError, ValueError, FloatingPointError):
+                caught.append(getattr(pin, "__name__", "lambda"))
+    assert caught, f"no pin caught the planted mistake: {name}"
