@@ -1,0 +1,235 @@
+/*
+ * gs2d — tile-based 2D Gaussian-splatting rasterizer for NVIDIA B300 (sm_103a).
+ *
+ * An image is represented by N Gaussians of 8 parameters each: position
+ * (2), covariance (3) given as a lower-triangular Cholesky factor, and RGB
+ * colour (3) (GaussianImage project page, Overview; DrawingWithGaussians
+ * README, MLX-specific notes).  The forward render is the accumulated sum
+ *     C(p) = sum_i rgb_i * exp(-q_i(p)/2),   q_i(p) = d^T Sigma_i^-1 d,  d = p - mu_i
+ * (GaussianImage project page, Overview: accumulated-sum rendering; FlashImgs
+ * README, Python API: gate folded into the colour, additive RGB), with an
+ * optional front-to-back, per-tile depth-ordered alpha-composited variant
+ * over a background (DrawingWithGaussians README, Overview, 2D fitting).
+ * The backward pass gives the gradient of an L2 image loss (FlashImgs
+ * README, Configuration: l2_loss_ratio) with respect to xy, L and RGB (and,
+ * composite, opacity and background).  Gaussians are binned into 16x16
+ * pixel tiles (fVDB radiance_fields API, GaussianSplatReconstructionConfig
+ * tile_size).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  Coordinates: pixel units; pixel (row i, column j) has its centre at
+ *    (j + 0.5, i + 0.5); x to the right, y down.
+ *  Touch rule: Gaussian i touches pixel p when p lies in i's pixel box (the
+ *    tight axis-aligned box of the ellipse q <= k^2, k = cutoff_sigma,
+ *    clipped to the image) and q_i(p) <= k^2, evaluated in FP32 in a fixed
+ *    operation order, so the decision is reproducible bit for bit.
+ *  Memory: every pointer argument is DEVICE memory unless marked "host".
+ *    The caller owns every buffer; the library allocates nothing and keeps
+ *    no state between calls (all per-call state lives in `workspace`).
+ *    Buffers are contiguous and element-aligned; gs2d_record arrays, rect,
+ *    tile_ranges and the workspace must be 16-byte aligned (cudaMalloc and
+ *    torch allocations are 256-byte aligned).  Calls that share a workspace
+ *    must be ordered (one stream, or events between streams).
+ *  Streams: every call enqueues its kernels on `stream` and returns without
+ *    waiting, except gs2d_bin_and_sort with a non-NULL `pairs_out` and
+ *    gs2d_read_status, which wait for the stream.  Outputs are complete when
+ *    the stream reaches the point after the call.
+ *  Errors: arguments are checked on the host before anything is enqueued;
+ *    a failed check returns GS2D_ERR_INVALID_ARG and enqueues nothing.  A
+ *    CUDA launch failure returns GS2D_ERR_CUDA.  No call aborts, throws or
+ *    traps.  Gaussians with non-finite or degenerate parameters are culled
+ *    (they touch nothing and get a zero gradient); that is not an error.
+ *  Limits: 1 <= width, height <= 32768; tile == 16; 0 <= n < 2^31;
+ *    pair capacity < 2^30.
+ */
+#ifndef GS2D_H
+#define GS2D_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GS2D_API __attribute__((visibility("default")))
+#else
+#define GS2D_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st* gs2d_stream_t;
+
+typedef enum gs2d_status {
+  GS2D_OK = 0,
+  GS2D_ERR_INVALID_ARG = 1, /* a host-side argument check failed; nothing was enqueued */
+  GS2D_ERR_CAPACITY = 2,    /* the (tile, Gaussian) pairs exceed pair_capacity */
+  GS2D_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
+  GS2D_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (results invalid) */
+  GS2D_ERR_OVERFLOW = 5     /* the pair count reached 2^30 */
+} gs2d_status;
+
+enum { GS2D_MODE_SUM = 0, GS2D_MODE_COMPOSITE = 1 };
+
+/* Device status flags, read back by gs2d_read_status. */
+enum {
+  GS2D_FLAG_CAPACITY = 1u << 0,
+  GS2D_FLAG_OVERFLOW = 1u << 1,
+  GS2D_FLAG_TIMEOUT = 1u << 2
+};
+
+typedef struct gs2d_config {
+  int32_t width;        /* image width in pixels */
+  int32_t height;       /* image height in pixels */
+  int32_t tile;         /* tile edge in pixels; must be 16 */
+  int32_t mode;         /* GS2D_MODE_SUM or GS2D_MODE_COMPOSITE */
+  float cutoff_sigma;   /* k > 0, finite: the touch rule is q <= k*k; 3 by default */
+  float t_min;          /* composite only, in [0, 1]: a Gaussian contributes only
+                           while the transmittance in front of it is >= t_min;
+                           1e-4 by default */
+} gs2d_config;
+
+/*
+ * Projected record of one Gaussian, written by gs2d_project (48 bytes,
+ * 16-byte aligned).  conic = (A, B, C) are the entries of Sigma^-1 =
+ * [[A, B], [B, C]] in FP32; box_x = x0 | (x1 << 16) and box_y = y0 | (y1 << 16)
+ * are the inclusive pixel box.  A culled Gaussian has an all-zero record
+ * except box_x = box_y = 0x0000FFFF (an empty box).
+ */
+typedef struct gs2d_record {
+  float mean_x, mean_y;
+  float conic_a, conic_b;
+  float conic_c;
+  float red, green, blue;
+  uint32_t box_x, box_y;
+  float opacity;  /* composite: the Gaussian's opacity; 0 in sum mode */
+  float depth;    /* composite: the Gaussian's depth; 0 in sum mode */
+} gs2d_record;
+
+/*
+ * Bytes of device workspace needed by gs2d_bin_and_sort, gs2d_loss_l2 and
+ * gs2d_render_bwd for this configuration, n Gaussians and a pair capacity.
+ * The same workspace must be passed to gs2d_bin_and_sort and to the
+ * gs2d_render_bwd that follows it (the backward reads the per-Gaussian
+ * pair offsets the binning left there).  The contents need no
+ * initialisation.  Returns 0 for arguments that fail the checks above.
+ */
+GS2D_API size_t gs2d_workspace_size(const gs2d_config* cfg, int32_t n, int64_t pair_capacity);
+
+/*
+ * Projection (one thread per Gaussian).  For each Gaussian i: cull test,
+ * Sigma^-1 from L = [[l11, 0], [l21, l22]] (Sigma = L L^T), the pixel box,
+ * the tile rectangle and the number of tiles it covers.
+ *   xy[n,2]       mean in pixels
+ *   chol[n,3]     (l11, l21, l22); the signs of l11 and l22 do not matter
+ *   rgb[n,3]      colour (sum mode: the amplitude; no clamp)
+ *   depth[n]      composite only (NULL in sum mode): front-to-back order key
+ *   opacity[n]    composite only (NULL in sum mode): in [0, 1), else culled
+ *   rec[n]        out: projected records
+ *   rect[n,4]     out: tile rectangle (tx0, ty0, tx1, ty1), inclusive;
+ *                 (0, 0, -1, -1) when culled
+ *   count[n]      out: tiles in rect, 0 when culled
+ */
+GS2D_API gs2d_status gs2d_project(const gs2d_config* cfg, int32_t n, const float* xy, const float* chol,
+                         const float* rgb, const float* depth, const float* opacity,
+                         gs2d_record* rec, int32_t* rect, int32_t* count, gs2d_stream_t stream);
+
+/*
+ * Tile binning and sort.  Every (tile, Gaussian) pair with the tile inside
+ * the Gaussian's rect is listed under its tile; lists are concatenated in
+ * row-major tile order.  Sum mode: ascending Gaussian index within a tile.
+ * Composite: ascending depth (IEEE order; -0 equals +0), ties by ascending
+ * index.  (Per-tile depth sort: DrawingWithGaussians README, Overview,
+ * gsplat-style projection/rasterization.)
+ *   rec, rect, count   from gs2d_project
+ *   pair_capacity      length of sorted_gid and the capacity the workspace
+ *                      was sized for
+ *   pairs_out          host, may be NULL.  Non-NULL: the call waits for the
+ *                      stream, stores the pair count P and returns
+ *                      GS2D_ERR_CAPACITY when P > pair_capacity (retry with
+ *                      a larger capacity) or GS2D_ERR_OVERFLOW/TIMEOUT.
+ *                      NULL: nothing waits; P and the flags stay in the
+ *                      workspace for gs2d_read_status, and on overflow the
+ *                      lists are left empty so later calls render nothing.
+ *   tile_ranges[T,2]   out: [start, end) of tile t in sorted_gid,
+ *                      T = ceil(W/16) * ceil(H/16)
+ *   sorted_gid[cap]    out: Gaussian indices, the first P entries valid
+ *   workspace          gs2d_workspace_size(cfg, n, pair_capacity) bytes
+ */
+GS2D_API gs2d_status gs2d_bin_and_sort(const gs2d_config* cfg, int32_t n, const gs2d_record* rec,
+                              const int32_t* rect, const int32_t* count, int64_t pair_capacity,
+                              int64_t* pairs_out, int32_t* tile_ranges, int32_t* sorted_gid,
+                              void* workspace, gs2d_stream_t stream);
+
+/*
+ * Forward render, one thread block per 16x16 tile.
+ * Sum:        C(p) = sum over touching i of rgb_i * w_i(p), w = exp(-q/2).
+ * Composite:  T = 1; for the touching Gaussians in list order, while
+ *             T >= t_min: alpha = opacity_i * w_i, C += rgb_i * alpha * T,
+ *             T *= (1 - alpha); finally C += T * background.
+ *   background[3]  composite: background colour (NULL = black); ignored in sum mode
+ *   image[3,H,W]   out: planar RGB
+ *   t_final[H,W]   out, composite (required for the backward; may be NULL
+ *                  otherwise): final transmittance
+ *   last[H,W]      out, composite (same): 1 + position within the tile's list
+ *                  of the last Gaussian that contributed, 0 if none
+ */
+GS2D_API gs2d_status gs2d_render_fwd(const gs2d_config* cfg, int32_t n, const gs2d_record* rec,
+                            const int32_t* tile_ranges, const int32_t* sorted_gid,
+                            const float* background, float* image, float* t_final, int32_t* last,
+                            gs2d_stream_t stream);
+
+/*
+ * L2 image loss: loss = (1/(3HW)) sum (image - target)^2 and
+ * d_image = 2 (image - target) / (3HW).  FP32 with a fixed-order two-level
+ * reduction, so the result is bit-reproducible.
+ *   image, target [3,H,W];  loss: one float (device);  d_image [3,H,W] out
+ *   workspace: any workspace from gs2d_workspace_size (uses its first 16 KiB)
+ */
+GS2D_API gs2d_status gs2d_loss_l2(int32_t height, int32_t width, const float* image, const float* target,
+                         float* loss, float* d_image, void* workspace, gs2d_stream_t stream);
+
+/*
+ * Backward render: gradients of the loss given d_image = dL/dC.
+ * The touch and early-termination decisions are held fixed (their
+ * derivative is zero almost everywhere).  Per-pair partial gradients are
+ * written to the workspace and then summed per Gaussian in a fixed order,
+ * so the result is bit-reproducible.  Every output element is written
+ * (culled Gaussians get 0); outputs need no initialisation.
+ *   chol[n,3]            the Cholesky factors given to gs2d_project
+ *   rec, rect            from gs2d_project
+ *   tile_ranges, sorted_gid, workspace   from gs2d_bin_and_sort
+ *   background, t_final, last            composite, as given to / returned by
+ *                                        gs2d_render_fwd (ignored in sum mode)
+ *   d_image[3,H,W]       dL/dC
+ *   d_xy[n,2], d_chol[n,3], d_rgb[n,3]   out
+ *   d_opacity[n]         out, composite (may be NULL)
+ *   d_background[3]      out, composite (may be NULL)
+ */
+GS2D_API gs2d_status gs2d_render_bwd(const gs2d_config* cfg, int32_t n, const float* chol,
+                            const gs2d_record* rec, const int32_t* rect,
+                            const int32_t* tile_ranges, const int32_t* sorted_gid,
+                            const float* background, const float* t_final, const int32_t* last,
+                            const float* d_image, float* d_xy, float* d_chol, float* d_rgb,
+                            float* d_opacity, float* d_background, void* workspace,
+                            gs2d_stream_t stream);
+
+/*
+ * Waits for `stream`, then reads what the last gs2d_bin_and_sort left in
+ * the workspace: the pair count (host *pairs, may be NULL) and the
+ * GS2D_FLAG_* bits (host *flags, may be NULL).  Returns the status those
+ * flags map to (GS2D_OK when none is set).
+ */
+GS2D_API gs2d_status gs2d_read_status(const void* workspace, int64_t* pairs, uint32_t* flags,
+                             gs2d_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+GS2D_API const char* gs2d_status_string(gs2d_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GS2D_H */

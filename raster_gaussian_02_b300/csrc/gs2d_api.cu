@@ -1,0 +1,167 @@
+// The C ABI (include/gs2d.h): host-side argument checks, workspace sizing,
+// and the launches of each call on the caller's stream.  Every check runs
+// before anything is enqueued; no call aborts, throws or traps.
+#include <math.h>
+#include <stdint.h>
+
+#include "gs2d_internal.cuh"
+
+using namespace gs2d;
+
+namespace {
+
+constexpr int kMaxSide = 32768;
+constexpr long long kMaxCapacity = (1ll << 30) - 1;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool config_ok(const gs2d_config* c) {
+  if (!c) return false;
+  if (c->width < 1 || c->width > kMaxSide || c->height < 1 || c->height > kMaxSide) return false;
+  if (c->tile != kTile) return false;
+  if (c->mode != GS2D_MODE_SUM && c->mode != GS2D_MODE_COMPOSITE) return false;
+  if (!isfinite(c->cutoff_sigma) || !(c->cutoff_sigma > 0.0f)) return false;
+  if (!isfinite(c->cutoff_sigma * c->cutoff_sigma)) return false;
+  if (c->mode == GS2D_MODE_COMPOSITE && !(c->t_min >= 0.0f && c->t_min <= 1.0f)) return false;
+  return true;
+}
+
+gs2d_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GS2D_OK : GS2D_ERR_CUDA; }
+
+gs2d_status from_flags(unsigned int f) {
+  if (f & GS2D_FLAG_TIMEOUT) return GS2D_ERR_TIMEOUT;
+  if (f & GS2D_FLAG_OVERFLOW) return GS2D_ERR_OVERFLOW;
+  if (f & GS2D_FLAG_CAPACITY) return GS2D_ERR_CAPACITY;
+  return GS2D_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gs2d_workspace_size(const gs2d_config* cfg, int32_t n, int64_t pair_capacity) {
+  if (!config_ok(cfg) || n < 0 || pair_capacity < 0 || pair_capacity > kMaxCapacity) return 0;
+  return layout_of(*cfg, n, pair_capacity).total;
+}
+
+gs2d_status gs2d_project(const gs2d_config* cfg, int32_t n, const float* xy, const float* chol,
+                         const float* rgb, const float* depth, const float* opacity,
+                         gs2d_record* rec, int32_t* rect, int32_t* count, gs2d_stream_t stream) {
+  if (!config_ok(cfg) || n < 0) return GS2D_ERR_INVALID_ARG;
+  if (n == 0) return GS2D_OK;
+  if (!xy || !chol || !rgb || !rec || !rect || !count) return GS2D_ERR_INVALID_ARG;
+  if (cfg->mode == GS2D_MODE_COMPOSITE && (!depth || !opacity)) return GS2D_ERR_INVALID_ARG;
+  if (!aligned(rec, 16) || !aligned(rect, 16) || !aligned(xy, 4) || !aligned(chol, 4) ||
+      !aligned(rgb, 4) || !aligned(count, 4) || (depth && !aligned(depth, 4)) ||
+      (opacity && !aligned(opacity, 4)))
+    return GS2D_ERR_INVALID_ARG;
+  return from_cuda(launch_project(*cfg, n, xy, chol, rgb, depth, opacity, rec, rect, count,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gs2d_status gs2d_bin_and_sort(const gs2d_config* cfg, int32_t n, const gs2d_record* rec,
+                              const int32_t* rect, const int32_t* count, int64_t pair_capacity,
+                              int64_t* pairs_out, int32_t* tile_ranges, int32_t* sorted_gid,
+                              void* workspace, gs2d_stream_t stream) {
+  if (!config_ok(cfg) || n < 0) return GS2D_ERR_INVALID_ARG;
+  if (pair_capacity < 0 || pair_capacity > kMaxCapacity) return GS2D_ERR_INVALID_ARG;
+  if (!tile_ranges || !workspace || !aligned(tile_ranges, 16) || !aligned(workspace, 16))
+    return GS2D_ERR_INVALID_ARG;
+  if (pair_capacity > 0 && (!sorted_gid || !aligned(sorted_gid, 4))) return GS2D_ERR_INVALID_ARG;
+  if (n > 0 && (!rec || !rect || !count || !aligned(rec, 16) || !aligned(rect, 16) ||
+                !aligned(count, 4)))
+    return GS2D_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_binning(*cfg, n, rec, rect, count, pair_capacity, tile_ranges, sorted_gid,
+                                 static_cast<unsigned char*>(workspace), s);
+  if (e != cudaSuccess) return GS2D_ERR_CUDA;
+  if (!pairs_out) return GS2D_OK;
+  uint32_t flags = 0;
+  const gs2d_status st = gs2d_read_status(workspace, pairs_out, &flags, stream);
+  return st;
+}
+
+gs2d_status gs2d_render_fwd(const gs2d_config* cfg, int32_t n, const gs2d_record* rec,
+                            const int32_t* tile_ranges, const int32_t* sorted_gid,
+                            const float* background, float* image, float* t_final, int32_t* last,
+                            gs2d_stream_t stream) {
+  if (!config_ok(cfg) || n < 0) return GS2D_ERR_INVALID_ARG;
+  if (!tile_ranges || !image || !aligned(tile_ranges, 16) || !aligned(image, 4))
+    return GS2D_ERR_INVALID_ARG;
+  if (n > 0 && (!rec || !sorted_gid || !aligned(rec, 16) || !aligned(sorted_gid, 4)))
+    return GS2D_ERR_INVALID_ARG;
+  if ((t_final && !aligned(t_final, 4)) || (last && !aligned(last, 4)) ||
+      (background && !aligned(background, 4)))
+    return GS2D_ERR_INVALID_ARG;
+  return from_cuda(launch_render_fwd(*cfg, rec, tile_ranges, sorted_gid, background, image, t_final,
+                                     last, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gs2d_status gs2d_loss_l2(int32_t height, int32_t width, const float* image, const float* target,
+                         float* loss, float* d_image, void* workspace, gs2d_stream_t stream) {
+  if (height < 1 || width < 1 || height > kMaxSide || width > kMaxSide) return GS2D_ERR_INVALID_ARG;
+  if (!image || !target || !loss || !d_image || !workspace) return GS2D_ERR_INVALID_ARG;
+  if (!aligned(image, 4) || !aligned(target, 4) || !aligned(loss, 4) || !aligned(d_image, 4) ||
+      !aligned(workspace, 16))
+    return GS2D_ERR_INVALID_ARG;
+  return from_cuda(launch_loss_l2(height, width, image, target, loss, d_image,
+                                  static_cast<unsigned char*>(workspace),
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gs2d_status gs2d_render_bwd(const gs2d_config* cfg, int32_t n, const float* chol,
+                            const gs2d_record* rec, const int32_t* rect,
+                            const int32_t* tile_ranges, const int32_t* sorted_gid,
+                            const float* background, const float* t_final, const int32_t* last,
+                            const float* d_image, float* d_xy, float* d_chol, float* d_rgb,
+                            float* d_opacity, float* d_background, void* workspace,
+                            gs2d_stream_t stream) {
+  if (!config_ok(cfg) || n < 0) return GS2D_ERR_INVALID_ARG;
+  const bool comp = cfg->mode == GS2D_MODE_COMPOSITE;
+  if (!tile_ranges || !d_image || !workspace || !aligned(tile_ranges, 16) ||
+      !aligned(d_image, 4) || !aligned(workspace, 16))
+    return GS2D_ERR_INVALID_ARG;
+  if (n > 0 && (!chol || !rec || !rect || !sorted_gid || !d_xy || !d_chol || !d_rgb ||
+                !aligned(rec, 16) || !aligned(rect, 16) || !aligned(chol, 4) ||
+                !aligned(sorted_gid, 4) || !aligned(d_xy, 4) || !aligned(d_chol, 4) ||
+                !aligned(d_rgb, 4)))
+    return GS2D_ERR_INVALID_ARG;
+  if (comp && (!t_final || !last || !aligned(t_final, 4) || !aligned(last, 4)))
+    return GS2D_ERR_INVALID_ARG;
+  if ((d_opacity && !aligned(d_opacity, 4)) || (d_background && !aligned(d_background, 4)) ||
+      (background && !aligned(background, 4)))
+    return GS2D_ERR_INVALID_ARG;
+  return from_cuda(launch_render_bwd(*cfg, n, chol, rec, rect, tile_ranges, sorted_gid,
+                                     comp ? background : nullptr, t_final, last, d_image, d_xy,
+                                     d_chol, d_rgb, comp ? d_opacity : nullptr,
+                                     comp ? d_background : nullptr,
+                                     static_cast<unsigned char*>(workspace),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gs2d_status gs2d_read_status(const void* workspace, int64_t* pairs, uint32_t* flags,
+                             gs2d_stream_t stream) {
+  if (!workspace || !aligned(workspace, 16)) return GS2D_ERR_INVALID_ARG;
+  Header h;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&h, workspace, sizeof(Header), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return GS2D_ERR_CUDA;
+  if (pairs) *pairs = h.pairs;
+  if (flags) *flags = h.flags;
+  return from_flags(h.flags);
+}
+
+const char* gs2d_status_string(gs2d_status status) {
+  switch (status) {
+    case GS2D_OK: return "ok";
+    case GS2D_ERR_INVALID_ARG: return "invalid argument";
+    case GS2D_ERR_CAPACITY: return "pair capacity exceeded";
+    case GS2D_ERR_CUDA: return "CUDA error";
+    case GS2D_ERR_TIMEOUT: return "device wait timed out";
+    case GS2D_ERR_OVERFLOW: return "pair count overflow";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

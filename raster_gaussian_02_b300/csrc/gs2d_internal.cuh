@@ -1,0 +1,165 @@
+// Internal declarations of the gs2d CUDA library: workspace layout, device
+// helpers for the FP32 touch rule, and the kernel launchers each .cu file
+// provides.  Not part of the public interface (include/gs2d.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gs2d.h"
+
+namespace gs2d {
+
+constexpr int kTile = 16;
+constexpr int kTilePixels = kTile * kTile;
+
+// Workspace layout (byte offsets; every region 256-byte aligned).  The
+// regions the backward reads come before every region whose size depends on
+// the pair capacity, so their offsets follow from (cfg, n) alone.
+//   [0, 256)        Header
+//   [256, 4352)     loss partial sums (kLossMaxBlocks floats)
+//   [4352, 12544)   radix digit histograms [kMaxPasses][256]
+//   then            scan look-back words [ceil(n / kScanItems) + 1] (uint64)
+//   then            per-Gaussian pair offsets [n] (int32)
+//   then            background partials [T] x 4 floats (composite)
+//   then            backward partials [cap] x 8 floats (sum) or x 12 (composite)
+//   then            radix look-back words [passes][partitions(cap)][256] (uint32)
+//   then            keys A, keys B [cap] (uint32 sum, uint64 composite)
+//   then            values scratch [cap] (uint32)
+struct Header {
+  long long pairs;           // P, written by the binning
+  unsigned int flags;        // GS2D_FLAG_*
+  unsigned int scan_ticket;  // block order for the scan look-back
+  unsigned int radix_ticket[8];
+};
+
+constexpr int kMaxPasses = 8;
+constexpr size_t kOffLoss = 256;
+constexpr int kLossMaxBlocks = 1024;
+constexpr size_t kOffHist = kOffLoss + kLossMaxBlocks * 4;  // 4352
+constexpr size_t kOffScan = kOffHist + kMaxPasses * 256 * 4; // 12544
+
+constexpr int kScanThreads = 256;
+constexpr int kScanPerThread = 4;
+constexpr int kScanItems = kScanThreads * kScanPerThread;  // Gaussians per scan block
+
+constexpr int kRadixThreads = 256;
+constexpr int kRadixPerThread = 8;
+constexpr int kRadixItems = kRadixThreads * kRadixPerThread;  // keys per partition
+
+// Bounded device-side waits: after this many polls a waiting thread gives up,
+// sets GS2D_FLAG_TIMEOUT and continues, so a kernel always terminates.
+constexpr unsigned int kSpinLimit = 1u << 22;
+
+struct Layout {
+  size_t scan, offsets, bg_partials, partials, radix_status, keys_a, keys_b, vals_tmp, total;
+  int passes, tile_bits, key_bytes, partial_floats;
+  long long partitions;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline int tiles_x(const gs2d_config& c) { return (c.width + kTile - 1) / kTile; }
+inline int tiles_y(const gs2d_config& c) { return (c.height + kTile - 1) / kTile; }
+inline int num_tiles(const gs2d_config& c) { return tiles_x(c) * tiles_y(c); }
+
+inline int bits_for(long long values) {  // bits needed to hold 0 .. values-1
+  int b = 0;
+  while ((1ll << b) < values) ++b;
+  return b;
+}
+
+inline Layout layout_of(const gs2d_config& c, long long n, long long cap) {
+  Layout L{};
+  const int T = num_tiles(c);
+  L.tile_bits = bits_for(T);
+  const bool comp = c.mode == GS2D_MODE_COMPOSITE;
+  const int key_bits = L.tile_bits + (comp ? 32 : 0);
+  L.passes = (key_bits + 7) / 8;
+  L.key_bytes = comp ? 8 : 4;
+  L.partial_floats = comp ? 12 : 8;
+  L.partitions = (cap + kRadixItems - 1) / kRadixItems;
+  size_t o = kOffScan;
+  L.scan = o;
+  o = align256(o + 8 * size_t((n + kScanItems - 1) / kScanItems + 1));
+  L.offsets = o;
+  o = align256(o + 4 * size_t(n));
+  L.bg_partials = o;
+  if (comp) o = align256(o + 16 * size_t(T));
+  L.partials = o;
+  o = align256(o + 4 * size_t(L.partial_floats) * size_t(cap));
+  L.radix_status = o;
+  o = align256(o + 4 * size_t(L.passes) * size_t(L.partitions) * 256);
+  L.keys_a = o;
+  o = align256(o + size_t(L.key_bytes) * size_t(cap));
+  L.keys_b = o;
+  o = align256(o + size_t(L.key_bytes) * size_t(cap));
+  L.vals_tmp = o;
+  o = align256(o + 4 * size_t(cap));
+  L.total = o < 16384 ? 16384 : o;
+  return L;
+}
+
+// ------------------------------------------------------------ device side --
+
+// The FP32 touch rule.  Every operation is an explicitly rounded intrinsic so
+// that the compiler can neither contract nor reorder it; the oracle evaluates
+// the same sequence on the CPU.
+//   q = fma(dx, fma(A, dx, (2B) * dy), (C * dy) * dy)
+__device__ __forceinline__ float touch_q(float dx, float dy, float A, float B2, float C) {
+  const float cdy = __fmul_rn(C, dy);
+  const float cdydy = __fmul_rn(cdy, dy);
+  const float inner = __fmaf_rn(A, dx, __fmul_rn(B2, dy));
+  return __fmaf_rn(dx, inner, cdydy);
+}
+
+// 2^x with the hardware approximation (the PTX ex2.approx instruction).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// exp(-q/2) = 2^(q * (-log2(e)/2)).
+constexpr float kNegHalfLog2e = -0.72134752044448170368f;
+
+__device__ __forceinline__ unsigned int box_lo(unsigned int b) { return b & 0xFFFFu; }
+__device__ __forceinline__ unsigned int box_hi(unsigned int b) { return b >> 16; }
+
+// Monotone map of a finite float to uint32 (IEEE order, -0 mapped as +0).
+__device__ __forceinline__ unsigned int depth_key(float d) {
+  unsigned int u = __float_as_uint(d);
+  if ((u << 1) == 0u) u = 0u;  // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ------------------------------------------------------------- launchers --
+// Each returns cudaGetLastError() after enqueueing.
+
+cudaError_t launch_project(const gs2d_config& c, int n, const float* xy, const float* chol,
+                           const float* rgb, const float* depth, const float* opacity,
+                           gs2d_record* rec, int* rect, int* count, cudaStream_t s);
+
+cudaError_t launch_binning(const gs2d_config& c, int n, const gs2d_record* rec, const int* rect,
+                           const int* count, long long cap, int* tile_ranges, int* sorted_gid,
+                           unsigned char* ws, cudaStream_t s);
+
+cudaError_t launch_render_fwd(const gs2d_config& c, const gs2d_record* rec, const int* ranges,
+                              const int* sorted_gid, const float* bg, float* image, float* t_final,
+                              int* last, cudaStream_t s);
+
+cudaError_t launch_loss_l2(int h, int w, const float* image, const float* target, float* loss,
+                           float* d_image, unsigned char* ws, cudaStream_t s);
+
+cudaError_t launch_gather(const gs2d_config& c, int n, const float* chol, const gs2d_record* rec,
+                          const int* rect, const unsigned char* ws, float* d_xy, float* d_chol,
+                          float* d_rgb, float* d_opacity, float* d_bg, cudaStream_t s);
+
+cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
+                              const gs2d_record* rec, const int* rect, const int* ranges,
+                              const int* sorted_gid, const float* bg, const float* t_final,
+                              const int* last, const float* d_image, float* d_xy, float* d_chol,
+                              float* d_rgb, float* d_opacity, float* d_bg, unsigned char* ws,
+                              cudaStream_t s);
+
+}  // namespace gs2d

@@ -1,0 +1,87 @@
+// L2 image loss (FlashImgs README, Configuration: l2_loss_ratio, the L2/MSE
+// weight):  loss = (1/(3HW)) sum (C - target)^2,  dL/dC = 2 (C - target)/(3HW).
+// Two kernels, no atomics: every block writes the partial sum of a fixed
+// grid-stride set of elements, then one block adds the partials in order,
+// so the loss is bit-reproducible.
+#include "gs2d_internal.cuh"
+
+namespace gs2d {
+
+namespace {
+
+constexpr int kLossThreads = 256;
+
+__device__ __forceinline__ float block_sum_256(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float s = 0.f;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kLossThreads / 32; ++w) s += red[w];
+  return s;
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kLossThreads)
+k_loss_partial(long long m, const float* __restrict__ image, const float* __restrict__ target,
+               float scale, float* __restrict__ d_image, float* __restrict__ partials) {
+  __shared__ float red[kLossThreads / 32];
+  float acc = 0.f;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  if (kVec) {
+    const float4* a = reinterpret_cast<const float4*>(image);
+    const float4* b = reinterpret_cast<const float4*>(target);
+    float4* d = reinterpret_cast<float4*>(d_image);
+    for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < m / 4; k += stride) {
+      const float4 x = a[k], y = b[k];
+      const float4 e = make_float4(x.x - y.x, x.y - y.y, x.z - y.z, x.w - y.w);
+      d[k] = make_float4(e.x * scale, e.y * scale, e.z * scale, e.w * scale);
+      acc = fmaf(e.x, e.x, acc);
+      acc = fmaf(e.y, e.y, acc);
+      acc = fmaf(e.z, e.z, acc);
+      acc = fmaf(e.w, e.w, acc);
+    }
+  } else {
+    for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < m; k += stride) {
+      const float e = image[k] - target[k];
+      d_image[k] = e * scale;
+      acc = fmaf(e, e, acc);
+    }
+  }
+  const float s = block_sum_256(acc, red);
+  if (threadIdx.x == 0) partials[blockIdx.x] = s;
+}
+
+__global__ void __launch_bounds__(kLossThreads)
+k_loss_final(int nb, const float* __restrict__ partials, float m, float* __restrict__ loss) {
+  __shared__ float red[kLossThreads / 32];
+  float acc = 0.f;
+  for (int k = threadIdx.x; k < nb; k += blockDim.x) acc += partials[k];
+  const float s = block_sum_256(acc, red);
+  if (threadIdx.x == 0) *loss = s / m;
+}
+
+}  // namespace
+
+cudaError_t launch_loss_l2(int h, int w, const float* image, const float* target, float* loss,
+                           float* d_image, unsigned char* ws, cudaStream_t s) {
+  const long long m = 3ll * h * w;
+  float* partials = reinterpret_cast<float*>(ws + kOffLoss);
+  const bool vec = (m % 4 == 0) && ((reinterpret_cast<uintptr_t>(image) |
+                                     reinterpret_cast<uintptr_t>(target) |
+                                     reinterpret_cast<uintptr_t>(d_image)) & 15) == 0;
+  const long long work = vec ? m / 4 : m;
+  long long blocks = (work + kLossThreads * 4 - 1) / (kLossThreads * 4);
+  if (blocks < 1) blocks = 1;
+  if (blocks > kLossMaxBlocks) blocks = kLossMaxBlocks;
+  const float scale = float(2.0 / double(m));
+  if (vec)
+    k_loss_partial<true><<<int(blocks), kLossThreads, 0, s>>>(m, image, target, scale, d_image, partials);
+  else
+    k_loss_partial<false><<<int(blocks), kLossThreads, 0, s>>>(m, image, target, scale, d_image, partials);
+  k_loss_final<<<1, kLossThreads, 0, s>>>(int(blocks), partials, float(m), loss);
+  return cudaGetLastError();
+}
+
+}  // namespace gs2d

@@ -1,0 +1,198 @@
+// Projection (Cholesky factor -> inverse covariance, 3-sigma pixel box, tile
+// rectangle) and its backward (per-pair partial gradients summed per
+// Gaussian, then the chain rule from the inverse covariance to L).
+//
+// Sigma = L L^T with L = [[a, 0], [b, c]] (DrawingWithGaussians README,
+// MLX-specific notes: lower-triangular L); the 8 parameters per Gaussian are
+// position, covariance and colour (GaussianImage project page, Overview).
+#include "gs2d_internal.cuh"
+
+namespace gs2d {
+
+namespace {
+
+__global__ void __launch_bounds__(256)
+k_project(gs2d_config c, int n, const float* __restrict__ xy, const float* __restrict__ chol,
+          const float* __restrict__ rgb, const float* __restrict__ depth,
+          const float* __restrict__ opacity, float4* __restrict__ rec, int4* __restrict__ rect,
+          int* __restrict__ count) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float mx = xy[2 * i], my = xy[2 * i + 1];
+  const float a = chol[3 * i], b = chol[3 * i + 1], cc = chol[3 * i + 2];
+  const float r = rgb[3 * i], g = rgb[3 * i + 1], bl = rgb[3 * i + 2];
+  const bool comp = c.mode == GS2D_MODE_COMPOSITE;
+  float o = 0.0f, d = 0.0f;
+  if (comp) {
+    o = opacity[i];
+    d = depth[i];
+  }
+  bool ok = isfinite(mx) && isfinite(my) && isfinite(a) && isfinite(b) && isfinite(cc) &&
+            isfinite(r) && isfinite(g) && isfinite(bl) && a != 0.0f && cc != 0.0f;
+  if (comp) ok = ok && isfinite(d) && isfinite(o) && o >= 0.0f && o < 1.0f;
+
+  // Sigma^-1 = [[A, B], [B, C]]: A = (b^2 + c^2)/(a^2 c^2), B = -b/(a c^2),
+  // C = 1/c^2, in this FP32 order (IEEE division, explicit rounding).
+  float A = 0.0f, B = 0.0f, C = 0.0f;
+  if (ok) {
+    const float ia = __fdiv_rn(1.0f, a);
+    const float ic = __fdiv_rn(1.0f, cc);
+    C = __fmul_rn(ic, ic);
+    const float t = __fmul_rn(b, ia);
+    B = -__fmul_rn(t, C);
+    A = __fmaf_rn(__fmul_rn(t, t), C, __fmul_rn(ia, ia));
+    ok = isfinite(A) && isfinite(B) && isfinite(C);
+  }
+  // Tight box of the ellipse q <= k^2: half widths k*sqrt(Sigma_xx) = k|a| and
+  // k*sqrt(Sigma_yy) = k*sqrt(b^2 + c^2); column j is inside when its centre
+  // j + 0.5 lies in [mu_x - r_x, mu_x + r_x].
+  int x0 = 0, y0 = 0, x1 = -1, y1 = -1;
+  if (ok) {
+    const float k = c.cutoff_sigma;
+    const float rx = __fmul_rn(k, fabsf(a));
+    const float ry = __fmul_rn(k, __fsqrt_rn(__fmaf_rn(b, b, __fmul_rn(cc, cc))));
+    const float fx0 = ceilf(__fsub_rn(__fsub_rn(mx, rx), 0.5f));
+    const float fx1 = floorf(__fsub_rn(__fadd_rn(mx, rx), 0.5f));
+    const float fy0 = ceilf(__fsub_rn(__fsub_rn(my, ry), 0.5f));
+    const float fy1 = floorf(__fsub_rn(__fadd_rn(my, ry), 0.5f));
+    const float wmax = float(c.width - 1), hmax = float(c.height - 1);
+    ok = (fx0 <= fx1) && (fy0 <= fy1) && !(fx0 > wmax || fx1 < 0.0f || fy0 > hmax || fy1 < 0.0f);
+    if (ok) {
+      x0 = int(fmaxf(fx0, 0.0f));
+      y0 = int(fmaxf(fy0, 0.0f));
+      x1 = int(fminf(fx1, wmax));
+      y1 = int(fminf(fy1, hmax));
+    }
+  }
+  float4* out = rec + 3 * size_t(i);
+  if (ok) {
+    out[0] = make_float4(mx, my, A, B);
+    out[1] = make_float4(C, r, g, bl);
+    out[2] = make_float4(__uint_as_float(unsigned(x0) | (unsigned(x1) << 16)),
+                         __uint_as_float(unsigned(y0) | (unsigned(y1) << 16)), o, d);
+    const int4 rc = make_int4(x0 / kTile, y0 / kTile, x1 / kTile, y1 / kTile);
+    rect[i] = rc;
+    count[i] = (rc.z - rc.x + 1) * (rc.w - rc.y + 1);
+  } else {
+    out[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    out[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    out[2] = make_float4(__uint_as_float(0xFFFFu), __uint_as_float(0xFFFFu), 0.f, 0.f);
+    rect[i] = make_int4(0, 0, -1, -1);
+    count[i] = 0;
+  }
+}
+
+// Per Gaussian: sum its per-pair partials (one per tile of its rectangle, in
+// emission order) and apply the chain rule to L:
+//   dA/da = -2A/a,        dA/db = 2b/(a^2 c^2),  dA/dc = -2b^2/(a^2 c^3)
+//   dB/da = b/(a^2 c^2),  dB/db = -1/(a c^2),    dB/dc = 2b/(a c^3)
+//   dC/dc = -2/c^3;       d(xy) = d(mean).
+// The last block also sums the per-tile background partials (composite).
+template <bool kComposite>
+__global__ void __launch_bounds__(256)
+k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
+         const int4* __restrict__ rect, const int* __restrict__ offsets,
+         const float4* __restrict__ partials, const Header* __restrict__ hdr,
+         float* __restrict__ d_xy, float* __restrict__ d_chol, float* __restrict__ d_rgb,
+         float* __restrict__ d_opacity, int T, const float4* __restrict__ bg_partials,
+         float* __restrict__ d_bg) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const bool bad = (hdr->flags & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) != 0;
+  if (i < n) {
+    const int4 rc = rect[i];
+    const int cnt = (rc.z >= rc.x) ? (rc.z - rc.x + 1) * (rc.w - rc.y + 1) : 0;
+    float s[9] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (!bad && cnt > 0) {
+      constexpr int kStride = kComposite ? 3 : 2;
+      const float4* p = partials + size_t(offsets[i]) * kStride;
+      for (int k = 0; k < cnt; ++k, p += kStride) {
+        const float4 u = p[0], v = p[1];
+        s[0] += u.x; s[1] += u.y; s[2] += u.z; s[3] += u.w;
+        s[4] += v.x; s[5] += v.y; s[6] += v.z; s[7] += v.w;
+        if (kComposite) s[8] += p[2].x;
+      }
+    }
+    float g0 = 0.f, g1 = 0.f, g2 = 0.f;
+    if (cnt > 0 && !bad) {
+      const float a = chol[3 * i], b = chol[3 * i + 1], c = chol[3 * i + 2];
+      const float A = rec[3 * size_t(i)].z;
+      const float ia = 1.0f / a, ic = 1.0f / c;
+      const float ia2ic2 = ia * ia * ic * ic;
+      const float dA = s[2], dB = s[3], dC = s[4];
+      g0 = dA * (-2.0f * A * ia) + dB * (b * ia2ic2);
+      g1 = dA * (2.0f * b * ia2ic2) + dB * (-ia * ic * ic);
+      g2 = dA * (-2.0f * b * b * ia2ic2 * ic) + dB * (2.0f * b * ia * ic * ic * ic) +
+           dC * (-2.0f * ic * ic * ic);
+    } else {
+      for (int k = 0; k < 9; ++k) s[k] = 0.f;
+    }
+    d_xy[2 * i] = s[0];
+    d_xy[2 * i + 1] = s[1];
+    d_chol[3 * i] = g0;
+    d_chol[3 * i + 1] = g1;
+    d_chol[3 * i + 2] = g2;
+    d_rgb[3 * i] = s[5];
+    d_rgb[3 * i + 1] = s[6];
+    d_rgb[3 * i + 2] = s[7];
+    if (kComposite && d_opacity) d_opacity[i] = s[8];
+  }
+  if (kComposite && d_bg && blockIdx.x == gridDim.x - 1) {
+    // fixed-order reduction of the per-tile background partials
+    __shared__ float red[3][256];
+    float x = 0.f, y = 0.f, z = 0.f;
+    if (!bad)
+      for (int t = threadIdx.x; t < T; t += blockDim.x) {
+        const float4 v = bg_partials[t];
+        x += v.x; y += v.y; z += v.z;
+      }
+    red[0][threadIdx.x] = x;
+    red[1][threadIdx.x] = y;
+    red[2][threadIdx.x] = z;
+    __syncthreads();
+    for (int h = blockDim.x / 2; h > 0; h >>= 1) {
+      if (threadIdx.x < h)
+        for (int q = 0; q < 3; ++q) red[q][threadIdx.x] += red[q][threadIdx.x + h];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      d_bg[0] = red[0][0];
+      d_bg[1] = red[1][0];
+      d_bg[2] = red[2][0];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_project(const gs2d_config& c, int n, const float* xy, const float* chol,
+                           const float* rgb, const float* depth, const float* opacity,
+                           gs2d_record* rec, int* rect, int* count, cudaStream_t s) {
+  if (n > 0)
+    k_project<<<(n + 255) / 256, 256, 0, s>>>(c, n, xy, chol, rgb, depth, opacity,
+                                              reinterpret_cast<float4*>(rec),
+                                              reinterpret_cast<int4*>(rect), count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const gs2d_config& c, int n, const float* chol, const gs2d_record* rec,
+                          const int* rect, const unsigned char* ws, float* d_xy, float* d_chol,
+                          float* d_rgb, float* d_opacity, float* d_bg, cudaStream_t s) {
+  const Layout L = layout_of(c, n, 0);
+  const int T = num_tiles(c);
+  const int blocks = n > 0 ? (n + 255) / 256 : 1;
+  const Header* hdr = reinterpret_cast<const Header*>(ws);
+  if (c.mode == GS2D_MODE_COMPOSITE)
+    k_gather<true><<<blocks, 256, 0, s>>>(
+        n, chol, reinterpret_cast<const float4*>(rec), reinterpret_cast<const int4*>(rect),
+        reinterpret_cast<const int*>(ws + L.offsets), reinterpret_cast<const float4*>(ws + L.partials),
+        hdr, d_xy, d_chol, d_rgb, d_opacity, T, reinterpret_cast<const float4*>(ws + L.bg_partials),
+        d_bg);
+  else
+    k_gather<false><<<blocks, 256, 0, s>>>(
+        n, chol, reinterpret_cast<const float4*>(rec), reinterpret_cast<const int4*>(rect),
+        reinterpret_cast<const int*>(ws + L.offsets), reinterpret_cast<const float4*>(ws + L.partials),
+        hdr, d_xy, d_chol, d_rgb, nullptr, T, nullptr, nullptr);
+  return cudaGetLastError();
+}
+
+}  // namespace gs2d

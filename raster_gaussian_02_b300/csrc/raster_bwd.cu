@@ -1,0 +1,304 @@
+// Backward raster.  Gradients of the loss given dL/dC, with the touch and
+// early-termination decisions held fixed.  Every (tile, Gaussian) pair
+// writes its partial gradient to its own slot (the pair's emission slot:
+// the Gaussian's pair offset plus the tile's position in its rectangle), so
+// no atomics are needed and the per-Gaussian sums, taken later in a fixed
+// order, are bit-reproducible.
+//
+// With q = A dx^2 + 2B dx dy + C dy^2 (dx = px - mu_x, dy = py - mu_y) and
+// w = exp(-q/2), write t = w * dL/dw at a pixel.  Then dL/dq = -t/2 and
+//     dL/dmu_x = sum t (A dx + B dy),   dL/dmu_y = sum t (B dx + C dy),
+//     dL/dA = -1/2 sum t dx^2,  dL/dB = -sum t dx dy,  dL/dC = -1/2 sum t dy^2.
+// Sum mode: dL/dw = sum_k g_k rgb_k and dL/drgb_k = sum g_k w (g = dL/dC).
+// Composite: with alpha = o w, T the transmittance in front of the
+// Gaussian and S the colour accumulated behind it (including T_final * bg),
+//     dL/dalpha = sum_k g_k (rgb_k T - S_k / (1 - alpha)),
+//     dL/do = w dL/dalpha,  dL/dw = o dL/dalpha,  dL/drgb_k = g_k alpha T,
+//     dL/dbg_k = sum over pixels of T_final g_k.
+#include "gs2d_internal.cuh"
+
+namespace gs2d {
+
+namespace {
+
+constexpr int kBwdSumThreads = 128;
+
+// Sum mode: one thread per (tile, Gaussian) pair, walking exactly the
+// pixels of the Gaussian's box inside the tile.  dL/dC of the tile is
+// staged in shared memory.
+__global__ void __launch_bounds__(kBwdSumThreads)
+k_render_bwd_sum(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
+                 const int4* __restrict__ rect, const int2* __restrict__ ranges,
+                 const int* __restrict__ sorted_gid, const int* __restrict__ offsets,
+                 const float* __restrict__ d_image, float4* __restrict__ partials) {
+  __shared__ float4 s_g[kTilePixels];
+  const int tile = blockIdx.x;
+  const int2 rg = ranges[tile];
+  if (rg.x == rg.y) return;
+  const int tx = tile % tiles_x, ty = tile / tiles_x;
+  const int X0 = tx * kTile, Y0 = ty * kTile;
+  const size_t HW = size_t(c.width) * c.height;
+  for (int p = threadIdx.x; p < kTilePixels; p += blockDim.x) {
+    const int x = X0 + (p & 15), y = Y0 + (p >> 4);
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (x < c.width && y < c.height) {
+      const size_t o = size_t(y) * c.width + x;
+      g = make_float4(d_image[o], d_image[HW + o], d_image[2 * HW + o], 0.f);
+    }
+    s_g[p] = g;
+  }
+  __syncthreads();
+  const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
+  for (int k = rg.x + threadIdx.x; k < rg.y; k += blockDim.x) {
+    const int gid = sorted_gid[k];
+    const float4* r = rec + 3 * size_t(gid);
+    const float4 p0 = r[0], p1 = r[1], p2 = r[2];
+    const float mx = p0.x, my = p0.y, A = p0.z, B = p0.w, B2 = 2.0f * p0.w, C = p1.x;
+    const unsigned int bx = __float_as_uint(p2.x), by = __float_as_uint(p2.y);
+    const int xa = max(int(box_lo(bx)), X0), xb = min(int(box_hi(bx)), X0 + kTile - 1);
+    const int ya = max(int(box_lo(by)), Y0), yb = min(int(box_hi(by)), Y0 + kTile - 1);
+    float sr = 0.f, sg = 0.f, sb = 0.f, Sx = 0.f, Sy = 0.f, Sxx = 0.f, Sxy = 0.f, Syy = 0.f;
+    for (int y = ya; y <= yb; ++y) {
+      const float dy = __fsub_rn(float(y) + 0.5f, my);
+      const float b2dy = __fmul_rn(B2, dy);
+      const float cdydy = __fmul_rn(__fmul_rn(C, dy), dy);
+      float r0 = 0.f, rx = 0.f, rxx = 0.f;
+      const int row = (y - Y0) * kTile - X0;
+      float pxf = float(xa) + 0.5f;
+      for (int x = xa; x <= xb; ++x, pxf += 1.0f) {
+        const float dx = __fsub_rn(pxf, mx);
+        const float q = __fmaf_rn(dx, __fmaf_rn(A, dx, b2dy), cdydy);
+        if (q <= kk) {
+          const float w = ex2_approx(q * kNegHalfLog2e);
+          const float4 g = s_g[row + x];
+          sr = fmaf(g.x, w, sr);
+          sg = fmaf(g.y, w, sg);
+          sb = fmaf(g.z, w, sb);
+          const float t = w * fmaf(g.x, p1.y, fmaf(g.y, p1.z, g.z * p1.w));
+          r0 += t;
+          const float tdx = t * dx;
+          rx += tdx;
+          rxx = fmaf(tdx, dx, rxx);
+        }
+      }
+      Sx += rx;
+      Sy = fmaf(r0, dy, Sy);
+      Sxx += rxx;
+      Sxy = fmaf(rx, dy, Sxy);
+      Syy = fmaf(r0 * dy, dy, Syy);
+    }
+    const int4 rc = rect[gid];
+    const int slot = offsets[gid] + (ty - rc.y) * (rc.z - rc.x + 1) + (tx - rc.x);
+    float4* out = partials + 2 * size_t(slot);
+    out[0] = make_float4(fmaf(A, Sx, B * Sy), fmaf(B, Sx, C * Sy), -0.5f * Sxx, -Sxy);
+    out[1] = make_float4(-0.5f * Syy, sr, sg, sb);
+  }
+}
+
+constexpr int kBwdCompThreads = 256;
+constexpr int kCompChunk = 128;
+constexpr int kCompVals = 9;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+struct CompStage {
+  float4 mc[kCompChunk];  // mean_x, mean_y, A, 2B
+  float4 cr[kCompChunk];  // C, r, g, b
+  uint2 box[kCompChunk];
+  float op[kCompChunk];
+  int gid[kCompChunk];
+  unsigned char list[8][kCompChunk];
+  float acc[8][kCompChunk][kCompVals];  // per-warp partials, summed over warps in order
+  float bgred[8][3];
+};
+
+// Composite: one block per tile, one pixel per thread (8x4 sub-block per
+// warp as in the forward), walking the tile's list back to front from each
+// pixel's last contributor.
+__global__ void __launch_bounds__(kBwdCompThreads)
+k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
+                  const int4* __restrict__ rect, const int2* __restrict__ ranges,
+                  const int* __restrict__ sorted_gid, const int* __restrict__ offsets,
+                  const float* __restrict__ bg, const float* __restrict__ t_final,
+                  const int* __restrict__ last, const float* __restrict__ d_image,
+                  float4* __restrict__ partials, float4* __restrict__ bg_partials) {
+  __shared__ CompStage sm;
+  const int tile = blockIdx.x;
+  const int tx = tile % tiles_x, ty = tile / tiles_x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bx0 = tx * kTile + (warp & 1) * 8;
+  const int by0 = ty * kTile + (warp >> 1) * 4;
+  const int px = bx0 + (lane & 7), py = by0 + (lane >> 3);
+  const float pxf = float(px) + 0.5f, pyf = float(py) + 0.5f;
+  const bool inside = px < c.width && py < c.height;
+  const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
+  const unsigned int lt = (1u << lane) - 1u;
+  const int2 rg = ranges[tile];
+  const size_t HW = size_t(c.width) * c.height;
+  const float bgr = bg ? bg[0] : 0.f, bgg = bg ? bg[1] : 0.f, bgb = bg ? bg[2] : 0.f;
+
+  float T = 1.f, gr = 0.f, gg = 0.f, gb = 0.f;
+  int lst = 0;
+  if (inside) {
+    const size_t p = size_t(py) * c.width + px;
+    T = t_final[p];
+    lst = last[p];
+    gr = d_image[p];
+    gg = d_image[HW + p];
+    gb = d_image[2 * HW + p];
+  }
+  // background gradient: T_final * g summed over the tile, fixed order
+  {
+    const float vr = warp_sum(inside ? T * gr : 0.f);
+    const float vg = warp_sum(inside ? T * gg : 0.f);
+    const float vb = warp_sum(inside ? T * gb : 0.f);
+    if (lane == 0) {
+      sm.bgred[warp][0] = vr;
+      sm.bgred[warp][1] = vg;
+      sm.bgred[warp][2] = vb;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float x = 0.f, y = 0.f, z = 0.f;
+      for (int w = 0; w < 8; ++w) {
+        x += sm.bgred[w][0];
+        y += sm.bgred[w][1];
+        z += sm.bgred[w][2];
+      }
+      bg_partials[tile] = make_float4(x, y, z, 0.f);
+    }
+  }
+  float Sr = T * bgr, Sg = T * bgg, Sb = T * bgb;
+  const int len = rg.y - rg.x;
+  const int nchunks = (len + kCompChunk - 1) / kCompChunk;
+  for (int ci = nchunks - 1; ci >= 0; --ci) {
+    const int cb = rg.x + ci * kCompChunk;
+    const int cnt = min(kCompChunk, rg.y - cb);
+    if (tid < cnt) {
+      const int gid = sorted_gid[cb + tid];
+      const float4* r = rec + 3 * size_t(gid);
+      const float4 p0 = r[0], p1 = r[1], p2 = r[2];
+      sm.mc[tid] = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
+      sm.cr[tid] = p1;
+      sm.box[tid] = make_uint2(__float_as_uint(p2.x), __float_as_uint(p2.y));
+      sm.op[tid] = p2.z;
+      sm.gid[tid] = gid;
+    }
+    __syncthreads();
+    int nl = 0;
+    for (int j0 = 0; j0 < cnt; j0 += 32) {
+      const int j = j0 + lane;
+      bool hit = false;
+      if (j < cnt) {
+        const uint2 b = sm.box[j];
+        hit = int(box_lo(b.x)) <= bx0 + 7 && int(box_hi(b.x)) >= bx0 &&
+              int(box_lo(b.y)) <= by0 + 3 && int(box_hi(b.y)) >= by0;
+        if (!hit)
+#pragma unroll
+          for (int v = 0; v < kCompVals; ++v) sm.acc[warp][j][v] = 0.f;
+      }
+      const unsigned int m = __ballot_sync(0xffffffffu, hit);
+      if (hit) sm.list[warp][nl + __popc(m & lt)] = (unsigned char)j;
+      nl += __popc(m);
+    }
+    __syncwarp();
+    for (int e = nl - 1; e >= 0; --e) {
+      const int j = sm.list[warp][e];
+      const int idx = cb - rg.x + j;  // position in the tile's list
+      const float4 mc = sm.mc[j];
+      const float4 cr = sm.cr[j];
+      const uint2 b = sm.box[j];
+      const float dx = __fsub_rn(pxf, mc.x);
+      const float dy = __fsub_rn(pyf, mc.y);
+      const float q = touch_q(dx, dy, mc.z, mc.w, cr.x);
+      const bool act = inside && idx < lst && q <= kk &&
+                       unsigned(px - int(box_lo(b.x))) <= unsigned(int(box_hi(b.x)) - int(box_lo(b.x))) &&
+                       unsigned(py - int(box_lo(b.y))) <= unsigned(int(box_hi(b.y)) - int(box_lo(b.y)));
+      float v[kCompVals];
+#pragma unroll
+      for (int u = 0; u < kCompVals; ++u) v[u] = 0.f;
+      if (act) {
+        const float o = sm.op[j];
+        const float w = ex2_approx(q * kNegHalfLog2e);
+        const float alpha = o * w;
+        const float inv = 1.0f / (1.0f - alpha);
+        const float Tb = T * inv;  // transmittance in front of this Gaussian
+        const float aT = alpha * Tb;
+        const float dal = gr * (cr.y * Tb - Sr * inv) + gg * (cr.z * Tb - Sg * inv) +
+                          gb * (cr.w * Tb - Sb * inv);
+        const float t = w * o * dal;
+        v[0] = t * dx;
+        v[1] = t * dy;
+        v[2] = t * dx * dx;
+        v[3] = t * dx * dy;
+        v[4] = t * dy * dy;
+        v[5] = gr * aT;
+        v[6] = gg * aT;
+        v[7] = gb * aT;
+        v[8] = dal * w;
+        Sr = fmaf(cr.y, aT, Sr);
+        Sg = fmaf(cr.z, aT, Sg);
+        Sb = fmaf(cr.w, aT, Sb);
+        T = Tb;
+      }
+      if (__any_sync(0xffffffffu, act)) {
+#pragma unroll
+        for (int u = 0; u < kCompVals; ++u) v[u] = warp_sum(v[u]);
+      }
+      if (lane == 0)
+#pragma unroll
+        for (int u = 0; u < kCompVals; ++u) sm.acc[warp][j][u] = v[u];
+    }
+    __syncthreads();
+    if (tid < cnt) {
+      float s[kCompVals];
+#pragma unroll
+      for (int u = 0; u < kCompVals; ++u) s[u] = 0.f;
+      for (int w = 0; w < 8; ++w)
+#pragma unroll
+        for (int u = 0; u < kCompVals; ++u) s[u] += sm.acc[w][tid][u];
+      const int gid = sm.gid[tid];
+      const float A = sm.mc[tid].z, B = 0.5f * sm.mc[tid].w, C = sm.cr[tid].x;
+      const int4 rc = rect[gid];
+      const int slot = offsets[gid] + (ty - rc.y) * (rc.z - rc.x + 1) + (tx - rc.x);
+      float4* out = partials + 3 * size_t(slot);
+      out[0] = make_float4(fmaf(A, s[0], B * s[1]), fmaf(B, s[0], C * s[1]), -0.5f * s[2], -s[3]);
+      out[1] = make_float4(-0.5f * s[4], s[5], s[6], s[7]);
+      out[2] = make_float4(s[8], 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
+                              const gs2d_record* rec, const int* rect, const int* ranges,
+                              const int* sorted_gid, const float* bg, const float* t_final,
+                              const int* last, const float* d_image, float* d_xy, float* d_chol,
+                              float* d_rgb, float* d_opacity, float* d_bg, unsigned char* ws,
+                              cudaStream_t s) {
+  const Layout L = layout_of(c, n, 0);
+  const int T = num_tiles(c);
+  const float4* r = reinterpret_cast<const float4*>(rec);
+  const int4* rc = reinterpret_cast<const int4*>(rect);
+  const int2* rg = reinterpret_cast<const int2*>(ranges);
+  const int* offsets = reinterpret_cast<const int*>(ws + L.offsets);
+  float4* partials = reinterpret_cast<float4*>(ws + L.partials);
+  if (c.mode == GS2D_MODE_COMPOSITE)
+    k_render_bwd_comp<<<T, kBwdCompThreads, 0, s>>>(
+        c, tiles_x(c), r, rc, rg, sorted_gid, offsets, bg, t_final, last, d_image, partials,
+        reinterpret_cast<float4*>(ws + L.bg_partials));
+  else
+    k_render_bwd_sum<<<T, kBwdSumThreads, 0, s>>>(c, tiles_x(c), r, rc, rg, sorted_gid, offsets,
+                                                  d_image, partials);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_gather(c, n, chol, rec, rect, ws, d_xy, d_chol, d_rgb, d_opacity, d_bg, s);
+}
+
+}  // namespace gs2d

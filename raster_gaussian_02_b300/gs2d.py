@@ -1,0 +1,273 @@
+"""Python binding of the gs2d C ABI (include/gs2d.h).
+
+Argument marshalling only: each function below has the C entry point's name,
+checks that the torch tensors it is given are CUDA, contiguous and of the
+right dtype, and passes their device pointers and the current CUDA stream to
+libgs2d.so.  Every step of the rasterizer runs in the library's kernels;
+there is no fallback.  If the library is missing the first call raises.
+
+`Rasterizer` strings the calls together for a fixed configuration, owning
+the torch buffers they need.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgs2d.so")
+
+GS2D_OK, GS2D_ERR_INVALID_ARG, GS2D_ERR_CAPACITY, GS2D_ERR_CUDA, GS2D_ERR_TIMEOUT, GS2D_ERR_OVERFLOW = range(6)
+GS2D_MODE_SUM, GS2D_MODE_COMPOSITE = 0, 1
+GS2D_FLAG_CAPACITY, GS2D_FLAG_OVERFLOW, GS2D_FLAG_TIMEOUT = 1, 2, 4
+RECORD_BYTES = 48
+TILE = 16
+
+
+class gs2d_config(C.Structure):
+    _fields_ = [("width", C.c_int32), ("height", C.c_int32), ("tile", C.c_int32),
+                ("mode", C.c_int32), ("cutoff_sigma", C.c_float), ("t_min", C.c_float)]
+
+
+def make_config(width: int, height: int, mode: int = GS2D_MODE_SUM, cutoff_sigma: float = 3.0,
+                t_min: float = 1e-4) -> gs2d_config:
+    return gs2d_config(int(width), int(height), TILE, int(mode), float(cutoff_sigma), float(t_min))
+
+
+class Gs2dError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+_p = C.c_void_p
+_cfgp = C.POINTER(gs2d_config)
+
+
+def lib() -> C.CDLL:
+    """The loaded libgs2d.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"gs2d CUDA library not built: {LIB_PATH} is missing "
+                               "(run raster_gaussian_02_b300/build.py)")
+        L = C.CDLL(LIB_PATH)
+        L.gs2d_workspace_size.argtypes = [_cfgp, C.c_int32, C.c_int64]
+        L.gs2d_workspace_size.restype = C.c_size_t
+        L.gs2d_project.argtypes = [_cfgp, C.c_int32] + [_p] * 8 + [_p]
+        L.gs2d_project.restype = C.c_int
+        L.gs2d_bin_and_sort.argtypes = [_cfgp, C.c_int32, _p, _p, _p, C.c_int64,
+                                        C.POINTER(C.c_int64), _p, _p, _p, _p]
+        L.gs2d_bin_and_sort.restype = C.c_int
+        L.gs2d_render_fwd.argtypes = [_cfgp, C.c_int32] + [_p] * 7 + [_p]
+        L.gs2d_render_fwd.restype = C.c_int
+        L.gs2d_loss_l2.argtypes = [C.c_int32, C.c_int32] + [_p] * 5 + [_p]
+        L.gs2d_loss_l2.restype = C.c_int
+        L.gs2d_render_bwd.argtypes = [_cfgp, C.c_int32] + [_p] * 15 + [_p]
+        L.gs2d_render_bwd.restype = C.c_int
+        L.gs2d_read_status.argtypes = [_p, C.POINTER(C.c_int64), C.POINTER(C.c_uint32), _p]
+        L.gs2d_read_status.restype = C.c_int
+        L.gs2d_status_string.argtypes = [C.c_int]
+        L.gs2d_status_string.restype = C.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gs2d_status_string(int(status)).decode()
+
+
+def check(status: int, where: str) -> None:
+    if status != GS2D_OK:
+        raise Gs2dError(status, where)
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t, dtype=None, what="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what}: expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{what}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what}: expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+_f32, _i32, _u8 = torch.float32, torch.int32, torch.uint8
+
+
+# --------------------------------------------------------- the C entry points
+
+def gs2d_workspace_size(cfg: gs2d_config, n: int, pair_capacity: int) -> int:
+    return int(lib().gs2d_workspace_size(C.byref(cfg), int(n), int(pair_capacity)))
+
+
+def gs2d_project(cfg, n, xy, chol, rgb, depth, opacity, rec, rect, count, stream=None) -> int:
+    return lib().gs2d_project(C.byref(cfg), int(n), _ptr(xy, _f32, "xy"), _ptr(chol, _f32, "chol"),
+                              _ptr(rgb, _f32, "rgb"), _ptr(depth, _f32, "depth"),
+                              _ptr(opacity, _f32, "opacity"), _ptr(rec, None, "rec"),
+                              _ptr(rect, _i32, "rect"), _ptr(count, _i32, "count"), _stream(stream))
+
+
+def gs2d_bin_and_sort(cfg, n, rec, rect, count, pair_capacity, pairs_out, tile_ranges, sorted_gid,
+                      workspace, stream=None) -> int:
+    """pairs_out: None (no wait) or a ctypes.c_int64 that receives P."""
+    po = C.byref(pairs_out) if pairs_out is not None else None
+    return lib().gs2d_bin_and_sort(C.byref(cfg), int(n), _ptr(rec, None, "rec"),
+                                   _ptr(rect, _i32, "rect"), _ptr(count, _i32, "count"),
+                                   int(pair_capacity), po, _ptr(tile_ranges, _i32, "tile_ranges"),
+                                   _ptr(sorted_gid, _i32, "sorted_gid"),
+                                   _ptr(workspace, None, "workspace"), _stream(stream))
+
+
+def gs2d_render_fwd(cfg, n, rec, tile_ranges, sorted_gid, background, image, t_final, last,
+                    stream=None) -> int:
+    return lib().gs2d_render_fwd(C.byref(cfg), int(n), _ptr(rec, None, "rec"),
+                                 _ptr(tile_ranges, _i32, "tile_ranges"),
+                                 _ptr(sorted_gid, _i32, "sorted_gid"),
+                                 _ptr(background, _f32, "background"), _ptr(image, _f32, "image"),
+                                 _ptr(t_final, _f32, "t_final"), _ptr(last, _i32, "last"),
+                                 _stream(stream))
+
+
+def gs2d_loss_l2(height, width, image, target, loss, d_image, workspace, stream=None) -> int:
+    return lib().gs2d_loss_l2(int(height), int(width), _ptr(image, _f32, "image"),
+                              _ptr(target, _f32, "target"), _ptr(loss, _f32, "loss"),
+                              _ptr(d_image, _f32, "d_image"), _ptr(workspace, None, "workspace"),
+                              _stream(stream))
+
+
+def gs2d_render_bwd(cfg, n, chol, rec, rect, tile_ranges, sorted_gid, background, t_final, last,
+                    d_image, d_xy, d_chol, d_rgb, d_opacity, d_background, workspace,
+                    stream=None) -> int:
+    return lib().gs2d_render_bwd(
+        C.byref(cfg), int(n), _ptr(chol, _f32, "chol"), _ptr(rec, None, "rec"),
+        _ptr(rect, _i32, "rect"), _ptr(tile_ranges, _i32, "tile_ranges"),
+        _ptr(sorted_gid, _i32, "sorted_gid"), _ptr(background, _f32, "background"),
+        _ptr(t_final, _f32, "t_final"), _ptr(last, _i32, "last"), _ptr(d_image, _f32, "d_image"),
+        _ptr(d_xy, _f32, "d_xy"), _ptr(d_chol, _f32, "d_chol"), _ptr(d_rgb, _f32, "d_rgb"),
+        _ptr(d_opacity, _f32, "d_opacity"), _ptr(d_background, _f32, "d_background"),
+        _ptr(workspace, None, "workspace"), _stream(stream))
+
+
+def gs2d_read_status(workspace, stream=None):
+    """Waits for the stream; returns (status, pairs, flags)."""
+    pairs, flags = C.c_int64(0), C.c_uint32(0)
+    st = lib().gs2d_read_status(_ptr(workspace, None, "workspace"), C.byref(pairs),
+                                C.byref(flags), _stream(stream))
+    return st, pairs.value, flags.value
+
+
+# ------------------------------------------------------------- convenience
+
+class Rasterizer:
+    """Buffers and call sequence for one configuration and Gaussian count.
+
+    project -> bin_and_sort -> render_fwd [-> loss_l2 -> render_bwd].
+    All tensors live on `device`; nothing here computes, it only allocates
+    and calls the library.
+    """
+
+    def __init__(self, width, height, n, mode=GS2D_MODE_SUM, cutoff_sigma=3.0, t_min=1e-4,
+                 pair_capacity=None, device="cuda"):
+        self.cfg = make_config(width, height, mode, cutoff_sigma, t_min)
+        self.width, self.height, self.n, self.mode = int(width), int(height), int(n), int(mode)
+        self.device = torch.device(device)
+        self.num_tiles = ((width + TILE - 1) // TILE) * ((height + TILE - 1) // TILE)
+        d = self.device
+        self.rec = torch.empty(max(n, 1) * RECORD_BYTES, dtype=_u8, device=d)
+        self.rect = torch.empty((max(n, 1), 4), dtype=_i32, device=d)
+        self.count = torch.empty(max(n, 1), dtype=_i32, device=d)
+        self.tile_ranges = torch.empty((self.num_tiles, 2), dtype=_i32, device=d)
+        self.image = torch.empty((3, height, width), dtype=_f32, device=d)
+        comp = mode == GS2D_MODE_COMPOSITE
+        self.t_final = torch.empty((height, width), dtype=_f32, device=d) if comp else None
+        self.last = torch.empty((height, width), dtype=_i32, device=d) if comp else None
+        self.loss = torch.empty(1, dtype=_f32, device=d)
+        self.d_image = torch.empty((3, height, width), dtype=_f32, device=d)
+        self.d_xy = torch.empty((max(n, 1), 2), dtype=_f32, device=d)
+        self.d_chol = torch.empty((max(n, 1), 3), dtype=_f32, device=d)
+        self.d_rgb = torch.empty((max(n, 1), 3), dtype=_f32, device=d)
+        self.d_opacity = torch.empty(max(n, 1), dtype=_f32, device=d) if comp else None
+        self.d_background = torch.empty(3, dtype=_f32, device=d) if comp else None
+        self.pairs = None
+        self._alloc_pairs(int(pair_capacity) if pair_capacity is not None else 4 * max(n, 1))
+
+    def _alloc_pairs(self, cap):
+        self.capacity = int(cap)
+        self.sorted_gid = torch.empty(max(self.capacity, 1), dtype=_i32, device=self.device)
+        ws = gs2d_workspace_size(self.cfg, self.n, self.capacity)
+        if ws == 0:
+            raise ValueError("invalid configuration for gs2d_workspace_size")
+        self.workspace = torch.empty(ws, dtype=_u8, device=self.device)
+
+    def project(self, xy, chol, rgb, depth=None, opacity=None):
+        self.xy, self.chol, self.rgb, self.depth, self.opacity = xy, chol, rgb, depth, opacity
+        check(gs2d_project(self.cfg, self.n, xy, chol, rgb, depth, opacity, self.rec, self.rect,
+                           self.count), "gs2d_project")
+
+    def bin_and_sort(self, sync: bool = True, grow: bool = True):
+        """sync=True reads P back (and, with grow, reallocates and retries on
+        a capacity miss); sync=False leaves everything on the device."""
+        if not sync:
+            check(gs2d_bin_and_sort(self.cfg, self.n, self.rec, self.rect, self.count,
+                                    self.capacity, None, self.tile_ranges, self.sorted_gid,
+                                    self.workspace), "gs2d_bin_and_sort")
+            return None
+        while True:
+            P = C.c_int64(0)
+            st = gs2d_bin_and_sort(self.cfg, self.n, self.rec, self.rect, self.count,
+                                   self.capacity, P, self.tile_ranges, self.sorted_gid,
+                                   self.workspace)
+            if st == GS2D_ERR_CAPACITY and grow:
+                self._alloc_pairs(int(P.value * 1.25) + 1024)
+                continue
+            check(st, "gs2d_bin_and_sort")
+            self.pairs = int(P.value)
+            return self.pairs
+
+    def render_fwd(self, background=None):
+        self.background = background
+        check(gs2d_render_fwd(self.cfg, self.n, self.rec, self.tile_ranges, self.sorted_gid,
+                              background, self.image, self.t_final, self.last), "gs2d_render_fwd")
+        return self.image
+
+    def loss_l2(self, target):
+        check(gs2d_loss_l2(self.height, self.width, self.image, target, self.loss, self.d_image,
+                           self.workspace), "gs2d_loss_l2")
+        return self.loss
+
+    def render_bwd(self, d_image=None):
+        d_image = self.d_image if d_image is None else d_image
+        check(gs2d_render_bwd(self.cfg, self.n, self.chol, self.rec, self.rect, self.tile_ranges,
+                              self.sorted_gid, self.background, self.t_final, self.last, d_image,
+                              self.d_xy, self.d_chol, self.d_rgb, self.d_opacity,
+                              self.d_background, self.workspace), "gs2d_render_bwd")
+
+    def step(self, xy, chol, rgb, target, depth=None, opacity=None, background=None, sync=False):
+        """One pass of the whole path: project, bin and sort, forward, L2
+        loss, backward.  Returns the device loss tensor."""
+        self.project(xy, chol, rgb, depth, opacity)
+        self.bin_and_sort(sync=sync)
+        self.render_fwd(background)
+        self.loss_l2(target)
+        self.render_bwd()
+        return self.loss
+
+    def records(self):
+        """The projected records decoded into named tensors (for tests)."""
+        f = self.rec.view(torch.float32).view(-1, 12)[: self.n]
+        u = self.rec.view(torch.int32).view(-1, 12)[: self.n]
+        return dict(mean=f[:, 0:2], conic=f[:, 2:5], rgb=f[:, 5:8],
+                    box_x=u[:, 8], box_y=u[:, 9], opacity=f[:, 10], depth=f[:, 11])

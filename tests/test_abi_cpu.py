@@ -1,0 +1,124 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function include/gs2d.h declares, sizes workspaces, and rejects bad
+arguments on the host before touching CUDA (these calls never reach the
+device, so they run on a machine without one)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from raster_gaussian_02_b300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gs2d.h")
+
+
+@pytest.fixture(scope="module")
+def gs2d():
+    lib_build.build()
+    from raster_gaussian_02_b300 import gs2d as g
+    g.lib()
+    return g
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"GS2D_API\s+[\w\s\*]+?\b(gs2d_\w+)\s*\(", text)
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ("gs2d_project", "gs2d_bin_and_sort", "gs2d_render_fwd", "gs2d_render_bwd",
+              "gs2d_loss_l2"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(gs2d):
+    lib = C.CDLL(gs2d.LIB_PATH)
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_nm_shows_only_the_abi(gs2d):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", gs2d.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    gs = {e for e in exported if e.startswith("gs2d_")}
+    assert gs == set(declared_functions())
+
+
+def test_status_strings(gs2d):
+    for s in range(6):
+        assert gs2d.status_string(s)
+    assert gs2d.status_string(99) == "unknown status"
+
+
+def test_workspace_size(gs2d):
+    cfg = gs2d.make_config(768, 512)
+    a = gs2d.gs2d_workspace_size(cfg, 50_000, 200_000)
+    b = gs2d.gs2d_workspace_size(cfg, 50_000, 400_000)
+    assert 0 < a < b
+    assert gs2d.gs2d_workspace_size(cfg, 0, 0) >= 16384
+    comp = gs2d.make_config(768, 512, gs2d.GS2D_MODE_COMPOSITE)
+    assert gs2d.gs2d_workspace_size(comp, 50_000, 200_000) > a  # 64-bit keys, wider partials
+    bad = [gs2d.gs2d_config(0, 512, 16, 0, 3.0, 1e-4), gs2d.gs2d_config(768, 512, 8, 0, 3.0, 1e-4),
+           gs2d.gs2d_config(768, 512, 16, 2, 3.0, 1e-4), gs2d.gs2d_config(768, 512, 16, 0, 0.0, 1e-4),
+           gs2d.gs2d_config(768, 512, 16, 0, float("nan"), 1e-4),
+           gs2d.gs2d_config(40000, 512, 16, 0, 3.0, 1e-4),
+           gs2d.gs2d_config(768, 512, 16, 1, 3.0, 2.0)]
+    for c in bad:
+        assert gs2d.gs2d_workspace_size(c, 10, 10) == 0
+    assert gs2d.gs2d_workspace_size(cfg, -1, 10) == 0
+    assert gs2d.gs2d_workspace_size(cfg, 10, 1 << 30) == 0
+
+
+def test_host_checks_reject_bad_arguments(gs2d):
+    """Every one of these returns GS2D_ERR_INVALID_ARG on the host."""
+    L = gs2d.lib()
+    INVALID = gs2d.GS2D_ERR_INVALID_ARG
+    good = gs2d.make_config(64, 64)
+    bad = gs2d.gs2d_config(64, 64, 8, 0, 3.0, 1e-4)
+    fake = C.c_void_p(0x10000)       # 16-byte aligned, never dereferenced
+    odd = C.c_void_p(0x10004)        # 4-byte aligned only
+    null = None
+    # project
+    assert L.gs2d_project(C.byref(bad), 4, fake, fake, fake, null, null, fake, fake, fake, null) == INVALID
+    assert L.gs2d_project(C.byref(good), -1, fake, fake, fake, null, null, fake, fake, fake, null) == INVALID
+    assert L.gs2d_project(C.byref(good), 4, null, fake, fake, null, null, fake, fake, fake, null) == INVALID
+    assert L.gs2d_project(C.byref(good), 4, fake, fake, fake, null, null, odd, fake, fake, null) == INVALID
+    assert L.gs2d_project(C.byref(good), 4, fake, fake, fake, null, null, fake, odd, fake, null) == INVALID
+    comp = gs2d.make_config(64, 64, gs2d.GS2D_MODE_COMPOSITE)
+    assert L.gs2d_project(C.byref(comp), 4, fake, fake, fake, null, fake, fake, fake, fake, null) == INVALID
+    assert L.gs2d_project(None, 4, fake, fake, fake, null, null, fake, fake, fake, null) == INVALID
+    # n == 0 is a no-op that succeeds without touching anything
+    assert L.gs2d_project(C.byref(good), 0, null, null, null, null, null, null, null, null, null) == 0
+    # bin_and_sort
+    assert L.gs2d_bin_and_sort(C.byref(good), 4, fake, fake, fake, 10, None, fake, fake, null, null) == INVALID
+    assert L.gs2d_bin_and_sort(C.byref(good), 4, fake, fake, fake, -1, None, fake, fake, fake, null) == INVALID
+    assert L.gs2d_bin_and_sort(C.byref(good), 4, fake, fake, fake, 1 << 30, None, fake, fake, fake, null) == INVALID
+    assert L.gs2d_bin_and_sort(C.byref(good), 4, fake, fake, fake, 10, None, odd, fake, fake, null) == INVALID
+    assert L.gs2d_bin_and_sort(C.byref(good), 4, fake, fake, fake, 10, None, fake, null, fake, null) == INVALID
+    assert L.gs2d_bin_and_sort(C.byref(good), 4, null, fake, fake, 10, None, fake, fake, fake, null) == INVALID
+    # render_fwd
+    assert L.gs2d_render_fwd(C.byref(good), 4, fake, fake, fake, null, null, null, null, null) == INVALID
+    assert L.gs2d_render_fwd(C.byref(good), 4, odd, fake, fake, null, fake, null, null, null) == INVALID
+    assert L.gs2d_render_fwd(C.byref(bad), 4, fake, fake, fake, null, fake, null, null, null) == INVALID
+    # loss
+    assert L.gs2d_loss_l2(0, 64, fake, fake, fake, fake, fake, null) == INVALID
+    assert L.gs2d_loss_l2(64, 64, fake, null, fake, fake, fake, null) == INVALID
+    assert L.gs2d_loss_l2(64, 64, fake, fake, fake, fake, null, null) == INVALID
+    assert L.gs2d_loss_l2(64, 64, fake, fake, fake, fake, odd, null) == INVALID
+    # render_bwd: composite needs t_final and last
+    args = [fake] * 15
+    args[6] = null  # t_final
+    assert L.gs2d_render_bwd(C.byref(comp), 4, *args, null) == INVALID
+    args = [fake] * 15
+    args[0] = null  # chol
+    assert L.gs2d_render_bwd(C.byref(good), 4, *args, null) == INVALID
+    # read_status
+    assert L.gs2d_read_status(None, None, None, None) == INVALID
+    assert L.gs2d_read_status(odd, None, None, None) == INVALID
