@@ -15,37 +15,38 @@ constexpr int kTilePixels = kTile * kTile;
 
 // Workspace layout (byte offsets; every region 256-byte aligned).  The
 // regions the backward reads come before every region whose size depends on
-// the pair capacity, so their offsets follow from (cfg, n) alone.
-//   [0, 256)        Header
-//   [256, 4352)     loss partial sums (kLossMaxBlocks floats)
-//   [4352, 12544)   radix digit histograms [kMaxPasses][256]
-//   then            scan look-back words [ceil(n / kScanItems) + 1] (uint64)
-//   then            per-Gaussian pair offsets [n] (int32)
-//   then            background partials [T] x 4 floats (composite)
-//   then            backward partials [cap] x 8 floats (sum) or x 12 (composite)
-//   then            radix look-back words [passes][partitions(cap)][256] (uint32)
-//   then            keys A, keys B [cap] (uint32 sum, uint64 composite)
-//   then            values scratch [cap] (uint32)
+// the pair capacity, so their offsets follow from (cfg, n) alone; the one
+// exception, the sorted keys, is located through Header::keys_final.
+//   [0, 256)          Header
+//   [256, 4352)       loss partial sums (kLossMaxBlocks floats)
+//   [4352, 12544)     radix digit histograms [kMaxPasses][kMaxRadix]
+//   then              scan look-back words [ceil(n / kScanItems) + 1] (uint64)
+//   then              per-Gaussian pair offsets [n] (int32)
+//   then              background partials [T] x 4 floats (composite)
+//   then              backward partials [cap] x 8 floats (sum) or x 12 (composite)
+//   then              radix look-back words [passes][radix][partitions(cap) rounded up to 4]
+//   then              keys A, keys B [cap] (uint32 sum, uint64 composite)
+//   then              values scratch [cap] (uint32)
 struct Header {
-  long long pairs;           // P, written by the binning
-  unsigned int flags;        // GS2D_FLAG_*
-  unsigned int scan_ticket;  // block order for the scan look-back
-  unsigned int radix_ticket[8];
+  long long pairs;                 // P, written by the binning
+  unsigned int flags;              // GS2D_FLAG_*
+  unsigned int scan_ticket;        // block order for the scan look-back
+  unsigned int radix_ticket[8];    // block order of each radix pass
+  unsigned long long keys_final;   // byte offset of the sorted keys
 };
 
 constexpr int kMaxPasses = 8;
+constexpr int kMaxDigitBits = 8;
+constexpr int kMaxRadix = 1 << kMaxDigitBits;
 constexpr size_t kOffLoss = 256;
 constexpr int kLossMaxBlocks = 1024;
-constexpr size_t kOffHist = kOffLoss + kLossMaxBlocks * 4;  // 4352
-constexpr size_t kOffScan = kOffHist + kMaxPasses * 256 * 4; // 12544
+constexpr size_t kOffHist = kOffLoss + kLossMaxBlocks * 4;           // 4352
+constexpr size_t kOffScan = kOffHist + size_t(kMaxPasses) * kMaxRadix * 4;  // 12544
 
 constexpr int kScanThreads = 256;
-constexpr int kScanPerThread = 4;
-constexpr int kScanItems = kScanThreads * kScanPerThread;  // Gaussians per scan block
+constexpr int kScanItems = kScanThreads;  // Gaussians per scan block, one per thread
 
 constexpr int kRadixThreads = 256;
-constexpr int kRadixPerThread = 8;
-constexpr int kRadixItems = kRadixThreads * kRadixPerThread;  // keys per partition
 
 // Bounded device-side waits: after this many polls a waiting thread gives up,
 // sets GS2D_FLAG_TIMEOUT and continues, so a kernel always terminates.
@@ -53,8 +54,8 @@ constexpr unsigned int kSpinLimit = 1u << 22;
 
 struct Layout {
   size_t scan, offsets, bg_partials, partials, radix_status, keys_a, keys_b, vals_tmp, total;
-  int passes, tile_bits, key_bytes, partial_floats;
-  long long partitions;
+  int passes, digit_bits, tile_bits, key_bits, key_bytes, partial_floats, radix_per_thread;
+  long long partitions, partitions4;  // radix partitions, and rounded up to a multiple of 4
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -69,16 +70,26 @@ inline int bits_for(long long values) {  // bits needed to hold 0 .. values-1
   return b;
 }
 
+// Keys per radix partition = kRadixThreads * radix_per_thread.  Measured on a
+// B300 at 1.2e5 pairs: 2048-key partitions beat 1024 (the look-back chain is
+// shorter) and match 4096.
+inline int radix_per_thread(long long) { return 8; }
+
 inline Layout layout_of(const gs2d_config& c, long long n, long long cap) {
   Layout L{};
   const int T = num_tiles(c);
   L.tile_bits = bits_for(T);
   const bool comp = c.mode == GS2D_MODE_COMPOSITE;
-  const int key_bits = L.tile_bits + (comp ? 32 : 0);
-  L.passes = (key_bits + 7) / 8;
+  L.key_bits = L.tile_bits + (comp ? 32 : 0);
+  L.passes = (L.key_bits + kMaxDigitBits - 1) / kMaxDigitBits;
+  L.digit_bits = L.passes ? (L.key_bits + L.passes - 1) / L.passes : 0;
   L.key_bytes = comp ? 8 : 4;
   L.partial_floats = comp ? 12 : 8;
-  L.partitions = (cap + kRadixItems - 1) / kRadixItems;
+  L.radix_per_thread = radix_per_thread(cap);
+  const long long items = (long long)kRadixThreads * L.radix_per_thread;
+  L.partitions = (cap + items - 1) / items;
+  L.partitions4 = (L.partitions + 3) & ~3ll;
+  const size_t radix = size_t(1) << L.digit_bits;
   size_t o = kOffScan;
   L.scan = o;
   o = align256(o + 8 * size_t((n + kScanItems - 1) / kScanItems + 1));
@@ -89,14 +100,14 @@ inline Layout layout_of(const gs2d_config& c, long long n, long long cap) {
   L.partials = o;
   o = align256(o + 4 * size_t(L.partial_floats) * size_t(cap));
   L.radix_status = o;
-  o = align256(o + 4 * size_t(L.passes) * size_t(L.partitions) * 256);
+  o = align256(o + 4 * size_t(L.passes) * size_t(L.partitions4) * radix);
   L.keys_a = o;
   o = align256(o + size_t(L.key_bytes) * size_t(cap));
   L.keys_b = o;
   o = align256(o + size_t(L.key_bytes) * size_t(cap));
   L.vals_tmp = o;
   o = align256(o + 4 * size_t(cap));
-  L.total = o < 16384 ? 16384 : o;
+  L.total = o < 16384 ? 16384 : o;  // the loss alone needs the first 16 KiB
   return L;
 }
 

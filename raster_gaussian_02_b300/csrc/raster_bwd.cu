@@ -21,77 +21,181 @@ namespace gs2d {
 
 namespace {
 
-constexpr int kBwdSumThreads = 128;
+constexpr int kChunkPairs = 256;   // pairs per block, one per thread
+constexpr int kStageTiles = 8;     // tiles of dL/dC staged at a time
 
-// Sum mode: one thread per (tile, Gaussian) pair, walking exactly the
-// pixels of the Gaussian's box inside the tile.  dL/dC of the tile is
-// staged in shared memory.
-__global__ void __launch_bounds__(kBwdSumThreads)
-k_render_bwd_sum(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
-                 const int4* __restrict__ rect, const int2* __restrict__ ranges,
-                 const int* __restrict__ sorted_gid, const int* __restrict__ offsets,
-                 const float* __restrict__ d_image, float4* __restrict__ partials) {
-  __shared__ float4 s_g[kTilePixels];
-  const int tile = blockIdx.x;
-  const int2 rg = ranges[tile];
-  if (rg.x == rg.y) return;
-  const int tx = tile % tiles_x, ty = tile / tiles_x;
-  const int X0 = tx * kTile, Y0 = ty * kTile;
-  const size_t HW = size_t(c.width) * c.height;
-  for (int p = threadIdx.x; p < kTilePixels; p += blockDim.x) {
-    const int x = X0 + (p & 15), y = Y0 + (p >> 4);
-    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (x < c.width && y < c.height) {
-      const size_t o = size_t(y) * c.width + x;
-      g = make_float4(d_image[o], d_image[HW + o], d_image[2 * HW + o], 0.f);
-    }
-    s_g[p] = g;
+struct BwdSumSmem {
+  float4 g[kStageTiles][kTilePixels];  // dL/dC of the staged tiles (r, g, b, 0)
+  float4 rec[kChunkPairs][3];          // the chunk's records
+  int gid[kChunkPairs];
+  int slot[kChunkPairs];               // index of the pair's tile among the chunk's tiles
+  int tiles[kChunkPairs];              // the chunk's distinct tiles, in order
+  int perm[kChunkPairs];               // processing order (similar boxes side by side)
+  unsigned int bucket[256];
+  int ntiles;
+};
+
+__device__ __forceinline__ int block_inclusive_count_256(int flag, int* total, int* warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned int b = __ballot_sync(0xffffffffu, flag != 0);
+  const int in_warp = __popc(b & ((2u << lane) - 1u));
+  if (lane == 31) warp_tot[warp] = __popc(b);
+  __syncthreads();
+  int before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const int v = warp_tot[w];
+    if (w < warp) before += v;
+    all += v;
   }
   __syncthreads();
-  const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
-  for (int k = rg.x + threadIdx.x; k < rg.y; k += blockDim.x) {
-    const int gid = sorted_gid[k];
-    const float4* r = rec + 3 * size_t(gid);
-    const float4 p0 = r[0], p1 = r[1], p2 = r[2];
-    const float mx = p0.x, my = p0.y, A = p0.z, B = p0.w, B2 = 2.0f * p0.w, C = p1.x;
-    const unsigned int bx = __float_as_uint(p2.x), by = __float_as_uint(p2.y);
-    const int xa = max(int(box_lo(bx)), X0), xb = min(int(box_hi(bx)), X0 + kTile - 1);
-    const int ya = max(int(box_lo(by)), Y0), yb = min(int(box_hi(by)), Y0 + kTile - 1);
-    float sr = 0.f, sg = 0.f, sb = 0.f, Sx = 0.f, Sy = 0.f, Sxx = 0.f, Sxy = 0.f, Syy = 0.f;
-    for (int y = ya; y <= yb; ++y) {
-      const float dy = __fsub_rn(float(y) + 0.5f, my);
-      const float b2dy = __fmul_rn(B2, dy);
-      const float cdydy = __fmul_rn(__fmul_rn(C, dy), dy);
-      float r0 = 0.f, rx = 0.f, rxx = 0.f;
-      const int row = (y - Y0) * kTile - X0;
-      float pxf = float(xa) + 0.5f;
-      for (int x = xa; x <= xb; ++x, pxf += 1.0f) {
-        const float dx = __fsub_rn(pxf, mx);
-        const float q = __fmaf_rn(dx, __fmaf_rn(A, dx, b2dy), cdydy);
-        if (q <= kk) {
-          const float w = ex2_approx(q * kNegHalfLog2e);
-          const float4 g = s_g[row + x];
-          sr = fmaf(g.x, w, sr);
-          sg = fmaf(g.y, w, sg);
-          sb = fmaf(g.z, w, sb);
-          const float t = w * fmaf(g.x, p1.y, fmaf(g.y, p1.z, g.z * p1.w));
-          r0 += t;
-          const float tdx = t * dx;
-          rx += tdx;
-          rxx = fmaf(tdx, dx, rxx);
-        }
-      }
-      Sx += rx;
-      Sy = fmaf(r0, dy, Sy);
-      Sxx += rxx;
-      Sxy = fmaf(rx, dy, Sxy);
-      Syy = fmaf(r0 * dy, dy, Syy);
+  *total = all;
+  return before + in_warp;
+}
+
+// Sum mode: one thread per (tile, Gaussian) pair, walking exactly the pixels
+// of the Gaussian's box inside the tile.  Blocks take fixed chunks of the
+// sorted pair list, whatever the tile boundaries, so heavy tiles spread over
+// many blocks; inside a block the pairs are reordered so that lanes of a
+// warp walk boxes of the same shape.
+__global__ void __launch_bounds__(kChunkPairs)
+k_render_bwd_sum(gs2d_config c, int tiles_x, const Header* __restrict__ hdr,
+                 const unsigned char* __restrict__ ws, const float4* __restrict__ rec,
+                 const int4* __restrict__ rect, const int* __restrict__ sorted_gid,
+                 const int* __restrict__ offsets, const float* __restrict__ d_image,
+                 float4* __restrict__ partials) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  BwdSumSmem& sm = *reinterpret_cast<BwdSumSmem*>(smem_raw);
+  __shared__ int warp_tot[8];
+  const int tid = threadIdx.x;
+  const unsigned int f = hdr->flags;
+  const long long n = (f & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) ? 0
+                      : hdr->pairs;
+  const unsigned int* keys = reinterpret_cast<const unsigned int*>(ws + hdr->keys_final);
+  for (long long k0 = (long long)blockIdx.x * kChunkPairs; k0 < n;
+       k0 += (long long)gridDim.x * kChunkPairs) {
+    const long long k = k0 + tid;
+    const bool valid = k < n;
+    const int tile = valid ? int(keys[k]) : -1;
+    const int prev = (valid && tid > 0) ? int(keys[k - 1]) : -2;
+    int ntiles;
+    const int slot = block_inclusive_count_256(valid && tile != prev, &ntiles, warp_tot) - 1;
+    if (valid && tile != prev) sm.tiles[slot] = tile;
+    int gid = 0;
+    int key = 255;  // sort key: boxes of the same shape (h, w) side by side, largest first
+    if (valid) {
+      gid = sorted_gid[k];
+      const float4* r = rec + 3 * size_t(gid);
+      const float4 p0 = r[0], p1 = r[1], p2 = r[2];
+      sm.rec[tid][0] = p0;
+      sm.rec[tid][1] = p1;
+      sm.rec[tid][2] = p2;
+      const int X0 = (tile % tiles_x) * kTile, Y0 = (tile / tiles_x) * kTile;
+      const unsigned int bx = __float_as_uint(p2.x), by = __float_as_uint(p2.y);
+      const int w = min(int(box_hi(bx)), X0 + kTile - 1) - max(int(box_lo(bx)), X0) + 1;
+      const int h = min(int(box_hi(by)), Y0 + kTile - 1) - max(int(box_lo(by)), Y0) + 1;
+      key = (kTile - h) * kTile + (kTile - w);
     }
-    const int4 rc = rect[gid];
-    const int slot = offsets[gid] + (ty - rc.y) * (rc.z - rc.x + 1) + (tx - rc.x);
-    float4* out = partials + 2 * size_t(slot);
-    out[0] = make_float4(fmaf(A, Sx, B * Sy), fmaf(B, Sx, C * Sy), -0.5f * Sxx, -Sxy);
-    out[1] = make_float4(-0.5f * Syy, sr, sg, sb);
+    sm.gid[tid] = gid;
+    sm.slot[tid] = slot;
+    sm.bucket[tid] = 0u;
+    __syncthreads();
+    if (ntiles <= kStageTiles) {
+      atomicAdd(&sm.bucket[key], 1u);
+      __syncthreads();
+      // exclusive scan of the 256 bucket counts, one per thread
+      const unsigned int cnt = sm.bucket[tid];
+      unsigned int incl = cnt;
+      const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) warp_tot[warp] = int(incl);
+      __syncthreads();
+      unsigned int before = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w)
+        if (w < warp) before += unsigned(warp_tot[w]);
+      __syncthreads();
+      sm.bucket[tid] = before + incl - cnt;
+      __syncthreads();
+      const unsigned int pos = atomicAdd(&sm.bucket[key], 1u);
+      sm.perm[pos] = tid;
+    } else {
+      sm.perm[tid] = tid;
+    }
+    __syncthreads();
+
+    const size_t HW = size_t(c.width) * c.height;
+    const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
+    const int me = sm.perm[tid];
+    const bool mine_valid = (k0 + me) < n;
+    for (int t0 = 0; t0 < ntiles; t0 += kStageTiles) {
+      const int nst = min(kStageTiles, ntiles - t0);
+      for (int q = tid; q < nst * kTilePixels; q += kChunkPairs) {
+        const int s = q >> 8, pp = q & 255;
+        const int t = sm.tiles[t0 + s];
+        const int x = (t % tiles_x) * kTile + (pp & 15), y = (t / tiles_x) * kTile + (pp >> 4);
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (x < c.width && y < c.height) {
+          const size_t o = size_t(y) * c.width + x;
+          g = make_float4(d_image[o], d_image[HW + o], d_image[2 * HW + o], 0.f);
+        }
+        sm.g[s][pp] = g;
+      }
+      __syncthreads();
+      const int ms = sm.slot[me] - t0;
+      if (mine_valid && ms >= 0 && ms < nst) {
+        const int t = sm.tiles[t0 + ms];
+        const int tx = t % tiles_x, ty = t / tiles_x;
+        const int X0 = tx * kTile, Y0 = ty * kTile;
+        const float4 p0 = sm.rec[me][0], p1 = sm.rec[me][1], p2 = sm.rec[me][2];
+        const float mx = p0.x, my = p0.y, A = p0.z, B = p0.w, B2 = 2.0f * p0.w, C = p1.x;
+        const unsigned int bx = __float_as_uint(p2.x), by = __float_as_uint(p2.y);
+        const int xa = max(int(box_lo(bx)), X0), xb = min(int(box_hi(bx)), X0 + kTile - 1);
+        const int ya = max(int(box_lo(by)), Y0), yb = min(int(box_hi(by)), Y0 + kTile - 1);
+        const float4* gt = sm.g[ms];
+        float sr = 0.f, sg = 0.f, sb = 0.f, Sx = 0.f, Sy = 0.f, Sxx = 0.f, Sxy = 0.f, Syy = 0.f;
+        for (int y = ya; y <= yb; ++y) {
+          const float dy = __fsub_rn(float(y) + 0.5f, my);
+          const float b2dy = __fmul_rn(B2, dy);
+          const float cdydy = __fmul_rn(__fmul_rn(C, dy), dy);
+          float r0 = 0.f, rx = 0.f, rxx = 0.f;
+          int gi = (y - Y0) * kTile + (xa - X0);
+          float pxf = float(xa) + 0.5f;
+  #pragma unroll 2
+          for (int x = xa; x <= xb; ++x, ++gi, pxf += 1.0f) {
+            const float dx = __fsub_rn(pxf, mx);
+            const float q = __fmaf_rn(dx, __fmaf_rn(A, dx, b2dy), cdydy);
+            float w = ex2_approx(q * kNegHalfLog2e);
+            w = (q <= kk) ? w : 0.f;
+            const float4 g = gt[gi];
+            sr = fmaf(g.x, w, sr);
+            sg = fmaf(g.y, w, sg);
+            sb = fmaf(g.z, w, sb);
+            const float t = w * fmaf(g.x, p1.y, fmaf(g.y, p1.z, g.z * p1.w));
+            r0 += t;
+            const float tdx = t * dx;
+            rx += tdx;
+            rxx = fmaf(tdx, dx, rxx);
+          }
+          Sx += rx;
+          Sy = fmaf(r0, dy, Sy);
+          Sxx += rxx;
+          Sxy = fmaf(rx, dy, Sxy);
+          Syy = fmaf(r0 * dy, dy, Syy);
+        }
+        const int gid_me = sm.gid[me];
+        const int4 rc = rect[gid_me];
+        const int pslot = offsets[gid_me] + (ty - rc.y) * (rc.z - rc.x + 1) + (tx - rc.x);
+        float4* out = partials + 2 * size_t(pslot);
+        out[0] = make_float4(fmaf(A, Sx, B * Sy), fmaf(B, Sx, C * Sy), -0.5f * Sxx, -Sxy);
+        out[1] = make_float4(-0.5f * Syy, sr, sg, sb);
+      }
+      __syncthreads();
+    }
   }
 }
 
@@ -293,9 +397,18 @@ cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
     k_render_bwd_comp<<<T, kBwdCompThreads, 0, s>>>(
         c, tiles_x(c), r, rc, rg, sorted_gid, offsets, bg, t_final, last, d_image, partials,
         reinterpret_cast<float4*>(ws + L.bg_partials));
-  else
-    k_render_bwd_sum<<<T, kBwdSumThreads, 0, s>>>(c, tiles_x(c), r, rc, rg, sorted_gid, offsets,
-                                                  d_image, partials);
+  else {
+    const size_t smem = sizeof(BwdSumSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_render_bwd_sum, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    k_render_bwd_sum<<<4 * sms, kChunkPairs, smem, s>>>(
+        c, tiles_x(c), reinterpret_cast<const Header*>(ws), ws, r, rc, sorted_gid, offsets,
+        d_image, partials);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_gather(c, n, chol, rec, rect, ws, d_xy, d_chol, d_rgb, d_opacity, d_bg, s);

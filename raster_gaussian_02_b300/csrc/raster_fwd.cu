@@ -1,9 +1,13 @@
-// Forward raster: one 256-thread block per 16x16 tile, one pixel per thread.
+// Forward raster: one block per 16x16 tile, one pixel per thread.
 //
-// The tile's Gaussian list is staged through shared memory in chunks of 256
-// records (one coalesced gather per thread).  Each warp owns an 8x4 pixel
-// sub-block and first compacts, with a ballot, the chunk entries whose pixel
-// box meets its sub-block; it then evaluates only those, in list order.
+// Warps own 8x4-pixel sub-blocks of the tile.  The tile's Gaussian list is
+// staged through shared memory (one coalesced record gather per thread);
+// each warp then culls a window of 64 staged entries with one lane per
+// entry, keeping, in list order, those whose pixel box meets its sub-block
+// together with a 32-bit mask of the warp's lanes inside the box, so that
+// the per-pixel box test is a single bit test.  Sum mode splits each staged
+// round of the list between kGroups groups of eight warps that cover the
+// same tile, and adds the groups' partial sums in a fixed order at the end.
 //
 // Sum (GaussianImage project page, Overview: accumulated-sum rendering;
 // FlashImgs README: additive RGB, gate folded into the colour):
@@ -18,24 +22,146 @@ namespace gs2d {
 
 namespace {
 
-constexpr int kFwdThreads = 256;
-constexpr int kChunk = 256;
+constexpr int kWindow = 64;  // entries culled per warp at a time
 
-struct FwdStage {
-  float4 mc[kChunk];  // mean_x, mean_y, A, 2B
-  float4 cr[kChunk];  // C, r, g, b
-  uint2 box[kChunk];  // packed pixel box
-  float op[kChunk];   // opacity (composite)
-  unsigned char list[8][kChunk];
+// The lanes of a warp whose pixel lies in the box [x0, x1] x [y0, y1]; the
+// warp covers columns bx0..bx0+7 and rows by0..by0+3, lane = 8 * row + col.
+// Returns 0 when the box misses the sub-block.
+__device__ __forceinline__ unsigned int box_lanes(uint2 b, int bx0, int by0) {
+  const int cl = max(int(box_lo(b.x)) - bx0, 0), ch = min(int(box_hi(b.x)) - bx0, 7);
+  const int rl = max(int(box_lo(b.y)) - by0, 0), rh = min(int(box_hi(b.y)) - by0, 3);
+  if (cl > ch || rl > rh) return 0u;
+  const unsigned int cols = (0xFFu >> (7 - ch)) & (0xFFu << cl);
+  const unsigned int rows = (0xFFFFFFFFu >> (8 * (3 - rh))) & (0xFFFFFFFFu << (8 * rl));
+  return (cols * 0x01010101u) & rows;
+}
+
+struct Staged {
+  float4 mc;  // mean_x, mean_y, A, 2B
+  float4 cr;  // C, r, g, b
 };
 
-template <bool kComposite>
-__global__ void __launch_bounds__(kFwdThreads)
-k_render_fwd(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
-             const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
-             const float* __restrict__ bg, float* __restrict__ image, float* __restrict__ t_final,
-             int* __restrict__ last) {
-  __shared__ FwdStage sm;
+template <int kGroups>
+struct SumSmem {
+  Staged g[256 * kGroups];
+  uint2 box[256 * kGroups];
+  uint2 list[8 * kGroups][kWindow];  // (staged index, lane mask)
+  float3 part[kGroups > 1 ? kGroups - 1 : 1][kTilePixels];
+};
+
+template <int kGroups>
+__global__ void __launch_bounds__(256 * kGroups, 2048 / (256 * kGroups))
+k_render_fwd_sum(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
+                 const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
+                 float* __restrict__ image) {
+  constexpr int kThreads = 256 * kGroups;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SumSmem<kGroups>& sm = *reinterpret_cast<SumSmem<kGroups>*>(smem_raw);
+  const int tile = blockIdx.x;
+  const int tx = tile % tiles_x, ty = tile / tiles_x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int group = warp >> 3, wg = warp & 7;
+  const int bx0 = tx * kTile + (wg & 1) * 8;
+  const int by0 = ty * kTile + (wg >> 1) * 4;
+  const int px = bx0 + (lane & 7), py = by0 + (lane >> 3);
+  const float pxf = float(px) + 0.5f, pyf = float(py) + 0.5f;
+  const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
+  const unsigned int lt = (1u << lane) - 1u, bit = 1u << lane;
+  const int2 rg = ranges[tile];
+  uint2* list = sm.list[warp];
+
+  float ar = 0.f, ag = 0.f, ab = 0.f;
+  for (int rb = rg.x; rb < rg.y; rb += kThreads) {
+    const int cnt = min(kThreads, rg.y - rb);
+    if (tid < cnt) {
+      const float4* r = rec + 3 * size_t(sorted_gid[rb + tid]);
+      const float4 p0 = r[0], p1 = r[1], p2 = r[2];
+      sm.g[tid].mc = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
+      sm.g[tid].cr = p1;
+      sm.box[tid] = make_uint2(__float_as_uint(p2.x), __float_as_uint(p2.y));
+    }
+    __syncthreads();
+    const int lo = (group * cnt) / kGroups, hi = ((group + 1) * cnt) / kGroups;
+    for (int wb = lo; wb < hi; wb += kWindow) {
+      const int wend = min(wb + kWindow, hi);
+      int nl = 0;
+#pragma unroll
+      for (int j0 = 0; j0 < kWindow; j0 += 32) {
+        const int j = wb + j0 + lane;
+        unsigned int m = 0;
+        if (j < wend) m = box_lanes(sm.box[j], bx0, by0);
+        const unsigned int hits = __ballot_sync(0xffffffffu, m != 0u);
+        if (m) list[nl + __popc(hits & lt)] = make_uint2(unsigned(j), m);
+        nl += __popc(hits);
+      }
+      __syncwarp();
+      int e = 0;
+      for (; e + 1 < nl; e += 2) {
+        const uint2 u0 = list[e], u1 = list[e + 1];
+        const Staged s0 = sm.g[u0.x], s1 = sm.g[u1.x];
+        const float q0 = touch_q(__fsub_rn(pxf, s0.mc.x), __fsub_rn(pyf, s0.mc.y), s0.mc.z, s0.mc.w, s0.cr.x);
+        const float q1 = touch_q(__fsub_rn(pxf, s1.mc.x), __fsub_rn(pyf, s1.mc.y), s1.mc.z, s1.mc.w, s1.cr.x);
+        float w0 = ex2_approx(q0 * kNegHalfLog2e);
+        float w1 = ex2_approx(q1 * kNegHalfLog2e);
+        w0 = (q0 <= kk && (u0.y & bit)) ? w0 : 0.f;
+        w1 = (q1 <= kk && (u1.y & bit)) ? w1 : 0.f;
+        ar = fmaf(s0.cr.y, w0, ar);
+        ag = fmaf(s0.cr.z, w0, ag);
+        ab = fmaf(s0.cr.w, w0, ab);
+        ar = fmaf(s1.cr.y, w1, ar);
+        ag = fmaf(s1.cr.z, w1, ag);
+        ab = fmaf(s1.cr.w, w1, ab);
+      }
+      if (e < nl) {
+        const uint2 u0 = list[e];
+        const Staged s0 = sm.g[u0.x];
+        const float q0 = touch_q(__fsub_rn(pxf, s0.mc.x), __fsub_rn(pyf, s0.mc.y), s0.mc.z, s0.mc.w, s0.cr.x);
+        float w0 = ex2_approx(q0 * kNegHalfLog2e);
+        w0 = (q0 <= kk && (u0.y & bit)) ? w0 : 0.f;
+        ar = fmaf(s0.cr.y, w0, ar);
+        ag = fmaf(s0.cr.z, w0, ag);
+        ab = fmaf(s0.cr.w, w0, ab);
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+  }
+  // Fixed-order combination of the groups' partial sums.
+  const int pix = (py - ty * kTile) * kTile + (px - tx * kTile);
+  if (kGroups > 1) {
+    if (group > 0) sm.part[group - 1][pix] = make_float3(ar, ag, ab);
+    __syncthreads();
+    if (group > 0) return;
+#pragma unroll
+    for (int g = 0; g < kGroups - 1; ++g) {
+      const float3 v = sm.part[g][pix];
+      ar += v.x;
+      ag += v.y;
+      ab += v.z;
+    }
+  }
+  if (px < c.width && py < c.height) {
+    const size_t HW = size_t(c.width) * c.height;
+    const size_t p = size_t(py) * c.width + px;
+    image[p] = ar;
+    image[HW + p] = ag;
+    image[2 * HW + p] = ab;
+  }
+}
+
+struct CompSmem {
+  Staged g[256];
+  uint2 box[256];
+  float op[256];
+  uint2 list[8][kWindow];
+};
+
+__global__ void __launch_bounds__(256)
+k_render_fwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
+                  const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
+                  const float* __restrict__ bg, float* __restrict__ image,
+                  float* __restrict__ t_final, int* __restrict__ last) {
+  __shared__ CompSmem sm;
   const int tile = blockIdx.x;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -45,101 +171,81 @@ k_render_fwd(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
   const float pxf = float(px) + 0.5f, pyf = float(py) + 0.5f;
   const bool inside = px < c.width && py < c.height;
   const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
-  const unsigned int lt = (1u << lane) - 1u;
+  const unsigned int lt = (1u << lane) - 1u, bit = 1u << lane;
   const int2 rg = ranges[tile];
-  const int start = rg.x, end = rg.y;
+  uint2* list = sm.list[warp];
 
   float ar = 0.f, ag = 0.f, ab = 0.f, T = 1.f;
   int lst = 0;
   bool done = !inside;
-
-  for (int cb = start; cb < end; cb += kChunk) {
-    if (kComposite) {
-      if (__syncthreads_and(done)) break;
-    }
-    const int k = cb + tid;
-    if (k < end) {
-      const float4* r = rec + 3 * size_t(sorted_gid[k]);
+  for (int rb = rg.x; rb < rg.y; rb += 256) {
+    if (__syncthreads_and(done)) break;
+    const int cnt = min(256, rg.y - rb);
+    if (tid < cnt) {
+      const float4* r = rec + 3 * size_t(sorted_gid[rb + tid]);
       const float4 p0 = r[0], p1 = r[1], p2 = r[2];
-      sm.mc[tid] = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
-      sm.cr[tid] = p1;
+      sm.g[tid].mc = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
+      sm.g[tid].cr = p1;
       sm.box[tid] = make_uint2(__float_as_uint(p2.x), __float_as_uint(p2.y));
-      if (kComposite) sm.op[tid] = p2.z;
+      sm.op[tid] = p2.z;
     }
     __syncthreads();
-    const int cnt = min(kChunk, end - cb);
-    bool skip = false;
-    if (kComposite) skip = __all_sync(0xffffffffu, done);
-    if (!skip) {
+    for (int wb = 0; wb < cnt; wb += kWindow) {
+      if (__all_sync(0xffffffffu, done)) break;
+      const int wend = min(wb + kWindow, cnt);
       int nl = 0;
-      for (int j0 = 0; j0 < cnt; j0 += 32) {
-        const int j = j0 + lane;
-        bool hit = false;
-        if (j < cnt) {
-          const uint2 b = sm.box[j];
-          hit = int(box_lo(b.x)) <= bx0 + 7 && int(box_hi(b.x)) >= bx0 &&
-                int(box_lo(b.y)) <= by0 + 3 && int(box_hi(b.y)) >= by0;
-        }
-        const unsigned int m = __ballot_sync(0xffffffffu, hit);
-        if (hit) sm.list[warp][nl + __popc(m & lt)] = (unsigned char)j;
-        nl += __popc(m);
+#pragma unroll
+      for (int j0 = 0; j0 < kWindow; j0 += 32) {
+        const int j = wb + j0 + lane;
+        unsigned int m = 0;
+        if (j < wend) m = box_lanes(sm.box[j], bx0, by0);
+        const unsigned int hits = __ballot_sync(0xffffffffu, m != 0u);
+        if (m) list[nl + __popc(hits & lt)] = make_uint2(unsigned(j), m);
+        nl += __popc(hits);
       }
       __syncwarp();
       for (int e = 0; e < nl; ++e) {
-        const int j = sm.list[warp][e];
-        const float4 mc = sm.mc[j];
-        const float4 cr = sm.cr[j];
-        const uint2 b = sm.box[j];
-        const float dx = __fsub_rn(pxf, mc.x);
-        const float dy = __fsub_rn(pyf, mc.y);
-        const float q = touch_q(dx, dy, mc.z, mc.w, cr.x);
-        const bool in = q <= kk &&
-                        unsigned(px - int(box_lo(b.x))) <= unsigned(int(box_hi(b.x)) - int(box_lo(b.x))) &&
-                        unsigned(py - int(box_lo(b.y))) <= unsigned(int(box_hi(b.y)) - int(box_lo(b.y)));
-        if (kComposite) {
-          if (in && !done) {
-            if (T < c.t_min) {
-              done = true;
-            } else {
-              const float w = ex2_approx(q * kNegHalfLog2e);
-              const float alpha = sm.op[j] * w;
-              const float aT = alpha * T;
-              ar = fmaf(cr.y, aT, ar);
-              ag = fmaf(cr.z, aT, ag);
-              ab = fmaf(cr.w, aT, ab);
-              T = T * (1.0f - alpha);
-              lst = cb - start + j + 1;
-            }
-          }
-        } else {
-          if (in) {
+        const uint2 u = list[e];
+        const Staged s = sm.g[u.x];
+        const float q = touch_q(__fsub_rn(pxf, s.mc.x), __fsub_rn(pyf, s.mc.y), s.mc.z, s.mc.w, s.cr.x);
+        if (q <= kk && (u.y & bit) && !done) {
+          if (T < c.t_min) {
+            done = true;
+          } else {
             const float w = ex2_approx(q * kNegHalfLog2e);
-            ar = fmaf(cr.y, w, ar);
-            ag = fmaf(cr.z, w, ag);
-            ab = fmaf(cr.w, w, ab);
+            const float alpha = sm.op[u.x] * w;
+            const float aT = alpha * T;
+            ar = fmaf(s.cr.y, aT, ar);
+            ag = fmaf(s.cr.z, aT, ag);
+            ab = fmaf(s.cr.w, aT, ab);
+            T = T * (1.0f - alpha);
+            lst = rb - rg.x + int(u.x) + 1;
           }
         }
       }
+      __syncwarp();
     }
     __syncthreads();
   }
   if (inside) {
     const size_t HW = size_t(c.width) * c.height;
     const size_t p = size_t(py) * c.width + px;
-    if (kComposite) {
-      if (bg) {
-        ar = fmaf(T, bg[0], ar);
-        ag = fmaf(T, bg[1], ag);
-        ab = fmaf(T, bg[2], ab);
-      }
-      if (t_final) t_final[p] = T;
-      if (last) last[p] = lst;
+    if (bg) {
+      ar = fmaf(T, bg[0], ar);
+      ag = fmaf(T, bg[1], ag);
+      ab = fmaf(T, bg[2], ab);
     }
+    if (t_final) t_final[p] = T;
+    if (last) last[p] = lst;
     image[p] = ar;
     image[HW + p] = ag;
     image[2 * HW + p] = ab;
   }
 }
+
+// One group of eight warps per tile: splitting the list across 2 or 4 groups
+// measured no faster on a B300 (the per-warp fixed costs grow with the split).
+constexpr int kSumGroups = 1;
 
 }  // namespace
 
@@ -149,12 +255,16 @@ cudaError_t launch_render_fwd(const gs2d_config& c, const gs2d_record* rec, cons
   const int T = num_tiles(c);
   const float4* r = reinterpret_cast<const float4*>(rec);
   const int2* rg = reinterpret_cast<const int2*>(ranges);
-  if (c.mode == GS2D_MODE_COMPOSITE)
-    k_render_fwd<true><<<T, kFwdThreads, 0, s>>>(c, tiles_x(c), r, rg, sorted_gid, bg, image,
-                                                 t_final, last);
-  else
-    k_render_fwd<false><<<T, kFwdThreads, 0, s>>>(c, tiles_x(c), r, rg, sorted_gid, nullptr, image,
-                                                  nullptr, nullptr);
+  if (c.mode == GS2D_MODE_COMPOSITE) {
+    k_render_fwd_comp<<<T, 256, 0, s>>>(c, tiles_x(c), r, rg, sorted_gid, bg, image, t_final, last);
+  } else {
+    const size_t smem = sizeof(SumSmem<kSumGroups>);
+    cudaError_t e = cudaFuncSetAttribute(k_render_fwd_sum<kSumGroups>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    k_render_fwd_sum<kSumGroups><<<T, 256 * kSumGroups, smem, s>>>(c, tiles_x(c), r, rg, sorted_gid,
+                                                                  image);
+  }
   return cudaGetLastError();
 }
 
