@@ -217,6 +217,31 @@ GS2D_API gs2d_status gs2d_render_bwd(const gs2d_config* cfg, int32_t n, const fl
                             gs2d_stream_t stream);
 
 /*
+ * The L2 loss of gs2d_loss_l2 for callers that cannot supply a workspace.
+ * (This call has no counterpart in the method's pages; it serves callers.)
+ * Some callers cannot hand the library device memory beyond the image,
+ * target and outputs -- code that receives its buffers from another
+ * framework and has no allocator to call, or a loop that must not call
+ * cudaMalloc (it synchronises the device, and is not allowed while a
+ * stream capture is running).  This call allocates nothing: it keeps the
+ * reduction's block partial sums in a 4 KiB array in the library's own
+ * device memory, one per GPU, held until the process exits.
+ *   Same arguments and results as gs2d_loss_l2, without the workspace.
+ *   Limits: 1 <= height, width <= 32768, else GS2D_ERR_INVALID_ARG (every
+ *   such image fits the fixed array: the reduction uses at most 1024
+ *   blocks).
+ *   The first call on each device looks the array's address up
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   All calls on a device share the array: calls that overlap on the GPU
+ *   (different streams, no ordering between them) race and give wrong
+ *   losses.  Nothing in the array needs clearing between calls: every call
+ *   writes each partial it reads.
+ */
+GS2D_API gs2d_status gs2d_loss_l2_noalloc(int32_t height, int32_t width, const float* image,
+                                          const float* target, float* loss, float* d_image,
+                                          gs2d_stream_t stream);
+
+/*
  * Waits for `stream`, then reads what the last gs2d_bin_and_sort left in
  * the workspace: the pair count (host *pairs, may be NULL) and the
  * GS2D_FLAG_* bits (host *flags, may be NULL).  Returns the status those

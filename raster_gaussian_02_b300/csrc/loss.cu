@@ -3,6 +3,9 @@
 // Two kernels, no atomics: every block writes the partial sum of a fixed
 // grid-stride set of elements, then one block adds the partials in order,
 // so the loss is bit-reproducible.
+#include <atomic>
+#include <mutex>
+
 #include "gs2d_internal.cuh"
 
 namespace gs2d {
@@ -85,3 +88,83 @@ cudaError_t launch_loss_l2(int h, int w, const float* image, const float* target
 }
 
 }  // namespace gs2d
+
+// ---------------------------------------------------------------------------
+// L2 loss without a caller-supplied workspace.
+//
+// Some callers cannot hand the library any device memory beyond the image,
+// target and outputs: code that receives its buffers from another framework
+// and has no allocator of its own to call, or a loop that must not call
+// cudaMalloc because it implicitly synchronises the device or is not allowed
+// while a stream capture is in progress.  For them the block partial sums
+// of the loss live in this fixed device array instead of the workspace.
+// The array is 4 KiB (kLossMaxBlocks floats); every GPU that loads the
+// library holds one copy until the process exits.  The reduction never uses
+// more than kLossMaxBlocks blocks, so every image within the library's
+// 32768 x 32768 limit fits; larger ones are rejected.
+static __device__ __align__(256) float g_loss_scratch[gs2d::kLossMaxBlocks];
+
+namespace gs2d {
+
+namespace {
+
+constexpr int kMaxDevices = 256;
+std::atomic<float*> g_loss_scratch_addr[kMaxDevices];  // per device, set once
+std::mutex g_loss_scratch_mu;
+
+// The device address of g_loss_scratch on the current device, looked up the
+// first time each device is seen.
+cudaError_t loss_scratch_address(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  float* p = g_loss_scratch_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_loss_scratch_mu);
+    p = g_loss_scratch_addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+      void* addr = nullptr;
+      e = cudaGetSymbolAddress(&addr, g_loss_scratch);
+      if (e != cudaSuccess) return e;
+      p = static_cast<float*>(addr);
+      g_loss_scratch_addr[dev].store(p, std::memory_order_release);
+    }
+  }
+  *out = p;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+}  // namespace gs2d
+
+extern "C" gs2d_status gs2d_loss_l2_noalloc(int32_t height, int32_t width, const float* image,
+                                            const float* target, float* loss, float* d_image,
+                                            gs2d_stream_t stream) {
+  using namespace gs2d;
+  if (height < 1 || width < 1 || height > 32768 || width > 32768) return GS2D_ERR_INVALID_ARG;
+  if (!image || !target || !loss || !d_image) return GS2D_ERR_INVALID_ARG;
+  const uintptr_t bits = reinterpret_cast<uintptr_t>(image) | reinterpret_cast<uintptr_t>(target) |
+                         reinterpret_cast<uintptr_t>(loss) | reinterpret_cast<uintptr_t>(d_image);
+  if (bits & 3) return GS2D_ERR_INVALID_ARG;
+  float* partials = nullptr;
+  if (loss_scratch_address(&partials) != cudaSuccess) return GS2D_ERR_CUDA;
+  // The same two kernels as gs2d_loss_l2, with the partials in the fixed array.
+  const long long m = 3ll * height * width;
+  const bool vec = (m % 4 == 0) && ((reinterpret_cast<uintptr_t>(image) |
+                                     reinterpret_cast<uintptr_t>(target) |
+                                     reinterpret_cast<uintptr_t>(d_image)) & 15) == 0;
+  const long long work = vec ? m / 4 : m;
+  long long blocks = (work + kLossThreads * 4 - 1) / (kLossThreads * 4);
+  if (blocks < 1) blocks = 1;
+  if (blocks > gs2d::kLossMaxBlocks) blocks = gs2d::kLossMaxBlocks;
+  const float scale = float(2.0 / double(m));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (vec)
+    k_loss_partial<true><<<int(blocks), kLossThreads, 0, s>>>(m, image, target, scale, d_image, partials);
+  else
+    k_loss_partial<false><<<int(blocks), kLossThreads, 0, s>>>(m, image, target, scale, d_image, partials);
+  k_loss_final<<<1, kLossThreads, 0, s>>>(int(blocks), partials, float(m), loss);
+  return cudaGetLastError() == cudaSuccess ? GS2D_OK : GS2D_ERR_CUDA;
+}

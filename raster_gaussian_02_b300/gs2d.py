@@ -68,6 +68,8 @@ def lib() -> C.CDLL:
         L.gs2d_loss_l2.restype = C.c_int
         L.gs2d_render_bwd.argtypes = [_cfgp, C.c_int32] + [_p] * 15 + [_p]
         L.gs2d_render_bwd.restype = C.c_int
+        L.gs2d_loss_l2_noalloc.argtypes = [C.c_int32, C.c_int32] + [_p] * 4 + [_p]
+        L.gs2d_loss_l2_noalloc.restype = C.c_int
         L.gs2d_read_status.argtypes = [_p, C.POINTER(C.c_int64), C.POINTER(C.c_uint32), _p]
         L.gs2d_read_status.restype = C.c_int
         L.gs2d_status_string.argtypes = [C.c_int]
@@ -146,6 +148,15 @@ def gs2d_loss_l2(height, width, image, target, loss, d_image, workspace, stream=
                               _ptr(target, _f32, "target"), _ptr(loss, _f32, "loss"),
                               _ptr(d_image, _f32, "d_image"), _ptr(workspace, None, "workspace"),
                               _stream(stream))
+
+
+def gs2d_loss_l2_noalloc(height, width, image, target, loss, d_image, stream=None) -> int:
+    """The L2 loss without a workspace (for callers that cannot allocate;
+    the library keeps the reduction's partial sums in its own fixed 4 KiB
+    device array, shared by every call on the device)."""
+    return lib().gs2d_loss_l2_noalloc(int(height), int(width), _ptr(image, _f32, "image"),
+                                      _ptr(target, _f32, "target"), _ptr(loss, _f32, "loss"),
+                                      _ptr(d_image, _f32, "d_image"), _stream(stream))
 
 
 def gs2d_render_bwd(cfg, n, chol, rec, rect, tile_ranges, sorted_gid, background, t_final, last,
