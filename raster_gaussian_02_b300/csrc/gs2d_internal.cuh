@@ -20,18 +20,17 @@ constexpr int kTilePixels = kTile * kTile;
 //   [0, 256)          Header
 //   [256, 4352)       loss partial sums (kLossMaxBlocks floats)
 //   [4352, 12544)     radix digit histograms [kMaxPasses][kMaxRadix]
-//   then              scan look-back words [ceil(n / kScanItems) + 1] (uint64)
+//   then              per-block pair totals, then offsets [ceil(n / kScanItems) + 1] (int64)
 //   then              per-Gaussian pair offsets [n] (int32)
 //   then              background partials [T] x 4 floats (composite)
 //   then              backward partials [cap] x 8 floats (sum) or x 12 (composite)
-//   then              radix look-back words [passes][radix][partitions(cap) rounded up to 4]
+//   then              radix count tables [passes][radix][partitions(cap) rounded up to 4]
 //   then              keys A, keys B [cap] (uint32 sum, uint64 composite)
 //   then              values scratch [cap] (uint32)
 struct Header {
   long long pairs;                 // P, written by the binning
   unsigned int flags;              // GS2D_FLAG_*
-  unsigned int scan_ticket;        // block order for the scan look-back
-  unsigned int radix_ticket[8];    // block order of each radix pass
+  unsigned int blocks_done;        // count of finished blocks (last one finishes the scan)
   unsigned long long keys_final;   // byte offset of the sorted keys
 };
 
@@ -48,12 +47,8 @@ constexpr int kScanItems = kScanThreads;  // Gaussians per scan block, one per t
 
 constexpr int kRadixThreads = 256;
 
-// Bounded device-side waits: after this many polls a waiting thread gives up,
-// sets GS2D_FLAG_TIMEOUT and continues, so a kernel always terminates.
-constexpr unsigned int kSpinLimit = 1u << 22;
-
 struct Layout {
-  size_t scan, offsets, bg_partials, partials, radix_status, keys_a, keys_b, vals_tmp, total;
+  size_t block_off, offsets, bg_partials, partials, tables, keys_a, keys_b, vals_tmp, total;
   int passes, digit_bits, tile_bits, key_bits, key_bytes, partial_floats, radix_per_thread;
   long long partitions, partitions4;  // radix partitions, and rounded up to a multiple of 4
 };
@@ -82,16 +77,16 @@ inline Layout layout_of(const gs2d_config& c, long long n, long long cap) {
   const bool comp = c.mode == GS2D_MODE_COMPOSITE;
   L.key_bits = L.tile_bits + (comp ? 32 : 0);
   L.passes = (L.key_bits + kMaxDigitBits - 1) / kMaxDigitBits;
-  L.digit_bits = L.passes ? (L.key_bits + L.passes - 1) / L.passes : 0;
+  L.digit_bits = kMaxDigitBits;  // every pass sorts a full 8-bit digit (256 buckets)
   L.key_bytes = comp ? 8 : 4;
   L.partial_floats = comp ? 12 : 8;
   L.radix_per_thread = radix_per_thread(cap);
   const long long items = (long long)kRadixThreads * L.radix_per_thread;
   L.partitions = (cap + items - 1) / items;
   L.partitions4 = (L.partitions + 3) & ~3ll;
-  const size_t radix = size_t(1) << L.digit_bits;
+  const size_t radix = kMaxRadix;
   size_t o = kOffScan;
-  L.scan = o;
+  L.block_off = o;
   o = align256(o + 8 * size_t((n + kScanItems - 1) / kScanItems + 1));
   L.offsets = o;
   o = align256(o + 4 * size_t(n));
@@ -99,7 +94,7 @@ inline Layout layout_of(const gs2d_config& c, long long n, long long cap) {
   if (comp) o = align256(o + 16 * size_t(T));
   L.partials = o;
   o = align256(o + 4 * size_t(L.partial_floats) * size_t(cap));
-  L.radix_status = o;
+  L.tables = o;
   o = align256(o + 4 * size_t(L.passes) * size_t(L.partitions4) * radix);
   L.keys_a = o;
   o = align256(o + size_t(L.key_bytes) * size_t(cap));
@@ -136,6 +131,18 @@ constexpr float kNegHalfLog2e = -0.72134752044448170368f;
 
 __device__ __forceinline__ unsigned int box_lo(unsigned int b) { return b & 0xFFFFu; }
 __device__ __forceinline__ unsigned int box_hi(unsigned int b) { return b >> 16; }
+
+// The lanes of a warp whose pixel lies in the box [x0, x1] x [y0, y1]; the
+// warp covers columns bx0..bx0+7 and rows by0..by0+3, lane = 8 * row + col.
+// Returns 0 when the box misses the sub-block.
+__device__ __forceinline__ unsigned int box_lanes(uint2 b, int bx0, int by0) {
+  const int cl = max(int(box_lo(b.x)) - bx0, 0), ch = min(int(box_hi(b.x)) - bx0, 7);
+  const int rl = max(int(box_lo(b.y)) - by0, 0), rh = min(int(box_hi(b.y)) - by0, 3);
+  if (cl > ch || rl > rh) return 0u;
+  const unsigned int cols = (0xFFu >> (7 - ch)) & (0xFFu << cl);
+  const unsigned int rows = (0xFFFFFFFFu >> (8 * (3 - rh))) & (0xFFFFFFFFu << (8 * rl));
+  return (cols * 0x01010101u) & rows;
+}
 
 // Monotone map of a finite float to uint32 (IEEE order, -0 mapped as +0).
 __device__ __forceinline__ unsigned int depth_key(float d) {

@@ -209,20 +209,44 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Butterfly reduce-scatter of eight per-lane values over the warp: returns,
+// in every lane, the warp total of value ((lane >> 2) & 7) in the order
+// v[0..7] (lane bit 4 picks values 4-7, bit 3 values +2, bit 2 values +1).
+__device__ __forceinline__ float warp_reduce_scatter8(const float (&v)[8], int lane) {
+  float a[4], b[2];
+  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = u16 ? v[i + 4] : v[i], send = u16 ? v[i] : v[i + 4];
+    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = u8 ? a[i + 2] : a[i], send = u8 ? a[i] : a[i + 2];
+    b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  float c = (u4 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, u4 ? b[0] : b[1], 4);
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  return c;
+}
+
 struct CompStage {
   float4 mc[kCompChunk];  // mean_x, mean_y, A, 2B
   float4 cr[kCompChunk];  // C, r, g, b
   uint2 box[kCompChunk];
   float op[kCompChunk];
   int gid[kCompChunk];
-  unsigned char list[8][kCompChunk];
+  uint2 list[8][kCompChunk];            // (chunk index, lane mask) per warp
   float acc[8][kCompChunk][kCompVals];  // per-warp partials, summed over warps in order
   float bgred[8][3];
 };
 
 // Composite: one block per tile, one pixel per thread (8x4 sub-block per
 // warp as in the forward), walking the tile's list back to front from each
-// pixel's last contributor.
+// pixel's last contributor.  Per (warp, Gaussian) the nine partial
+// derivatives are reduced over the warp and kept in a per-warp slot; the
+// slots are summed in warp order per chunk entry.
 __global__ void __launch_bounds__(kBwdCompThreads)
 k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
                   const int4* __restrict__ rect, const int2* __restrict__ ranges,
@@ -230,7 +254,8 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
                   const float* __restrict__ bg, const float* __restrict__ t_final,
                   const int* __restrict__ last, const float* __restrict__ d_image,
                   float4* __restrict__ partials, float4* __restrict__ bg_partials) {
-  __shared__ CompStage sm;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  CompStage& sm = *reinterpret_cast<CompStage*>(smem_raw);
   const int tile = blockIdx.x;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -240,10 +265,11 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
   const float pxf = float(px) + 0.5f, pyf = float(py) + 0.5f;
   const bool inside = px < c.width && py < c.height;
   const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
-  const unsigned int lt = (1u << lane) - 1u;
+  const unsigned int lt = (1u << lane) - 1u, bit = 1u << lane;
   const int2 rg = ranges[tile];
   const size_t HW = size_t(c.width) * c.height;
   const float bgr = bg ? bg[0] : 0.f, bgg = bg ? bg[1] : 0.f, bgb = bg ? bg[2] : 0.f;
+  uint2* list = sm.list[warp];
 
   float T = 1.f, gr = 0.f, gg = 0.f, gb = 0.f;
   int lst = 0;
@@ -296,35 +322,30 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
     int nl = 0;
     for (int j0 = 0; j0 < cnt; j0 += 32) {
       const int j = j0 + lane;
-      bool hit = false;
+      unsigned int m = 0;
       if (j < cnt) {
-        const uint2 b = sm.box[j];
-        hit = int(box_lo(b.x)) <= bx0 + 7 && int(box_hi(b.x)) >= bx0 &&
-              int(box_lo(b.y)) <= by0 + 3 && int(box_hi(b.y)) >= by0;
-        if (!hit)
+        m = box_lanes(sm.box[j], bx0, by0);
+        if (!m)
 #pragma unroll
           for (int v = 0; v < kCompVals; ++v) sm.acc[warp][j][v] = 0.f;
       }
-      const unsigned int m = __ballot_sync(0xffffffffu, hit);
-      if (hit) sm.list[warp][nl + __popc(m & lt)] = (unsigned char)j;
-      nl += __popc(m);
+      const unsigned int hits = __ballot_sync(0xffffffffu, m != 0u);
+      if (m) list[nl + __popc(hits & lt)] = make_uint2(unsigned(j), m);
+      nl += __popc(hits);
     }
     __syncwarp();
     for (int e = nl - 1; e >= 0; --e) {
-      const int j = sm.list[warp][e];
+      const uint2 u = list[e];
+      const int j = int(u.x);
       const int idx = cb - rg.x + j;  // position in the tile's list
       const float4 mc = sm.mc[j];
       const float4 cr = sm.cr[j];
-      const uint2 b = sm.box[j];
       const float dx = __fsub_rn(pxf, mc.x);
       const float dy = __fsub_rn(pyf, mc.y);
       const float q = touch_q(dx, dy, mc.z, mc.w, cr.x);
-      const bool act = inside && idx < lst && q <= kk &&
-                       unsigned(px - int(box_lo(b.x))) <= unsigned(int(box_hi(b.x)) - int(box_lo(b.x))) &&
-                       unsigned(py - int(box_lo(b.y))) <= unsigned(int(box_hi(b.y)) - int(box_lo(b.y)));
-      float v[kCompVals];
-#pragma unroll
-      for (int u = 0; u < kCompVals; ++u) v[u] = 0.f;
+      const bool act = inside && (u.y & bit) && idx < lst && q <= kk;
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float v8 = 0.f;
       if (act) {
         const float o = sm.op[j];
         const float w = ex2_approx(q * kNegHalfLog2e);
@@ -337,25 +358,26 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
         const float t = w * o * dal;
         v[0] = t * dx;
         v[1] = t * dy;
-        v[2] = t * dx * dx;
-        v[3] = t * dx * dy;
-        v[4] = t * dy * dy;
+        v[2] = v[0] * dx;
+        v[3] = v[0] * dy;
+        v[4] = v[1] * dy;
         v[5] = gr * aT;
         v[6] = gg * aT;
         v[7] = gb * aT;
-        v[8] = dal * w;
+        v8 = dal * w;
         Sr = fmaf(cr.y, aT, Sr);
         Sg = fmaf(cr.z, aT, Sg);
         Sb = fmaf(cr.w, aT, Sb);
         T = Tb;
       }
       if (__any_sync(0xffffffffu, act)) {
-#pragma unroll
-        for (int u = 0; u < kCompVals; ++u) v[u] = warp_sum(v[u]);
+        const float tot = warp_reduce_scatter8(v, lane);
+        const float tot8 = warp_sum(v8);
+        if ((lane & 3) == 0) sm.acc[warp][j][(lane >> 2) & 7] = tot;
+        if (lane == 0) sm.acc[warp][j][8] = tot8;
+      } else if (lane < kCompVals) {
+        sm.acc[warp][j][lane] = 0.f;
       }
-      if (lane == 0)
-#pragma unroll
-        for (int u = 0; u < kCompVals; ++u) sm.acc[warp][j][u] = v[u];
     }
     __syncthreads();
     if (tid < cnt) {
@@ -393,11 +415,15 @@ cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
   const int2* rg = reinterpret_cast<const int2*>(ranges);
   const int* offsets = reinterpret_cast<const int*>(ws + L.offsets);
   float4* partials = reinterpret_cast<float4*>(ws + L.partials);
-  if (c.mode == GS2D_MODE_COMPOSITE)
-    k_render_bwd_comp<<<T, kBwdCompThreads, 0, s>>>(
+  if (c.mode == GS2D_MODE_COMPOSITE) {
+    const size_t smem = sizeof(CompStage);
+    cudaError_t e = cudaFuncSetAttribute(k_render_bwd_comp, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
+    if (e != cudaSuccess) return e;
+    k_render_bwd_comp<<<T, kBwdCompThreads, smem, s>>>(
         c, tiles_x(c), r, rc, rg, sorted_gid, offsets, bg, t_final, last, d_image, partials,
         reinterpret_cast<float4*>(ws + L.bg_partials));
-  else {
+  } else {
     const size_t smem = sizeof(BwdSumSmem);
     cudaError_t e = cudaFuncSetAttribute(k_render_bwd_sum, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));

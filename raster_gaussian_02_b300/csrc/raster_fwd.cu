@@ -24,18 +24,6 @@ namespace {
 
 constexpr int kWindow = 64;  // entries culled per warp at a time
 
-// The lanes of a warp whose pixel lies in the box [x0, x1] x [y0, y1]; the
-// warp covers columns bx0..bx0+7 and rows by0..by0+3, lane = 8 * row + col.
-// Returns 0 when the box misses the sub-block.
-__device__ __forceinline__ unsigned int box_lanes(uint2 b, int bx0, int by0) {
-  const int cl = max(int(box_lo(b.x)) - bx0, 0), ch = min(int(box_hi(b.x)) - bx0, 7);
-  const int rl = max(int(box_lo(b.y)) - by0, 0), rh = min(int(box_hi(b.y)) - by0, 3);
-  if (cl > ch || rl > rh) return 0u;
-  const unsigned int cols = (0xFFu >> (7 - ch)) & (0xFFu << cl);
-  const unsigned int rows = (0xFFFFFFFFu >> (8 * (3 - rh))) & (0xFFFFFFFFu << (8 * rl));
-  return (cols * 0x01010101u) & rows;
-}
-
 struct Staged {
   float4 mc;  // mean_x, mean_y, A, 2B
   float4 cr;  // C, r, g, b

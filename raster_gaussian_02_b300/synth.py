@@ -254,6 +254,12 @@ def render_4096x4096(seed: int = 5000, n: int = 2_000_000) -> Workload:
     return render_uniform(4096, 4096, n, seed)
 
 
+def render_2048x2048(seed: int = 5000, n: int = 500_000) -> Workload:
+    """A quarter of the 4096x4096 render scene (same density and sizes), small
+    enough for profiler captures."""
+    return render_uniform(2048, 2048, n, seed)
+
+
 def random_scene(width: int, height: int, n: int, seed: int, mode: int = SUM,
                  diag=(0.5, 3.0), offdiag_sigma: float = 0.5, margin: float = 0.0) -> Workload:
     """Small random scene for parity and edge cases; `margin` px of the
@@ -287,4 +293,5 @@ WORKLOADS = {
     "heavy_2048x1360_300k": heavy_2048x1360,
     "composite_768x512_50k": composite_768x512,
     "render_4096x4096_2m": render_4096x4096,
+    "render_2048x2048_500k": render_2048x2048,
 }
