@@ -159,6 +159,23 @@ class ClockSampler:
                 "samples": len(rows), "samples_in_timed_region": len(inside)}
 
 
+# ---------------------------------------------------------- aggregation ---
+
+def aggregate_replicas(local_ms: float, steps: int, world: int, device=None):
+    """Whole-job throughput of `world` independent replicas: every rank ran
+    `steps` steps in `local_ms`; the job time is the slowest rank's.  Returns
+    (steps per second over all ranks, job time in ms).  Needs an initialised
+    process group when world > 1 (gloo on CPU tensors, nccl on `device`)."""
+    job_ms = float(local_ms)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([job_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        job_ms = float(t.item())
+    return world * steps / (job_ms / 1e3), job_ms
+
+
 # ------------------------------------------------------------ reference ---
 
 def oracle_step(wl):
@@ -328,12 +345,7 @@ def run_gs2d(args):
     st, pairs_now, flags = gs2d.gs2d_read_status(R.workspace)
     if st != gs2d.GS2D_OK:
         raise RuntimeError(f"device status after the timed region: {gs2d.status_string(st)}")
-    total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    value = world * args.steps / (total_ms / 1e3)
+    value, total_ms = aggregate_replicas(sum(step_ms), args.steps, world, dev)
     clocks = sampler.summary()
 
     # ---- secondary numbers (each after an L2 flush, same stream)
@@ -414,11 +426,7 @@ def run_gs2d(args):
 
     k3 = max(20, min(args.steps, 500))
     e2e_ms = timed(e2e_step, k3, 5)
-    e2e_val = world * k3 / (sum(e2e_ms) / 1e3)
-    if world > 1:
-        tt = torch.tensor([sum(e2e_ms)], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_val = world * k3 / (float(tt.item()) / 1e3)
+    e2e_val, _ = aggregate_replicas(sum(e2e_ms), k3, world, dev)
 
     # ---- CPU baseline (rank 0, one GPU only)
     cpu = None
