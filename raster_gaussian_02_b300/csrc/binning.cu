@@ -87,6 +87,7 @@ k_count_scan(int n, long long cap, const int* __restrict__ count, Header* hdr,
              long long* __restrict__ block_off, unsigned int* __restrict__ zero_a,
              long long zero_a_words, unsigned int* __restrict__ zero_b, long long zero_b_words,
              unsigned long long keys_final) {
+  pdl_enter();
   const int tid = threadIdx.x;
   const long long gstride = (long long)gridDim.x * blockDim.x;
   for (long long k = (long long)blockIdx.x * blockDim.x + tid; k < zero_a_words; k += gstride)
@@ -134,6 +135,7 @@ k_emit(int n, int tiles_x, int passes, long long cap, long long partitions4,
        unsigned int* __restrict__ hist, unsigned int* __restrict__ table0,
        int* __restrict__ offsets, KeyOf<kComposite>* __restrict__ keys,
        unsigned int* __restrict__ vals) {
+  pdl_enter();
   using Key = KeyOf<kComposite>;
   __shared__ long long s_excl[kScanItems + 1];
   __shared__ int4 s_rect[kScanItems];
@@ -211,6 +213,7 @@ __global__ void __launch_bounds__(256)
 k_digit_offsets(int pass, long long cap, long long partitions, long long partitions4,
                 const Header* __restrict__ hdr, const unsigned int* __restrict__ hist,
                 unsigned int* __restrict__ table) {
+  pdl_enter();
   const long long n = usable_pairs(hdr, cap);
   if (n == 0) return;
   const int d = blockIdx.x, tid = threadIdx.x;
@@ -245,6 +248,7 @@ k_radix_scatter(int pass, long long cap, long long partitions4, bool own_offsets
                 const Key* __restrict__ keys_in,
                 const unsigned int* __restrict__ vals_in, Key* __restrict__ keys_out,
                 unsigned int* __restrict__ vals_out) {
+  pdl_enter();
   constexpr int kItems = kRadixThreads * kPerThread;
   __shared__ unsigned short s_whist[8][kMaxRadix];  // per-warp counts, then exclusive offsets
   __shared__ unsigned int s_base[kMaxRadix];
@@ -322,6 +326,7 @@ template <typename Key>
 __global__ void __launch_bounds__(kRadixThreads)
 k_radix_count(int pass, long long cap, long long partitions4, const Header* __restrict__ hdr,
               const Key* __restrict__ keys, unsigned int* __restrict__ table) {
+  pdl_enter();
   __shared__ unsigned int s_cnt[kMaxRadix];
   const long long n = usable_pairs(hdr, cap);
   const long long part = blockIdx.x;
@@ -344,6 +349,7 @@ template <typename Key>
 __global__ void __launch_bounds__(256)
 k_tile_bounds(long long cap, const Header* __restrict__ hdr, const Key* __restrict__ keys,
               int2* __restrict__ ranges, int tile_shift) {
+  pdl_enter();
   const long long n = usable_pairs(hdr, cap);
   int* rg = reinterpret_cast<int*>(ranges);
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -380,13 +386,12 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
   Key* kb = reinterpret_cast<Key*>(ws + L.keys_b);
   const size_t keys_final = (L.passes % 2 == 0) ? L.keys_a : L.keys_b;
   const int blocks = n > 0 ? (n + kScanItems - 1) / kScanItems : 1;
-  k_count_scan<<<blocks, kScanThreads, 0, s>>>(n, cap, count, hdr, block_off, tables,
+  GS2D_TRY(launch(k_count_scan, dim3(blocks), dim3(kScanThreads), 0, s, n, cap, count, hdr, block_off, tables,
                                                L.passes * table_words,
                                                reinterpret_cast<unsigned int*>(tile_ranges), 2ll * T,
-                                               (unsigned long long)keys_final);
-  k_emit<kComposite><<<blocks, kScanThreads, 0, s>>>(
-      n, tiles_x(c), L.passes, cap, L.partitions4, reinterpret_cast<const int4*>(rect), count,
-      reinterpret_cast<const float4*>(rec), block_off, hist, tables, offsets, ka, vals_a);
+                                               (unsigned long long)keys_final));
+  GS2D_TRY(launch(k_emit<kComposite>, dim3(blocks), dim3(kScanThreads), 0, s, n, tiles_x(c), L.passes, cap, L.partitions4, reinterpret_cast<const int4*>(rect), count,
+      reinterpret_cast<const float4*>(rec), block_off, hist, tables, offsets, ka, vals_a));
   // Up to 128 partitions each scatter block sums its own offsets (at most 128
   // counts per digit); beyond that one k_digit_offsets launch per pass does.
   const bool own = L.partitions <= 128;
@@ -394,20 +399,19 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
     const bool even = (p % 2) == 0;
     unsigned int* table = tables + p * table_words;
     if (p > 0)  // pass 0 counts come from k_emit
-      k_radix_count<Key><<<int(L.partitions), kRadixThreads, 0, s>>>(p, cap, L.partitions4, hdr,
-                                                                    even ? ka : kb, table);
+      GS2D_TRY(launch(k_radix_count<Key>, dim3(int(L.partitions)), dim3(kRadixThreads), 0, s, p, cap, L.partitions4, hdr,
+                                                                    even ? ka : kb, table));
     if (!own)
-      k_digit_offsets<<<kMaxRadix, 256, 0, s>>>(p, cap, L.partitions, L.partitions4, hdr, hist, table);
-    k_radix_scatter<Key, 8><<<int(L.partitions), kRadixThreads, 0, s>>>(
-        p, cap, L.partitions4, own, hist, hdr, table, even ? ka : kb, even ? vals_a : vals_b,
-        even ? kb : ka, even ? vals_b : vals_a);
+      GS2D_TRY(launch(k_digit_offsets, dim3(kMaxRadix), dim3(256), 0, s, p, cap, L.partitions, L.partitions4, hdr, hist, table));
+    GS2D_TRY(launch(k_radix_scatter<Key, 8>, dim3(int(L.partitions)), dim3(kRadixThreads), 0, s, p, cap, L.partitions4, own, hist, hdr, table, even ? ka : kb, even ? vals_a : vals_b,
+        even ? kb : ka, even ? vals_b : vals_a));
   }
   if (cap > 0) {
     long long tb = (cap + 255) / 256;
     if (tb > 148 * 16) tb = 148 * 16;
-    k_tile_bounds<Key><<<int(tb), 256, 0, s>>>(cap, hdr, reinterpret_cast<const Key*>(ws + keys_final),
+    GS2D_TRY(launch(k_tile_bounds<Key>, dim3(int(tb)), dim3(256), 0, s, cap, hdr, reinterpret_cast<const Key*>(ws + keys_final),
                                               reinterpret_cast<int2*>(tile_ranges),
-                                              kComposite ? 32 : 0);
+                                              kComposite ? 32 : 0));
   }
   return cudaGetLastError();
 }

@@ -59,6 +59,15 @@ inline int tiles_x(const gs2d_config& c) { return (c.width + kTile - 1) / kTile;
 inline int tiles_y(const gs2d_config& c) { return (c.height + kTile - 1) / kTile; }
 inline int num_tiles(const gs2d_config& c) { return tiles_x(c) * tiles_y(c); }
 
+// Streaming multiprocessors of the current device (148 if the query fails).
+inline int sm_count() {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  return sms;
+}
+
 inline int bits_for(long long values) {  // bits needed to hold 0 .. values-1
   int b = 0;
   while ((1ll << b) < values) ++b;
@@ -150,6 +159,47 @@ __device__ __forceinline__ unsigned int depth_key(float d) {
   if ((u << 1) == 0u) u = 0u;  // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+
+// ------------------------------------------------- dependent launches --
+// Every kernel is launched with programmatic stream serialization: its
+// blocks may be scheduled while the kernel before it on the stream drains,
+// and each kernel starts with pdl_wait(), which returns once that kernel
+// has completed and its writes are visible (a no-op for launches without
+// the attribute).  pdl_trigger() then lets the next kernel start scheduling.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_trigger();
+}
+
+// Measured on a B300 (768x512 and 2048x2048 steps in CUDA graphs): within
+// +-1.5 % of plain stream order, so it is left off.
+constexpr bool kDependentLaunch = false;
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = kDependentLaunch ? 1 : 0;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+#define GS2D_TRY(expr)                    \
+  do {                                    \
+    const cudaError_t err_ = (expr);      \
+    if (err_ != cudaSuccess) return err_; \
+  } while (0)
 
 // ------------------------------------------------------------- launchers --
 // Each returns cudaGetLastError() after enqueueing.

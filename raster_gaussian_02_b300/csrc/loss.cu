@@ -29,6 +29,7 @@ template <bool kVec>
 __global__ void __launch_bounds__(kLossThreads)
 k_loss_partial(long long m, const float* __restrict__ image, const float* __restrict__ target,
                float scale, float* __restrict__ d_image, float* __restrict__ partials) {
+  pdl_enter();
   __shared__ float red[kLossThreads / 32];
   float acc = 0.f;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -58,6 +59,7 @@ k_loss_partial(long long m, const float* __restrict__ image, const float* __rest
 
 __global__ void __launch_bounds__(kLossThreads)
 k_loss_final(int nb, const float* __restrict__ partials, float m, float* __restrict__ loss) {
+  pdl_enter();
   __shared__ float red[kLossThreads / 32];
   float acc = 0.f;
   for (int k = threadIdx.x; k < nb; k += blockDim.x) acc += partials[k];
@@ -80,10 +82,10 @@ cudaError_t launch_loss_l2(int h, int w, const float* image, const float* target
   if (blocks > kLossMaxBlocks) blocks = kLossMaxBlocks;
   const float scale = float(2.0 / double(m));
   if (vec)
-    k_loss_partial<true><<<int(blocks), kLossThreads, 0, s>>>(m, image, target, scale, d_image, partials);
+    GS2D_TRY(launch(k_loss_partial<true>, dim3(int(blocks)), dim3(kLossThreads), 0, s, m, image, target, scale, d_image, partials));
   else
-    k_loss_partial<false><<<int(blocks), kLossThreads, 0, s>>>(m, image, target, scale, d_image, partials);
-  k_loss_final<<<1, kLossThreads, 0, s>>>(int(blocks), partials, float(m), loss);
+    GS2D_TRY(launch(k_loss_partial<false>, dim3(int(blocks)), dim3(kLossThreads), 0, s, m, image, target, scale, d_image, partials));
+  GS2D_TRY(launch(k_loss_final, dim3(1), dim3(kLossThreads), 0, s, int(blocks), partials, float(m), loss));
   return cudaGetLastError();
 }
 
@@ -161,10 +163,16 @@ extern "C" gs2d_status gs2d_loss_l2_noalloc(int32_t height, int32_t width, const
   if (blocks > gs2d::kLossMaxBlocks) blocks = gs2d::kLossMaxBlocks;
   const float scale = float(2.0 / double(m));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (vec)
-    k_loss_partial<true><<<int(blocks), kLossThreads, 0, s>>>(m, image, target, scale, d_image, partials);
-  else
-    k_loss_partial<false><<<int(blocks), kLossThreads, 0, s>>>(m, image, target, scale, d_image, partials);
-  k_loss_final<<<1, kLossThreads, 0, s>>>(int(blocks), partials, float(m), loss);
+  cudaError_t e;
+  if (vec) {
+    e = launch(k_loss_partial<true>, dim3(int(blocks)), dim3(kLossThreads), 0, s, m, image, target,
+               scale, d_image, partials);
+  } else {
+    e = launch(k_loss_partial<false>, dim3(int(blocks)), dim3(kLossThreads), 0, s, m, image, target,
+               scale, d_image, partials);
+  }
+  if (e != cudaSuccess) return GS2D_ERR_CUDA;
+  e = launch(k_loss_final, dim3(1), dim3(kLossThreads), 0, s, int(blocks), partials, float(m), loss);
+  if (e != cudaSuccess) return GS2D_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? GS2D_OK : GS2D_ERR_CUDA;
 }

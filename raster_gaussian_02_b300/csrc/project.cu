@@ -16,6 +16,7 @@ k_project(gs2d_config c, int n, const float* __restrict__ xy, const float* __res
           const float* __restrict__ rgb, const float* __restrict__ depth,
           const float* __restrict__ opacity, float4* __restrict__ rec, int4* __restrict__ rect,
           int* __restrict__ count) {
+  pdl_enter();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const float mx = xy[2 * i], my = xy[2 * i + 1];
@@ -96,6 +97,7 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
          float* __restrict__ d_xy, float* __restrict__ d_chol, float* __restrict__ d_rgb,
          float* __restrict__ d_opacity, int T, const float4* __restrict__ bg_partials,
          float* __restrict__ d_bg) {
+  pdl_enter();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   const bool bad = (hdr->flags & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) != 0;
   if (i < n) {
@@ -168,9 +170,9 @@ cudaError_t launch_project(const gs2d_config& c, int n, const float* xy, const f
                            const float* rgb, const float* depth, const float* opacity,
                            gs2d_record* rec, int* rect, int* count, cudaStream_t s) {
   if (n > 0)
-    k_project<<<(n + 255) / 256, 256, 0, s>>>(c, n, xy, chol, rgb, depth, opacity,
+    GS2D_TRY(launch(k_project, dim3((n + 255) / 256), dim3(256), 0, s, c, n, xy, chol, rgb, depth, opacity,
                                               reinterpret_cast<float4*>(rec),
-                                              reinterpret_cast<int4*>(rect), count);
+                                              reinterpret_cast<int4*>(rect), count));
   return cudaGetLastError();
 }
 
@@ -182,16 +184,14 @@ cudaError_t launch_gather(const gs2d_config& c, int n, const float* chol, const 
   const int blocks = n > 0 ? (n + 255) / 256 : 1;
   const Header* hdr = reinterpret_cast<const Header*>(ws);
   if (c.mode == GS2D_MODE_COMPOSITE)
-    k_gather<true><<<blocks, 256, 0, s>>>(
-        n, chol, reinterpret_cast<const float4*>(rec), reinterpret_cast<const int4*>(rect),
+    GS2D_TRY(launch(k_gather<true>, dim3(blocks), dim3(256), 0, s, n, chol, reinterpret_cast<const float4*>(rec), reinterpret_cast<const int4*>(rect),
         reinterpret_cast<const int*>(ws + L.offsets), reinterpret_cast<const float4*>(ws + L.partials),
         hdr, d_xy, d_chol, d_rgb, d_opacity, T, reinterpret_cast<const float4*>(ws + L.bg_partials),
-        d_bg);
+        d_bg));
   else
-    k_gather<false><<<blocks, 256, 0, s>>>(
-        n, chol, reinterpret_cast<const float4*>(rec), reinterpret_cast<const int4*>(rect),
+    GS2D_TRY(launch(k_gather<false>, dim3(blocks), dim3(256), 0, s, n, chol, reinterpret_cast<const float4*>(rec), reinterpret_cast<const int4*>(rect),
         reinterpret_cast<const int*>(ws + L.offsets), reinterpret_cast<const float4*>(ws + L.partials),
-        hdr, d_xy, d_chol, d_rgb, nullptr, T, nullptr, nullptr);
+        hdr, d_xy, d_chol, d_rgb, nullptr, T, nullptr, nullptr));
   return cudaGetLastError();
 }
 

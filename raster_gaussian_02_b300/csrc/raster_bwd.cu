@@ -64,6 +64,7 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, const Header* __restrict__ hdr,
                  const int4* __restrict__ rect, const int* __restrict__ sorted_gid,
                  const int* __restrict__ offsets, const float* __restrict__ d_image,
                  float4* __restrict__ partials) {
+  pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   BwdSumSmem& sm = *reinterpret_cast<BwdSumSmem*>(smem_raw);
   __shared__ int warp_tot[8];
@@ -254,6 +255,7 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
                   const float* __restrict__ bg, const float* __restrict__ t_final,
                   const int* __restrict__ last, const float* __restrict__ d_image,
                   float4* __restrict__ partials, float4* __restrict__ bg_partials) {
+  pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   CompStage& sm = *reinterpret_cast<CompStage*>(smem_raw);
   const int tile = blockIdx.x;
@@ -420,20 +422,15 @@ cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
     cudaError_t e = cudaFuncSetAttribute(k_render_bwd_comp, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;
-    k_render_bwd_comp<<<T, kBwdCompThreads, smem, s>>>(
-        c, tiles_x(c), r, rc, rg, sorted_gid, offsets, bg, t_final, last, d_image, partials,
-        reinterpret_cast<float4*>(ws + L.bg_partials));
+    GS2D_TRY(launch(k_render_bwd_comp, dim3(T), dim3(kBwdCompThreads), smem, s, c, tiles_x(c), r, rc, rg, sorted_gid, offsets, bg, t_final, last, d_image, partials,
+        reinterpret_cast<float4*>(ws + L.bg_partials)));
   } else {
     const size_t smem = sizeof(BwdSumSmem);
     cudaError_t e = cudaFuncSetAttribute(k_render_bwd_sum, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    k_render_bwd_sum<<<4 * sms, kChunkPairs, smem, s>>>(
-        c, tiles_x(c), reinterpret_cast<const Header*>(ws), ws, r, rc, sorted_gid, offsets,
-        d_image, partials);
+    GS2D_TRY(launch(k_render_bwd_sum, dim3(4 * sm_count()), dim3(kChunkPairs), smem, s, c, tiles_x(c), reinterpret_cast<const Header*>(ws), ws, r, rc, sorted_gid, offsets,
+        d_image, partials));
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

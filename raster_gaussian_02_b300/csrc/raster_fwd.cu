@@ -5,9 +5,7 @@
 // each warp then culls a window of 64 staged entries with one lane per
 // entry, keeping, in list order, those whose pixel box meets its sub-block
 // together with a 32-bit mask of the warp's lanes inside the box, so that
-// the per-pixel box test is a single bit test.  Sum mode splits each staged
-// round of the list between kGroups groups of eight warps that cover the
-// same tile, and adds the groups' partial sums in a fixed order at the end.
+// the per-pixel box test is a single bit test.
 //
 // Sum (GaussianImage project page, Overview: accumulated-sum rendering;
 // FlashImgs README: additive RGB, gate folded into the colour):
@@ -29,28 +27,34 @@ struct Staged {
   float4 cr;  // C, r, g, b
 };
 
-template <int kGroups>
+template <int kWarps>
 struct SumSmem {
-  Staged g[256 * kGroups];
-  uint2 box[256 * kGroups];
-  uint2 list[8 * kGroups][kWindow];  // (staged index, lane mask)
-  float3 part[kGroups > 1 ? kGroups - 1 : 1][kTilePixels];
+  Staged g[256];
+  uint2 box[256];
+  uint2 list[kWarps][kWindow];  // (staged index, lane mask)
 };
 
-template <int kGroups>
-__global__ void __launch_bounds__(256 * kGroups, 2048 / (256 * kGroups))
+// A block of kWarps warps renders 8/kWarps of a tile (kWarps 8: the whole
+// tile; 4: a 16x8 half; 2: a 16x4 quarter).  Each warp owns an 8x4 pixel
+// sub-block.  Smaller blocks stage the tile's records more than once but let
+// the scheduler spread the heavy tiles (Gaussians crowd along image edges)
+// over more SMs.
+template <int kWarps>
+__global__ void __launch_bounds__(kWarps * 32, kWarps == 8 ? 8 : (kWarps == 4 ? 10 : 20))
 k_render_fwd_sum(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
                  const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
                  float* __restrict__ image) {
-  constexpr int kThreads = 256 * kGroups;
+  constexpr int kParts = 8 / kWarps;
+  constexpr int kThreads = kWarps * 32;
+  pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  SumSmem<kGroups>& sm = *reinterpret_cast<SumSmem<kGroups>*>(smem_raw);
-  const int tile = blockIdx.x;
+  SumSmem<kWarps>& sm = *reinterpret_cast<SumSmem<kWarps>*>(smem_raw);
+  const int tile = blockIdx.x / kParts;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int group = warp >> 3, wg = warp & 7;
-  const int bx0 = tx * kTile + (wg & 1) * 8;
-  const int by0 = ty * kTile + (wg >> 1) * 4;
+  const int sub = (blockIdx.x % kParts) * kWarps + warp;  // 8x4 sub-block 0..7 of the tile
+  const int bx0 = tx * kTile + (sub & 1) * 8;
+  const int by0 = ty * kTile + (sub >> 1) * 4;
   const int px = bx0 + (lane & 7), py = by0 + (lane >> 3);
   const float pxf = float(px) + 0.5f, pyf = float(py) + 0.5f;
   const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
@@ -59,19 +63,18 @@ k_render_fwd_sum(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
   uint2* list = sm.list[warp];
 
   float ar = 0.f, ag = 0.f, ab = 0.f;
-  for (int rb = rg.x; rb < rg.y; rb += kThreads) {
-    const int cnt = min(kThreads, rg.y - rb);
-    if (tid < cnt) {
-      const float4* r = rec + 3 * size_t(sorted_gid[rb + tid]);
+  for (int rb = rg.x; rb < rg.y; rb += 256) {
+    const int cnt = min(256, rg.y - rb);
+    for (int k = tid; k < cnt; k += kThreads) {
+      const float4* r = rec + 3 * size_t(sorted_gid[rb + k]);
       const float4 p0 = r[0], p1 = r[1], p2 = r[2];
-      sm.g[tid].mc = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
-      sm.g[tid].cr = p1;
-      sm.box[tid] = make_uint2(__float_as_uint(p2.x), __float_as_uint(p2.y));
+      sm.g[k].mc = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
+      sm.g[k].cr = p1;
+      sm.box[k] = make_uint2(__float_as_uint(p2.x), __float_as_uint(p2.y));
     }
     __syncthreads();
-    const int lo = (group * cnt) / kGroups, hi = ((group + 1) * cnt) / kGroups;
-    for (int wb = lo; wb < hi; wb += kWindow) {
-      const int wend = min(wb + kWindow, hi);
+    for (int wb = 0; wb < cnt; wb += kWindow) {
+      const int wend = min(wb + kWindow, cnt);
       int nl = 0;
 #pragma unroll
       for (int j0 = 0; j0 < kWindow; j0 += 32) {
@@ -114,20 +117,6 @@ k_render_fwd_sum(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
     }
     __syncthreads();
   }
-  // Fixed-order combination of the groups' partial sums.
-  const int pix = (py - ty * kTile) * kTile + (px - tx * kTile);
-  if (kGroups > 1) {
-    if (group > 0) sm.part[group - 1][pix] = make_float3(ar, ag, ab);
-    __syncthreads();
-    if (group > 0) return;
-#pragma unroll
-    for (int g = 0; g < kGroups - 1; ++g) {
-      const float3 v = sm.part[g][pix];
-      ar += v.x;
-      ag += v.y;
-      ab += v.z;
-    }
-  }
   if (px < c.width && py < c.height) {
     const size_t HW = size_t(c.width) * c.height;
     const size_t p = size_t(py) * c.width + px;
@@ -149,6 +138,7 @@ k_render_fwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
                   const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
                   const float* __restrict__ bg, float* __restrict__ image,
                   float* __restrict__ t_final, int* __restrict__ last) {
+  pdl_enter();
   __shared__ CompSmem sm;
   const int tile = blockIdx.x;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
@@ -231,9 +221,16 @@ k_render_fwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
   }
 }
 
-// One group of eight warps per tile: splitting the list across 2 or 4 groups
-// measured no faster on a B300 (the per-warp fixed costs grow with the split).
-constexpr int kSumGroups = 1;
+template <int kWarps>
+cudaError_t launch_fwd_sum(const gs2d_config& c, const float4* r, const int2* rg, const int* sorted_gid,
+                           float* image, cudaStream_t s) {
+  const size_t smem = sizeof(SumSmem<kWarps>);
+  auto kern = k_render_fwd_sum<kWarps>;
+  GS2D_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+  GS2D_TRY(launch(kern, dim3(num_tiles(c) * (8 / kWarps)), dim3(kWarps * 32), smem, s, c, tiles_x(c), r,
+                  rg, sorted_gid, image));
+  return cudaSuccess;
+}
 
 }  // namespace
 
@@ -244,14 +241,17 @@ cudaError_t launch_render_fwd(const gs2d_config& c, const gs2d_record* rec, cons
   const float4* r = reinterpret_cast<const float4*>(rec);
   const int2* rg = reinterpret_cast<const int2*>(ranges);
   if (c.mode == GS2D_MODE_COMPOSITE) {
-    k_render_fwd_comp<<<T, 256, 0, s>>>(c, tiles_x(c), r, rg, sorted_gid, bg, image, t_final, last);
+    GS2D_TRY(launch(k_render_fwd_comp, dim3(T), dim3(256), 0, s, c, tiles_x(c), r, rg, sorted_gid, bg, image, t_final, last));
   } else {
-    const size_t smem = sizeof(SumSmem<kSumGroups>);
-    cudaError_t e = cudaFuncSetAttribute(k_render_fwd_sum<kSumGroups>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    k_render_fwd_sum<kSumGroups><<<T, 256 * kSumGroups, smem, s>>>(c, tiles_x(c), r, rg, sorted_gid,
-                                                                  image);
+    // Half-tile blocks when the whole-tile blocks would fill at most two
+    // waves of the GPU (8 resident per SM): the heavy tiles then spread over
+    // more SMs.  With more tiles than that, staging each tile's records
+    // twice costs more than the balance gains (measured on a B300: 768x512
+    // 29.3 -> 27.2 us; 2048x2048 156 -> 168 us).
+    if (T <= 2 * 8 * sm_count())
+      GS2D_TRY(launch_fwd_sum<4>(c, r, rg, sorted_gid, image, s));
+    else
+      GS2D_TRY(launch_fwd_sum<8>(c, r, rg, sorted_gid, image, s));
   }
   return cudaGetLastError();
 }
