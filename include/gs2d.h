@@ -109,8 +109,10 @@ typedef struct gs2d_record {
 } gs2d_record;
 
 /*
- * Bytes of device workspace needed by gs2d_bin_and_sort, gs2d_loss_l2 and
- * gs2d_render_bwd for this configuration, n Gaussians and a pair capacity.
+ * Bytes of device workspace needed by gs2d_bin_and_sort, gs2d_loss_l2,
+ * gs2d_render_bwd and gs2d_render_fwd_bwd_l2 for this configuration, n
+ * Gaussians and a pair capacity (in sum mode it includes room for the fused
+ * pass's dL/dC, 12 bytes per pixel).
  * The same workspace must be passed to gs2d_bin_and_sort and to the
  * gs2d_render_bwd that follows it (the backward reads the per-Gaussian
  * pair offsets the binning left there).  The contents need no
@@ -215,6 +217,34 @@ GS2D_API gs2d_status gs2d_render_bwd(const gs2d_config* cfg, int32_t n, const fl
                             const float* d_image, float* d_xy, float* d_chol, float* d_rgb,
                             float* d_opacity, float* d_background, void* workspace,
                             gs2d_stream_t stream);
+
+/*
+ * Fused training pass: what gs2d_render_fwd, gs2d_loss_l2 and
+ * gs2d_render_bwd compute, with dL/dC = 2 (C - target) / (3HW) formed at
+ * each pixel as soon as its colour is known (FlashImgs README, Project
+ * Structure: training-time rasterization, fused fwd/bwd).  Composite: one
+ * per-tile kernel renders and back-propagates, keeping dL/dC on chip.  Sum:
+ * the forward kernel also takes the loss and leaves dL/dC in the workspace
+ * for the pair-parallel backward.  Results equal the three separate calls
+ * up to the order of floating-point additions; every sum is taken in a
+ * fixed order, so they are bit-reproducible.
+ *   chol, rec, rect      as for gs2d_render_bwd
+ *   tile_ranges, sorted_gid, workspace   from gs2d_bin_and_sort
+ *   background[3]        composite (NULL: black; ignored in sum mode)
+ *   target[3,H,W]        the image to fit
+ *   image[3,H,W]         out, may be NULL (not written)
+ *   loss                 out: one float (device), (1/(3HW)) sum (C - target)^2
+ *   d_xy[n,2], d_chol[n,3], d_rgb[n,3]   out, every element written
+ *   d_opacity[n], d_background[3]        out, composite (may be NULL)
+ * Errors as for gs2d_render_bwd; target and loss must be non-NULL.
+ */
+GS2D_API gs2d_status gs2d_render_fwd_bwd_l2(const gs2d_config* cfg, int32_t n, const float* chol,
+                                            const gs2d_record* rec, const int32_t* rect,
+                                            const int32_t* tile_ranges, const int32_t* sorted_gid,
+                                            const float* background, const float* target,
+                                            float* image, float* loss, float* d_xy, float* d_chol,
+                                            float* d_rgb, float* d_opacity, float* d_background,
+                                            void* workspace, gs2d_stream_t stream);
 
 /*
  * The L2 loss of gs2d_loss_l2 for callers that cannot supply a workspace.

@@ -1,0 +1,112 @@
+// Fused training pass: render, L2 loss and backward (FlashImgs README,
+// Project Structure: training-time rasterization with fused forward/backward).
+// dL/dC = 2 (C - target) / (3HW) is formed at each pixel as soon as the
+// pixel's colour is known, so no separate loss pass reads the image back.
+// Results equal the separate forward, loss and backward calls up to the
+// order of floating-point additions; the per-pair partials go to the same
+// emission slots and the same gather kernel sums them per Gaussian.
+//
+// Composite: one block per tile runs the forward and the backward bodies
+// back to back, the pixel's transmittance, last contributor and dL/dC kept
+// in registers; neither dL/dC nor (image NULL) the image touches memory.
+// Sum: the forward also takes the loss and writes dL/dC to the workspace,
+// then the pair-parallel backward runs.  (A per-tile sum backward, one warp
+// per pair with dL/dC kept in shared memory, measured 1.4-1.8x slower on a
+// B300: every pair ends in a serial shuffle reduction and a dependent
+// load, and the tile's pairs cannot spread over other SMs.)
+#include "tile_bodies.cuh"
+
+namespace gs2d {
+
+namespace {
+
+struct FusedCompSmem {
+  union {
+    CompSmem f;
+    CompStage b;
+  } u;
+  float red[8];
+};
+
+__global__ void __launch_bounds__(256)
+k_fused_comp(gs2d_config c, int tiles_x, float scale, const float4* __restrict__ rec,
+             const int4* __restrict__ rect, const int2* __restrict__ ranges,
+             const int* __restrict__ sorted_gid, const int* __restrict__ offsets,
+             const float* __restrict__ bg, const float* __restrict__ target,
+             float* __restrict__ image, float4* __restrict__ partials,
+             float4* __restrict__ tile_partials, float* __restrict__ loss_partials) {
+  pdl_enter();
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  FusedCompSmem& sm = *reinterpret_cast<FusedCompSmem*>(smem_raw);
+  const int tile = blockIdx.x;
+  const int tx = tile % tiles_x, ty = tile / tiles_x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bx0 = tx * kTile + (warp & 1) * 8;
+  const int by0 = ty * kTile + (warp >> 1) * 4;
+  const int px = bx0 + (lane & 7), py = by0 + (lane >> 3);
+  const float pxf = float(px) + 0.5f, pyf = float(py) + 0.5f;
+  const bool inside = px < c.width && py < c.height;
+  const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
+  const int2 rg = ranges[tile];
+  // every thread has passed its last read of the forward's staging area when
+  // comp_tile_forward returns (each round ends at a block barrier)
+  const CompFwdOut o = comp_tile_forward(sm.u.f, c, rg, bx0, by0, pxf, pyf, inside, kk, rec, sorted_gid);
+  float er = 0.f, eg = 0.f, eb = 0.f;
+  if (inside) {
+    const size_t HW = size_t(c.width) * c.height;
+    const size_t p = size_t(py) * c.width + px;
+    float ar = o.r, ag = o.g, ab = o.b;
+    if (bg) {
+      ar = fmaf(o.T, bg[0], ar);
+      ag = fmaf(o.T, bg[1], ag);
+      ab = fmaf(o.T, bg[2], ab);
+    }
+    if (image) {
+      image[p] = ar;
+      image[HW + p] = ag;
+      image[2 * HW + p] = ab;
+    }
+    er = ar - target[p];
+    eg = ag - target[HW + p];
+    eb = ab - target[2 * HW + p];
+  }
+  const float tl = block_sum_ordered<8>(fmaf(eb, eb, fmaf(eg, eg, er * er)), sm.red);
+  if (threadIdx.x == 0) loss_partials[tile] = tl;
+  comp_tile_backward(sm.u.b, c, tile, tx, ty, rg, bx0, by0, pxf, pyf, inside, kk, o.T, o.last,
+                     er * scale, eg * scale, eb * scale, bg, rec, rect, sorted_gid, offsets, partials,
+                     tile_partials);
+}
+
+}  // namespace
+
+cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* chol,
+                                   const gs2d_record* rec, const int* rect, const int* ranges,
+                                   const int* sorted_gid, const float* bg, const float* target,
+                                   float* image, float* loss, float* d_xy, float* d_chol,
+                                   float* d_rgb, float* d_opacity, float* d_bg, unsigned char* ws,
+                                   cudaStream_t s) {
+  const Layout L = layout_of(c, n, 0);
+  const int T = num_tiles(c);
+  const float4* r = reinterpret_cast<const float4*>(rec);
+  const int4* rc = reinterpret_cast<const int4*>(rect);
+  const int2* rg = reinterpret_cast<const int2*>(ranges);
+  const int* offsets = reinterpret_cast<const int*>(ws + L.offsets);
+  float4* tp = reinterpret_cast<float4*>(ws + L.tile_partials);
+  // the same scale as the L2 loss kernel: 2 / (3HW)
+  const float scale = float(2.0 / (3.0 * double(c.width) * double(c.height)));
+  float* lp = reinterpret_cast<float*>(ws + L.loss_partials);
+  if (c.mode == GS2D_MODE_COMPOSITE) {
+    const size_t smem = sizeof(FusedCompSmem);
+    GS2D_TRY(cudaFuncSetAttribute(k_fused_comp, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+    GS2D_TRY(launch(k_fused_comp, dim3(T), dim3(256), smem, s, c, tiles_x(c), scale, r, rc, rg, sorted_gid,
+                    offsets, bg, target, image, reinterpret_cast<float4*>(ws + L.partials), tp, lp));
+    return launch_gather(c, n, chol, rec, rect, ws, d_xy, d_chol, d_rgb, d_opacity, d_bg, loss, T, s);
+  }
+  float* d_image = reinterpret_cast<float*>(ws + L.dimage);
+  int blocks = 0;
+  GS2D_TRY(launch_render_fwd_loss(c, rec, ranges, sorted_gid, target, scale, image, d_image, lp, &blocks, s));
+  return launch_render_bwd(c, n, chol, rec, rect, ranges, sorted_gid, nullptr, nullptr, nullptr, d_image,
+                           d_xy, d_chol, d_rgb, nullptr, nullptr, ws, s, loss, blocks);
+}
+
+}  // namespace gs2d

@@ -139,6 +139,34 @@ gs2d_status gs2d_render_bwd(const gs2d_config* cfg, int32_t n, const float* chol
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
+gs2d_status gs2d_render_fwd_bwd_l2(const gs2d_config* cfg, int32_t n, const float* chol,
+                                   const gs2d_record* rec, const int32_t* rect,
+                                   const int32_t* tile_ranges, const int32_t* sorted_gid,
+                                   const float* background, const float* target, float* image,
+                                   float* loss, float* d_xy, float* d_chol, float* d_rgb,
+                                   float* d_opacity, float* d_background, void* workspace,
+                                   gs2d_stream_t stream) {
+  if (!config_ok(cfg) || n < 0) return GS2D_ERR_INVALID_ARG;
+  const bool comp = cfg->mode == GS2D_MODE_COMPOSITE;
+  if (!tile_ranges || !target || !loss || !workspace || !aligned(tile_ranges, 16) ||
+      !aligned(target, 4) || !aligned(loss, 4) || !aligned(workspace, 16))
+    return GS2D_ERR_INVALID_ARG;
+  if (n > 0 && (!chol || !rec || !rect || !sorted_gid || !d_xy || !d_chol || !d_rgb ||
+                !aligned(rec, 16) || !aligned(rect, 16) || !aligned(chol, 4) ||
+                !aligned(sorted_gid, 4) || !aligned(d_xy, 4) || !aligned(d_chol, 4) ||
+                !aligned(d_rgb, 4)))
+    return GS2D_ERR_INVALID_ARG;
+  if ((image && !aligned(image, 4)) || (d_opacity && !aligned(d_opacity, 4)) ||
+      (d_background && !aligned(d_background, 4)) || (background && !aligned(background, 4)))
+    return GS2D_ERR_INVALID_ARG;
+  return from_cuda(launch_render_fused_l2(*cfg, n, chol, rec, rect, tile_ranges, sorted_gid,
+                                          comp ? background : nullptr, target, image, loss, d_xy,
+                                          d_chol, d_rgb, comp ? d_opacity : nullptr,
+                                          comp ? d_background : nullptr,
+                                          static_cast<unsigned char*>(workspace),
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 gs2d_status gs2d_read_status(const void* workspace, int64_t* pairs, uint32_t* flags,
                              gs2d_stream_t stream) {
   if (!workspace || !aligned(workspace, 16)) return GS2D_ERR_INVALID_ARG;

@@ -48,7 +48,7 @@ constexpr int kScanItems = kScanThreads;  // Gaussians per scan block, one per t
 constexpr int kRadixThreads = 256;
 
 struct Layout {
-  size_t block_off, offsets, bg_partials, partials, tables, keys_a, keys_b, vals_tmp, total;
+  size_t block_off, offsets, tile_partials, loss_partials, dimage, partials, tables, keys_a, keys_b, vals_tmp, total;
   int passes, digit_bits, tile_bits, key_bits, key_bytes, partial_floats, radix_per_thread;
   long long partitions, partitions4;  // radix partitions, and rounded up to a multiple of 4
 };
@@ -99,8 +99,12 @@ inline Layout layout_of(const gs2d_config& c, long long n, long long cap) {
   o = align256(o + 8 * size_t((n + kScanItems - 1) / kScanItems + 1));
   L.offsets = o;
   o = align256(o + 4 * size_t(n));
-  L.bg_partials = o;
-  if (comp) o = align256(o + 16 * size_t(T));
+  L.tile_partials = o;  // per tile: background gradient (x, y, z)
+  o = align256(o + 16 * size_t(T));
+  L.loss_partials = o;  // fused pass: per block (at most two per tile) loss sums
+  o = align256(o + 8 * size_t(T));
+  L.dimage = o;  // fused pass, sum mode: dL/dC [3,H,W]
+  if (!comp) o = align256(o + 12 * size_t(c.width) * size_t(c.height));
   L.partials = o;
   o = align256(o + 4 * size_t(L.partial_floats) * size_t(cap));
   L.tables = o;
@@ -219,15 +223,33 @@ cudaError_t launch_render_fwd(const gs2d_config& c, const gs2d_record* rec, cons
 cudaError_t launch_loss_l2(int h, int w, const float* image, const float* target, float* loss,
                            float* d_image, unsigned char* ws, cudaStream_t s);
 
+// loss (may be NULL): the fused pass's loss, the sum of the first
+// loss_blocks entries of the workspace's loss partials divided by 3HW.
 cudaError_t launch_gather(const gs2d_config& c, int n, const float* chol, const gs2d_record* rec,
                           const int* rect, const unsigned char* ws, float* d_xy, float* d_chol,
-                          float* d_rgb, float* d_opacity, float* d_bg, cudaStream_t s);
+                          float* d_rgb, float* d_opacity, float* d_bg, float* loss,
+                          int loss_blocks, cudaStream_t s);
 
 cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
                               const gs2d_record* rec, const int* rect, const int* ranges,
                               const int* sorted_gid, const float* bg, const float* t_final,
                               const int* last, const float* d_image, float* d_xy, float* d_chol,
                               float* d_rgb, float* d_opacity, float* d_bg, unsigned char* ws,
-                              cudaStream_t s);
+                              cudaStream_t s, float* loss = nullptr, int loss_blocks = 0);
+
+// Sum forward that also takes the L2 loss: writes image (if non-NULL),
+// dL/dC = scale (C - target) to d_image and one loss partial per block to
+// loss_partials; returns the number of blocks in *blocks.
+cudaError_t launch_render_fwd_loss(const gs2d_config& c, const gs2d_record* rec, const int* ranges,
+                                   const int* sorted_gid, const float* target, float scale,
+                                   float* image, float* d_image, float* loss_partials, int* blocks,
+                                   cudaStream_t s);
+
+cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* chol,
+                                   const gs2d_record* rec, const int* rect, const int* ranges,
+                                   const int* sorted_gid, const float* bg, const float* target,
+                                   float* image, float* loss, float* d_xy, float* d_chol,
+                                   float* d_rgb, float* d_opacity, float* d_bg, unsigned char* ws,
+                                   cudaStream_t s);
 
 }  // namespace gs2d

@@ -88,15 +88,19 @@ k_project(gs2d_config c, int n, const float* __restrict__ xy, const float* __res
 //   dA/da = -2A/a,        dA/db = 2b/(a^2 c^2),  dA/dc = -2b^2/(a^2 c^3)
 //   dB/da = b/(a^2 c^2),  dB/db = -1/(a c^2),    dB/dc = 2b/(a c^3)
 //   dC/dc = -2/c^3;       d(xy) = d(mean).
-// The last block also sums the per-tile background partials (composite).
+// The last block also sums, in a fixed order, the per-tile background
+// partials (composite, d_bg non-null) and the fused pass's per-block loss
+// partials (loss non-null; the total is divided by m, the number of image
+// values).
 template <bool kComposite>
 __global__ void __launch_bounds__(256)
 k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
          const int4* __restrict__ rect, const int* __restrict__ offsets,
          const float4* __restrict__ partials, const Header* __restrict__ hdr,
          float* __restrict__ d_xy, float* __restrict__ d_chol, float* __restrict__ d_rgb,
-         float* __restrict__ d_opacity, int T, const float4* __restrict__ bg_partials,
-         float* __restrict__ d_bg) {
+         float* __restrict__ d_opacity, int T, const float4* __restrict__ tile_partials,
+         float* __restrict__ d_bg, const float* __restrict__ loss_partials, int loss_blocks,
+         float* __restrict__ loss, float m) {
   pdl_enter();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   const bool bad = (hdr->flags & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) != 0;
@@ -138,28 +142,34 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
     d_rgb[3 * i + 2] = s[7];
     if (kComposite && d_opacity) d_opacity[i] = s[8];
   }
-  if (kComposite && d_bg && blockIdx.x == gridDim.x - 1) {
-    // fixed-order reduction of the per-tile background partials
-    __shared__ float red[3][256];
-    float x = 0.f, y = 0.f, z = 0.f;
-    if (!bad)
+  if ((d_bg || loss) && blockIdx.x == gridDim.x - 1) {
+    // fixed-order reduction of the per-tile partials
+    __shared__ float red[4][256];
+    float x = 0.f, y = 0.f, z = 0.f, l = 0.f;
+    if (d_bg)
       for (int t = threadIdx.x; t < T; t += blockDim.x) {
-        const float4 v = bg_partials[t];
+        const float4 v = tile_partials[t];
         x += v.x; y += v.y; z += v.z;
       }
+    if (loss)
+      for (int t = threadIdx.x; t < loss_blocks; t += blockDim.x) l += loss_partials[t];
     red[0][threadIdx.x] = x;
     red[1][threadIdx.x] = y;
     red[2][threadIdx.x] = z;
+    red[3][threadIdx.x] = l;
     __syncthreads();
     for (int h = blockDim.x / 2; h > 0; h >>= 1) {
       if (threadIdx.x < h)
-        for (int q = 0; q < 3; ++q) red[q][threadIdx.x] += red[q][threadIdx.x + h];
+        for (int q = 0; q < 4; ++q) red[q][threadIdx.x] += red[q][threadIdx.x + h];
       __syncthreads();
     }
     if (threadIdx.x == 0) {
-      d_bg[0] = red[0][0];
-      d_bg[1] = red[1][0];
-      d_bg[2] = red[2][0];
+      if (d_bg) {
+        d_bg[0] = bad ? 0.f : red[0][0];
+        d_bg[1] = bad ? 0.f : red[1][0];
+        d_bg[2] = bad ? 0.f : red[2][0];
+      }
+      if (loss) *loss = red[3][0] / m;
     }
   }
 }
@@ -178,20 +188,26 @@ cudaError_t launch_project(const gs2d_config& c, int n, const float* xy, const f
 
 cudaError_t launch_gather(const gs2d_config& c, int n, const float* chol, const gs2d_record* rec,
                           const int* rect, const unsigned char* ws, float* d_xy, float* d_chol,
-                          float* d_rgb, float* d_opacity, float* d_bg, cudaStream_t s) {
+                          float* d_rgb, float* d_opacity, float* d_bg, float* loss,
+                          int loss_blocks, cudaStream_t s) {
   const Layout L = layout_of(c, n, 0);
   const int T = num_tiles(c);
   const int blocks = n > 0 ? (n + 255) / 256 : 1;
   const Header* hdr = reinterpret_cast<const Header*>(ws);
+  const float m = float(3.0 * double(c.width) * double(c.height));
+  const float4* tp = reinterpret_cast<const float4*>(ws + L.tile_partials);
+  const float* lp = reinterpret_cast<const float*>(ws + L.loss_partials);
+  const int* offsets = reinterpret_cast<const int*>(ws + L.offsets);
+  const float4* partials = reinterpret_cast<const float4*>(ws + L.partials);
+  const float4* r = reinterpret_cast<const float4*>(rec);
+  const int4* rc = reinterpret_cast<const int4*>(rect);
   if (c.mode == GS2D_MODE_COMPOSITE)
-    GS2D_TRY(launch(k_gather<true>, dim3(blocks), dim3(256), 0, s, n, chol, reinterpret_cast<const float4*>(rec), reinterpret_cast<const int4*>(rect),
-        reinterpret_cast<const int*>(ws + L.offsets), reinterpret_cast<const float4*>(ws + L.partials),
-        hdr, d_xy, d_chol, d_rgb, d_opacity, T, reinterpret_cast<const float4*>(ws + L.bg_partials),
-        d_bg));
+    GS2D_TRY(launch(k_gather<true>, dim3(blocks), dim3(256), 0, s, n, chol, r, rc, offsets, partials, hdr,
+                    d_xy, d_chol, d_rgb, d_opacity, T, tp, d_bg, lp, loss_blocks, loss, m));
   else
-    GS2D_TRY(launch(k_gather<false>, dim3(blocks), dim3(256), 0, s, n, chol, reinterpret_cast<const float4*>(rec), reinterpret_cast<const int4*>(rect),
-        reinterpret_cast<const int*>(ws + L.offsets), reinterpret_cast<const float4*>(ws + L.partials),
-        hdr, d_xy, d_chol, d_rgb, nullptr, T, nullptr, nullptr));
+    GS2D_TRY(launch(k_gather<false>, dim3(blocks), dim3(256), 0, s, n, chol, r, rc, offsets, partials, hdr,
+                    d_xy, d_chol, d_rgb, static_cast<float*>(nullptr), T, tp,
+                    static_cast<float*>(nullptr), lp, loss_blocks, loss, m));
   return cudaGetLastError();
 }
 

@@ -15,7 +15,7 @@
 //     dL/dalpha = sum_k g_k (rgb_k T - S_k / (1 - alpha)),
 //     dL/do = w dL/dalpha,  dL/dw = o dL/dalpha,  dL/drgb_k = g_k alpha T,
 //     dL/dbg_k = sum over pixels of T_final g_k.
-#include "gs2d_internal.cuh"
+#include "tile_bodies.cuh"
 
 namespace gs2d {
 
@@ -201,78 +201,29 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, const Header* __restrict__ hdr,
 }
 
 constexpr int kBwdCompThreads = 256;
-constexpr int kCompChunk = 128;
-constexpr int kCompVals = 9;
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Butterfly reduce-scatter of eight per-lane values over the warp: returns,
-// in every lane, the warp total of value ((lane >> 2) & 7) in the order
-// v[0..7] (lane bit 4 picks values 4-7, bit 3 values +2, bit 2 values +1).
-__device__ __forceinline__ float warp_reduce_scatter8(const float (&v)[8], int lane) {
-  float a[4], b[2];
-  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float keep = u16 ? v[i + 4] : v[i], send = u16 ? v[i] : v[i + 4];
-    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float keep = u8 ? a[i + 2] : a[i], send = u8 ? a[i] : a[i + 2];
-    b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-  }
-  float c = (u4 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, u4 ? b[0] : b[1], 4);
-  c += __shfl_xor_sync(0xffffffffu, c, 2);
-  c += __shfl_xor_sync(0xffffffffu, c, 1);
-  return c;
-}
-
-struct CompStage {
-  float4 mc[kCompChunk];  // mean_x, mean_y, A, 2B
-  float4 cr[kCompChunk];  // C, r, g, b
-  uint2 box[kCompChunk];
-  float op[kCompChunk];
-  int gid[kCompChunk];
-  uint2 list[8][kCompChunk];            // (chunk index, lane mask) per warp
-  float acc[8][kCompChunk][kCompVals];  // per-warp partials, summed over warps in order
-  float bgred[8][3];
-};
 
 // Composite: one block per tile, one pixel per thread (8x4 sub-block per
 // warp as in the forward), walking the tile's list back to front from each
-// pixel's last contributor.  Per (warp, Gaussian) the nine partial
-// derivatives are reduced over the warp and kept in a per-warp slot; the
-// slots are summed in warp order per chunk entry.
+// pixel's last contributor (comp_tile_backward).
 __global__ void __launch_bounds__(kBwdCompThreads)
 k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
                   const int4* __restrict__ rect, const int2* __restrict__ ranges,
                   const int* __restrict__ sorted_gid, const int* __restrict__ offsets,
                   const float* __restrict__ bg, const float* __restrict__ t_final,
                   const int* __restrict__ last, const float* __restrict__ d_image,
-                  float4* __restrict__ partials, float4* __restrict__ bg_partials) {
+                  float4* __restrict__ partials, float4* __restrict__ tile_partials) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   CompStage& sm = *reinterpret_cast<CompStage*>(smem_raw);
   const int tile = blockIdx.x;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bx0 = tx * kTile + (warp & 1) * 8;
   const int by0 = ty * kTile + (warp >> 1) * 4;
   const int px = bx0 + (lane & 7), py = by0 + (lane >> 3);
-  const float pxf = float(px) + 0.5f, pyf = float(py) + 0.5f;
   const bool inside = px < c.width && py < c.height;
   const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
-  const unsigned int lt = (1u << lane) - 1u, bit = 1u << lane;
-  const int2 rg = ranges[tile];
   const size_t HW = size_t(c.width) * c.height;
-  const float bgr = bg ? bg[0] : 0.f, bgg = bg ? bg[1] : 0.f, bgb = bg ? bg[2] : 0.f;
-  uint2* list = sm.list[warp];
-
   float T = 1.f, gr = 0.f, gg = 0.f, gb = 0.f;
   int lst = 0;
   if (inside) {
@@ -283,123 +234,9 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
     gg = d_image[HW + p];
     gb = d_image[2 * HW + p];
   }
-  // background gradient: T_final * g summed over the tile, fixed order
-  {
-    const float vr = warp_sum(inside ? T * gr : 0.f);
-    const float vg = warp_sum(inside ? T * gg : 0.f);
-    const float vb = warp_sum(inside ? T * gb : 0.f);
-    if (lane == 0) {
-      sm.bgred[warp][0] = vr;
-      sm.bgred[warp][1] = vg;
-      sm.bgred[warp][2] = vb;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float x = 0.f, y = 0.f, z = 0.f;
-      for (int w = 0; w < 8; ++w) {
-        x += sm.bgred[w][0];
-        y += sm.bgred[w][1];
-        z += sm.bgred[w][2];
-      }
-      bg_partials[tile] = make_float4(x, y, z, 0.f);
-    }
-  }
-  float Sr = T * bgr, Sg = T * bgg, Sb = T * bgb;
-  const int len = rg.y - rg.x;
-  const int nchunks = (len + kCompChunk - 1) / kCompChunk;
-  for (int ci = nchunks - 1; ci >= 0; --ci) {
-    const int cb = rg.x + ci * kCompChunk;
-    const int cnt = min(kCompChunk, rg.y - cb);
-    if (tid < cnt) {
-      const int gid = sorted_gid[cb + tid];
-      const float4* r = rec + 3 * size_t(gid);
-      const float4 p0 = r[0], p1 = r[1], p2 = r[2];
-      sm.mc[tid] = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
-      sm.cr[tid] = p1;
-      sm.box[tid] = make_uint2(__float_as_uint(p2.x), __float_as_uint(p2.y));
-      sm.op[tid] = p2.z;
-      sm.gid[tid] = gid;
-    }
-    __syncthreads();
-    int nl = 0;
-    for (int j0 = 0; j0 < cnt; j0 += 32) {
-      const int j = j0 + lane;
-      unsigned int m = 0;
-      if (j < cnt) {
-        m = box_lanes(sm.box[j], bx0, by0);
-        if (!m)
-#pragma unroll
-          for (int v = 0; v < kCompVals; ++v) sm.acc[warp][j][v] = 0.f;
-      }
-      const unsigned int hits = __ballot_sync(0xffffffffu, m != 0u);
-      if (m) list[nl + __popc(hits & lt)] = make_uint2(unsigned(j), m);
-      nl += __popc(hits);
-    }
-    __syncwarp();
-    for (int e = nl - 1; e >= 0; --e) {
-      const uint2 u = list[e];
-      const int j = int(u.x);
-      const int idx = cb - rg.x + j;  // position in the tile's list
-      const float4 mc = sm.mc[j];
-      const float4 cr = sm.cr[j];
-      const float dx = __fsub_rn(pxf, mc.x);
-      const float dy = __fsub_rn(pyf, mc.y);
-      const float q = touch_q(dx, dy, mc.z, mc.w, cr.x);
-      const bool act = inside && (u.y & bit) && idx < lst && q <= kk;
-      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float v8 = 0.f;
-      if (act) {
-        const float o = sm.op[j];
-        const float w = ex2_approx(q * kNegHalfLog2e);
-        const float alpha = o * w;
-        const float inv = 1.0f / (1.0f - alpha);
-        const float Tb = T * inv;  // transmittance in front of this Gaussian
-        const float aT = alpha * Tb;
-        const float dal = gr * (cr.y * Tb - Sr * inv) + gg * (cr.z * Tb - Sg * inv) +
-                          gb * (cr.w * Tb - Sb * inv);
-        const float t = w * o * dal;
-        v[0] = t * dx;
-        v[1] = t * dy;
-        v[2] = v[0] * dx;
-        v[3] = v[0] * dy;
-        v[4] = v[1] * dy;
-        v[5] = gr * aT;
-        v[6] = gg * aT;
-        v[7] = gb * aT;
-        v8 = dal * w;
-        Sr = fmaf(cr.y, aT, Sr);
-        Sg = fmaf(cr.z, aT, Sg);
-        Sb = fmaf(cr.w, aT, Sb);
-        T = Tb;
-      }
-      if (__any_sync(0xffffffffu, act)) {
-        const float tot = warp_reduce_scatter8(v, lane);
-        const float tot8 = warp_sum(v8);
-        if ((lane & 3) == 0) sm.acc[warp][j][(lane >> 2) & 7] = tot;
-        if (lane == 0) sm.acc[warp][j][8] = tot8;
-      } else if (lane < kCompVals) {
-        sm.acc[warp][j][lane] = 0.f;
-      }
-    }
-    __syncthreads();
-    if (tid < cnt) {
-      float s[kCompVals];
-#pragma unroll
-      for (int u = 0; u < kCompVals; ++u) s[u] = 0.f;
-      for (int w = 0; w < 8; ++w)
-#pragma unroll
-        for (int u = 0; u < kCompVals; ++u) s[u] += sm.acc[w][tid][u];
-      const int gid = sm.gid[tid];
-      const float A = sm.mc[tid].z, B = 0.5f * sm.mc[tid].w, C = sm.cr[tid].x;
-      const int4 rc = rect[gid];
-      const int slot = offsets[gid] + (ty - rc.y) * (rc.z - rc.x + 1) + (tx - rc.x);
-      float4* out = partials + 3 * size_t(slot);
-      out[0] = make_float4(fmaf(A, s[0], B * s[1]), fmaf(B, s[0], C * s[1]), -0.5f * s[2], -s[3]);
-      out[1] = make_float4(-0.5f * s[4], s[5], s[6], s[7]);
-      out[2] = make_float4(s[8], 0.f, 0.f, 0.f);
-    }
-    __syncthreads();
-  }
+  comp_tile_backward(sm, c, tile, tx, ty, ranges[tile], bx0, by0, float(px) + 0.5f, float(py) + 0.5f,
+                     inside, kk, T, lst, gr, gg, gb, bg, rec, rect, sorted_gid, offsets, partials,
+                     tile_partials);
 }
 
 }  // namespace
@@ -409,7 +246,7 @@ cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
                               const int* sorted_gid, const float* bg, const float* t_final,
                               const int* last, const float* d_image, float* d_xy, float* d_chol,
                               float* d_rgb, float* d_opacity, float* d_bg, unsigned char* ws,
-                              cudaStream_t s) {
+                              cudaStream_t s, float* loss, int loss_blocks) {
   const Layout L = layout_of(c, n, 0);
   const int T = num_tiles(c);
   const float4* r = reinterpret_cast<const float4*>(rec);
@@ -423,7 +260,7 @@ cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
                                          int(smem));
     if (e != cudaSuccess) return e;
     GS2D_TRY(launch(k_render_bwd_comp, dim3(T), dim3(kBwdCompThreads), smem, s, c, tiles_x(c), r, rc, rg, sorted_gid, offsets, bg, t_final, last, d_image, partials,
-        reinterpret_cast<float4*>(ws + L.bg_partials)));
+        reinterpret_cast<float4*>(ws + L.tile_partials)));
   } else {
     const size_t smem = sizeof(BwdSumSmem);
     cudaError_t e = cudaFuncSetAttribute(k_render_bwd_sum, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -434,7 +271,8 @@ cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_gather(c, n, chol, rec, rect, ws, d_xy, d_chol, d_rgb, d_opacity, d_bg, s);
+  return launch_gather(c, n, chol, rec, rect, ws, d_xy, d_chol, d_rgb, d_opacity, d_bg, loss, loss_blocks,
+                       s);
 }
 
 }  // namespace gs2d

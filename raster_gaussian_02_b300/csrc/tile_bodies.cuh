@@ -1,0 +1,392 @@
+// Per-tile bodies shared by the forward, backward and fused kernels: one
+// block per 16x16 tile, one pixel per thread, each warp owning an 8x4-pixel
+// sub-block (warp w covers columns 8 (w & 1) .. +7 and rows 4 (w >> 1) .. +3
+// of the tile).
+//
+// The tile's Gaussian list is staged through shared memory (one coalesced
+// record gather per thread); each warp then culls a window of staged
+// entries with one lane per entry, keeping, in list order, those whose
+// pixel box meets its sub-block together with a 32-bit mask of the warp's
+// lanes inside the box, so that the per-pixel box test is a single bit test.
+#pragma once
+
+#include "gs2d_internal.cuh"
+
+namespace gs2d {
+
+constexpr int kWindow = 64;  // entries culled per warp at a time
+
+struct Staged {
+  float4 mc;  // mean_x, mean_y, A, 2B
+  float4 cr;  // C, r, g, b
+};
+
+// Staging area of the sum forward (kWarps warps per block).
+template <int kWarps>
+struct SumSmem {
+  Staged g[256];
+  uint2 box[256];
+  uint2 list[kWarps][kWindow];  // (staged index, lane mask)
+  float red[kWarps];
+};
+
+// Loads records sorted_gid[rb .. rb + cnt) into the staging area (cnt <= 256).
+template <typename Smem>
+__device__ __forceinline__ void stage_records(Smem& sm, int rb, int cnt, int tid, int nthreads,
+                                              const float4* __restrict__ rec,
+                                              const int* __restrict__ sorted_gid) {
+  for (int k = tid; k < cnt; k += nthreads) {
+    const float4* r = rec + 3 * size_t(sorted_gid[rb + k]);
+    const float4 p0 = r[0], p1 = r[1], p2 = r[2];
+    sm.g[k].mc = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
+    sm.g[k].cr = p1;
+    sm.box[k] = make_uint2(__float_as_uint(p2.x), __float_as_uint(p2.y));
+  }
+}
+
+// Sum forward over the list [rg.x, rg.y) for the calling thread's pixel
+// (pixel centre pxf, pyf; the warp's sub-block starts at bx0, by0):
+//     C(p) = sum over touching Gaussians i of rgb_i * exp(-q/2)
+// (GaussianImage project page, Overview: accumulated-sum rendering; FlashImgs
+// README: additive RGB, gate folded into the colour).  Every thread of the
+// block must call it.
+template <int kWarps>
+__device__ __forceinline__ float3 sum_tile_forward(SumSmem<kWarps>& sm, int2 rg, int bx0, int by0,
+                                                   float pxf, float pyf, float kk,
+                                                   const float4* __restrict__ rec,
+                                                   const int* __restrict__ sorted_gid) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const unsigned int lt = (1u << lane) - 1u, bit = 1u << lane;
+  uint2* list = sm.list[warp];
+  float ar = 0.f, ag = 0.f, ab = 0.f;
+  for (int rb = rg.x; rb < rg.y; rb += 256) {
+    const int cnt = min(256, rg.y - rb);
+    if (rb != rg.x) __syncthreads();  // the previous round is no longer read
+    stage_records(sm, rb, cnt, tid, kWarps * 32, rec, sorted_gid);
+    __syncthreads();
+    for (int wb = 0; wb < cnt; wb += kWindow) {
+      const int wend = min(wb + kWindow, cnt);
+      int nl = 0;
+#pragma unroll
+      for (int j0 = 0; j0 < kWindow; j0 += 32) {
+        const int j = wb + j0 + lane;
+        unsigned int m = 0;
+        if (j < wend) m = box_lanes(sm.box[j], bx0, by0);
+        const unsigned int hits = __ballot_sync(0xffffffffu, m != 0u);
+        if (m) list[nl + __popc(hits & lt)] = make_uint2(unsigned(j), m);
+        nl += __popc(hits);
+      }
+      __syncwarp();
+      int e = 0;
+      for (; e + 1 < nl; e += 2) {
+        const uint2 u0 = list[e], u1 = list[e + 1];
+        const Staged s0 = sm.g[u0.x], s1 = sm.g[u1.x];
+        const float q0 = touch_q(__fsub_rn(pxf, s0.mc.x), __fsub_rn(pyf, s0.mc.y), s0.mc.z, s0.mc.w, s0.cr.x);
+        const float q1 = touch_q(__fsub_rn(pxf, s1.mc.x), __fsub_rn(pyf, s1.mc.y), s1.mc.z, s1.mc.w, s1.cr.x);
+        float w0 = ex2_approx(q0 * kNegHalfLog2e);
+        float w1 = ex2_approx(q1 * kNegHalfLog2e);
+        w0 = (q0 <= kk && (u0.y & bit)) ? w0 : 0.f;
+        w1 = (q1 <= kk && (u1.y & bit)) ? w1 : 0.f;
+        ar = fmaf(s0.cr.y, w0, ar);
+        ag = fmaf(s0.cr.z, w0, ag);
+        ab = fmaf(s0.cr.w, w0, ab);
+        ar = fmaf(s1.cr.y, w1, ar);
+        ag = fmaf(s1.cr.z, w1, ag);
+        ab = fmaf(s1.cr.w, w1, ab);
+      }
+      if (e < nl) {
+        const uint2 u0 = list[e];
+        const Staged s0 = sm.g[u0.x];
+        const float q0 = touch_q(__fsub_rn(pxf, s0.mc.x), __fsub_rn(pyf, s0.mc.y), s0.mc.z, s0.mc.w, s0.cr.x);
+        float w0 = ex2_approx(q0 * kNegHalfLog2e);
+        w0 = (q0 <= kk && (u0.y & bit)) ? w0 : 0.f;
+        ar = fmaf(s0.cr.y, w0, ar);
+        ag = fmaf(s0.cr.z, w0, ag);
+        ab = fmaf(s0.cr.w, w0, ab);
+      }
+      __syncwarp();
+    }
+  }
+  return make_float3(ar, ag, ab);
+}
+
+struct CompSmem {
+  Staged g[256];
+  uint2 box[256];
+  float op[256];
+  uint2 list[8][kWindow];
+};
+
+struct CompFwdOut {
+  float r, g, b;  // colour before the background term
+  float T;        // transmittance after the last contributor
+  int last;       // 1 + list position of the last contributor (0: none)
+};
+
+// Composite forward for the calling thread's pixel (256 threads), front to
+// back in list (depth) order (DrawingWithGaussians README, Overview: alpha
+// compositing over a trainable background):
+//     while T >= t_min: alpha = o_i exp(-q/2); C += rgb_i alpha T; T *= 1 - alpha
+// The caller adds T * background.  Every thread of the block must call it.
+__device__ __forceinline__ CompFwdOut comp_tile_forward(CompSmem& sm, const gs2d_config& c, int2 rg,
+                                                        int bx0, int by0, float pxf, float pyf,
+                                                        bool inside, float kk,
+                                                        const float4* __restrict__ rec,
+                                                        const int* __restrict__ sorted_gid) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const unsigned int lt = (1u << lane) - 1u, bit = 1u << lane;
+  uint2* list = sm.list[warp];
+  float ar = 0.f, ag = 0.f, ab = 0.f, T = 1.f;
+  int lst = 0;
+  bool done = !inside;
+  for (int rb = rg.x; rb < rg.y; rb += 256) {
+    if (__syncthreads_and(done)) break;
+    const int cnt = min(256, rg.y - rb);
+    if (tid < cnt) {
+      const float4* r = rec + 3 * size_t(sorted_gid[rb + tid]);
+      const float4 p0 = r[0], p1 = r[1], p2 = r[2];
+      sm.g[tid].mc = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
+      sm.g[tid].cr = p1;
+      sm.box[tid] = make_uint2(__float_as_uint(p2.x), __float_as_uint(p2.y));
+      sm.op[tid] = p2.z;
+    }
+    __syncthreads();
+    for (int wb = 0; wb < cnt; wb += kWindow) {
+      if (__all_sync(0xffffffffu, done)) break;
+      const int wend = min(wb + kWindow, cnt);
+      int nl = 0;
+#pragma unroll
+      for (int j0 = 0; j0 < kWindow; j0 += 32) {
+        const int j = wb + j0 + lane;
+        unsigned int m = 0;
+        if (j < wend) m = box_lanes(sm.box[j], bx0, by0);
+        const unsigned int hits = __ballot_sync(0xffffffffu, m != 0u);
+        if (m) list[nl + __popc(hits & lt)] = make_uint2(unsigned(j), m);
+        nl += __popc(hits);
+      }
+      __syncwarp();
+      for (int e = 0; e < nl; ++e) {
+        const uint2 u = list[e];
+        const Staged s = sm.g[u.x];
+        const float q = touch_q(__fsub_rn(pxf, s.mc.x), __fsub_rn(pyf, s.mc.y), s.mc.z, s.mc.w, s.cr.x);
+        if (q <= kk && (u.y & bit) && !done) {
+          if (T < c.t_min) {
+            done = true;
+          } else {
+            const float w = ex2_approx(q * kNegHalfLog2e);
+            const float alpha = sm.op[u.x] * w;
+            const float aT = alpha * T;
+            ar = fmaf(s.cr.y, aT, ar);
+            ag = fmaf(s.cr.z, aT, ag);
+            ab = fmaf(s.cr.w, aT, ab);
+            T = T * (1.0f - alpha);
+            lst = rb - rg.x + int(u.x) + 1;
+          }
+        }
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+  }
+  return CompFwdOut{ar, ag, ab, T, lst};
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Butterfly reduce-scatter of eight per-lane values over the warp: returns,
+// in every lane, the warp total of value ((lane >> 2) & 7) in the order
+// v[0..7] (lane bit 4 picks values 4-7, bit 3 values +2, bit 2 values +1).
+__device__ __forceinline__ float warp_reduce_scatter8(const float (&v)[8], int lane) {
+  float a[4], b[2];
+  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = u16 ? v[i + 4] : v[i], send = u16 ? v[i] : v[i + 4];
+    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = u8 ? a[i + 2] : a[i], send = u8 ? a[i] : a[i + 2];
+    b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  float c = (u4 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, u4 ? b[0] : b[1], 4);
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  return c;
+}
+
+// Sum of one value over the kWarps warps of a block: warp totals, then the
+// warps in order.  The result is valid in thread 0.  `red` holds kWarps
+// floats; the caller synchronises before reusing it.
+template <int kWarps>
+__device__ __forceinline__ float block_sum_ordered(float v, float* red) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float s = 0.f;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kWarps; ++w) s += red[w];
+  return s;
+}
+
+constexpr int kCompChunk = 128;
+constexpr int kCompVals = 9;
+
+struct CompStage {
+  float4 mc[kCompChunk];  // mean_x, mean_y, A, 2B
+  float4 cr[kCompChunk];  // C, r, g, b
+  uint2 box[kCompChunk];
+  float op[kCompChunk];
+  int gid[kCompChunk];
+  uint2 list[8][kCompChunk];            // (chunk index, lane mask) per warp
+  float acc[8][kCompChunk][kCompVals];  // per-warp partials, summed over warps in order
+  float bgred[8][3];
+};
+
+// Composite backward for the calling thread's pixel (256 threads), walking
+// the tile's list back to front from the pixel's last contributor.  T is the
+// pixel's final transmittance, lst its last contributor, (gr, gg, gb) its
+// dL/dC.  With alpha = o w, T_i the transmittance in front of Gaussian i and
+// S the colour accumulated behind it (including T_final * bg):
+//     dL/dalpha = sum_k g_k (rgb_k T_i - S_k / (1 - alpha)),
+//     dL/do = w dL/dalpha,  dL/dw = o dL/dalpha,  dL/drgb_k = g_k alpha T_i,
+//     dL/dbg_k = sum over pixels of T_final g_k.
+// Per (warp, Gaussian) the nine partial derivatives are reduced over the
+// warp and kept in a per-warp slot; the slots are summed in warp order and
+// written to the pair's emission slot (3 float4 per pair).  The tile's
+// background partial goes to tile_partials[tile].
+__device__ __forceinline__ void comp_tile_backward(
+    CompStage& sm, const gs2d_config& c, int tile, int tx, int ty, int2 rg, int bx0, int by0,
+    float pxf, float pyf, bool inside, float kk, float T, int lst, float gr, float gg, float gb,
+    const float* __restrict__ bg, const float4* __restrict__ rec,
+    const int4* __restrict__ rect, const int* __restrict__ sorted_gid,
+    const int* __restrict__ offsets, float4* __restrict__ partials,
+    float4* __restrict__ tile_partials) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const unsigned int lt = (1u << lane) - 1u, bit = 1u << lane;
+  const float bgr = bg ? bg[0] : 0.f, bgg = bg ? bg[1] : 0.f, bgb = bg ? bg[2] : 0.f;
+  uint2* list = sm.list[warp];
+  // background gradient: T_final * g summed over the tile, fixed order
+  {
+    const float vr = warp_sum(inside ? T * gr : 0.f);
+    const float vg = warp_sum(inside ? T * gg : 0.f);
+    const float vb = warp_sum(inside ? T * gb : 0.f);
+    if (lane == 0) {
+      sm.bgred[warp][0] = vr;
+      sm.bgred[warp][1] = vg;
+      sm.bgred[warp][2] = vb;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float x = 0.f, y = 0.f, z = 0.f;
+      for (int w = 0; w < 8; ++w) {
+        x += sm.bgred[w][0];
+        y += sm.bgred[w][1];
+        z += sm.bgred[w][2];
+      }
+      tile_partials[tile] = make_float4(x, y, z, 0.f);
+    }
+  }
+  float Sr = T * bgr, Sg = T * bgg, Sb = T * bgb;
+  const int len = rg.y - rg.x;
+  const int nchunks = (len + kCompChunk - 1) / kCompChunk;
+  for (int ci = nchunks - 1; ci >= 0; --ci) {
+    const int cb = rg.x + ci * kCompChunk;
+    const int cnt = min(kCompChunk, rg.y - cb);
+    if (tid < cnt) {
+      const int gid = sorted_gid[cb + tid];
+      const float4* r = rec + 3 * size_t(gid);
+      const float4 p0 = r[0], p1 = r[1], p2 = r[2];
+      sm.mc[tid] = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
+      sm.cr[tid] = p1;
+      sm.box[tid] = make_uint2(__float_as_uint(p2.x), __float_as_uint(p2.y));
+      sm.op[tid] = p2.z;
+      sm.gid[tid] = gid;
+    }
+    __syncthreads();
+    int nl = 0;
+    for (int j0 = 0; j0 < cnt; j0 += 32) {
+      const int j = j0 + lane;
+      unsigned int m = 0;
+      if (j < cnt) {
+        m = box_lanes(sm.box[j], bx0, by0);
+        if (!m)
+#pragma unroll
+          for (int v = 0; v < kCompVals; ++v) sm.acc[warp][j][v] = 0.f;
+      }
+      const unsigned int hits = __ballot_sync(0xffffffffu, m != 0u);
+      if (m) list[nl + __popc(hits & lt)] = make_uint2(unsigned(j), m);
+      nl += __popc(hits);
+    }
+    __syncwarp();
+    for (int e = nl - 1; e >= 0; --e) {
+      const uint2 u = list[e];
+      const int j = int(u.x);
+      const int idx = cb - rg.x + j;  // position in the tile's list
+      const float4 mc = sm.mc[j];
+      const float4 cr = sm.cr[j];
+      const float dx = __fsub_rn(pxf, mc.x);
+      const float dy = __fsub_rn(pyf, mc.y);
+      const float q = touch_q(dx, dy, mc.z, mc.w, cr.x);
+      const bool act = inside && (u.y & bit) && idx < lst && q <= kk;
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float v8 = 0.f;
+      if (act) {
+        const float o = sm.op[j];
+        const float w = ex2_approx(q * kNegHalfLog2e);
+        const float alpha = o * w;
+        const float inv = 1.0f / (1.0f - alpha);
+        const float Tb = T * inv;  // transmittance in front of this Gaussian
+        const float aT = alpha * Tb;
+        const float dal = gr * (cr.y * Tb - Sr * inv) + gg * (cr.z * Tb - Sg * inv) +
+                          gb * (cr.w * Tb - Sb * inv);
+        const float t = w * o * dal;
+        v[0] = t * dx;
+        v[1] = t * dy;
+        v[2] = v[0] * dx;
+        v[3] = v[0] * dy;
+        v[4] = v[1] * dy;
+        v[5] = gr * aT;
+        v[6] = gg * aT;
+        v[7] = gb * aT;
+        v8 = dal * w;
+        Sr = fmaf(cr.y, aT, Sr);
+        Sg = fmaf(cr.z, aT, Sg);
+        Sb = fmaf(cr.w, aT, Sb);
+        T = Tb;
+      }
+      if (__any_sync(0xffffffffu, act)) {
+        const float tot = warp_reduce_scatter8(v, lane);
+        const float tot8 = warp_sum(v8);
+        if ((lane & 3) == 0) sm.acc[warp][j][(lane >> 2) & 7] = tot;
+        if (lane == 0) sm.acc[warp][j][8] = tot8;
+      } else if (lane < kCompVals) {
+        sm.acc[warp][j][lane] = 0.f;
+      }
+    }
+    __syncthreads();
+    if (tid < cnt) {
+      float s[kCompVals];
+#pragma unroll
+      for (int u = 0; u < kCompVals; ++u) s[u] = 0.f;
+      for (int w = 0; w < 8; ++w)
+#pragma unroll
+        for (int u = 0; u < kCompVals; ++u) s[u] += sm.acc[w][tid][u];
+      const int gid = sm.gid[tid];
+      const float A = sm.mc[tid].z, B = 0.5f * sm.mc[tid].w, C = sm.cr[tid].x;
+      const int4 rc = rect[gid];
+      const int slot = offsets[gid] + (ty - rc.y) * (rc.z - rc.x + 1) + (tx - rc.x);
+      float4* out = partials + 3 * size_t(slot);
+      out[0] = make_float4(fmaf(A, s[0], B * s[1]), fmaf(B, s[0], C * s[1]), -0.5f * s[2], -s[3]);
+      out[1] = make_float4(-0.5f * s[4], s[5], s[6], s[7]);
+      out[2] = make_float4(s[8], 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace gs2d

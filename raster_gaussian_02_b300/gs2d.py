@@ -68,6 +68,8 @@ def lib() -> C.CDLL:
         L.gs2d_loss_l2.restype = C.c_int
         L.gs2d_render_bwd.argtypes = [_cfgp, C.c_int32] + [_p] * 15 + [_p]
         L.gs2d_render_bwd.restype = C.c_int
+        L.gs2d_render_fwd_bwd_l2.argtypes = [_cfgp, C.c_int32] + [_p] * 15 + [_p]
+        L.gs2d_render_fwd_bwd_l2.restype = C.c_int
         L.gs2d_loss_l2_noalloc.argtypes = [C.c_int32, C.c_int32] + [_p] * 4 + [_p]
         L.gs2d_loss_l2_noalloc.restype = C.c_int
         L.gs2d_read_status.argtypes = [_p, C.POINTER(C.c_int64), C.POINTER(C.c_uint32), _p]
@@ -172,6 +174,19 @@ def gs2d_render_bwd(cfg, n, chol, rec, rect, tile_ranges, sorted_gid, background
         _ptr(workspace, None, "workspace"), _stream(stream))
 
 
+def gs2d_render_fwd_bwd_l2(cfg, n, chol, rec, rect, tile_ranges, sorted_gid, background, target,
+                           image, loss, d_xy, d_chol, d_rgb, d_opacity, d_background, workspace,
+                           stream=None) -> int:
+    return lib().gs2d_render_fwd_bwd_l2(
+        C.byref(cfg), int(n), _ptr(chol, _f32, "chol"), _ptr(rec, None, "rec"),
+        _ptr(rect, _i32, "rect"), _ptr(tile_ranges, _i32, "tile_ranges"),
+        _ptr(sorted_gid, _i32, "sorted_gid"), _ptr(background, _f32, "background"),
+        _ptr(target, _f32, "target"), _ptr(image, _f32, "image"), _ptr(loss, _f32, "loss"),
+        _ptr(d_xy, _f32, "d_xy"), _ptr(d_chol, _f32, "d_chol"), _ptr(d_rgb, _f32, "d_rgb"),
+        _ptr(d_opacity, _f32, "d_opacity"), _ptr(d_background, _f32, "d_background"),
+        _ptr(workspace, None, "workspace"), _stream(stream))
+
+
 def gs2d_read_status(workspace, stream=None):
     """Waits for the stream; returns (status, pairs, flags)."""
     pairs, flags = C.c_int64(0), C.c_uint32(0)
@@ -266,11 +281,27 @@ class Rasterizer:
                               self.d_xy, self.d_chol, self.d_rgb, self.d_opacity,
                               self.d_background, self.workspace), "gs2d_render_bwd")
 
-    def step(self, xy, chol, rgb, target, depth=None, opacity=None, background=None, sync=False):
+    def render_fwd_bwd_l2(self, target, background=None, write_image=True):
+        """Fused forward + L2 loss + backward (one per-tile kernel and the
+        gather).  Fills loss and the d_* gradients, and the image unless
+        write_image is False; d_image, t_final and last are not written."""
+        self.background = background
+        check(gs2d_render_fwd_bwd_l2(self.cfg, self.n, self.chol, self.rec, self.rect,
+                                     self.tile_ranges, self.sorted_gid, background, target,
+                                     self.image if write_image else None, self.loss, self.d_xy,
+                                     self.d_chol, self.d_rgb, self.d_opacity, self.d_background,
+                                     self.workspace), "gs2d_render_fwd_bwd_l2")
+        return self.loss
+
+    def step(self, xy, chol, rgb, target, depth=None, opacity=None, background=None, sync=False,
+             fused=False):
         """One pass of the whole path: project, bin and sort, forward, L2
-        loss, backward.  Returns the device loss tensor."""
+        loss, backward (fused=True: the last three in one fused call).
+        Returns the device loss tensor."""
         self.project(xy, chol, rgb, depth, opacity)
         self.bin_and_sort(sync=sync)
+        if fused:
+            return self.render_fwd_bwd_l2(target, background)
         self.render_fwd(background)
         self.loss_l2(target)
         self.render_bwd()

@@ -119,6 +119,21 @@ def test_host_checks_reject_bad_arguments(gs2d):
     args = [fake] * 15
     args[0] = null  # chol
     assert L.gs2d_render_bwd(C.byref(good), 4, *args, null) == INVALID
+    # fused fwd + L2 + bwd: target, loss and workspace are required
+    # (chol rec rect ranges gid bg target image loss dxy dchol drgb dop dbg ws)
+    args = [fake] * 15
+    args[6] = null  # target
+    assert L.gs2d_render_fwd_bwd_l2(C.byref(good), 4, *args, null) == INVALID
+    args = [fake] * 15
+    args[8] = null  # loss
+    assert L.gs2d_render_fwd_bwd_l2(C.byref(good), 4, *args, null) == INVALID
+    args = [fake] * 15
+    args[14] = odd  # workspace
+    assert L.gs2d_render_fwd_bwd_l2(C.byref(good), 4, *args, null) == INVALID
+    args = [fake] * 15
+    args[3] = odd  # tile_ranges
+    assert L.gs2d_render_fwd_bwd_l2(C.byref(good), 4, *args, null) == INVALID
+    assert L.gs2d_render_fwd_bwd_l2(C.byref(bad), 4, *([fake] * 15), null) == INVALID
     # read_status
     assert L.gs2d_read_status(None, None, None, None) == INVALID
     assert L.gs2d_read_status(odd, None, None, None) == INVALID
