@@ -156,7 +156,7 @@ GS2D_API gs2d_status gs2d_project(const gs2d_config* cfg, int32_t n, const float
  *                      workspace for gs2d_read_status, and on overflow the
  *                      lists are left empty so later calls render nothing.
  *   tile_ranges[T,2]   out: [start, end) of tile t in sorted_gid,
- *                      T = ceil(W/16) * ceil(H/16)
+ *                      T = ceil(W/16) * ceil(H/16); [0, 0) for an empty tile
  *   sorted_gid[cap]    out: Gaussian indices, the first P entries valid
  *   workspace          gs2d_workspace_size(cfg, n, pair_capacity) bytes
  */

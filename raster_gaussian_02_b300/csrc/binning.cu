@@ -1,5 +1,6 @@
 // Tile binning and sort, as reduce-then-scan steps that never wait on
-// another block.
+// another block.  Sum mode with few tiles takes the counting sort further
+// down; otherwise:
 //
 //   k_count_scan   sum of the tile counts of every 256-Gaussian block; the
 //                  last block to finish scans the block sums into block
@@ -80,23 +81,13 @@ __device__ __forceinline__ long long usable_pairs(const Header* hdr, long long c
 template <bool kComposite>
 using KeyOf = typename std::conditional<kComposite, unsigned long long, unsigned int>::type;
 
-// Block sums of the tile counts; the last block scans them.  Also clears the
-// count tables and the tile ranges for the kernels that follow.
-__global__ void __launch_bounds__(kScanThreads)
-k_count_scan(int n, long long cap, const int* __restrict__ count, Header* hdr,
-             long long* __restrict__ block_off, unsigned int* __restrict__ zero_a,
-             long long zero_a_words, unsigned int* __restrict__ zero_b, long long zero_b_words,
-             unsigned long long keys_final) {
-  pdl_enter();
+// Called by every thread of every block once the block's pair total is
+// known: the last block to arrive scans all block totals into block offsets
+// and writes P, the flags and the offset of the final keys.
+__device__ __forceinline__ void finish_block_totals(long long total, Header* hdr,
+                                                    long long* __restrict__ block_off, long long cap,
+                                                    unsigned long long keys_final) {
   const int tid = threadIdx.x;
-  const long long gstride = (long long)gridDim.x * blockDim.x;
-  for (long long k = (long long)blockIdx.x * blockDim.x + tid; k < zero_a_words; k += gstride)
-    zero_a[k] = 0u;
-  for (long long k = (long long)blockIdx.x * blockDim.x + tid; k < zero_b_words; k += gstride)
-    zero_b[k] = 0u;
-  const long long g = (long long)blockIdx.x * kScanItems + tid;
-  long long total;
-  block_exclusive_scan_256<long long>((g < n) ? count[g] : 0, &total);
   __shared__ bool last;
   if (tid == 0) {
     block_off[blockIdx.x] = total;
@@ -124,6 +115,202 @@ k_count_scan(int n, long long cap, const int* __restrict__ count, Header* hdr,
     if (carry > cap) f |= GS2D_FLAG_CAPACITY;
     if (carry >= (1ll << 30)) f |= GS2D_FLAG_OVERFLOW;
     if (f) atomicOr(&hdr->flags, f);
+  }
+}
+
+// Block sums of the tile counts; the last block scans them.  Also clears the
+// count tables and the tile ranges for the kernels that follow.
+__global__ void __launch_bounds__(kScanThreads)
+k_count_scan(int n, long long cap, const int* __restrict__ count, Header* hdr,
+             long long* __restrict__ block_off, unsigned int* __restrict__ zero_a,
+             long long zero_a_words, unsigned int* __restrict__ zero_b, long long zero_b_words,
+             unsigned long long keys_final) {
+  pdl_enter();
+  const int tid = threadIdx.x;
+  const long long gstride = (long long)gridDim.x * blockDim.x;
+  for (long long k = (long long)blockIdx.x * blockDim.x + tid; k < zero_a_words; k += gstride)
+    zero_a[k] = 0u;
+  for (long long k = (long long)blockIdx.x * blockDim.x + tid; k < zero_b_words; k += gstride)
+    zero_b[k] = 0u;
+  const long long g = (long long)blockIdx.x * kScanItems + tid;
+  long long total;
+  block_exclusive_scan_256<long long>((g < n) ? count[g] : 0, &total);
+  finish_block_totals(total, hdr, block_off, cap, keys_final);
+}
+
+// ---------------------------------------------------------------------------
+// Sum mode with at most kCountSortMaxTiles tiles: a counting sort by tile in
+// three kernels, writing the final lists directly.
+//   k_tile_hist     per 256-Gaussian block b: H[t][b] = how many of the
+//                   block's Gaussians cover tile t, and the block's pair
+//                   total; the last block scans the totals (block offsets, P).
+//   k_tile_scan     per tile t (one warp): exclusive scan of H[t][.] over the
+//                   blocks, in place, and the row total R[t]; the last block
+//                   scans the totals into the tile ranges.  (Ranges of empty
+//                   tiles are [0, 0), as the radix path leaves them.)
+//   k_tile_scatter  per block: the pair (Gaussian g, tile t) goes to
+//                   start(t) + H[t][b] + the number of the block's Gaussians
+//                   before g that cover t, read off a per-tile 256-bit mask of
+//                   the block's Gaussians.
+// Within a tile the list comes out in ascending index, as the radix passes
+// give it; the sorted tile ids are written too (the backward reads them).
+
+__global__ void __launch_bounds__(kScanThreads)
+k_tile_hist(int n, int T, int tiles_x, long long cap, const int4* __restrict__ rect,
+            const int* __restrict__ count, Header* hdr, long long* __restrict__ block_off,
+            unsigned int* __restrict__ H, unsigned long long keys_final) {
+  pdl_enter();
+  __shared__ unsigned int s_h[kCountSortMaxTiles];
+  const int tid = threadIdx.x;
+  for (int t = tid; t < T; t += blockDim.x) s_h[t] = 0u;
+  const long long g = (long long)blockIdx.x * kScanItems + tid;
+  const int cnt = g < n ? count[g] : 0;
+  const int4 r = g < n ? rect[g] : make_int4(0, 0, -1, -1);
+  long long total;
+  block_exclusive_scan_256<long long>(cnt, &total);  // its barriers order the clears
+  if (cnt > 0)
+    for (int y = r.y; y <= r.w; ++y)
+      for (int x = r.x; x <= r.z; ++x) atomicAdd(&s_h[y * tiles_x + x], 1u);
+  __syncthreads();
+  const size_t B = gridDim.x;
+  for (int t = tid; t < T; t += blockDim.x) H[size_t(t) * B + blockIdx.x] = s_h[t];
+  finish_block_totals(total, hdr, block_off, cap, keys_final);
+}
+
+__global__ void __launch_bounds__(256)
+k_tile_scan(int T, int B, long long cap, Header* hdr, unsigned int* __restrict__ H,
+            unsigned int* __restrict__ R, int2* __restrict__ ranges) {
+  pdl_enter();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = blockIdx.x * 8 + warp;
+  __shared__ bool last;
+  if (t < T) {
+    unsigned int* row = H + size_t(t) * B;
+    unsigned int carry = 0;
+    for (int b0 = 0; b0 < B; b0 += 256) {  // lane: 8 consecutive entries
+      unsigned int v[8], ex[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int b = b0 + lane * 8 + j;
+        v[j] = b < B ? row[b] : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        ex[j] = sum;
+        sum += v[j];
+      }
+      unsigned int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned int before = carry + incl - sum;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int b = b0 + lane * 8 + j;
+        if (b < B) row[b] = before + ex[j];
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) R[t] = carry;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last = atomicAdd(&hdr->blocks_done2, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  // The last block: tile starts = exclusive scan of the row totals (thread
+  // i takes tiles 8i .. 8i+7; T <= 2048), then the ranges.
+  __threadfence();
+  const bool ok = (*reinterpret_cast<const volatile unsigned int*>(&hdr->flags) & kBadFlags) == 0;
+  unsigned int v[8], ex[8], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int u = tid * 8 + j;
+    v[j] = u < T ? __ldcg(R + u) : 0u;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    ex[j] = sum;
+    sum += v[j];
+  }
+  unsigned int total;
+  const unsigned int before = block_exclusive_scan_256<unsigned int>(sum, &total);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int u = tid * 8 + j;
+    if (u < T) {
+      const unsigned int start = before + ex[j];
+      ranges[u] = (ok && v[j]) ? make_int2(int(start), int(start + v[j])) : make_int2(0, 0);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+k_tile_scatter(int n, int T, int tiles_x, long long cap, const Header* __restrict__ hdr,
+               const int4* __restrict__ rect, const int* __restrict__ count,
+               const long long* __restrict__ block_off, const unsigned int* __restrict__ H,
+               const int2* __restrict__ ranges, int* __restrict__ offsets,
+               int* __restrict__ sorted_gid, unsigned int* __restrict__ keys_out) {
+  pdl_enter();
+  extern __shared__ __align__(16) unsigned int s_mask[];  // [T][8]: bit i = local Gaussian i covers t
+  __shared__ long long s_excl[kScanItems + 1];
+  __shared__ int4 s_rect[kScanItems];
+  __shared__ unsigned int s_base[kCountSortMaxTiles];  // where the block's part of list t starts
+  const int tid = threadIdx.x;
+  for (int k = tid; k < T * 8; k += blockDim.x) s_mask[k] = 0u;
+  const long long g0 = (long long)blockIdx.x * kScanItems;
+  const long long g = g0 + tid;
+  const int cnt = g < n ? count[g] : 0;
+  const int4 r = g < n ? rect[g] : make_int4(0, 0, -1, -1);
+  s_rect[tid] = r;
+  long long total;
+  const long long excl = block_exclusive_scan_256<long long>(cnt, &total);  // orders the clears
+  s_excl[tid] = excl;
+  if (tid == 0) s_excl[kScanItems] = total;
+  if (g < n) {
+    const long long o = block_off[blockIdx.x] + excl;
+    offsets[g] = o < (1ll << 31) ? int(o) : 0x7fffffff;
+  }
+  if (cnt > 0) {
+    const unsigned int bit = 1u << (tid & 31);
+    for (int y = r.y; y <= r.w; ++y)
+      for (int x = r.x; x <= r.z; ++x) atomicOr(&s_mask[(y * tiles_x + x) * 8 + (tid >> 5)], bit);
+  }
+  const size_t B = gridDim.x;
+  {
+    unsigned int st[kCountSortMaxTiles / kScanThreads], hb[kCountSortMaxTiles / kScanThreads];
+#pragma unroll
+    for (int j = 0; j < kCountSortMaxTiles / kScanThreads; ++j) {
+      const int u = tid + j * kScanThreads;
+      st[j] = u < T ? unsigned(ranges[u].x) : 0u;
+      hb[j] = u < T ? H[size_t(u) * B + blockIdx.x] : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kCountSortMaxTiles / kScanThreads; ++j) {
+      const int u = tid + j * kScanThreads;
+      if (u < T) s_base[u] = st[j] + hb[j];
+    }
+  }
+  __syncthreads();
+  if (usable_pairs(hdr, cap) == 0) return;  // P > capacity, overflow, or no pairs
+  for (long long e = tid; e < total; e += blockDim.x) {
+    int lo = 0, hi = kScanItems - 1;  // the local Gaussian of pair e (as in k_emit)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_excl[mid] <= e) lo = mid; else hi = mid - 1;
+    }
+    const int k = int(e - s_excl[lo]);
+    const int4 q = s_rect[lo];
+    const int rw = q.z - q.x + 1;
+    const int t = (q.y + k / rw) * tiles_x + q.x + k % rw;
+    const unsigned int* m = s_mask + t * 8;
+    unsigned int rank = __popc(m[lo >> 5] & ((1u << (lo & 31)) - 1u));
+    for (int j = 0; j < (lo >> 5); ++j) rank += __popc(m[j]);
+    const long long dst = (long long)s_base[t] + rank;
+    sorted_gid[dst] = int(g0 + lo);
+    keys_out[dst] = unsigned(t);
   }
 }
 
@@ -386,6 +573,26 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
   Key* kb = reinterpret_cast<Key*>(ws + L.keys_b);
   const size_t keys_final = (L.passes % 2 == 0) ? L.keys_a : L.keys_b;
   const int blocks = n > 0 ? (n + kScanItems - 1) / kScanItems : 1;
+  if constexpr (!kComposite) {
+    if (L.count_sort) {
+      unsigned int* H = reinterpret_cast<unsigned int*>(ws + L.tile_hist);
+      unsigned int* R = H + size_t(T) * size_t(blocks);
+      const int2* rg = reinterpret_cast<const int2*>(tile_ranges);
+      GS2D_TRY(launch(k_tile_hist, dim3(blocks), dim3(kScanThreads), 0, s, n, T, tiles_x(c), cap,
+                      reinterpret_cast<const int4*>(rect), count, hdr, block_off, H,
+                      (unsigned long long)L.keys_a));
+      GS2D_TRY(launch(k_tile_scan, dim3((T + 7) / 8), dim3(256), 0, s, T, blocks, cap, hdr, H, R,
+                      reinterpret_cast<int2*>(tile_ranges)));
+      const size_t smem = size_t(T) * 8 * sizeof(unsigned int);
+      GS2D_TRY(cudaFuncSetAttribute(k_tile_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    int(size_t(kCountSortMaxTiles) * 8 * sizeof(unsigned int))));
+      GS2D_TRY(launch(k_tile_scatter, dim3(blocks), dim3(kScanThreads), smem, s, n, T, tiles_x(c), cap,
+                      static_cast<const Header*>(hdr), reinterpret_cast<const int4*>(rect), count,
+                      static_cast<const long long*>(block_off), static_cast<const unsigned int*>(H), rg,
+                      offsets, sorted_gid, reinterpret_cast<unsigned int*>(ws + L.keys_a)));
+      return cudaGetLastError();
+    }
+  }
   GS2D_TRY(launch(k_count_scan, dim3(blocks), dim3(kScanThreads), 0, s, n, cap, count, hdr, block_off, tables,
                                                L.passes * table_words,
                                                reinterpret_cast<unsigned int*>(tile_ranges), 2ll * T,

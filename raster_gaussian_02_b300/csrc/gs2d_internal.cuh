@@ -32,6 +32,7 @@ struct Header {
   unsigned int flags;              // GS2D_FLAG_*
   unsigned int blocks_done;        // count of finished blocks (last one finishes the scan)
   unsigned long long keys_final;   // byte offset of the sorted keys
+  unsigned int blocks_done2;       // the same for a second kernel
 };
 
 constexpr int kMaxPasses = 8;
@@ -46,10 +47,16 @@ constexpr int kScanThreads = 256;
 constexpr int kScanItems = kScanThreads;  // Gaussians per scan block, one per thread
 
 constexpr int kRadixThreads = 256;
+// Sum mode with at most this many tiles (and Gaussians) sorts by counting:
+// the per-tile Gaussian masks of one 256-Gaussian block take 32 bytes per
+// tile of shared memory.
+constexpr int kCountSortMaxTiles = 2048;
+constexpr long long kCountSortMaxGaussians = 1 << 20;
 
 struct Layout {
-  size_t block_off, offsets, tile_partials, loss_partials, dimage, partials, tables, keys_a, keys_b, vals_tmp, total;
+  size_t block_off, offsets, tile_partials, loss_partials, dimage, tile_hist, partials, tables, keys_a, keys_b, vals_tmp, total;
   int passes, digit_bits, tile_bits, key_bits, key_bytes, partial_floats, radix_per_thread;
+  bool count_sort;  // sum mode with few tiles: counting sort by tile instead of radix passes
   long long partitions, partitions4;  // radix partitions, and rounded up to a multiple of 4
 };
 
@@ -105,6 +112,12 @@ inline Layout layout_of(const gs2d_config& c, long long n, long long cap) {
   o = align256(o + 8 * size_t(T));
   L.dimage = o;  // fused pass, sum mode: dL/dC [3,H,W]
   if (!comp) o = align256(o + 12 * size_t(c.width) * size_t(c.height));
+  L.tile_hist = o;  // counting sort by tile: [T][blocks] counts, then row totals [T]
+  L.count_sort = !comp && T <= kCountSortMaxTiles && n <= kCountSortMaxGaussians;
+  if (L.count_sort) {
+    const long long B = n > 0 ? (n + kScanItems - 1) / kScanItems : 1;
+    o = align256(o + 4 * size_t(T) * size_t(B) + 4 * size_t(T));
+  }
   L.partials = o;
   o = align256(o + 4 * size_t(L.partial_floats) * size_t(cap));
   L.tables = o;

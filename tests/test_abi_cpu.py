@@ -64,7 +64,9 @@ def test_workspace_size(gs2d):
     assert 0 < a < b
     assert gs2d.gs2d_workspace_size(cfg, 0, 0) >= 16384
     comp = gs2d.make_config(768, 512, gs2d.GS2D_MODE_COMPOSITE)
-    assert gs2d.gs2d_workspace_size(comp, 50_000, 200_000) > a  # 64-bit keys, wider partials
+    # per pair, composite needs more (64-bit keys, 12-float partials)
+    ca, cb = (gs2d.gs2d_workspace_size(comp, 50_000, k) for k in (200_000, 400_000))
+    assert cb - ca > b - a
     bad = [gs2d.gs2d_config(0, 512, 16, 0, 3.0, 1e-4), gs2d.gs2d_config(768, 512, 8, 0, 3.0, 1e-4),
            gs2d.gs2d_config(768, 512, 16, 2, 3.0, 1e-4), gs2d.gs2d_config(768, 512, 16, 0, 0.0, 1e-4),
            gs2d.gs2d_config(768, 512, 16, 0, float("nan"), 1e-4),

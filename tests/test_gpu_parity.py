@@ -54,6 +54,25 @@ def test_long_tile_lists():
         full_parity(wl)
 
 
+@pytest.mark.parametrize("mode", [synth.SUM, synth.COMPOSITE])
+def test_empty_tiles(mode):
+    """Few Gaussians on a large image: most tiles have empty lists."""
+    wl = synth.random_scene(300, 200, 25, seed=21, mode=mode, diag=(0.5, 6.0))
+    g, s, _ = full_parity(wl)
+    assert (s.ranges[:, 0] == s.ranges[:, 1]).sum() > 100
+
+
+@pytest.mark.parametrize("w,h,n", [(1024, 512, 20000), (1040, 512, 20000), (720, 720, 3000)])
+def test_sum_sort_paths_near_the_tile_limit(w, h, n):
+    """2048, 2080 and 2025 tiles: the counting sort by tile (at most 2048
+    tiles) and, above it, the radix passes give the oracle's lists."""
+    wl = synth.random_scene(w, h, n, seed=w + n, diag=(0.5, 12.0))
+    g = gpu_run(wl)
+    s = oracle_scene(wl)
+    check_projection(g, s)
+    check_lists(g, s)
+
+
 def test_composite_early_termination_dense():
     wl = synth.random_scene(96, 80, 4000, seed=12, mode=synth.COMPOSITE, diag=(1.0, 4.0))
     wl.opacity[:] = 0.95
