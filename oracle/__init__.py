@@ -54,10 +54,14 @@ class use_library:
 
 class RefCfg(C.Structure):
     _fields_ = [("width", C.c_int32), ("height", C.c_int32), ("tile", C.c_int32),
-                ("mode", C.c_int32), ("cutoff_sigma", C.c_float), ("t_min", C.c_float)]
+                ("mode", C.c_int32), ("cutoff_sigma", C.c_float), ("t_min", C.c_float),
+                ("param", C.c_int32)]
 
 
 SUM, COMPOSITE = 0, 1
+# Shape parameters per Gaussian: a Cholesky factor (l11, l21, l22) or a scale
+# and rotation angle (s_x, s_y, theta).
+CHOLESKY, SCALE_ROT = 0, 1
 
 _p = C.c_void_p
 _i32, _i64 = C.c_int32, C.c_int64
@@ -93,9 +97,11 @@ class Config:
     cutoff_sigma: float = 3.0
     t_min: float = 1e-4
     tile: int = 16
+    param: int = CHOLESKY
 
     def c(self) -> RefCfg:
-        return RefCfg(self.width, self.height, self.tile, self.mode, self.cutoff_sigma, self.t_min)
+        return RefCfg(self.width, self.height, self.tile, self.mode, self.cutoff_sigma, self.t_min,
+                      self.param)
 
     @property
     def tiles_x(self) -> int:

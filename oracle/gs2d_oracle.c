@@ -16,7 +16,10 @@
  *   - The covariance is given by a lower-triangular Cholesky factor L,
  *     Sigma = L L^T (DrawingWithGaussians README, MLX-specific notes;
  *     GaussianImage project page, "Representation" scripts for the Cholesky
- *     variant).
+ *     variant), or by a scale and a rotation angle (FlashImgs README, Python
+ *     API: project_gaussians_2d_scale_rot and the (xy, scale, rot, feat)
+ *     parameters; GaussianImage project page, the "rs" scripts):
+ *     Sigma = R(theta) diag(s_x^2, s_y^2) R(theta)^T.
  *   - In the sum form there is no opacity: the gate is folded into the colour,
  *     and colours add (FlashImgs README, Python API and Web viewer sections).
  *   - The optional variant alpha-composites depth-ordered Gaussians front to
@@ -40,10 +43,13 @@
  *     ascending depth with ties broken by ascending index;
  *   - composite: a masked Gaussian contributes only while the transmittance
  *     before it is >= t_min; the background is added with weight T_final;
- *   - Gaussians with non-finite parameters, a zero diagonal entry of L, a
- *     non-finite FP32 inverse covariance, an empty box, or (composite) an
- *     opacity outside [0, 1) are culled: they touch no pixel and get a zero
- *     gradient.
+ *   - Gaussians with non-finite parameters, a zero diagonal entry of L (or
+ *     a zero scale), a non-finite FP32 inverse covariance, an empty box, or
+ *     (composite) an opacity outside [0, 1) are culled: they touch no pixel
+ *     and get a zero gradient;
+ *   - scale-rotation: R(theta) = [[cos, -sin], [sin, cos]] with theta in
+ *     radians, scales in pixels; the FP32 mask data use cos and sin taken in
+ *     double and rounded to FP32.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (oracle/build.py).
  * -ffp-contract=off keeps every FP32 product and sum separately rounded, so
@@ -61,10 +67,13 @@ typedef struct {
   int32_t mode;          /* 0: accumulated sum, 1: alpha composite */
   float cutoff_sigma;    /* k: the mask is q <= k*k */
   float t_min;           /* composite early-termination threshold */
+  int32_t param;         /* 0: Cholesky factor (l11, l21, l22); 1: scale-rotation (s_x, s_y, theta) */
 } ref_cfg;
 
 #define REF_MODE_SUM 0
 #define REF_MODE_COMPOSITE 1
+#define REF_PARAM_CHOLESKY 0
+#define REF_PARAM_SCALE_ROT 1
 
 static int32_t ref_tiles_x(const ref_cfg* cfg) { return (cfg->width + cfg->tile - 1) / cfg->tile; }
 static int32_t ref_tiles_y(const ref_cfg* cfg) { return (cfg->height + cfg->tile - 1) / cfg->tile; }
@@ -123,6 +132,53 @@ static int ref_mask_data(const ref_cfg* cfg, float mx, float my, float a, float 
 }
 
 /*
+ * Mask data from a scale and rotation: Sigma = R diag(s_x^2, s_y^2) R^T, so
+ * Sigma^-1 = R diag(u, v) R^T with u = 1/s_x^2, v = 1/s_y^2:
+ *     A = c^2 u + s^2 v,   B = c s (u - v),   C = s^2 u + c^2 v   (c = cos, s = sin),
+ * and Sigma_xx = c^2 s_x^2 + s^2 s_y^2, Sigma_yy = s^2 s_x^2 + c^2 s_y^2.  FP32
+ * order: cos and sin in double rounded to FP32; isx = 1/s_x, u = isx*isx (and
+ * v alike); A = fma(c*c, u, (s*s)*v), B = (c*s)*(u - v), C = fma(s*s, u, (c*c)*v);
+ * r_x = k*sqrt(fma(c*c, s_x*s_x, (s*s)*(s_y*s_y))), r_y = k*sqrt(fma(s*s, s_x*s_x,
+ * (c*c)*(s_y*s_y))).  The box rule is that of ref_mask_data.
+ */
+static int ref_mask_data_sr(const ref_cfg* cfg, float mx, float my, float sx, float sy,
+                            float th, float conic[3], int32_t aabb[4]) {
+  if (sx == 0.0f || sy == 0.0f) return 0;
+  const float co = (float)cos((double)th);
+  const float si = (float)sin((double)th);
+  const float isx = 1.0f / sx;
+  const float isy = 1.0f / sy;
+  const float u = isx * isx;
+  const float v = isy * isy;
+  const float cc = co * co, ss = si * si, cs = co * si;
+  const float A = fmaf(cc, u, ss * v);
+  const float B = cs * (u - v);
+  const float C = fmaf(ss, u, cc * v);
+  if (!isfinite(A) || !isfinite(B) || !isfinite(C)) return 0;
+
+  const float k = cfg->cutoff_sigma;
+  const float sx2 = sx * sx, sy2 = sy * sy;
+  const float rx = k * sqrtf(fmaf(cc, sx2, ss * sy2));
+  const float ry = k * sqrtf(fmaf(ss, sx2, cc * sy2));
+  const float fx0 = ceilf((mx - rx) - 0.5f);
+  const float fx1 = floorf((mx + rx) - 0.5f);
+  const float fy0 = ceilf((my - ry) - 0.5f);
+  const float fy1 = floorf((my + ry) - 0.5f);
+  const float wmax = (float)(cfg->width - 1);
+  const float hmax = (float)(cfg->height - 1);
+  if (!(fx0 <= fx1) || !(fy0 <= fy1)) return 0;
+  if (fx0 > wmax || fx1 < 0.0f || fy0 > hmax || fy1 < 0.0f) return 0;
+  conic[0] = A;
+  conic[1] = B;
+  conic[2] = C;
+  aabb[0] = (int32_t)fmaxf(fx0, 0.0f);
+  aabb[1] = (int32_t)fmaxf(fy0, 0.0f);
+  aabb[2] = (int32_t)fminf(fx1, wmax);
+  aabb[3] = (int32_t)fminf(fy1, hmax);
+  return 1;
+}
+
+/*
  * Per-Gaussian projection for n Gaussians.
  *   conic[n,3]  FP32 (A, B, C) of Sigma^-1, zero when culled
  *   aabb[n,4]   pixel box (x0, y0, x1, y1) inclusive, (0, 0, -1, -1) when culled
@@ -159,9 +215,13 @@ int32_t gs2dref_project(const ref_cfg* cfg, int32_t n, const float* xy, const fl
 
     float cf[3];
     int32_t b4[4];
-    if (!ref_mask_data(cfg, xy[2 * (int64_t)i], xy[2 * (int64_t)i + 1], chol[3 * (int64_t)i],
-                       chol[3 * (int64_t)i + 1], chol[3 * (int64_t)i + 2], cf, b4))
-      continue;
+    const float* sh = chol + 3 * (int64_t)i;  /* shape parameters, per cfg->param */
+    const int kept = (cfg->param == REF_PARAM_SCALE_ROT)
+                         ? ref_mask_data_sr(cfg, xy[2 * (int64_t)i], xy[2 * (int64_t)i + 1], sh[0],
+                                            sh[1], sh[2], cf, b4)
+                         : ref_mask_data(cfg, xy[2 * (int64_t)i], xy[2 * (int64_t)i + 1], sh[0],
+                                         sh[1], sh[2], cf, b4);
+    if (!kept) continue;
     memcpy(cn, cf, sizeof cf);
     memcpy(bb, b4, sizeof b4);
     rc[0] = b4[0] / cfg->tile;
@@ -253,9 +313,22 @@ static int ref_touches(const ref_cfg* cfg, const float* xy, const float* conic, 
   return q <= kk;
 }
 
-/* Sigma^-1 of L = [[a,0],[b,c]] in double: adj(Sigma)/det(Sigma). */
-static void ref_inverse_cov(const double* L, double* A, double* B, double* C) {
-  const double a = L[0], b = L[1], c = L[2];
+/*
+ * Sigma^-1 = [[A, B], [B, C]] in double from the shape parameters P.
+ * Cholesky, L = [[a,0],[b,c]]: adj(Sigma)/det(Sigma) of Sigma = L L^T.
+ * Scale-rotation (s_x, s_y, theta): R diag(1/s_x^2, 1/s_y^2) R^T.
+ */
+static void ref_inverse_cov(const ref_cfg* cfg, const double* P, double* A, double* B,
+                            double* C) {
+  if (cfg->param == REF_PARAM_SCALE_ROT) {
+    const double c = cos(P[2]), s = sin(P[2]);
+    const double u = 1.0 / (P[0] * P[0]), v = 1.0 / (P[1] * P[1]);
+    *A = c * c * u + s * s * v;
+    *B = c * s * (u - v);
+    *C = s * s * u + c * c * v;
+    return;
+  }
+  const double a = P[0], b = P[1], c = P[2];
   const double sxx = a * a, sxy = a * b, syy = b * b + c * c;
   const double det = sxx * syy - sxy * sxy;
   *A = syy / det;
@@ -264,10 +337,10 @@ static void ref_inverse_cov(const double* L, double* A, double* B, double* C) {
 }
 
 /* One Gaussian at one pixel centre, in double: w = exp(-q/2), plus dx, dy. */
-static double ref_weight(const double* xy, const double* L, int32_t i, int32_t j, double* dx,
-                         double* dy) {
+static double ref_weight(const ref_cfg* cfg, const double* xy, const double* L, int32_t i,
+                         int32_t j, double* dx, double* dy) {
   double A, B, C;
-  ref_inverse_cov(L, &A, &B, &C);
+  ref_inverse_cov(cfg, L, &A, &B, &C);
   *dx = ((double)j + 0.5) - xy[0];
   *dy = ((double)i + 0.5) - xy[1];
   const double q = A * (*dx) * (*dx) + 2.0 * B * (*dx) * (*dy) + C * (*dy) * (*dy);
@@ -318,7 +391,8 @@ static void ref_pixel_fwd(const ref_scene* s, const int32_t* list, int64_t len, 
       continue;
     ++nm;
     double dx, dy;
-    const double w = ref_weight(s->xy + 2 * (int64_t)g, s->chol + 3 * (int64_t)g, i, j, &dx, &dy);
+    const double w =
+        ref_weight(cfg, s->xy + 2 * (int64_t)g, s->chol + 3 * (int64_t)g, i, j, &dx, &dy);
     const double* c = s->rgb + 3 * (int64_t)g;
     if (cfg->mode == REF_MODE_SUM) {
       for (int d = 0; d < 3; ++d) C[d] += c[d] * w;
@@ -487,10 +561,10 @@ typedef struct {
  * w = exp(-q/2):  dw/dq = -w/2,  dq/dmu_x = -2(A dx + B dy),
  * dq/dmu_y = -2(B dx + C dy),  dq/dA = dx^2, dq/dB = 2 dx dy, dq/dC = dy^2.
  */
-static void ref_accumulate_w(ref_grad* g, const double* L, double w, double dLdw, double dx,
-                             double dy) {
+static void ref_accumulate_w(const ref_cfg* cfg, ref_grad* g, const double* L, double w,
+                             double dLdw, double dx, double dy) {
   double A, B, C;
-  ref_inverse_cov(L, &A, &B, &C);
+  ref_inverse_cov(cfg, L, &A, &B, &C);
   const double dq = dLdw * (-0.5 * w);
   g->dmu[0] += dq * (-2.0) * (A * dx + B * dy);
   g->dmu[1] += dq * (-2.0) * (B * dx + C * dy);
@@ -532,7 +606,7 @@ static void ref_pixel_bwd(const ref_scene* s, const int32_t* list, int64_t len, 
         g->drgb[d] += dimg3[d] * e->w;
         dLdw += dimg3[d] * c[d];
       }
-      ref_accumulate_w(g, s->chol + 3 * (int64_t)e->gid, e->w, dLdw, e->dx, e->dy);
+      ref_accumulate_w(cfg, g, s->chol + 3 * (int64_t)e->gid, e->w, dLdw, e->dx, e->dy);
     }
     return;
   }
@@ -553,32 +627,43 @@ static void ref_pixel_bwd(const ref_scene* s, const int32_t* list, int64_t len, 
       }
       const double o = s->opacity[e->gid];
       g->dopac += dLda * e->w;
-      ref_accumulate_w(g, s->chol + 3 * (int64_t)e->gid, e->w, dLda * o, e->dx, e->dy);
+      ref_accumulate_w(cfg, g, s->chol + 3 * (int64_t)e->gid, e->w, dLda * o, e->dx, e->dy);
     }
     for (int d = 0; d < 3; ++d) S[d] += c[d] * e->alpha * e->T;
   }
 }
 
 /*
- * From the inverse-covariance gradient to the Cholesky factor.  With
- * A = b^2/(a^2 c^2) + 1/a^2, B = -b/(a c^2), C = 1/c^2:
+ * From the inverse-covariance gradient to the shape parameters.
+ * Cholesky, with A = b^2/(a^2 c^2) + 1/a^2, B = -b/(a c^2), C = 1/c^2:
  *   dA/da = -2A/a,            dA/db = 2b/(a^2 c^2),  dA/dc = -2b^2/(a^2 c^3),
  *   dB/da = b/(a^2 c^2),      dB/db = -1/(a c^2),    dB/dc = 2b/(a c^3),
  *   dC/dc = -2/c^3.
+ * Scale-rotation, with u = 1/s_x^2, v = 1/s_y^2, c = cos theta, s = sin theta
+ * and A = c^2 u + s^2 v, B = c s (u - v), C = s^2 u + c^2 v:
+ *   d/du = (c^2, c s, s^2), d/dv = (s^2, -c s, c^2) on (A, B, C),
+ *   du/ds_x = -2/s_x^3, dv/ds_y = -2/s_y^3,
+ *   dA/dtheta = -2B, dB/dtheta = (c^2 - s^2)(u - v), dC/dtheta = 2B.
  * The position gradient is the mean gradient (xy is the mean).
  */
-static void ref_finish(const double* L, const ref_grad* g, double* dxy, double* dchol,
-                       double* drgb, double* dopac) {
-  const double a = L[0], b = L[1], c = L[2];
+static void ref_finish(const ref_cfg* cfg, const double* L, const ref_grad* g, double* dxy,
+                       double* dchol, double* drgb, double* dopac) {
   double A, B, C;
-  ref_inverse_cov(L, &A, &B, &C);
-  (void)B;
-  (void)C;
+  ref_inverse_cov(cfg, L, &A, &B, &C);
   const double dA = g->dconic[0], dB = g->dconic[1], dC = g->dconic[2];
-  dchol[0] = dA * (-2.0 * A / a) + dB * (b / (a * a * c * c));
-  dchol[1] = dA * (2.0 * b / (a * a * c * c)) + dB * (-1.0 / (a * c * c));
-  dchol[2] = dA * (-2.0 * b * b / (a * a * c * c * c)) + dB * (2.0 * b / (a * c * c * c)) +
-             dC * (-2.0 / (c * c * c));
+  if (cfg->param == REF_PARAM_SCALE_ROT) {
+    const double sx = L[0], sy = L[1], c = cos(L[2]), s = sin(L[2]);
+    const double u = 1.0 / (sx * sx), v = 1.0 / (sy * sy);
+    dchol[0] = (dA * c * c + dB * c * s + dC * s * s) * (-2.0 / (sx * sx * sx));
+    dchol[1] = (dA * s * s - dB * c * s + dC * c * c) * (-2.0 / (sy * sy * sy));
+    dchol[2] = dA * (-2.0 * B) + dB * (c * c - s * s) * (u - v) + dC * (2.0 * B);
+  } else {
+    const double a = L[0], b = L[1], c = L[2];
+    dchol[0] = dA * (-2.0 * A / a) + dB * (b / (a * a * c * c));
+    dchol[1] = dA * (2.0 * b / (a * a * c * c)) + dB * (-1.0 / (a * c * c));
+    dchol[2] = dA * (-2.0 * b * b / (a * a * c * c * c)) + dB * (2.0 * b / (a * c * c * c)) +
+               dC * (-2.0 / (c * c * c));
+  }
   dxy[0] = g->dmu[0];
   dxy[1] = g->dmu[1];
   for (int d = 0; d < 3; ++d) drgb[d] = g->drgb[d];
@@ -629,7 +714,7 @@ void gs2dref_render_bwd(const ref_cfg* cfg, int32_t n, const double* xy, const d
       if (d_conic) memset(d_conic + 3 * (int64_t)g, 0, 3 * sizeof(double));
       continue;
     }
-    ref_finish(chol + 3 * (int64_t)g, &grads[g], d_xy + 2 * (int64_t)g, d_chol + 3 * (int64_t)g,
+    ref_finish(cfg, chol + 3 * (int64_t)g, &grads[g], d_xy + 2 * (int64_t)g, d_chol + 3 * (int64_t)g,
                d_rgb + 3 * (int64_t)g, d_opacity ? d_opacity + g : &dummy);
     if (d_conic)
       for (int d = 0; d < 3; ++d) d_conic[3 * (int64_t)g + d] = grads[g].dconic[d];
@@ -677,7 +762,7 @@ void gs2dref_render_bwd_gaussians(const ref_cfg* cfg, int32_t n, const double* x
           ref_pixel_bwd(&s, sorted_gid + ranges[2 * t], ranges[2 * t + 1] - ranges[2 * t], i, j,
                         g3, &acc, g, NULL, scratch);
         }
-      ref_finish(chol + 3 * (int64_t)g, &acc, d_xy + 2 * (int64_t)k, d_chol + 3 * (int64_t)k,
+      ref_finish(cfg, chol + 3 * (int64_t)g, &acc, d_xy + 2 * (int64_t)k, d_chol + 3 * (int64_t)k,
                  d_rgb + 3 * (int64_t)k, d_opacity ? d_opacity + k : &dummy);
     } else {
       memset(d_xy + 2 * (int64_t)k, 0, 2 * sizeof(double));

@@ -10,9 +10,10 @@ DIV2K).  Those are not available here; the procedural targets below stand in
 for their shape: smooth regions plus hard edges, values in [0, 1].
 
 All arrays are float32, C-contiguous:
-  xy [N,2] pixel units, chol [N,3] = (l11, l21, l22) of the lower-triangular
-  Cholesky factor, rgb [N,3], depth [N], opacity [N], background [3],
-  target [3,H,W] planar.
+  xy [N,2] pixel units, chol [N,3] = the shape parameters: (l11, l21, l22) of
+  the lower-triangular Cholesky factor, or (s_x, s_y, theta) for workloads
+  with param == SCALE_ROT; rgb [N,3], depth [N], opacity [N], background
+  [3], target [3,H,W] planar.
 """
 from __future__ import annotations
 
@@ -22,6 +23,7 @@ import math
 import numpy as np
 
 SUM, COMPOSITE = 0, 1
+CHOLESKY, SCALE_ROT = 0, 1  # what a workload's shape parameters are
 
 
 # ---------------------------------------------------------------- targets --
@@ -171,6 +173,26 @@ def cholesky_heavy_tail(n: int, rng: np.random.Generator, median: float = 1.5,
     return np.stack([a, b, c], 1).astype(np.float32)
 
 
+def scale_rot_heavy_tail(n: int, rng: np.random.Generator, median: float = 1.5,
+                         log_sigma: float = 1.41, s_max: float = 40.0) -> np.ndarray:
+    """The draws of cholesky_heavy_tail handed over as they are:
+    (s_x, s_y, theta) = (major, minor, rotation)."""
+    s1 = np.minimum(s_max, np.exp(rng.normal(math.log(median), log_sigma, n)))
+    s2 = s1 * rng.uniform(0.3, 1.0, n)
+    th = rng.uniform(0.0, np.pi, n)
+    return np.stack([s1, s2, th], 1).astype(np.float32)
+
+
+def scale_rot_uniform(n: int, scale, rng: np.random.Generator) -> np.ndarray:
+    """(s_x, s_y, theta): scales U(scale) px with random signs (the
+    covariance does not depend on them), theta U(-pi, pi)."""
+    lo, hi = scale
+    sx = rng.uniform(lo, hi, n) * rng.choice([-1.0, 1.0], n)
+    sy = rng.uniform(lo, hi, n) * rng.choice([-1.0, 1.0], n)
+    th = rng.uniform(-np.pi, np.pi, n)
+    return np.stack([sx, sy, th], 1).astype(np.float32)
+
+
 # -------------------------------------------------------------- workloads --
 
 @dataclasses.dataclass
@@ -188,6 +210,7 @@ class Workload:
     background: np.ndarray | None = None
     cutoff_sigma: float = 3.0
     t_min: float = 1e-4
+    param: int = CHOLESKY
 
     @property
     def n(self) -> int:
@@ -228,6 +251,25 @@ def heavy_2048x1360(seed: int = 3000, n: int = 300_000) -> Workload:
                     cholesky_heavy_tail(n, rng), _rgb(n, rng), tgt)
 
 
+def image_768x512_sr(seed: int = 2000, n: int = 50_000) -> Workload:
+    """The 768x512 workload with scale-rotation shapes: scales U(0.7,2.5) px,
+    rotation U(-pi, pi)."""
+    rng = np.random.default_rng(seed)
+    h, w = 512, 768
+    tgt = target_noise_polygons(h, w, rng)
+    return Workload(f"image_768x512_{n // 1000}k_sr", w, h, SUM, positions_by_gradient(n, tgt, rng),
+                    scale_rot_uniform(n, (0.7, 2.5), rng), _rgb(n, rng), tgt, param=SCALE_ROT)
+
+
+def heavy_2048x1360_sr(seed: int = 3000, n: int = 300_000) -> Workload:
+    """heavy_2048x1360 with the same draws given as (scale, rotation)."""
+    rng = np.random.default_rng(seed)
+    h, w = 1360, 2048
+    tgt = target_noise_polygons(h, w, rng, lattice_scale=2048 / 768)
+    return Workload("heavy_2048x1360_300k_sr", w, h, SUM, positions_by_gradient(n, tgt, rng),
+                    scale_rot_heavy_tail(n, rng), _rgb(n, rng), tgt, param=SCALE_ROT)
+
+
 def composite_768x512(seed: int = 4000, n: int = 50_000) -> Workload:
     """The 768x512 workload, alpha-composited: depth U(0,1), opacity
     sigmoid(N(0,1)), background U(0,1)^3."""
@@ -261,19 +303,25 @@ def render_2048x2048(seed: int = 5000, n: int = 500_000) -> Workload:
 
 
 def random_scene(width: int, height: int, n: int, seed: int, mode: int = SUM,
-                 diag=(0.5, 3.0), offdiag_sigma: float = 0.5, margin: float = 0.0) -> Workload:
+                 diag=(0.5, 3.0), offdiag_sigma: float = 0.5, margin: float = 0.0,
+                 param: int = CHOLESKY) -> Workload:
     """Small random scene for parity and edge cases; `margin` px of the
-    positions may fall outside the image."""
+    positions may fall outside the image.  param == SCALE_ROT draws the
+    scales from `diag` instead of the Cholesky diagonal."""
     rng = np.random.default_rng(seed)
     xy = np.stack([rng.uniform(-margin, width + margin, n),
                    rng.uniform(-margin, height + margin, n)], 1).astype(np.float32)
-    chol = cholesky_uniform(n, diag, offdiag_sigma, rng)
-    # random signs on the diagonal: L L^T does not depend on them
-    chol[:, 0] *= rng.choice([-1.0, 1.0], n).astype(np.float32)
-    chol[:, 2] *= rng.choice([-1.0, 1.0], n).astype(np.float32)
+    if param == SCALE_ROT:
+        chol = scale_rot_uniform(n, diag, rng)
+    else:
+        chol = cholesky_uniform(n, diag, offdiag_sigma, rng)
+        # random signs on the diagonal: L L^T does not depend on them
+        chol[:, 0] *= rng.choice([-1.0, 1.0], n).astype(np.float32)
+        chol[:, 2] *= rng.choice([-1.0, 1.0], n).astype(np.float32)
     rgb = _rgb(n, rng)
     tgt = rng.uniform(0.0, 1.0, (3, height, width)).astype(np.float32)
-    wl = Workload(f"random_{width}x{height}_{n}", width, height, mode, xy, chol, rgb, tgt)
+    wl = Workload(f"random_{width}x{height}_{n}", width, height, mode, xy, chol, rgb, tgt,
+                  param=param)
     if mode == COMPOSITE:
         wl.depth = rng.uniform(0.0, 1.0, n).astype(np.float32)
         wl.opacity = (1.0 / (1.0 + np.exp(-rng.normal(0.0, 1.0, n)))).astype(np.float32)
@@ -291,6 +339,8 @@ WORKLOADS = {
     "small_64x64_1k": small_64x64,
     "image_768x512_50k": image_768x512,
     "heavy_2048x1360_300k": heavy_2048x1360,
+    "image_768x512_50k_sr": image_768x512_sr,
+    "heavy_2048x1360_300k_sr": heavy_2048x1360_sr,
     "composite_768x512_50k": composite_768x512,
     "render_4096x4096_2m": render_4096x4096,
     "render_2048x2048_500k": render_2048x2048,

@@ -13,6 +13,7 @@ import oracle
 from oracle import build as obuild
 
 import test_oracle_pins as pins
+import test_oracle_scale_rot as sr_pins
 
 # (name, text in the oracle source, replacement)
 MUTATIONS = [
@@ -32,6 +33,14 @@ MUTATIONS = [
     ("composite: transmittance from opacity", "T *= (1.0 - alpha);", "T *= (1.0 - s->opacity[g]);"),
     ("composite: no early termination", "if (T < (double)cfg->t_min) break;", "if (T < 0.0) break;"),
     ("loss gradient without the 2", "d_image[k] = 2.0 * e / (double)m;", "d_image[k] = e / (double)m;"),
+    ("scale-rot: fp32 off-diagonal sign", "const float B = cs * (u - v);",
+     "const float B = cs * (v - u);"),
+    ("scale-rot: double A with the axes swapped", "*A = c * c * u + s * s * v;",
+     "*A = s * s * u + c * c * v;"),
+    ("scale-rot: box radius from the other axis", "const float rx = k * sqrtf(fmaf(cc, sx2, ss * sy2));",
+     "const float rx = k * sqrtf(fmaf(ss, sx2, cc * sy2));"),
+    ("scale-rot: rotation gradient sign", "dchol[2] = dA * (-2.0 * B)", "dchol[2] = dA * (2.0 * B)"),
+    ("scale-rot: s_y gradient from s_x", "(-2.0 / (sy * sy * sy));", "(-2.0 / (sx * sy * sy));"),
     ("composite lists not depth sorted", "if (cfg->mode == REF_MODE_COMPOSITE) {\n      g_sort_depth = depth;\n      for",
      "if (0) {\n      g_sort_depth = depth;\n      for"),
 ]
@@ -50,6 +59,9 @@ PINS = [
     pins.test_sum_gradients_by_central_differences,
     pins.test_composite_gradients_by_central_differences,
     pins.test_loss_gradient_by_central_differences,
+    sr_pins.test_single_gaussian_matches_library_density,
+    sr_pins.test_pixel_box_is_the_ellipse_box,
+    sr_pins.test_sum_gradients_by_central_differences,
 ]
 
 
