@@ -81,6 +81,8 @@ def _declare(L):
     L.gs2dref_render_pixels.restype = None
     L.gs2dref_render_brute.argtypes = [cfgp, _i32] + [_p] * 12
     L.gs2dref_render_brute.restype = None
+    L.gs2dref_sincos_f32.argtypes = [_i32, _p, _p, _p]
+    L.gs2dref_sincos_f32.restype = None
     L.gs2dref_loss_l2.argtypes = [_i32, _i32, _p, _p, _p]
     L.gs2dref_loss_l2.restype = C.c_double
     L.gs2dref_render_bwd.argtypes = [cfgp, _i32] + [_p] * 18
@@ -161,6 +163,15 @@ def project(cfg: Config, xy, chol, rgb, depth=None, opacity=None) -> Projection:
     valid = lib().gs2dref_project(C.byref(c), n, _ptr(xy), _ptr(chol), _ptr(rgb), _ptr(depth),
                                   _ptr(opacity), _ptr(conic), _ptr(aabb), _ptr(rect), _ptr(count))
     return Projection(conic, aabb, rect, count, int(valid))
+
+
+def sincos_f32(theta):
+    """(sin, cos) of FP32 angles by the FP32 sequence the scale-rotation mask
+    data use."""
+    th = _f32(theta).ravel()
+    sn, cs = np.zeros_like(th), np.zeros_like(th)
+    lib().gs2dref_sincos_f32(int(th.size), _ptr(th), _ptr(sn), _ptr(cs))
+    return sn, cs
 
 
 def bin_tiles(cfg: Config, proj: Projection, depth=None):

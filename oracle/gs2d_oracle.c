@@ -48,8 +48,9 @@
  *     (composite) an opacity outside [0, 1) are culled: they touch no pixel
  *     and get a zero gradient;
  *   - scale-rotation: R(theta) = [[cos, -sin], [sin, cos]] with theta in
- *     radians, scales in pixels; the FP32 mask data use cos and sin taken in
- *     double and rounded to FP32.
+ *     radians, scales in pixels; the FP32 mask data take cos and sin from
+ *     the FP32 evaluation in ref_sincos_f32 (the kernel evaluates the same
+ *     sequence), |theta| > 65536 is culled.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (oracle/build.py).
  * -ffp-contract=off keeps every FP32 product and sum separately rounded, so
@@ -132,20 +133,59 @@ static int ref_mask_data(const ref_cfg* cfg, float mx, float my, float a, float 
 }
 
 /*
+ * sin and cos of theta in FP32, the sequence the kernel evaluates:
+ * Cody and Waite's additive range reduction, theta = k (pi/2) + r with
+ * k = rint(theta * 2/pi) and pi/2 split into three FP32 parts (each product
+ * fused, so r carries no rounding of k * pi/2), |r| <= pi/4 (up to rounding);
+ * the Taylor polynomials of sin r (to r^9) and cos r (to r^10) in Horner
+ * form with the FP32 values of 1/n!; then the quadrant k mod 4 picks
+ * (sin, cos) = (s, c), (c, -s), (-s, -c) or (-c, s).  For |theta| <= 65536,
+ * k is an exact integer.
+ */
+static void ref_sincos_f32(float th, float* sn, float* cs) {
+  const float k = rintf(th * 0.636619747f);
+  float r = fmaf(-k, 1.57079637f, th);
+  r = fmaf(-k, -4.37113883e-08f, r);
+  r = fmaf(-k, -1.71512451e-15f, r);
+  const float r2 = r * r;
+  float p = fmaf(2.75573188e-06f, r2, -1.98412701e-04f);
+  p = fmaf(p, r2, 8.33333377e-03f);
+  p = fmaf(p, r2, -1.66666672e-01f);
+  const float s = fmaf(p * r2, r, r);
+  float q = fmaf(-2.75573200e-07f, r2, 2.48015876e-05f);
+  q = fmaf(q, r2, -1.38888892e-03f);
+  q = fmaf(q, r2, 4.16666679e-02f);
+  q = fmaf(q, r2, -0.5f);
+  const float c = fmaf(q, r2, 1.0f);
+  const int quad = (int)(k - 4.0f * floorf(k * 0.25f));
+  switch (quad) {
+    case 0: *sn = s; *cs = c; break;
+    case 1: *sn = c; *cs = -s; break;
+    case 2: *sn = -s; *cs = -c; break;
+    default: *sn = -c; *cs = s; break;
+  }
+}
+
+/* Exported for the accuracy pin of the FP32 sin/cos. */
+void gs2dref_sincos_f32(int32_t m, const float* th, float* sn, float* cs) {
+  for (int32_t i = 0; i < m; ++i) ref_sincos_f32(th[i], sn + i, cs + i);
+}
+
+/*
  * Mask data from a scale and rotation: Sigma = R diag(s_x^2, s_y^2) R^T, so
  * Sigma^-1 = R diag(u, v) R^T with u = 1/s_x^2, v = 1/s_y^2:
  *     A = c^2 u + s^2 v,   B = c s (u - v),   C = s^2 u + c^2 v   (c = cos, s = sin),
  * and Sigma_xx = c^2 s_x^2 + s^2 s_y^2, Sigma_yy = s^2 s_x^2 + c^2 s_y^2.  FP32
- * order: cos and sin in double rounded to FP32; isx = 1/s_x, u = isx*isx (and
+ * order: cos and sin from ref_sincos_f32; isx = 1/s_x, u = isx*isx (and
  * v alike); A = fma(c*c, u, (s*s)*v), B = (c*s)*(u - v), C = fma(s*s, u, (c*c)*v);
  * r_x = k*sqrt(fma(c*c, s_x*s_x, (s*s)*(s_y*s_y))), r_y = k*sqrt(fma(s*s, s_x*s_x,
  * (c*c)*(s_y*s_y))).  The box rule is that of ref_mask_data.
  */
 static int ref_mask_data_sr(const ref_cfg* cfg, float mx, float my, float sx, float sy,
                             float th, float conic[3], int32_t aabb[4]) {
-  if (sx == 0.0f || sy == 0.0f) return 0;
-  const float co = (float)cos((double)th);
-  const float si = (float)sin((double)th);
+  if (sx == 0.0f || sy == 0.0f || !(fabsf(th) <= 65536.0f)) return 0;
+  float co, si;
+  ref_sincos_f32(th, &si, &co);
   const float isx = 1.0f / sx;
   const float isy = 1.0f / sy;
   const float u = isx * isx;

@@ -41,6 +41,9 @@ MUTATIONS = [
      "const float rx = k * sqrtf(fmaf(ss, sx2, cc * sy2));"),
     ("scale-rot: rotation gradient sign", "dchol[2] = dA * (-2.0 * B)", "dchol[2] = dA * (2.0 * B)"),
     ("scale-rot: s_y gradient from s_x", "(-2.0 / (sy * sy * sy));", "(-2.0 / (sx * sy * sy));"),
+    ("fp32 sin: wrong Taylor coefficient", "p = fmaf(p, r2, -1.66666672e-01f);",
+     "p = fmaf(p, r2, -1.66666672e-02f);"),
+    ("fp32 sincos: quadrant sign", "case 1: *sn = c; *cs = -s; break;", "case 1: *sn = c; *cs = s; break;"),
     ("composite lists not depth sorted", "if (cfg->mode == REF_MODE_COMPOSITE) {\n      g_sort_depth = depth;\n      for",
      "if (0) {\n      g_sort_depth = depth;\n      for"),
 ]
@@ -59,6 +62,7 @@ PINS = [
     pins.test_sum_gradients_by_central_differences,
     pins.test_composite_gradients_by_central_differences,
     pins.test_loss_gradient_by_central_differences,
+    sr_pins.test_fp32_sincos_accuracy,
     sr_pins.test_single_gaussian_matches_library_density,
     sr_pins.test_pixel_box_is_the_ellipse_box,
     sr_pins.test_sum_gradients_by_central_differences,
