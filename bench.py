@@ -180,7 +180,7 @@ def aggregate_replicas(local_ms: float, steps: int, world: int, device=None):
 
 def oracle_step(wl):
     import oracle
-    cfg = oracle.Config(wl.width, wl.height, wl.mode, wl.cutoff_sigma, wl.t_min)
+    cfg = oracle.Config(wl.width, wl.height, wl.mode, wl.cutoff_sigma, wl.t_min, param=wl.param)
     if wl.target is None:
         s = oracle.Scene(cfg, wl.xy, wl.chol, wl.rgb, wl.depth, wl.opacity, wl.background)
         s.render()
@@ -276,7 +276,8 @@ def run_gs2d(args):
     xy, chol, rgb = t(wl.xy), t(wl.chol), t(wl.rgb)
     depth, opac, bg, target = t(wl.depth), t(wl.opacity), t(wl.background), t(wl.target)
 
-    R = gs2d.Rasterizer(wl.width, wl.height, wl.n, wl.mode, wl.cutoff_sigma, wl.t_min, device=dev)
+    R = gs2d.Rasterizer(wl.width, wl.height, wl.n, wl.mode, wl.cutoff_sigma, wl.t_min, device=dev,
+                        param=wl.param)
     R.project(xy, chol, rgb, depth, opac)
     P = R.bin_and_sort(sync=True)
     R._alloc_pairs(int(P * 1.25) + 4096)  # headroom, as a fitting loop would keep
@@ -409,7 +410,7 @@ def run_gs2d(args):
         return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
     h_in = [pinned(a) for a in (wl.xy, wl.chol, wl.rgb, wl.depth, wl.opacity, wl.background, wl.target)]
     d_in = [xy, chol, rgb, depth, opac, bg, target]
-    outs = [R.loss] if fwd_only else [R.loss, R.d_xy, R.d_chol, R.d_rgb]
+    outs = [R.loss] if fwd_only else [R.loss, R.d_xy, R.d_shape, R.d_rgb]
     if fwd_only:
         outs = [R.image]
     h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]

@@ -73,6 +73,17 @@ typedef enum gs2d_status {
 
 enum { GS2D_MODE_SUM = 0, GS2D_MODE_COMPOSITE = 1 };
 
+/*
+ * What the three shape parameters of a Gaussian are (the `shape` arrays):
+ *   GS2D_PARAM_CHOLESKY   (l11, l21, l22): Sigma = L L^T, L = [[l11, 0], [l21, l22]]
+ *                         (DrawingWithGaussians README, MLX-specific notes);
+ *   GS2D_PARAM_SCALE_ROT  (s_x, s_y, theta): Sigma = R diag(s_x^2, s_y^2) R^T,
+ *                         R = [[cos, -sin], [sin, cos]], theta in radians
+ *                         (FlashImgs README, Python API:
+ *                         project_gaussians_2d_scale_rot).
+ */
+enum { GS2D_PARAM_CHOLESKY = 0, GS2D_PARAM_SCALE_ROT = 1 };
+
 /* Device status flags, read back by gs2d_read_status. */
 enum {
   GS2D_FLAG_CAPACITY = 1u << 0,
@@ -89,6 +100,7 @@ typedef struct gs2d_config {
   float t_min;          /* composite only, in [0, 1]: a Gaussian contributes only
                            while the transmittance in front of it is >= t_min;
                            1e-4 by default */
+  int32_t param;        /* GS2D_PARAM_CHOLESKY (0, the default) or GS2D_PARAM_SCALE_ROT */
 } gs2d_config;
 
 /*
@@ -122,10 +134,17 @@ GS2D_API size_t gs2d_workspace_size(const gs2d_config* cfg, int32_t n, int64_t p
 
 /*
  * Projection (one thread per Gaussian).  For each Gaussian i: cull test,
- * Sigma^-1 from L = [[l11, 0], [l21, l22]] (Sigma = L L^T), the pixel box,
- * the tile rectangle and the number of tiles it covers.
+ * Sigma^-1 from the shape parameters, the pixel box, the tile rectangle and
+ * the number of tiles it covers.
  *   xy[n,2]       mean in pixels
- *   chol[n,3]     (l11, l21, l22); the signs of l11 and l22 do not matter
+ *   shape[n,3]    per cfg->param: (l11, l21, l22) -- the signs of l11 and l22
+ *                 do not matter, l11 = 0 or l22 = 0 is culled -- or
+ *                 (s_x, s_y, theta) -- the signs of the scales do not matter,
+ *                 a zero scale or |theta| > 65536 is culled.  With the
+ *                 rotation, sin and cos are taken in FP32 by range reduction
+ *                 (Cody and Waite, pi/2 in three FP32 parts) and Taylor
+ *                 polynomials on [-pi/4, pi/4], within 4e-7 of the exact
+ *                 values for |theta| <= 1000.
  *   rgb[n,3]      colour (sum mode: the amplitude; no clamp)
  *   depth[n]      composite only (NULL in sum mode): front-to-back order key
  *   opacity[n]    composite only (NULL in sum mode): in [0, 1), else culled
@@ -134,7 +153,7 @@ GS2D_API size_t gs2d_workspace_size(const gs2d_config* cfg, int32_t n, int64_t p
  *                 (0, 0, -1, -1) when culled
  *   count[n]      out: tiles in rect, 0 when culled
  */
-GS2D_API gs2d_status gs2d_project(const gs2d_config* cfg, int32_t n, const float* xy, const float* chol,
+GS2D_API gs2d_status gs2d_project(const gs2d_config* cfg, int32_t n, const float* xy, const float* shape,
                          const float* rgb, const float* depth, const float* opacity,
                          gs2d_record* rec, int32_t* rect, int32_t* count, gs2d_stream_t stream);
 
@@ -200,21 +219,22 @@ GS2D_API gs2d_status gs2d_loss_l2(int32_t height, int32_t width, const float* im
  * written to the workspace and then summed per Gaussian in a fixed order,
  * so the result is bit-reproducible.  Every output element is written
  * (culled Gaussians get 0); outputs need no initialisation.
- *   chol[n,3]            the Cholesky factors given to gs2d_project
+ *   shape[n,3]           the shape parameters given to gs2d_project
  *   rec, rect            from gs2d_project
  *   tile_ranges, sorted_gid, workspace   from gs2d_bin_and_sort
  *   background, t_final, last            composite, as given to / returned by
  *                                        gs2d_render_fwd (ignored in sum mode)
  *   d_image[3,H,W]       dL/dC
- *   d_xy[n,2], d_chol[n,3], d_rgb[n,3]   out
+ *   d_xy[n,2], d_shape[n,3], d_rgb[n,3]  out (d_shape in the parameters of
+ *                                        cfg->param)
  *   d_opacity[n]         out, composite (may be NULL)
  *   d_background[3]      out, composite (may be NULL)
  */
-GS2D_API gs2d_status gs2d_render_bwd(const gs2d_config* cfg, int32_t n, const float* chol,
+GS2D_API gs2d_status gs2d_render_bwd(const gs2d_config* cfg, int32_t n, const float* shape,
                             const gs2d_record* rec, const int32_t* rect,
                             const int32_t* tile_ranges, const int32_t* sorted_gid,
                             const float* background, const float* t_final, const int32_t* last,
-                            const float* d_image, float* d_xy, float* d_chol, float* d_rgb,
+                            const float* d_image, float* d_xy, float* d_shape, float* d_rgb,
                             float* d_opacity, float* d_background, void* workspace,
                             gs2d_stream_t stream);
 
@@ -228,21 +248,21 @@ GS2D_API gs2d_status gs2d_render_bwd(const gs2d_config* cfg, int32_t n, const fl
  * for the pair-parallel backward.  Results equal the three separate calls
  * up to the order of floating-point additions; every sum is taken in a
  * fixed order, so they are bit-reproducible.
- *   chol, rec, rect      as for gs2d_render_bwd
+ *   shape, rec, rect     as for gs2d_render_bwd
  *   tile_ranges, sorted_gid, workspace   from gs2d_bin_and_sort
  *   background[3]        composite (NULL: black; ignored in sum mode)
  *   target[3,H,W]        the image to fit
  *   image[3,H,W]         out, may be NULL (not written)
  *   loss                 out: one float (device), (1/(3HW)) sum (C - target)^2
- *   d_xy[n,2], d_chol[n,3], d_rgb[n,3]   out, every element written
+ *   d_xy[n,2], d_shape[n,3], d_rgb[n,3]  out, every element written
  *   d_opacity[n], d_background[3]        out, composite (may be NULL)
  * Errors as for gs2d_render_bwd; target and loss must be non-NULL.
  */
-GS2D_API gs2d_status gs2d_render_fwd_bwd_l2(const gs2d_config* cfg, int32_t n, const float* chol,
+GS2D_API gs2d_status gs2d_render_fwd_bwd_l2(const gs2d_config* cfg, int32_t n, const float* shape,
                                             const gs2d_record* rec, const int32_t* rect,
                                             const int32_t* tile_ranges, const int32_t* sorted_gid,
                                             const float* background, const float* target,
-                                            float* image, float* loss, float* d_xy, float* d_chol,
+                                            float* image, float* loss, float* d_xy, float* d_shape,
                                             float* d_rgb, float* d_opacity, float* d_background,
                                             void* workspace, gs2d_stream_t stream);
 

@@ -170,6 +170,38 @@ __device__ __forceinline__ unsigned int box_lanes(uint2 b, int bx0, int by0) {
   return (cols * 0x01010101u) & rows;
 }
 
+// sin and cos of theta in FP32 for the scale-rotation shape: Cody and Waite's
+// additive range reduction, theta = k (pi/2) + r with k = rint(theta * 2/pi)
+// and pi/2 split into three FP32 parts (fused products, so r carries no
+// rounding of k * pi/2), |r| <= pi/4; the Taylor polynomials of sin r (to
+// r^9) and cos r (to r^10) in Horner form with the FP32 values of 1/n!; the
+// quadrant k mod 4 then swaps and negates them.  Every step is an explicitly
+// rounded operation so that the result is the same FP32 value wherever the
+// sequence is evaluated.  For |theta| <= 65536, k is an exact integer.
+__device__ __forceinline__ void sincos_fp32(float th, float* sn, float* cs) {
+  const float k = rintf(__fmul_rn(th, 0.636619747f));
+  float r = __fmaf_rn(-k, 1.57079637f, th);
+  r = __fmaf_rn(-k, -4.37113883e-08f, r);
+  r = __fmaf_rn(-k, -1.71512451e-15f, r);
+  const float r2 = __fmul_rn(r, r);
+  float p = __fmaf_rn(2.75573188e-06f, r2, -1.98412701e-04f);
+  p = __fmaf_rn(p, r2, 8.33333377e-03f);
+  p = __fmaf_rn(p, r2, -1.66666672e-01f);
+  const float s = __fmaf_rn(__fmul_rn(p, r2), r, r);
+  float q = __fmaf_rn(-2.75573200e-07f, r2, 2.48015876e-05f);
+  q = __fmaf_rn(q, r2, -1.38888892e-03f);
+  q = __fmaf_rn(q, r2, 4.16666679e-02f);
+  q = __fmaf_rn(q, r2, -0.5f);
+  const float c = __fmaf_rn(q, r2, 1.0f);
+  const int quad = int(__fsub_rn(k, __fmul_rn(4.0f, floorf(__fmul_rn(k, 0.25f)))));
+  switch (quad) {
+    case 0: *sn = s; *cs = c; break;
+    case 1: *sn = c; *cs = -s; break;
+    case 2: *sn = -s; *cs = -c; break;
+    default: *sn = -c; *cs = s; break;
+  }
+}
+
 // Monotone map of a finite float to uint32 (IEEE order, -0 mapped as +0).
 __device__ __forceinline__ unsigned int depth_key(float d) {
   unsigned int u = __float_as_uint(d);

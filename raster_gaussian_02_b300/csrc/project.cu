@@ -1,9 +1,11 @@
-// Projection (Cholesky factor -> inverse covariance, 3-sigma pixel box, tile
-// rectangle) and its backward (per-pair partial gradients summed per
-// Gaussian, then the chain rule from the inverse covariance to L).
+// Projection (shape parameters -> inverse covariance, 3-sigma pixel box,
+// tile rectangle) and its backward (per-pair partial gradients summed per
+// Gaussian, then the chain rule from the inverse covariance to the shape).
 //
 // Sigma = L L^T with L = [[a, 0], [b, c]] (DrawingWithGaussians README,
-// MLX-specific notes: lower-triangular L); the 8 parameters per Gaussian are
+// MLX-specific notes: lower-triangular L), or Sigma = R diag(s_x^2, s_y^2) R^T
+// (FlashImgs README, Python API: project_gaussians_2d_scale_rot; GaussianImage
+// project page, the "rs" scripts); the 8 parameters per Gaussian are
 // position, covariance and colour (GaussianImage project page, Overview).
 #include "gs2d_internal.cuh"
 
@@ -28,30 +30,50 @@ k_project(gs2d_config c, int n, const float* __restrict__ xy, const float* __res
     o = opacity[i];
     d = depth[i];
   }
+  const bool rot = c.param == GS2D_PARAM_SCALE_ROT;  // (a, b, cc) = (s_x, s_y, theta)
   bool ok = isfinite(mx) && isfinite(my) && isfinite(a) && isfinite(b) && isfinite(cc) &&
-            isfinite(r) && isfinite(g) && isfinite(bl) && a != 0.0f && cc != 0.0f;
+            isfinite(r) && isfinite(g) && isfinite(bl);
+  ok = ok && (rot ? (a != 0.0f && b != 0.0f && fabsf(cc) <= 65536.0f) : (a != 0.0f && cc != 0.0f));
   if (comp) ok = ok && isfinite(d) && isfinite(o) && o >= 0.0f && o < 1.0f;
 
-  // Sigma^-1 = [[A, B], [B, C]]: A = (b^2 + c^2)/(a^2 c^2), B = -b/(a c^2),
-  // C = 1/c^2, in this FP32 order (IEEE division, explicit rounding).
-  float A = 0.0f, B = 0.0f, C = 0.0f;
+  // Sigma^-1 = [[A, B], [B, C]] and the box half widths k*sqrt(Sigma_xx),
+  // k*sqrt(Sigma_yy), in these FP32 orders (IEEE division, explicit rounding):
+  //   Cholesky: A = (b^2 + c^2)/(a^2 c^2), B = -b/(a c^2), C = 1/c^2;
+  //     Sigma_xx = a^2, Sigma_yy = b^2 + c^2.
+  //   scale-rotation: u = 1/s_x^2, v = 1/s_y^2, c = cos, s = sin:
+  //     A = c^2 u + s^2 v, B = c s (u - v), C = s^2 u + c^2 v;
+  //     Sigma_xx = c^2 s_x^2 + s^2 s_y^2, Sigma_yy = s^2 s_x^2 + c^2 s_y^2.
+  float A = 0.0f, B = 0.0f, C = 0.0f, rx = 0.0f, ry = 0.0f;
   if (ok) {
-    const float ia = __fdiv_rn(1.0f, a);
-    const float ic = __fdiv_rn(1.0f, cc);
-    C = __fmul_rn(ic, ic);
-    const float t = __fmul_rn(b, ia);
-    B = -__fmul_rn(t, C);
-    A = __fmaf_rn(__fmul_rn(t, t), C, __fmul_rn(ia, ia));
+    const float k = c.cutoff_sigma;
+    if (rot) {
+      float sn, cs;
+      sincos_fp32(cc, &sn, &cs);
+      const float isx = __fdiv_rn(1.0f, a), isy = __fdiv_rn(1.0f, b);
+      const float u = __fmul_rn(isx, isx), v = __fmul_rn(isy, isy);
+      const float c2 = __fmul_rn(cs, cs), s2 = __fmul_rn(sn, sn), csn = __fmul_rn(cs, sn);
+      A = __fmaf_rn(c2, u, __fmul_rn(s2, v));
+      B = __fmul_rn(csn, __fsub_rn(u, v));
+      C = __fmaf_rn(s2, u, __fmul_rn(c2, v));
+      const float sx2 = __fmul_rn(a, a), sy2 = __fmul_rn(b, b);
+      rx = __fmul_rn(k, __fsqrt_rn(__fmaf_rn(c2, sx2, __fmul_rn(s2, sy2))));
+      ry = __fmul_rn(k, __fsqrt_rn(__fmaf_rn(s2, sx2, __fmul_rn(c2, sy2))));
+    } else {
+      const float ia = __fdiv_rn(1.0f, a);
+      const float ic = __fdiv_rn(1.0f, cc);
+      C = __fmul_rn(ic, ic);
+      const float t = __fmul_rn(b, ia);
+      B = -__fmul_rn(t, C);
+      A = __fmaf_rn(__fmul_rn(t, t), C, __fmul_rn(ia, ia));
+      rx = __fmul_rn(k, fabsf(a));
+      ry = __fmul_rn(k, __fsqrt_rn(__fmaf_rn(b, b, __fmul_rn(cc, cc))));
+    }
     ok = isfinite(A) && isfinite(B) && isfinite(C);
   }
-  // Tight box of the ellipse q <= k^2: half widths k*sqrt(Sigma_xx) = k|a| and
-  // k*sqrt(Sigma_yy) = k*sqrt(b^2 + c^2); column j is inside when its centre
+  // Tight box of the ellipse q <= k^2; column j is inside when its centre
   // j + 0.5 lies in [mu_x - r_x, mu_x + r_x].
   int x0 = 0, y0 = 0, x1 = -1, y1 = -1;
   if (ok) {
-    const float k = c.cutoff_sigma;
-    const float rx = __fmul_rn(k, fabsf(a));
-    const float ry = __fmul_rn(k, __fsqrt_rn(__fmaf_rn(b, b, __fmul_rn(cc, cc))));
     const float fx0 = ceilf(__fsub_rn(__fsub_rn(mx, rx), 0.5f));
     const float fx1 = floorf(__fsub_rn(__fadd_rn(mx, rx), 0.5f));
     const float fy0 = ceilf(__fsub_rn(__fsub_rn(my, ry), 0.5f));
@@ -84,10 +106,16 @@ k_project(gs2d_config c, int n, const float* __restrict__ xy, const float* __res
 }
 
 // Per Gaussian: sum its per-pair partials (one per tile of its rectangle, in
-// emission order) and apply the chain rule to L:
+// emission order) and apply the chain rule to the shape parameters.
+// Cholesky:
 //   dA/da = -2A/a,        dA/db = 2b/(a^2 c^2),  dA/dc = -2b^2/(a^2 c^3)
 //   dB/da = b/(a^2 c^2),  dB/db = -1/(a c^2),    dB/dc = 2b/(a c^3)
-//   dC/dc = -2/c^3;       d(xy) = d(mean).
+//   dC/dc = -2/c^3.
+// Scale-rotation (u = 1/s_x^2, v = 1/s_y^2, c = cos theta, s = sin theta):
+//   d(A, B, C)/du = (c^2, c s, s^2),  d(A, B, C)/dv = (s^2, -c s, c^2),
+//   du/ds_x = -2/s_x^3,  dv/ds_y = -2/s_y^3,
+//   d(A, B, C)/dtheta = (-2B, (c^2 - s^2)(u - v), 2B).
+// d(xy) = d(mean).
 // The last block also sums, in a fixed order, the per-tile background
 // partials (composite, d_bg non-null) and the fused pass's per-block loss
 // partials (loss non-null; the total is divided by m, the number of image
@@ -100,7 +128,7 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
          float* __restrict__ d_xy, float* __restrict__ d_chol, float* __restrict__ d_rgb,
          float* __restrict__ d_opacity, int T, const float4* __restrict__ tile_partials,
          float* __restrict__ d_bg, const float* __restrict__ loss_partials, int loss_blocks,
-         float* __restrict__ loss, float m) {
+         float* __restrict__ loss, float m, int param) {
   pdl_enter();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   const bool bad = (hdr->flags & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) != 0;
@@ -121,14 +149,26 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
     float g0 = 0.f, g1 = 0.f, g2 = 0.f;
     if (cnt > 0 && !bad) {
       const float a = chol[3 * i], b = chol[3 * i + 1], c = chol[3 * i + 2];
-      const float A = rec[3 * size_t(i)].z;
-      const float ia = 1.0f / a, ic = 1.0f / c;
-      const float ia2ic2 = ia * ia * ic * ic;
       const float dA = s[2], dB = s[3], dC = s[4];
-      g0 = dA * (-2.0f * A * ia) + dB * (b * ia2ic2);
-      g1 = dA * (2.0f * b * ia2ic2) + dB * (-ia * ic * ic);
-      g2 = dA * (-2.0f * b * b * ia2ic2 * ic) + dB * (2.0f * b * ia * ic * ic * ic) +
-           dC * (-2.0f * ic * ic * ic);
+      if (param == GS2D_PARAM_SCALE_ROT) {
+        float sn, cs;
+        sincos_fp32(c, &sn, &cs);
+        const float isx = 1.0f / a, isy = 1.0f / b;
+        const float u = isx * isx, v = isy * isy;
+        const float c2 = cs * cs, s2 = sn * sn, csn = cs * sn;
+        const float Bv = csn * (u - v);
+        g0 = (dA * c2 + dB * csn + dC * s2) * (-2.0f * u * isx);
+        g1 = (dA * s2 - dB * csn + dC * c2) * (-2.0f * v * isy);
+        g2 = 2.0f * Bv * (dC - dA) + dB * (c2 - s2) * (u - v);
+      } else {
+        const float A = rec[3 * size_t(i)].z;
+        const float ia = 1.0f / a, ic = 1.0f / c;
+        const float ia2ic2 = ia * ia * ic * ic;
+        g0 = dA * (-2.0f * A * ia) + dB * (b * ia2ic2);
+        g1 = dA * (2.0f * b * ia2ic2) + dB * (-ia * ic * ic);
+        g2 = dA * (-2.0f * b * b * ia2ic2 * ic) + dB * (2.0f * b * ia * ic * ic * ic) +
+             dC * (-2.0f * ic * ic * ic);
+      }
     } else {
       for (int k = 0; k < 9; ++k) s[k] = 0.f;
     }
@@ -203,11 +243,11 @@ cudaError_t launch_gather(const gs2d_config& c, int n, const float* chol, const 
   const int4* rc = reinterpret_cast<const int4*>(rect);
   if (c.mode == GS2D_MODE_COMPOSITE)
     GS2D_TRY(launch(k_gather<true>, dim3(blocks), dim3(256), 0, s, n, chol, r, rc, offsets, partials, hdr,
-                    d_xy, d_chol, d_rgb, d_opacity, T, tp, d_bg, lp, loss_blocks, loss, m));
+                    d_xy, d_chol, d_rgb, d_opacity, T, tp, d_bg, lp, loss_blocks, loss, m, int(c.param)));
   else
     GS2D_TRY(launch(k_gather<false>, dim3(blocks), dim3(256), 0, s, n, chol, r, rc, offsets, partials, hdr,
                     d_xy, d_chol, d_rgb, static_cast<float*>(nullptr), T, tp,
-                    static_cast<float*>(nullptr), lp, loss_blocks, loss, m));
+                    static_cast<float*>(nullptr), lp, loss_blocks, loss, m, int(c.param)));
   return cudaGetLastError();
 }
 

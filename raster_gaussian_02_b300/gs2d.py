@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libgs2d.so")
 
 GS2D_OK, GS2D_ERR_INVALID_ARG, GS2D_ERR_CAPACITY, GS2D_ERR_CUDA, GS2D_ERR_TIMEOUT, GS2D_ERR_OVERFLOW = range(6)
 GS2D_MODE_SUM, GS2D_MODE_COMPOSITE = 0, 1
+GS2D_PARAM_CHOLESKY, GS2D_PARAM_SCALE_ROT = 0, 1
 GS2D_FLAG_CAPACITY, GS2D_FLAG_OVERFLOW, GS2D_FLAG_TIMEOUT = 1, 2, 4
 RECORD_BYTES = 48
 TILE = 16
@@ -28,12 +29,14 @@ TILE = 16
 
 class gs2d_config(C.Structure):
     _fields_ = [("width", C.c_int32), ("height", C.c_int32), ("tile", C.c_int32),
-                ("mode", C.c_int32), ("cutoff_sigma", C.c_float), ("t_min", C.c_float)]
+                ("mode", C.c_int32), ("cutoff_sigma", C.c_float), ("t_min", C.c_float),
+                ("param", C.c_int32)]
 
 
 def make_config(width: int, height: int, mode: int = GS2D_MODE_SUM, cutoff_sigma: float = 3.0,
-                t_min: float = 1e-4) -> gs2d_config:
-    return gs2d_config(int(width), int(height), TILE, int(mode), float(cutoff_sigma), float(t_min))
+                t_min: float = 1e-4, param: int = GS2D_PARAM_CHOLESKY) -> gs2d_config:
+    return gs2d_config(int(width), int(height), TILE, int(mode), float(cutoff_sigma), float(t_min),
+                       int(param))
 
 
 class Gs2dError(RuntimeError):
@@ -117,8 +120,8 @@ def gs2d_workspace_size(cfg: gs2d_config, n: int, pair_capacity: int) -> int:
     return int(lib().gs2d_workspace_size(C.byref(cfg), int(n), int(pair_capacity)))
 
 
-def gs2d_project(cfg, n, xy, chol, rgb, depth, opacity, rec, rect, count, stream=None) -> int:
-    return lib().gs2d_project(C.byref(cfg), int(n), _ptr(xy, _f32, "xy"), _ptr(chol, _f32, "chol"),
+def gs2d_project(cfg, n, xy, shape, rgb, depth, opacity, rec, rect, count, stream=None) -> int:
+    return lib().gs2d_project(C.byref(cfg), int(n), _ptr(xy, _f32, "xy"), _ptr(shape, _f32, "shape"),
                               _ptr(rgb, _f32, "rgb"), _ptr(depth, _f32, "depth"),
                               _ptr(opacity, _f32, "opacity"), _ptr(rec, None, "rec"),
                               _ptr(rect, _i32, "rect"), _ptr(count, _i32, "count"), _stream(stream))
@@ -161,28 +164,28 @@ def gs2d_loss_l2_noalloc(height, width, image, target, loss, d_image, stream=Non
                                       _ptr(d_image, _f32, "d_image"), _stream(stream))
 
 
-def gs2d_render_bwd(cfg, n, chol, rec, rect, tile_ranges, sorted_gid, background, t_final, last,
-                    d_image, d_xy, d_chol, d_rgb, d_opacity, d_background, workspace,
+def gs2d_render_bwd(cfg, n, shape, rec, rect, tile_ranges, sorted_gid, background, t_final, last,
+                    d_image, d_xy, d_shape, d_rgb, d_opacity, d_background, workspace,
                     stream=None) -> int:
     return lib().gs2d_render_bwd(
-        C.byref(cfg), int(n), _ptr(chol, _f32, "chol"), _ptr(rec, None, "rec"),
+        C.byref(cfg), int(n), _ptr(shape, _f32, "shape"), _ptr(rec, None, "rec"),
         _ptr(rect, _i32, "rect"), _ptr(tile_ranges, _i32, "tile_ranges"),
         _ptr(sorted_gid, _i32, "sorted_gid"), _ptr(background, _f32, "background"),
         _ptr(t_final, _f32, "t_final"), _ptr(last, _i32, "last"), _ptr(d_image, _f32, "d_image"),
-        _ptr(d_xy, _f32, "d_xy"), _ptr(d_chol, _f32, "d_chol"), _ptr(d_rgb, _f32, "d_rgb"),
+        _ptr(d_xy, _f32, "d_xy"), _ptr(d_shape, _f32, "d_shape"), _ptr(d_rgb, _f32, "d_rgb"),
         _ptr(d_opacity, _f32, "d_opacity"), _ptr(d_background, _f32, "d_background"),
         _ptr(workspace, None, "workspace"), _stream(stream))
 
 
-def gs2d_render_fwd_bwd_l2(cfg, n, chol, rec, rect, tile_ranges, sorted_gid, background, target,
-                           image, loss, d_xy, d_chol, d_rgb, d_opacity, d_background, workspace,
+def gs2d_render_fwd_bwd_l2(cfg, n, shape, rec, rect, tile_ranges, sorted_gid, background, target,
+                           image, loss, d_xy, d_shape, d_rgb, d_opacity, d_background, workspace,
                            stream=None) -> int:
     return lib().gs2d_render_fwd_bwd_l2(
-        C.byref(cfg), int(n), _ptr(chol, _f32, "chol"), _ptr(rec, None, "rec"),
+        C.byref(cfg), int(n), _ptr(shape, _f32, "shape"), _ptr(rec, None, "rec"),
         _ptr(rect, _i32, "rect"), _ptr(tile_ranges, _i32, "tile_ranges"),
         _ptr(sorted_gid, _i32, "sorted_gid"), _ptr(background, _f32, "background"),
         _ptr(target, _f32, "target"), _ptr(image, _f32, "image"), _ptr(loss, _f32, "loss"),
-        _ptr(d_xy, _f32, "d_xy"), _ptr(d_chol, _f32, "d_chol"), _ptr(d_rgb, _f32, "d_rgb"),
+        _ptr(d_xy, _f32, "d_xy"), _ptr(d_shape, _f32, "d_shape"), _ptr(d_rgb, _f32, "d_rgb"),
         _ptr(d_opacity, _f32, "d_opacity"), _ptr(d_background, _f32, "d_background"),
         _ptr(workspace, None, "workspace"), _stream(stream))
 
@@ -206,8 +209,8 @@ class Rasterizer:
     """
 
     def __init__(self, width, height, n, mode=GS2D_MODE_SUM, cutoff_sigma=3.0, t_min=1e-4,
-                 pair_capacity=None, device="cuda"):
-        self.cfg = make_config(width, height, mode, cutoff_sigma, t_min)
+                 pair_capacity=None, device="cuda", param=GS2D_PARAM_CHOLESKY):
+        self.cfg = make_config(width, height, mode, cutoff_sigma, t_min, param)
         self.width, self.height, self.n, self.mode = int(width), int(height), int(n), int(mode)
         self.device = torch.device(device)
         self.num_tiles = ((width + TILE - 1) // TILE) * ((height + TILE - 1) // TILE)
@@ -223,7 +226,7 @@ class Rasterizer:
         self.loss = torch.empty(1, dtype=_f32, device=d)
         self.d_image = torch.empty((3, height, width), dtype=_f32, device=d)
         self.d_xy = torch.empty((max(n, 1), 2), dtype=_f32, device=d)
-        self.d_chol = torch.empty((max(n, 1), 3), dtype=_f32, device=d)
+        self.d_shape = torch.empty((max(n, 1), 3), dtype=_f32, device=d)
         self.d_rgb = torch.empty((max(n, 1), 3), dtype=_f32, device=d)
         self.d_opacity = torch.empty(max(n, 1), dtype=_f32, device=d) if comp else None
         self.d_background = torch.empty(3, dtype=_f32, device=d) if comp else None
@@ -238,9 +241,9 @@ class Rasterizer:
             raise ValueError("invalid configuration for gs2d_workspace_size")
         self.workspace = torch.empty(ws, dtype=_u8, device=self.device)
 
-    def project(self, xy, chol, rgb, depth=None, opacity=None):
-        self.xy, self.chol, self.rgb, self.depth, self.opacity = xy, chol, rgb, depth, opacity
-        check(gs2d_project(self.cfg, self.n, xy, chol, rgb, depth, opacity, self.rec, self.rect,
+    def project(self, xy, shape, rgb, depth=None, opacity=None):
+        self.xy, self.shape, self.rgb, self.depth, self.opacity = xy, shape, rgb, depth, opacity
+        check(gs2d_project(self.cfg, self.n, xy, shape, rgb, depth, opacity, self.rec, self.rect,
                            self.count), "gs2d_project")
 
     def bin_and_sort(self, sync: bool = True, grow: bool = True):
@@ -276,9 +279,9 @@ class Rasterizer:
 
     def render_bwd(self, d_image=None):
         d_image = self.d_image if d_image is None else d_image
-        check(gs2d_render_bwd(self.cfg, self.n, self.chol, self.rec, self.rect, self.tile_ranges,
+        check(gs2d_render_bwd(self.cfg, self.n, self.shape, self.rec, self.rect, self.tile_ranges,
                               self.sorted_gid, self.background, self.t_final, self.last, d_image,
-                              self.d_xy, self.d_chol, self.d_rgb, self.d_opacity,
+                              self.d_xy, self.d_shape, self.d_rgb, self.d_opacity,
                               self.d_background, self.workspace), "gs2d_render_bwd")
 
     def render_fwd_bwd_l2(self, target, background=None, write_image=True):
@@ -286,19 +289,19 @@ class Rasterizer:
         gather).  Fills loss and the d_* gradients, and the image unless
         write_image is False; d_image, t_final and last are not written."""
         self.background = background
-        check(gs2d_render_fwd_bwd_l2(self.cfg, self.n, self.chol, self.rec, self.rect,
+        check(gs2d_render_fwd_bwd_l2(self.cfg, self.n, self.shape, self.rec, self.rect,
                                      self.tile_ranges, self.sorted_gid, background, target,
                                      self.image if write_image else None, self.loss, self.d_xy,
-                                     self.d_chol, self.d_rgb, self.d_opacity, self.d_background,
+                                     self.d_shape, self.d_rgb, self.d_opacity, self.d_background,
                                      self.workspace), "gs2d_render_fwd_bwd_l2")
         return self.loss
 
-    def step(self, xy, chol, rgb, target, depth=None, opacity=None, background=None, sync=False,
+    def step(self, xy, shape, rgb, target, depth=None, opacity=None, background=None, sync=False,
              fused=False):
         """One pass of the whole path: project, bin and sort, forward, L2
         loss, backward (fused=True: the last three in one fused call).
         Returns the device loss tensor."""
-        self.project(xy, chol, rgb, depth, opacity)
+        self.project(xy, shape, rgb, depth, opacity)
         self.bin_and_sort(sync=sync)
         if fused:
             return self.render_fwd_bwd_l2(target, background)

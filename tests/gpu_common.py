@@ -34,13 +34,13 @@ def to_dev(a, dev="cuda"):
 
 
 def oracle_cfg(wl) -> oracle.Config:
-    return oracle.Config(wl.width, wl.height, wl.mode, wl.cutoff_sigma, wl.t_min)
+    return oracle.Config(wl.width, wl.height, wl.mode, wl.cutoff_sigma, wl.t_min, param=wl.param)
 
 
 def gpu_run(wl, d_image=None, capacity=None, sync=True, backward=True):
     """Whole path on the GPU; returns numpy copies of every output."""
     R = gs2d.Rasterizer(wl.width, wl.height, wl.n, wl.mode, wl.cutoff_sigma, wl.t_min,
-                        pair_capacity=capacity)
+                        pair_capacity=capacity, param=wl.param)
     xy, chol, rgb = to_dev(wl.xy), to_dev(wl.chol), to_dev(wl.rgb)
     depth, opac, bg = to_dev(wl.depth), to_dev(wl.opacity), to_dev(wl.background)
     R.project(xy, chol, rgb, depth, opac)
@@ -67,7 +67,7 @@ def gpu_run(wl, d_image=None, capacity=None, sync=True, backward=True):
     if backward:
         out["loss"] = float(R.loss.item()) if wl.target is not None else None
         out["d_image"] = R.d_image.cpu().numpy()
-        out["grads"] = dict(xy=R.d_xy[: wl.n].cpu().numpy(), chol=R.d_chol[: wl.n].cpu().numpy(),
+        out["grads"] = dict(xy=R.d_xy[: wl.n].cpu().numpy(), chol=R.d_shape[: wl.n].cpu().numpy(),
                             rgb=R.d_rgb[: wl.n].cpu().numpy())
         if R.d_opacity is not None:
             out["grads"]["opacity"] = R.d_opacity[: wl.n].cpu().numpy()
@@ -165,6 +165,22 @@ def full_parity(wl, composite=None, check_chain=True):
     else:
         check_grads(g["grads"], gr, keys)
     return g, s, ref
+
+
+def _sampled_bwd_common(g, s: oracle.Scene, wl, rng, m_pix=20000, m_gauss=1500):
+    """Full-size check by sampling: pixels against the oracle's per-pixel
+    forward, the loss, and Gaussians against its per-Gaussian backward."""
+    H, W = s.cfg.height, s.cfg.width
+    pix = rng.choice(H * W, size=min(m_pix, H * W), replace=False)
+    ref = s.render_pixels(pix)
+    err = image_errors(g["image"].reshape(3, -1)[:, pix].T, ref["rgb"])
+    assert err.max(initial=0) <= IMG_TOL, err.max()
+    loss_ref, _ = oracle.loss_l2(g["image"], wl.target)
+    assert abs(g["loss"] - loss_ref) <= 1e-5 * loss_ref
+    valid = np.nonzero(s.proj.count > 0)[0]
+    gids = np.sort(rng.choice(valid, size=min(m_gauss, len(valid)), replace=False)).astype(np.int32)
+    gr = s.render_bwd_gaussians(g["d_image"].astype(np.float64), gids)
+    check_grads({k: g["grads"][k][gids] for k in ("xy", "chol", "rgb")}, gr, ("xy", "chol", "rgb"))
 
 
 def _gaussians_touching(s: oracle.Scene, pix_mask):

@@ -71,10 +71,13 @@ def test_workspace_size(gs2d):
            gs2d.gs2d_config(768, 512, 16, 2, 3.0, 1e-4), gs2d.gs2d_config(768, 512, 16, 0, 0.0, 1e-4),
            gs2d.gs2d_config(768, 512, 16, 0, float("nan"), 1e-4),
            gs2d.gs2d_config(40000, 512, 16, 0, 3.0, 1e-4),
-           gs2d.gs2d_config(768, 512, 16, 1, 3.0, 2.0)]
+           gs2d.gs2d_config(768, 512, 16, 1, 3.0, 2.0),
+           gs2d.gs2d_config(768, 512, 16, 0, 3.0, 1e-4, 2)]
     for c in bad:
         assert gs2d.gs2d_workspace_size(c, 10, 10) == 0
     assert gs2d.gs2d_workspace_size(cfg, -1, 10) == 0
+    sr = gs2d.make_config(768, 512, param=gs2d.GS2D_PARAM_SCALE_ROT)
+    assert gs2d.gs2d_workspace_size(sr, 50_000, 200_000) == a
     assert gs2d.gs2d_workspace_size(cfg, 10, 1 << 30) == 0
 
 

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 def fused_run(wl, write_image=True, capacity=None):
     R = gs2d.Rasterizer(wl.width, wl.height, wl.n, wl.mode, wl.cutoff_sigma, wl.t_min,
-                        pair_capacity=capacity)
+                        pair_capacity=capacity, param=wl.param)
     R.project(to_dev(wl.xy), to_dev(wl.chol), to_dev(wl.rgb), to_dev(wl.depth),
               to_dev(wl.opacity))
     R.bin_and_sort(sync=True)
@@ -30,7 +30,7 @@ def fused_run(wl, write_image=True, capacity=None):
     R.render_fwd_bwd_l2(to_dev(wl.target), to_dev(wl.background), write_image=write_image)
     torch.cuda.synchronize()
     out = dict(image=R.image.cpu().numpy(), loss=float(R.loss.item()),
-               grads=dict(xy=R.d_xy[: wl.n].cpu().numpy(), chol=R.d_chol[: wl.n].cpu().numpy(),
+               grads=dict(xy=R.d_xy[: wl.n].cpu().numpy(), chol=R.d_shape[: wl.n].cpu().numpy(),
                           rgb=R.d_rgb[: wl.n].cpu().numpy()))
     if R.d_opacity is not None:
         out["grads"]["opacity"] = R.d_opacity[: wl.n].cpu().numpy()
