@@ -85,9 +85,9 @@ def _declare(L):
     L.gs2dref_sincos_f32.restype = None
     L.gs2dref_loss_l2.argtypes = [_i32, _i32, _p, _p, _p]
     L.gs2dref_loss_l2.restype = C.c_double
-    L.gs2dref_render_bwd.argtypes = [cfgp, _i32] + [_p] * 18
+    L.gs2dref_render_bwd.argtypes = [cfgp, _i32] + [_p] * 19
     L.gs2dref_render_bwd.restype = None
-    L.gs2dref_render_bwd_gaussians.argtypes = [cfgp, _i32] + [_p] * 12 + [_p, _i32] + [_p] * 4
+    L.gs2dref_render_bwd_gaussians.argtypes = [cfgp, _i32] + [_p] * 12 + [_p, _i32] + [_p] * 5
     L.gs2dref_render_bwd_gaussians.restype = None
 
 
@@ -267,24 +267,26 @@ class Scene:
         d_image = _f64(d_image, (3, self.cfg.height, self.cfg.width))
         n = self.n
         dxy = np.zeros((n, 2)); dchol = np.zeros((n, 3)); drgb = np.zeros((n, 3))
-        dop = np.zeros(n); dbg = np.zeros(3); dconic = np.zeros((n, 3))
+        dop = np.zeros(n); dbg = np.zeros(3); dconic = np.zeros((n, 3)); dabs = np.zeros((n, 2))
         c = self.cfg.c()
         lib().gs2dref_render_bwd(C.byref(c), n, *self._common(), _ptr(self.proj.count),
                                  *self._lists(), _ptr(d_image), _ptr(dxy), _ptr(dchol), _ptr(drgb),
-                                 _ptr(dop), _ptr(dbg), _ptr(dconic))
-        return dict(xy=dxy, chol=dchol, rgb=drgb, opacity=dop, background=dbg, conic=dconic)
+                                 _ptr(dop), _ptr(dbg), _ptr(dconic), _ptr(dabs))
+        return dict(xy=dxy, chol=dchol, rgb=drgb, opacity=dop, background=dbg, conic=dconic,
+                    xy_abs=dabs)
 
     def render_bwd_gaussians(self, d_image, gids):
         d_image = _f64(d_image, (3, self.cfg.height, self.cfg.width))
         gids = np.ascontiguousarray(gids, dtype=np.int32)
         m = gids.shape[0]
         dxy = np.zeros((m, 2)); dchol = np.zeros((m, 3)); drgb = np.zeros((m, 3)); dop = np.zeros(m)
+        dabs = np.zeros((m, 2))
         c = self.cfg.c()
         lib().gs2dref_render_bwd_gaussians(C.byref(c), self.n, *self._common(),
                                            _ptr(self.proj.count), *self._lists(), _ptr(d_image),
                                            _ptr(gids), m, _ptr(dxy), _ptr(dchol), _ptr(drgb),
-                                           _ptr(dop))
-        return dict(xy=dxy, chol=dchol, rgb=drgb, opacity=dop)
+                                           _ptr(dop), _ptr(dabs))
+        return dict(xy=dxy, chol=dchol, rgb=drgb, opacity=dop, xy_abs=dabs)
 
 
 def loss_l2(image, target):

@@ -592,11 +592,16 @@ double gs2dref_loss_l2(int32_t h, int32_t w, const double* image, const double* 
  */
 typedef struct {
   double dmu[2], dconic[3], drgb[3], dopac;
+  double dmu_abs[2]; /* absgrad: sum over pixels of |the pixel's share of dmu| */
 } ref_grad;
 
 /*
  * Chain rule through one touching pair, given dL/dw (how the loss moves with
- * the weight w of this Gaussian at this pixel).  With
+ * the weight w of this Gaussian at this pixel).  The pair's share of the mean
+ * gradient is also added in absolute value (absgrad: DrawingWithGaussians
+ * README, 3D fitting: gsplat-style absgrad, per-pixel absolute mean-gradient
+ * contributions; the three colour channels are summed before the absolute
+ * value, since dL/dw already holds all three).  With
  * q = A dx^2 + 2B dx dy + C dy^2, dx = px - mu_x, dy = py - mu_y and
  * w = exp(-q/2):  dw/dq = -w/2,  dq/dmu_x = -2(A dx + B dy),
  * dq/dmu_y = -2(B dx + C dy),  dq/dA = dx^2, dq/dB = 2 dx dy, dq/dC = dy^2.
@@ -606,8 +611,12 @@ static void ref_accumulate_w(const ref_cfg* cfg, ref_grad* g, const double* L, d
   double A, B, C;
   ref_inverse_cov(cfg, L, &A, &B, &C);
   const double dq = dLdw * (-0.5 * w);
-  g->dmu[0] += dq * (-2.0) * (A * dx + B * dy);
-  g->dmu[1] += dq * (-2.0) * (B * dx + C * dy);
+  const double gx = dq * (-2.0) * (A * dx + B * dy);
+  const double gy = dq * (-2.0) * (B * dx + C * dy);
+  g->dmu[0] += gx;
+  g->dmu[1] += gy;
+  g->dmu_abs[0] += fabs(gx);
+  g->dmu_abs[1] += fabs(gy);
   g->dconic[0] += dq * dx * dx;
   g->dconic[1] += dq * 2.0 * dx * dy;
   g->dconic[2] += dq * dy * dy;
@@ -687,7 +696,7 @@ static void ref_pixel_bwd(const ref_scene* s, const int32_t* list, int64_t len, 
  * The position gradient is the mean gradient (xy is the mean).
  */
 static void ref_finish(const ref_cfg* cfg, const double* L, const ref_grad* g, double* dxy,
-                       double* dchol, double* drgb, double* dopac) {
+                       double* dchol, double* drgb, double* dopac, double* dxy_abs) {
   double A, B, C;
   ref_inverse_cov(cfg, L, &A, &B, &C);
   const double dA = g->dconic[0], dB = g->dconic[1], dC = g->dconic[2];
@@ -706,6 +715,10 @@ static void ref_finish(const ref_cfg* cfg, const double* L, const ref_grad* g, d
   }
   dxy[0] = g->dmu[0];
   dxy[1] = g->dmu[1];
+  if (dxy_abs) {
+    dxy_abs[0] = g->dmu_abs[0];
+    dxy_abs[1] = g->dmu_abs[1];
+  }
   for (int d = 0; d < 3; ++d) drgb[d] = g->drgb[d];
   if (dopac) *dopac = g->dopac;
 }
@@ -721,14 +734,15 @@ static int64_t ref_max_list(const ref_cfg* cfg, const int32_t* ranges) {
  * Full backward: gradients of the loss for all n Gaussians, given
  * d_image[3,H,W] = dL/dC.  Outputs d_xy[n,2], d_chol[n,3], d_rgb[n,3],
  * d_opacity[n] (composite, may be NULL), d_bg[3] (composite, may be NULL),
- * d_conic[n,3] (may be NULL).  count[n] marks valid Gaussians.
+ * d_conic[n,3] (may be NULL), d_xy_abs[n,2] (absgrad, may be NULL).
+ * count[n] marks valid Gaussians.
  */
 void gs2dref_render_bwd(const ref_cfg* cfg, int32_t n, const double* xy, const double* chol,
                         const double* rgb, const double* opacity, const double* bg,
                         const float* xy_f, const float* conic_f, const int32_t* aabb,
                         const int32_t* count, const int32_t* ranges, const int32_t* sorted_gid,
                         const double* d_image, double* d_xy, double* d_chol, double* d_rgb,
-                        double* d_opacity, double* d_bg, double* d_conic) {
+                        double* d_opacity, double* d_bg, double* d_conic, double* d_xy_abs) {
   ref_scene s;
   ref_scene_init(&s, cfg, xy, chol, rgb, opacity, bg, xy_f, conic_f, aabb, ranges, sorted_gid);
   ref_grad* grads = (ref_grad*)calloc((size_t)(n > 0 ? n : 1), sizeof(ref_grad));
@@ -752,10 +766,12 @@ void gs2dref_render_bwd(const ref_cfg* cfg, int32_t n, const double* xy, const d
       memset(d_rgb + 3 * (int64_t)g, 0, 3 * sizeof(double));
       if (d_opacity) d_opacity[g] = 0.0;
       if (d_conic) memset(d_conic + 3 * (int64_t)g, 0, 3 * sizeof(double));
+      if (d_xy_abs) memset(d_xy_abs + 2 * (int64_t)g, 0, 2 * sizeof(double));
       continue;
     }
     ref_finish(cfg, chol + 3 * (int64_t)g, &grads[g], d_xy + 2 * (int64_t)g, d_chol + 3 * (int64_t)g,
-               d_rgb + 3 * (int64_t)g, d_opacity ? d_opacity + g : &dummy);
+               d_rgb + 3 * (int64_t)g, d_opacity ? d_opacity + g : &dummy,
+               d_xy_abs ? d_xy_abs + 2 * (int64_t)g : NULL);
     if (d_conic)
       for (int d = 0; d < 3; ++d) d_conic[3 * (int64_t)g + d] = grads[g].dconic[d];
   }
@@ -778,7 +794,7 @@ void gs2dref_render_bwd_gaussians(const ref_cfg* cfg, int32_t n, const double* x
                                   const int32_t* ranges, const int32_t* sorted_gid,
                                   const double* d_image, const int32_t* gids, int32_t m,
                                   double* d_xy, double* d_chol, double* d_rgb,
-                                  double* d_opacity) {
+                                  double* d_opacity, double* d_xy_abs) {
   (void)n;
   ref_scene s;
   ref_scene_init(&s, cfg, xy, chol, rgb, opacity, bg, xy_f, conic_f, aabb, ranges, sorted_gid);
@@ -803,8 +819,10 @@ void gs2dref_render_bwd_gaussians(const ref_cfg* cfg, int32_t n, const double* x
                         g3, &acc, g, NULL, scratch);
         }
       ref_finish(cfg, chol + 3 * (int64_t)g, &acc, d_xy + 2 * (int64_t)k, d_chol + 3 * (int64_t)k,
-                 d_rgb + 3 * (int64_t)k, d_opacity ? d_opacity + k : &dummy);
+                 d_rgb + 3 * (int64_t)k, d_opacity ? d_opacity + k : &dummy,
+                 d_xy_abs ? d_xy_abs + 2 * (int64_t)k : NULL);
     } else {
+      if (d_xy_abs) memset(d_xy_abs + 2 * (int64_t)k, 0, 2 * sizeof(double));
       memset(d_xy + 2 * (int64_t)k, 0, 2 * sizeof(double));
       memset(d_chol + 3 * (int64_t)k, 0, 3 * sizeof(double));
       memset(d_rgb + 3 * (int64_t)k, 0, 3 * sizeof(double));

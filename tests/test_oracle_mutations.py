@@ -14,6 +14,7 @@ from oracle import build as obuild
 
 import test_oracle_pins as pins
 import test_oracle_scale_rot as sr_pins
+import test_oracle_absgrad as abs_pins
 
 # (name, text in the oracle source, replacement)
 MUTATIONS = [
@@ -44,6 +45,8 @@ MUTATIONS = [
     ("fp32 sin: wrong Taylor coefficient", "p = fmaf(p, r2, -1.66666672e-01f);",
      "p = fmaf(p, r2, -1.66666672e-02f);"),
     ("fp32 sincos: quadrant sign", "case 1: *sn = c; *cs = -s; break;", "case 1: *sn = c; *cs = s; break;"),
+    ("absgrad: signed instead of absolute", "g->dmu_abs[0] += fabs(gx);", "g->dmu_abs[0] += gx;"),
+    ("absgrad: y from x", "g->dmu_abs[1] += fabs(gy);", "g->dmu_abs[1] += fabs(gx);"),
     ("composite lists not depth sorted", "if (cfg->mode == REF_MODE_COMPOSITE) {\n      g_sort_depth = depth;\n      for",
      "if (0) {\n      g_sort_depth = depth;\n      for"),
 ]
@@ -66,6 +69,8 @@ PINS = [
     sr_pins.test_single_gaussian_matches_library_density,
     sr_pins.test_pixel_box_is_the_ellipse_box,
     sr_pins.test_sum_gradients_by_central_differences,
+    lambda: abs_pins.test_absgrad_by_per_pixel_central_differences(oracle.SUM, oracle.CHOLESKY),
+    abs_pins.test_triangle_inequality_and_culled_zero,
 ]
 
 
