@@ -25,8 +25,8 @@ MUTATIONS = [
     ("box radius from the wrong factor", "const float rx = k * fabsf(a);",
      "const float rx = k * fabsf(c);"),
     ("tile rectangle end from the start", "rc[2] = b4[2] / cfg->tile;", "rc[2] = b4[0] / cfg->tile;"),
-    ("mean gradient uses C for B", "g->dmu[0] += dq * (-2.0) * (A * dx + B * dy);",
-     "g->dmu[0] += dq * (-2.0) * (A * dx + C * dy);"),
+    ("mean gradient uses C for B", "const double gx = dq * (-2.0) * (A * dx + B * dy);",
+     "const double gx = dq * (-2.0) * (A * dx + C * dy);"),
     ("chain rule dA/da halved", "dchol[0] = dA * (-2.0 * A / a)", "dchol[0] = dA * (-1.0 * A / a)"),
     ("chain rule dC/dc sign", "dC * (-2.0 / (c * c * c));", "dC * (2.0 / (c * c * c));"),
     ("composite: no division by 1-alpha", "S[d] / (1.0 - e->alpha)", "S[d]"),
