@@ -229,14 +229,21 @@ GS2D_API gs2d_status gs2d_loss_l2(int32_t height, int32_t width, const float* im
  *                                        cfg->param)
  *   d_opacity[n]         out, composite (may be NULL)
  *   d_background[3]      out, composite (may be NULL)
+ *   d_xy_abs[n,2]        out, may be NULL (not computed): absgrad, for each
+ *                        Gaussian the sum over pixels p of |dL_p/dmu_x| and
+ *                        of |dL_p/dmu_y|, L_p being pixel p's share of the
+ *                        loss -- the densification signal that does not
+ *                        cancel between pixels (DrawingWithGaussians README,
+ *                        Fit 3D Gaussians and export to SuperSplat: gsplat-style
+ *                        absgrad accumulated in the fused backward)
  */
 GS2D_API gs2d_status gs2d_render_bwd(const gs2d_config* cfg, int32_t n, const float* shape,
                             const gs2d_record* rec, const int32_t* rect,
                             const int32_t* tile_ranges, const int32_t* sorted_gid,
                             const float* background, const float* t_final, const int32_t* last,
                             const float* d_image, float* d_xy, float* d_shape, float* d_rgb,
-                            float* d_opacity, float* d_background, void* workspace,
-                            gs2d_stream_t stream);
+                            float* d_opacity, float* d_background, float* d_xy_abs,
+                            void* workspace, gs2d_stream_t stream);
 
 /*
  * Fused training pass: what gs2d_render_fwd, gs2d_loss_l2 and
@@ -256,6 +263,7 @@ GS2D_API gs2d_status gs2d_render_bwd(const gs2d_config* cfg, int32_t n, const fl
  *   loss                 out: one float (device), (1/(3HW)) sum (C - target)^2
  *   d_xy[n,2], d_shape[n,3], d_rgb[n,3]  out, every element written
  *   d_opacity[n], d_background[3]        out, composite (may be NULL)
+ *   d_xy_abs[n,2]        out, may be NULL: absgrad, as for gs2d_render_bwd
  * Errors as for gs2d_render_bwd; target and loss must be non-NULL.
  */
 GS2D_API gs2d_status gs2d_render_fwd_bwd_l2(const gs2d_config* cfg, int32_t n, const float* shape,
@@ -264,7 +272,7 @@ GS2D_API gs2d_status gs2d_render_fwd_bwd_l2(const gs2d_config* cfg, int32_t n, c
                                             const float* background, const float* target,
                                             float* image, float* loss, float* d_xy, float* d_shape,
                                             float* d_rgb, float* d_opacity, float* d_background,
-                                            void* workspace, gs2d_stream_t stream);
+                                            float* d_xy_abs, void* workspace, gs2d_stream_t stream);
 
 /*
  * The L2 loss of gs2d_loss_l2 for callers that cannot supply a workspace.

@@ -20,14 +20,16 @@ namespace gs2d {
 
 namespace {
 
+template <bool kAbs>
 struct FusedCompSmem {
   union {
     CompSmem f;
-    CompStage b;
+    CompStage<kAbs> b;
   } u;
   float red[8];
 };
 
+template <bool kAbs>
 __global__ void __launch_bounds__(256)
 k_fused_comp(gs2d_config c, int tiles_x, float scale, const float4* __restrict__ rec,
              const int4* __restrict__ rect, const int2* __restrict__ ranges,
@@ -37,7 +39,7 @@ k_fused_comp(gs2d_config c, int tiles_x, float scale, const float4* __restrict__
              float4* __restrict__ tile_partials, float* __restrict__ loss_partials) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  FusedCompSmem& sm = *reinterpret_cast<FusedCompSmem*>(smem_raw);
+  FusedCompSmem<kAbs>& sm = *reinterpret_cast<FusedCompSmem<kAbs>*>(smem_raw);
   const int tile = blockIdx.x;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -72,7 +74,7 @@ k_fused_comp(gs2d_config c, int tiles_x, float scale, const float4* __restrict__
   }
   const float tl = block_sum_ordered<8>(fmaf(eb, eb, fmaf(eg, eg, er * er)), sm.red);
   if (threadIdx.x == 0) loss_partials[tile] = tl;
-  comp_tile_backward(sm.u.b, c, tile, tx, ty, rg, bx0, by0, pxf, pyf, inside, kk, o.T, o.last,
+  comp_tile_backward<kAbs>(sm.u.b, c, tile, tx, ty, rg, bx0, by0, pxf, pyf, inside, kk, o.T, o.last,
                      er * scale, eg * scale, eb * scale, bg, rec, rect, sorted_gid, offsets, partials,
                      tile_partials);
 }
@@ -83,8 +85,8 @@ cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* cho
                                    const gs2d_record* rec, const int* rect, const int* ranges,
                                    const int* sorted_gid, const float* bg, const float* target,
                                    float* image, float* loss, float* d_xy, float* d_chol,
-                                   float* d_rgb, float* d_opacity, float* d_bg, unsigned char* ws,
-                                   cudaStream_t s) {
+                                   float* d_rgb, float* d_opacity, float* d_bg, float* d_xy_abs,
+                                   unsigned char* ws, cudaStream_t s) {
   const Layout L = layout_of(c, n, 0);
   const int T = num_tiles(c);
   const float4* r = reinterpret_cast<const float4*>(rec);
@@ -96,17 +98,24 @@ cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* cho
   const float scale = float(2.0 / (3.0 * double(c.width) * double(c.height)));
   float* lp = reinterpret_cast<float*>(ws + L.loss_partials);
   if (c.mode == GS2D_MODE_COMPOSITE) {
-    const size_t smem = sizeof(FusedCompSmem);
-    GS2D_TRY(cudaFuncSetAttribute(k_fused_comp, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-    GS2D_TRY(launch(k_fused_comp, dim3(T), dim3(256), smem, s, c, tiles_x(c), scale, r, rc, rg, sorted_gid,
-                    offsets, bg, target, image, reinterpret_cast<float4*>(ws + L.partials), tp, lp));
-    return launch_gather(c, n, chol, rec, rect, ws, d_xy, d_chol, d_rgb, d_opacity, d_bg, loss, T, s);
+    auto go = [&](auto kern, size_t smem) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      if (e != cudaSuccess) return e;
+      return launch(kern, dim3(T), dim3(256), smem, s, c, tiles_x(c), scale, r, rc, rg, sorted_gid,
+                    offsets, bg, target, image, reinterpret_cast<float4*>(ws + L.partials), tp, lp);
+    };
+    if (d_xy_abs)
+      GS2D_TRY(go(k_fused_comp<true>, sizeof(FusedCompSmem<true>)));
+    else
+      GS2D_TRY(go(k_fused_comp<false>, sizeof(FusedCompSmem<false>)));
+    return launch_gather(c, n, chol, rec, rect, ws, d_xy, d_chol, d_rgb, d_opacity, d_bg, d_xy_abs,
+                         loss, T, s);
   }
   float* d_image = reinterpret_cast<float*>(ws + L.dimage);
   int blocks = 0;
   GS2D_TRY(launch_render_fwd_loss(c, rec, ranges, sorted_gid, target, scale, image, d_image, lp, &blocks, s));
   return launch_render_bwd(c, n, chol, rec, rect, ranges, sorted_gid, nullptr, nullptr, nullptr, d_image,
-                           d_xy, d_chol, d_rgb, nullptr, nullptr, ws, s, loss, blocks);
+                           d_xy, d_chol, d_rgb, nullptr, nullptr, d_xy_abs, ws, s, loss, blocks);
 }
 
 }  // namespace gs2d

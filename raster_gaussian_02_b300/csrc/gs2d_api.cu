@@ -45,18 +45,18 @@ size_t gs2d_workspace_size(const gs2d_config* cfg, int32_t n, int64_t pair_capac
   return layout_of(*cfg, n, pair_capacity).total;
 }
 
-gs2d_status gs2d_project(const gs2d_config* cfg, int32_t n, const float* xy, const float* chol,
+gs2d_status gs2d_project(const gs2d_config* cfg, int32_t n, const float* xy, const float* shape,
                          const float* rgb, const float* depth, const float* opacity,
                          gs2d_record* rec, int32_t* rect, int32_t* count, gs2d_stream_t stream) {
   if (!config_ok(cfg) || n < 0) return GS2D_ERR_INVALID_ARG;
   if (n == 0) return GS2D_OK;
-  if (!xy || !chol || !rgb || !rec || !rect || !count) return GS2D_ERR_INVALID_ARG;
+  if (!xy || !shape || !rgb || !rec || !rect || !count) return GS2D_ERR_INVALID_ARG;
   if (cfg->mode == GS2D_MODE_COMPOSITE && (!depth || !opacity)) return GS2D_ERR_INVALID_ARG;
-  if (!aligned(rec, 16) || !aligned(rect, 16) || !aligned(xy, 4) || !aligned(chol, 4) ||
+  if (!aligned(rec, 16) || !aligned(rect, 16) || !aligned(xy, 4) || !aligned(shape, 4) ||
       !aligned(rgb, 4) || !aligned(count, 4) || (depth && !aligned(depth, 4)) ||
       (opacity && !aligned(opacity, 4)))
     return GS2D_ERR_INVALID_ARG;
-  return from_cuda(launch_project(*cfg, n, xy, chol, rgb, depth, opacity, rec, rect, count,
+  return from_cuda(launch_project(*cfg, n, xy, shape, rgb, depth, opacity, rec, rect, count,
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -110,60 +110,61 @@ gs2d_status gs2d_loss_l2(int32_t height, int32_t width, const float* image, cons
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
-gs2d_status gs2d_render_bwd(const gs2d_config* cfg, int32_t n, const float* chol,
+gs2d_status gs2d_render_bwd(const gs2d_config* cfg, int32_t n, const float* shape,
                             const gs2d_record* rec, const int32_t* rect,
                             const int32_t* tile_ranges, const int32_t* sorted_gid,
                             const float* background, const float* t_final, const int32_t* last,
-                            const float* d_image, float* d_xy, float* d_chol, float* d_rgb,
-                            float* d_opacity, float* d_background, void* workspace,
-                            gs2d_stream_t stream) {
+                            const float* d_image, float* d_xy, float* d_shape, float* d_rgb,
+                            float* d_opacity, float* d_background, float* d_xy_abs,
+                            void* workspace, gs2d_stream_t stream) {
   if (!config_ok(cfg) || n < 0) return GS2D_ERR_INVALID_ARG;
   const bool comp = cfg->mode == GS2D_MODE_COMPOSITE;
   if (!tile_ranges || !d_image || !workspace || !aligned(tile_ranges, 16) ||
       !aligned(d_image, 4) || !aligned(workspace, 16))
     return GS2D_ERR_INVALID_ARG;
-  if (n > 0 && (!chol || !rec || !rect || !sorted_gid || !d_xy || !d_chol || !d_rgb ||
-                !aligned(rec, 16) || !aligned(rect, 16) || !aligned(chol, 4) ||
-                !aligned(sorted_gid, 4) || !aligned(d_xy, 4) || !aligned(d_chol, 4) ||
+  if (n > 0 && (!shape || !rec || !rect || !sorted_gid || !d_xy || !d_shape || !d_rgb ||
+                !aligned(rec, 16) || !aligned(rect, 16) || !aligned(shape, 4) ||
+                !aligned(sorted_gid, 4) || !aligned(d_xy, 4) || !aligned(d_shape, 4) ||
                 !aligned(d_rgb, 4)))
     return GS2D_ERR_INVALID_ARG;
   if (comp && (!t_final || !last || !aligned(t_final, 4) || !aligned(last, 4)))
     return GS2D_ERR_INVALID_ARG;
   if ((d_opacity && !aligned(d_opacity, 4)) || (d_background && !aligned(d_background, 4)) ||
-      (background && !aligned(background, 4)))
+      (background && !aligned(background, 4)) || (d_xy_abs && !aligned(d_xy_abs, 4)))
     return GS2D_ERR_INVALID_ARG;
-  return from_cuda(launch_render_bwd(*cfg, n, chol, rec, rect, tile_ranges, sorted_gid,
+  return from_cuda(launch_render_bwd(*cfg, n, shape, rec, rect, tile_ranges, sorted_gid,
                                      comp ? background : nullptr, t_final, last, d_image, d_xy,
-                                     d_chol, d_rgb, comp ? d_opacity : nullptr,
-                                     comp ? d_background : nullptr,
+                                     d_shape, d_rgb, comp ? d_opacity : nullptr,
+                                     comp ? d_background : nullptr, n > 0 ? d_xy_abs : nullptr,
                                      static_cast<unsigned char*>(workspace),
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
-gs2d_status gs2d_render_fwd_bwd_l2(const gs2d_config* cfg, int32_t n, const float* chol,
+gs2d_status gs2d_render_fwd_bwd_l2(const gs2d_config* cfg, int32_t n, const float* shape,
                                    const gs2d_record* rec, const int32_t* rect,
                                    const int32_t* tile_ranges, const int32_t* sorted_gid,
                                    const float* background, const float* target, float* image,
-                                   float* loss, float* d_xy, float* d_chol, float* d_rgb,
-                                   float* d_opacity, float* d_background, void* workspace,
-                                   gs2d_stream_t stream) {
+                                   float* loss, float* d_xy, float* d_shape, float* d_rgb,
+                                   float* d_opacity, float* d_background, float* d_xy_abs,
+                                   void* workspace, gs2d_stream_t stream) {
   if (!config_ok(cfg) || n < 0) return GS2D_ERR_INVALID_ARG;
   const bool comp = cfg->mode == GS2D_MODE_COMPOSITE;
   if (!tile_ranges || !target || !loss || !workspace || !aligned(tile_ranges, 16) ||
       !aligned(target, 4) || !aligned(loss, 4) || !aligned(workspace, 16))
     return GS2D_ERR_INVALID_ARG;
-  if (n > 0 && (!chol || !rec || !rect || !sorted_gid || !d_xy || !d_chol || !d_rgb ||
-                !aligned(rec, 16) || !aligned(rect, 16) || !aligned(chol, 4) ||
-                !aligned(sorted_gid, 4) || !aligned(d_xy, 4) || !aligned(d_chol, 4) ||
+  if (n > 0 && (!shape || !rec || !rect || !sorted_gid || !d_xy || !d_shape || !d_rgb ||
+                !aligned(rec, 16) || !aligned(rect, 16) || !aligned(shape, 4) ||
+                !aligned(sorted_gid, 4) || !aligned(d_xy, 4) || !aligned(d_shape, 4) ||
                 !aligned(d_rgb, 4)))
     return GS2D_ERR_INVALID_ARG;
   if ((image && !aligned(image, 4)) || (d_opacity && !aligned(d_opacity, 4)) ||
-      (d_background && !aligned(d_background, 4)) || (background && !aligned(background, 4)))
+      (d_background && !aligned(d_background, 4)) || (background && !aligned(background, 4)) ||
+      (d_xy_abs && !aligned(d_xy_abs, 4)))
     return GS2D_ERR_INVALID_ARG;
-  return from_cuda(launch_render_fused_l2(*cfg, n, chol, rec, rect, tile_ranges, sorted_gid,
+  return from_cuda(launch_render_fused_l2(*cfg, n, shape, rec, rect, tile_ranges, sorted_gid,
                                           comp ? background : nullptr, target, image, loss, d_xy,
-                                          d_chol, d_rgb, comp ? d_opacity : nullptr,
-                                          comp ? d_background : nullptr,
+                                          d_shape, d_rgb, comp ? d_opacity : nullptr,
+                                          comp ? d_background : nullptr, n > 0 ? d_xy_abs : nullptr,
                                           static_cast<unsigned char*>(workspace),
                                           reinterpret_cast<cudaStream_t>(stream)));
 }

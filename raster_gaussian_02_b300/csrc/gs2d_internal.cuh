@@ -95,7 +95,9 @@ inline Layout layout_of(const gs2d_config& c, long long n, long long cap) {
   L.passes = (L.key_bits + kMaxDigitBits - 1) / kMaxDigitBits;
   L.digit_bits = kMaxDigitBits;  // every pass sorts a full 8-bit digit (256 buckets)
   L.key_bytes = comp ? 8 : 4;
-  L.partial_floats = comp ? 12 : 8;
+  // per pair: 8 floats (sum) or 9 (composite) of partial derivatives, plus
+  // 2 absgrad sums; slots of 3 float4 (sum without absgrad uses 2 of them)
+  L.partial_floats = 12;
   L.radix_per_thread = radix_per_thread(cap);
   const long long items = (long long)kRadixThreads * L.radix_per_thread;
   L.partitions = (cap + items - 1) / items;
@@ -272,15 +274,16 @@ cudaError_t launch_loss_l2(int h, int w, const float* image, const float* target
 // loss_blocks entries of the workspace's loss partials divided by 3HW.
 cudaError_t launch_gather(const gs2d_config& c, int n, const float* chol, const gs2d_record* rec,
                           const int* rect, const unsigned char* ws, float* d_xy, float* d_chol,
-                          float* d_rgb, float* d_opacity, float* d_bg, float* loss,
+                          float* d_rgb, float* d_opacity, float* d_bg, float* d_xy_abs, float* loss,
                           int loss_blocks, cudaStream_t s);
 
 cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
                               const gs2d_record* rec, const int* rect, const int* ranges,
                               const int* sorted_gid, const float* bg, const float* t_final,
                               const int* last, const float* d_image, float* d_xy, float* d_chol,
-                              float* d_rgb, float* d_opacity, float* d_bg, unsigned char* ws,
-                              cudaStream_t s, float* loss = nullptr, int loss_blocks = 0);
+                              float* d_rgb, float* d_opacity, float* d_bg, float* d_xy_abs,
+                              unsigned char* ws, cudaStream_t s, float* loss = nullptr,
+                              int loss_blocks = 0);
 
 // Sum forward that also takes the L2 loss: writes image (if non-NULL),
 // dL/dC = scale (C - target) to d_image and one loss partial per block to
@@ -294,7 +297,7 @@ cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* cho
                                    const gs2d_record* rec, const int* rect, const int* ranges,
                                    const int* sorted_gid, const float* bg, const float* target,
                                    float* image, float* loss, float* d_xy, float* d_chol,
-                                   float* d_rgb, float* d_opacity, float* d_bg, unsigned char* ws,
-                                   cudaStream_t s);
+                                   float* d_rgb, float* d_opacity, float* d_bg, float* d_xy_abs,
+                                   unsigned char* ws, cudaStream_t s);
 
 }  // namespace gs2d

@@ -116,11 +116,12 @@ k_project(gs2d_config c, int n, const float* __restrict__ xy, const float* __res
 //   du/ds_x = -2/s_x^3,  dv/ds_y = -2/s_y^3,
 //   d(A, B, C)/dtheta = (-2B, (c^2 - s^2)(u - v), 2B).
 // d(xy) = d(mean).
+// kAbs: also the pairs' absgrad sums (third float4 of the slot, .y and .z).
 // The last block also sums, in a fixed order, the per-tile background
 // partials (composite, d_bg non-null) and the fused pass's per-block loss
 // partials (loss non-null; the total is divided by m, the number of image
 // values).
-template <bool kComposite>
+template <bool kComposite, bool kAbs>
 __global__ void __launch_bounds__(256)
 k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
          const int4* __restrict__ rect, const int* __restrict__ offsets,
@@ -128,7 +129,7 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
          float* __restrict__ d_xy, float* __restrict__ d_chol, float* __restrict__ d_rgb,
          float* __restrict__ d_opacity, int T, const float4* __restrict__ tile_partials,
          float* __restrict__ d_bg, const float* __restrict__ loss_partials, int loss_blocks,
-         float* __restrict__ loss, float m, int param) {
+         float* __restrict__ loss, float m, int param, float* __restrict__ d_xy_abs) {
   pdl_enter();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   const bool bad = (hdr->flags & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) != 0;
@@ -136,14 +137,22 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
     const int4 rc = rect[i];
     const int cnt = (rc.z >= rc.x) ? (rc.z - rc.x + 1) * (rc.w - rc.y + 1) : 0;
     float s[9] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float ax = 0.f, ay = 0.f;
     if (!bad && cnt > 0) {
-      constexpr int kStride = kComposite ? 3 : 2;
+      constexpr int kStride = (kComposite || kAbs) ? 3 : 2;
       const float4* p = partials + size_t(offsets[i]) * kStride;
       for (int k = 0; k < cnt; ++k, p += kStride) {
         const float4 u = p[0], v = p[1];
         s[0] += u.x; s[1] += u.y; s[2] += u.z; s[3] += u.w;
         s[4] += v.x; s[5] += v.y; s[6] += v.z; s[7] += v.w;
-        if (kComposite) s[8] += p[2].x;
+        if constexpr (kComposite || kAbs) {
+          const float4 x = p[2];
+          if (kComposite) s[8] += x.x;
+          if (kAbs) {
+            ax += x.y;
+            ay += x.z;
+          }
+        }
       }
     }
     float g0 = 0.f, g1 = 0.f, g2 = 0.f;
@@ -181,6 +190,10 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
     d_rgb[3 * i + 1] = s[6];
     d_rgb[3 * i + 2] = s[7];
     if (kComposite && d_opacity) d_opacity[i] = s[8];
+    if constexpr (kAbs) {
+      d_xy_abs[2 * i] = ax;
+      d_xy_abs[2 * i + 1] = ay;
+    }
   }
   if ((d_bg || loss) && blockIdx.x == gridDim.x - 1) {
     // fixed-order reduction of the per-tile partials
@@ -228,8 +241,8 @@ cudaError_t launch_project(const gs2d_config& c, int n, const float* xy, const f
 
 cudaError_t launch_gather(const gs2d_config& c, int n, const float* chol, const gs2d_record* rec,
                           const int* rect, const unsigned char* ws, float* d_xy, float* d_chol,
-                          float* d_rgb, float* d_opacity, float* d_bg, float* loss,
-                          int loss_blocks, cudaStream_t s) {
+                          float* d_rgb, float* d_opacity, float* d_bg, float* d_xy_abs,
+                          float* loss, int loss_blocks, cudaStream_t s) {
   const Layout L = layout_of(c, n, 0);
   const int T = num_tiles(c);
   const int blocks = n > 0 ? (n + 255) / 256 : 1;
@@ -241,13 +254,18 @@ cudaError_t launch_gather(const gs2d_config& c, int n, const float* chol, const 
   const float4* partials = reinterpret_cast<const float4*>(ws + L.partials);
   const float4* r = reinterpret_cast<const float4*>(rec);
   const int4* rc = reinterpret_cast<const int4*>(rect);
-  if (c.mode == GS2D_MODE_COMPOSITE)
-    GS2D_TRY(launch(k_gather<true>, dim3(blocks), dim3(256), 0, s, n, chol, r, rc, offsets, partials, hdr,
-                    d_xy, d_chol, d_rgb, d_opacity, T, tp, d_bg, lp, loss_blocks, loss, m, int(c.param)));
+  const int param = int(c.param);
+  const bool comp = c.mode == GS2D_MODE_COMPOSITE;
+  float* d_op = comp ? d_opacity : nullptr;
+  float* d_b = comp ? d_bg : nullptr;
+  auto go = [&](auto kern) {
+    return launch(kern, dim3(blocks), dim3(256), 0, s, n, chol, r, rc, offsets, partials, hdr, d_xy,
+                  d_chol, d_rgb, d_op, T, tp, d_b, lp, loss_blocks, loss, m, param, d_xy_abs);
+  };
+  if (comp)
+    GS2D_TRY(d_xy_abs ? go(k_gather<true, true>) : go(k_gather<true, false>));
   else
-    GS2D_TRY(launch(k_gather<false>, dim3(blocks), dim3(256), 0, s, n, chol, r, rc, offsets, partials, hdr,
-                    d_xy, d_chol, d_rgb, static_cast<float*>(nullptr), T, tp,
-                    static_cast<float*>(nullptr), lp, loss_blocks, loss, m, int(c.param)));
+    GS2D_TRY(d_xy_abs ? go(k_gather<false, true>) : go(k_gather<false, false>));
   return cudaGetLastError();
 }
 

@@ -57,7 +57,10 @@ __device__ __forceinline__ int block_inclusive_count_256(int flag, int* total, i
 // of the Gaussian's box inside the tile.  Blocks take fixed chunks of the
 // sorted pair list, whatever the tile boundaries, so heavy tiles spread over
 // many blocks; inside a block the pairs are reordered so that lanes of a
-// warp walk boxes of the same shape.
+// warp walk boxes of the same shape.  kAbs: also the absgrad sums over the
+// pair's pixels of |t (A dx + B dy)| and |t (B dx + C dy)| (each pixel's
+// share of dL/dmu in absolute value), in a third float4 of the pair's slot.
+template <bool kAbs>
 __global__ void __launch_bounds__(kChunkPairs)
 k_render_bwd_sum(gs2d_config c, int tiles_x, const Header* __restrict__ hdr,
                  const unsigned char* __restrict__ ws, const float4* __restrict__ rec,
@@ -159,10 +162,12 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, const Header* __restrict__ hdr,
         const int ya = max(int(box_lo(by)), Y0), yb = min(int(box_hi(by)), Y0 + kTile - 1);
         const float4* gt = sm.g[ms];
         float sr = 0.f, sg = 0.f, sb = 0.f, Sx = 0.f, Sy = 0.f, Sxx = 0.f, Sxy = 0.f, Syy = 0.f;
+        float ax = 0.f, ay = 0.f;
         for (int y = ya; y <= yb; ++y) {
           const float dy = __fsub_rn(float(y) + 0.5f, my);
           const float b2dy = __fmul_rn(B2, dy);
           const float cdydy = __fmul_rn(__fmul_rn(C, dy), dy);
+          const float bdy = B * dy, cdy = C * dy;
           float r0 = 0.f, rx = 0.f, rxx = 0.f;
           int gi = (y - Y0) * kTile + (xa - X0);
           float pxf = float(xa) + 0.5f;
@@ -181,6 +186,10 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, const Header* __restrict__ hdr,
             const float tdx = t * dx;
             rx += tdx;
             rxx = fmaf(tdx, dx, rxx);
+            if constexpr (kAbs) {
+              ax += fabsf(t * fmaf(A, dx, bdy));
+              ay += fabsf(t * fmaf(B, dx, cdy));
+            }
           }
           Sx += rx;
           Sy = fmaf(r0, dy, Sy);
@@ -191,9 +200,10 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, const Header* __restrict__ hdr,
         const int gid_me = sm.gid[me];
         const int4 rc = rect[gid_me];
         const int pslot = offsets[gid_me] + (ty - rc.y) * (rc.z - rc.x + 1) + (tx - rc.x);
-        float4* out = partials + 2 * size_t(pslot);
+        float4* out = partials + (kAbs ? 3 : 2) * size_t(pslot);
         out[0] = make_float4(fmaf(A, Sx, B * Sy), fmaf(B, Sx, C * Sy), -0.5f * Sxx, -Sxy);
         out[1] = make_float4(-0.5f * Syy, sr, sg, sb);
+        if constexpr (kAbs) out[2] = make_float4(0.f, ax, ay, 0.f);
       }
       __syncthreads();
     }
@@ -205,6 +215,7 @@ constexpr int kBwdCompThreads = 256;
 // Composite: one block per tile, one pixel per thread (8x4 sub-block per
 // warp as in the forward), walking the tile's list back to front from each
 // pixel's last contributor (comp_tile_backward).
+template <bool kAbs>
 __global__ void __launch_bounds__(kBwdCompThreads)
 k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
                   const int4* __restrict__ rect, const int2* __restrict__ ranges,
@@ -214,7 +225,7 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
                   float4* __restrict__ partials, float4* __restrict__ tile_partials) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  CompStage& sm = *reinterpret_cast<CompStage*>(smem_raw);
+  CompStage<kAbs>& sm = *reinterpret_cast<CompStage<kAbs>*>(smem_raw);
   const int tile = blockIdx.x;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -234,9 +245,39 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
     gg = d_image[HW + p];
     gb = d_image[2 * HW + p];
   }
-  comp_tile_backward(sm, c, tile, tx, ty, ranges[tile], bx0, by0, float(px) + 0.5f, float(py) + 0.5f,
-                     inside, kk, T, lst, gr, gg, gb, bg, rec, rect, sorted_gid, offsets, partials,
-                     tile_partials);
+  comp_tile_backward<kAbs>(sm, c, tile, tx, ty, ranges[tile], bx0, by0, float(px) + 0.5f,
+                           float(py) + 0.5f, inside, kk, T, lst, gr, gg, gb, bg, rec, rect, sorted_gid,
+                           offsets, partials, tile_partials);
+}
+
+}  // namespace
+
+namespace {
+
+template <bool kAbs>
+cudaError_t launch_bwd_pairs(const gs2d_config& c, const Layout& L, const float4* r, const int4* rc,
+                             const int2* rg, const int* sorted_gid, const float* bg,
+                             const float* t_final, const int* last, const float* d_image,
+                             unsigned char* ws, cudaStream_t s) {
+  const int T = num_tiles(c);
+  const int* offsets = reinterpret_cast<const int*>(ws + L.offsets);
+  float4* partials = reinterpret_cast<float4*>(ws + L.partials);
+  if (c.mode == GS2D_MODE_COMPOSITE) {
+    const size_t smem = sizeof(CompStage<kAbs>);
+    auto kern = k_render_bwd_comp<kAbs>;
+    GS2D_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+    GS2D_TRY(launch(kern, dim3(T), dim3(kBwdCompThreads), smem, s, c, tiles_x(c), r, rc, rg, sorted_gid,
+                    offsets, bg, t_final, last, d_image, partials,
+                    reinterpret_cast<float4*>(ws + L.tile_partials)));
+  } else {
+    const size_t smem = sizeof(BwdSumSmem);
+    auto kern = k_render_bwd_sum<kAbs>;
+    GS2D_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+    GS2D_TRY(launch(kern, dim3(4 * sm_count()), dim3(kChunkPairs), smem, s, c, tiles_x(c),
+                    reinterpret_cast<const Header*>(ws), static_cast<const unsigned char*>(ws), r, rc,
+                    sorted_gid, offsets, d_image, partials));
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -245,34 +286,18 @@ cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
                               const gs2d_record* rec, const int* rect, const int* ranges,
                               const int* sorted_gid, const float* bg, const float* t_final,
                               const int* last, const float* d_image, float* d_xy, float* d_chol,
-                              float* d_rgb, float* d_opacity, float* d_bg, unsigned char* ws,
-                              cudaStream_t s, float* loss, int loss_blocks) {
+                              float* d_rgb, float* d_opacity, float* d_bg, float* d_xy_abs,
+                              unsigned char* ws, cudaStream_t s, float* loss, int loss_blocks) {
   const Layout L = layout_of(c, n, 0);
-  const int T = num_tiles(c);
   const float4* r = reinterpret_cast<const float4*>(rec);
   const int4* rc = reinterpret_cast<const int4*>(rect);
   const int2* rg = reinterpret_cast<const int2*>(ranges);
-  const int* offsets = reinterpret_cast<const int*>(ws + L.offsets);
-  float4* partials = reinterpret_cast<float4*>(ws + L.partials);
-  if (c.mode == GS2D_MODE_COMPOSITE) {
-    const size_t smem = sizeof(CompStage);
-    cudaError_t e = cudaFuncSetAttribute(k_render_bwd_comp, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(smem));
-    if (e != cudaSuccess) return e;
-    GS2D_TRY(launch(k_render_bwd_comp, dim3(T), dim3(kBwdCompThreads), smem, s, c, tiles_x(c), r, rc, rg, sorted_gid, offsets, bg, t_final, last, d_image, partials,
-        reinterpret_cast<float4*>(ws + L.tile_partials)));
-  } else {
-    const size_t smem = sizeof(BwdSumSmem);
-    cudaError_t e = cudaFuncSetAttribute(k_render_bwd_sum, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(smem));
-    if (e != cudaSuccess) return e;
-    GS2D_TRY(launch(k_render_bwd_sum, dim3(4 * sm_count()), dim3(kChunkPairs), smem, s, c, tiles_x(c), reinterpret_cast<const Header*>(ws), ws, r, rc, sorted_gid, offsets,
-        d_image, partials));
-  }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_gather(c, n, chol, rec, rect, ws, d_xy, d_chol, d_rgb, d_opacity, d_bg, loss, loss_blocks,
-                       s);
+  if (d_xy_abs)
+    GS2D_TRY(launch_bwd_pairs<true>(c, L, r, rc, rg, sorted_gid, bg, t_final, last, d_image, ws, s));
+  else
+    GS2D_TRY(launch_bwd_pairs<false>(c, L, r, rc, rg, sorted_gid, bg, t_final, last, d_image, ws, s));
+  return launch_gather(c, n, chol, rec, rect, ws, d_xy, d_chol, d_rgb, d_opacity, d_bg, d_xy_abs,
+                       loss, loss_blocks, s);
 }
 
 }  // namespace gs2d

@@ -236,6 +236,7 @@ __device__ __forceinline__ float block_sum_ordered(float v, float* red) {
 constexpr int kCompChunk = 128;
 constexpr int kCompVals = 9;
 
+template <bool kAbs>
 struct CompStage {
   float4 mc[kCompChunk];  // mean_x, mean_y, A, 2B
   float4 cr[kCompChunk];  // C, r, g, b
@@ -244,6 +245,7 @@ struct CompStage {
   int gid[kCompChunk];
   uint2 list[8][kCompChunk];            // (chunk index, lane mask) per warp
   float acc[8][kCompChunk][kCompVals];  // per-warp partials, summed over warps in order
+  float acc_abs[kAbs ? 8 : 1][kAbs ? kCompChunk : 1][2];  // per-warp absgrad sums
   float bgred[8][3];
 };
 
@@ -258,9 +260,12 @@ struct CompStage {
 // Per (warp, Gaussian) the nine partial derivatives are reduced over the
 // warp and kept in a per-warp slot; the slots are summed in warp order and
 // written to the pair's emission slot (3 float4 per pair).  The tile's
-// background partial goes to tile_partials[tile].
+// background partial goes to tile_partials[tile].  kAbs: also the absgrad
+// sums, over the pair's pixels, of |each pixel's share of dL/dmu_x| and of
+// dL/dmu_y (slot's third float4, .y and .z).
+template <bool kAbs>
 __device__ __forceinline__ void comp_tile_backward(
-    CompStage& sm, const gs2d_config& c, int tile, int tx, int ty, int2 rg, int bx0, int by0,
+    CompStage<kAbs>& sm, const gs2d_config& c, int tile, int tx, int ty, int2 rg, int bx0, int by0,
     float pxf, float pyf, bool inside, float kk, float T, int lst, float gr, float gg, float gb,
     const float* __restrict__ bg, const float4* __restrict__ rec,
     const int4* __restrict__ rect, const int* __restrict__ sorted_gid,
@@ -314,9 +319,11 @@ __device__ __forceinline__ void comp_tile_backward(
       unsigned int m = 0;
       if (j < cnt) {
         m = box_lanes(sm.box[j], bx0, by0);
-        if (!m)
+        if (!m) {
 #pragma unroll
           for (int v = 0; v < kCompVals; ++v) sm.acc[warp][j][v] = 0.f;
+          if constexpr (kAbs) sm.acc_abs[warp][j][0] = sm.acc_abs[warp][j][1] = 0.f;
+        }
       }
       const unsigned int hits = __ballot_sync(0xffffffffu, m != 0u);
       if (m) list[nl + __popc(hits & lt)] = make_uint2(unsigned(j), m);
@@ -334,7 +341,7 @@ __device__ __forceinline__ void comp_tile_backward(
       const float q = touch_q(dx, dy, mc.z, mc.w, cr.x);
       const bool act = inside && (u.y & bit) && idx < lst && q <= kk;
       float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float v8 = 0.f;
+      float v8 = 0.f, gxa = 0.f, gya = 0.f;
       if (act) {
         const float o = sm.op[j];
         const float w = ex2_approx(q * kNegHalfLog2e);
@@ -354,6 +361,11 @@ __device__ __forceinline__ void comp_tile_backward(
         v[6] = gg * aT;
         v[7] = gb * aT;
         v8 = dal * w;
+        if constexpr (kAbs) {
+          const float Bh = 0.5f * mc.w;
+          gxa = fabsf(fmaf(mc.z, v[0], Bh * v[1]));
+          gya = fabsf(fmaf(Bh, v[0], cr.x * v[1]));
+        }
         Sr = fmaf(cr.y, aT, Sr);
         Sg = fmaf(cr.z, aT, Sg);
         Sb = fmaf(cr.w, aT, Sb);
@@ -364,8 +376,17 @@ __device__ __forceinline__ void comp_tile_backward(
         const float tot8 = warp_sum(v8);
         if ((lane & 3) == 0) sm.acc[warp][j][(lane >> 2) & 7] = tot;
         if (lane == 0) sm.acc[warp][j][8] = tot8;
-      } else if (lane < kCompVals) {
-        sm.acc[warp][j][lane] = 0.f;
+        if constexpr (kAbs) {
+          const float tx_ = warp_sum(gxa), ty_ = warp_sum(gya);
+          if (lane == 0) {
+            sm.acc_abs[warp][j][0] = tx_;
+            sm.acc_abs[warp][j][1] = ty_;
+          }
+        }
+      } else {
+        if (lane < kCompVals) sm.acc[warp][j][lane] = 0.f;
+        if constexpr (kAbs)
+          if (lane < 2) sm.acc_abs[warp][j][lane] = 0.f;
       }
     }
     __syncthreads();
@@ -381,9 +402,15 @@ __device__ __forceinline__ void comp_tile_backward(
       const int4 rc = rect[gid];
       const int slot = offsets[gid] + (ty - rc.y) * (rc.z - rc.x + 1) + (tx - rc.x);
       float4* out = partials + 3 * size_t(slot);
+      float ax = 0.f, ay = 0.f;
+      if constexpr (kAbs)
+        for (int w = 0; w < 8; ++w) {
+          ax += sm.acc_abs[w][tid][0];
+          ay += sm.acc_abs[w][tid][1];
+        }
       out[0] = make_float4(fmaf(A, s[0], B * s[1]), fmaf(B, s[0], C * s[1]), -0.5f * s[2], -s[3]);
       out[1] = make_float4(-0.5f * s[4], s[5], s[6], s[7]);
-      out[2] = make_float4(s[8], 0.f, 0.f, 0.f);
+      out[2] = make_float4(s[8], ax, ay, 0.f);
     }
     __syncthreads();
   }

@@ -69,9 +69,9 @@ def lib() -> C.CDLL:
         L.gs2d_render_fwd.restype = C.c_int
         L.gs2d_loss_l2.argtypes = [C.c_int32, C.c_int32] + [_p] * 5 + [_p]
         L.gs2d_loss_l2.restype = C.c_int
-        L.gs2d_render_bwd.argtypes = [_cfgp, C.c_int32] + [_p] * 15 + [_p]
+        L.gs2d_render_bwd.argtypes = [_cfgp, C.c_int32] + [_p] * 16 + [_p]
         L.gs2d_render_bwd.restype = C.c_int
-        L.gs2d_render_fwd_bwd_l2.argtypes = [_cfgp, C.c_int32] + [_p] * 15 + [_p]
+        L.gs2d_render_fwd_bwd_l2.argtypes = [_cfgp, C.c_int32] + [_p] * 16 + [_p]
         L.gs2d_render_fwd_bwd_l2.restype = C.c_int
         L.gs2d_loss_l2_noalloc.argtypes = [C.c_int32, C.c_int32] + [_p] * 4 + [_p]
         L.gs2d_loss_l2_noalloc.restype = C.c_int
@@ -166,7 +166,7 @@ def gs2d_loss_l2_noalloc(height, width, image, target, loss, d_image, stream=Non
 
 def gs2d_render_bwd(cfg, n, shape, rec, rect, tile_ranges, sorted_gid, background, t_final, last,
                     d_image, d_xy, d_shape, d_rgb, d_opacity, d_background, workspace,
-                    stream=None) -> int:
+                    stream=None, d_xy_abs=None) -> int:
     return lib().gs2d_render_bwd(
         C.byref(cfg), int(n), _ptr(shape, _f32, "shape"), _ptr(rec, None, "rec"),
         _ptr(rect, _i32, "rect"), _ptr(tile_ranges, _i32, "tile_ranges"),
@@ -174,12 +174,12 @@ def gs2d_render_bwd(cfg, n, shape, rec, rect, tile_ranges, sorted_gid, backgroun
         _ptr(t_final, _f32, "t_final"), _ptr(last, _i32, "last"), _ptr(d_image, _f32, "d_image"),
         _ptr(d_xy, _f32, "d_xy"), _ptr(d_shape, _f32, "d_shape"), _ptr(d_rgb, _f32, "d_rgb"),
         _ptr(d_opacity, _f32, "d_opacity"), _ptr(d_background, _f32, "d_background"),
-        _ptr(workspace, None, "workspace"), _stream(stream))
+        _ptr(d_xy_abs, _f32, "d_xy_abs"), _ptr(workspace, None, "workspace"), _stream(stream))
 
 
 def gs2d_render_fwd_bwd_l2(cfg, n, shape, rec, rect, tile_ranges, sorted_gid, background, target,
                            image, loss, d_xy, d_shape, d_rgb, d_opacity, d_background, workspace,
-                           stream=None) -> int:
+                           stream=None, d_xy_abs=None) -> int:
     return lib().gs2d_render_fwd_bwd_l2(
         C.byref(cfg), int(n), _ptr(shape, _f32, "shape"), _ptr(rec, None, "rec"),
         _ptr(rect, _i32, "rect"), _ptr(tile_ranges, _i32, "tile_ranges"),
@@ -187,7 +187,7 @@ def gs2d_render_fwd_bwd_l2(cfg, n, shape, rec, rect, tile_ranges, sorted_gid, ba
         _ptr(target, _f32, "target"), _ptr(image, _f32, "image"), _ptr(loss, _f32, "loss"),
         _ptr(d_xy, _f32, "d_xy"), _ptr(d_shape, _f32, "d_shape"), _ptr(d_rgb, _f32, "d_rgb"),
         _ptr(d_opacity, _f32, "d_opacity"), _ptr(d_background, _f32, "d_background"),
-        _ptr(workspace, None, "workspace"), _stream(stream))
+        _ptr(d_xy_abs, _f32, "d_xy_abs"), _ptr(workspace, None, "workspace"), _stream(stream))
 
 
 def gs2d_read_status(workspace, stream=None):
@@ -230,6 +230,7 @@ class Rasterizer:
         self.d_rgb = torch.empty((max(n, 1), 3), dtype=_f32, device=d)
         self.d_opacity = torch.empty(max(n, 1), dtype=_f32, device=d) if comp else None
         self.d_background = torch.empty(3, dtype=_f32, device=d) if comp else None
+        self.d_xy_abs = None  # allocated on the first backward that asks for absgrad
         self.pairs = None
         self._alloc_pairs(int(pair_capacity) if pair_capacity is not None else 4 * max(n, 1))
 
@@ -277,14 +278,22 @@ class Rasterizer:
                            self.workspace), "gs2d_loss_l2")
         return self.loss
 
-    def render_bwd(self, d_image=None):
+    def _absgrad_out(self, absgrad):
+        if not absgrad:
+            return None
+        if self.d_xy_abs is None:
+            self.d_xy_abs = torch.empty((max(self.n, 1), 2), dtype=_f32, device=self.device)
+        return self.d_xy_abs
+
+    def render_bwd(self, d_image=None, absgrad=False):
         d_image = self.d_image if d_image is None else d_image
         check(gs2d_render_bwd(self.cfg, self.n, self.shape, self.rec, self.rect, self.tile_ranges,
                               self.sorted_gid, self.background, self.t_final, self.last, d_image,
                               self.d_xy, self.d_shape, self.d_rgb, self.d_opacity,
-                              self.d_background, self.workspace), "gs2d_render_bwd")
+                              self.d_background, self.workspace,
+                              d_xy_abs=self._absgrad_out(absgrad)), "gs2d_render_bwd")
 
-    def render_fwd_bwd_l2(self, target, background=None, write_image=True):
+    def render_fwd_bwd_l2(self, target, background=None, write_image=True, absgrad=False):
         """Fused forward + L2 loss + backward (one per-tile kernel and the
         gather).  Fills loss and the d_* gradients, and the image unless
         write_image is False; d_image, t_final and last are not written."""
@@ -293,7 +302,8 @@ class Rasterizer:
                                      self.tile_ranges, self.sorted_gid, background, target,
                                      self.image if write_image else None, self.loss, self.d_xy,
                                      self.d_shape, self.d_rgb, self.d_opacity, self.d_background,
-                                     self.workspace), "gs2d_render_fwd_bwd_l2")
+                                     self.workspace, d_xy_abs=self._absgrad_out(absgrad)),
+              "gs2d_render_fwd_bwd_l2")
         return self.loss
 
     def step(self, xy, shape, rgb, target, depth=None, opacity=None, background=None, sync=False,

@@ -37,7 +37,7 @@ def oracle_cfg(wl) -> oracle.Config:
     return oracle.Config(wl.width, wl.height, wl.mode, wl.cutoff_sigma, wl.t_min, param=wl.param)
 
 
-def gpu_run(wl, d_image=None, capacity=None, sync=True, backward=True):
+def gpu_run(wl, d_image=None, capacity=None, sync=True, backward=True, absgrad=False):
     """Whole path on the GPU; returns numpy copies of every output."""
     R = gs2d.Rasterizer(wl.width, wl.height, wl.n, wl.mode, wl.cutoff_sigma, wl.t_min,
                         pair_capacity=capacity, param=wl.param)
@@ -52,7 +52,7 @@ def gpu_run(wl, d_image=None, capacity=None, sync=True, backward=True):
     if backward:
         if wl.target is not None:
             R.loss_l2(to_dev(wl.target))
-        R.render_bwd(to_dev(d_image) if d_image is not None else None)
+        R.render_bwd(to_dev(d_image) if d_image is not None else None, absgrad=absgrad)
     torch.cuda.synchronize()
     rec = R.records()
     out.update(
@@ -72,6 +72,8 @@ def gpu_run(wl, d_image=None, capacity=None, sync=True, backward=True):
         if R.d_opacity is not None:
             out["grads"]["opacity"] = R.d_opacity[: wl.n].cpu().numpy()
             out["grads"]["background"] = R.d_background.cpu().numpy()
+        if absgrad:
+            out["grads"]["xy_abs"] = R.d_xy_abs[: wl.n].cpu().numpy()
     return out
 
 

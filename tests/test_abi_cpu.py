@@ -118,27 +118,30 @@ def test_host_checks_reject_bad_arguments(gs2d):
     assert L.gs2d_loss_l2(64, 64, fake, fake, fake, fake, null, null) == INVALID
     assert L.gs2d_loss_l2(64, 64, fake, fake, fake, fake, odd, null) == INVALID
     # render_bwd: composite needs t_final and last
-    args = [fake] * 15
+    args = [fake] * 16
     args[6] = null  # t_final
     assert L.gs2d_render_bwd(C.byref(comp), 4, *args, null) == INVALID
-    args = [fake] * 15
-    args[0] = null  # chol
+    args = [fake] * 16
+    args[0] = null  # shape
+    assert L.gs2d_render_bwd(C.byref(good), 4, *args, null) == INVALID
+    args = [fake] * 16
+    args[14] = C.c_void_p(0x10002)  # d_xy_abs misaligned
     assert L.gs2d_render_bwd(C.byref(good), 4, *args, null) == INVALID
     # fused fwd + L2 + bwd: target, loss and workspace are required
-    # (chol rec rect ranges gid bg target image loss dxy dchol drgb dop dbg ws)
-    args = [fake] * 15
+    # (shape rec rect ranges gid bg target image loss dxy dshape drgb dop dbg dabs ws)
+    args = [fake] * 16
     args[6] = null  # target
     assert L.gs2d_render_fwd_bwd_l2(C.byref(good), 4, *args, null) == INVALID
-    args = [fake] * 15
+    args = [fake] * 16
     args[8] = null  # loss
     assert L.gs2d_render_fwd_bwd_l2(C.byref(good), 4, *args, null) == INVALID
-    args = [fake] * 15
-    args[14] = odd  # workspace
+    args = [fake] * 16
+    args[15] = odd  # workspace
     assert L.gs2d_render_fwd_bwd_l2(C.byref(good), 4, *args, null) == INVALID
-    args = [fake] * 15
+    args = [fake] * 16
     args[3] = odd  # tile_ranges
     assert L.gs2d_render_fwd_bwd_l2(C.byref(good), 4, *args, null) == INVALID
-    assert L.gs2d_render_fwd_bwd_l2(C.byref(bad), 4, *([fake] * 15), null) == INVALID
+    assert L.gs2d_render_fwd_bwd_l2(C.byref(bad), 4, *([fake] * 16), null) == INVALID
     # read_status
     assert L.gs2d_read_status(None, None, None, None) == INVALID
     assert L.gs2d_read_status(odd, None, None, None) == INVALID

@@ -19,7 +19,7 @@ from gpu_common import (GRAD_TOL, _gaussians_touching, check_grads, check_image,
 pytestmark = pytest.mark.gpu
 
 
-def fused_run(wl, write_image=True, capacity=None):
+def fused_run(wl, write_image=True, capacity=None, absgrad=False):
     R = gs2d.Rasterizer(wl.width, wl.height, wl.n, wl.mode, wl.cutoff_sigma, wl.t_min,
                         pair_capacity=capacity, param=wl.param)
     R.project(to_dev(wl.xy), to_dev(wl.chol), to_dev(wl.rgb), to_dev(wl.depth),
@@ -27,7 +27,8 @@ def fused_run(wl, write_image=True, capacity=None):
     R.bin_and_sort(sync=True)
     if not write_image:
         R.image.fill_(-7.0)
-    R.render_fwd_bwd_l2(to_dev(wl.target), to_dev(wl.background), write_image=write_image)
+    R.render_fwd_bwd_l2(to_dev(wl.target), to_dev(wl.background), write_image=write_image,
+                        absgrad=absgrad)
     torch.cuda.synchronize()
     out = dict(image=R.image.cpu().numpy(), loss=float(R.loss.item()),
                grads=dict(xy=R.d_xy[: wl.n].cpu().numpy(), chol=R.d_shape[: wl.n].cpu().numpy(),
@@ -35,6 +36,8 @@ def fused_run(wl, write_image=True, capacity=None):
     if R.d_opacity is not None:
         out["grads"]["opacity"] = R.d_opacity[: wl.n].cpu().numpy()
         out["grads"]["background"] = R.d_background.cpu().numpy()
+    if absgrad:
+        out["grads"]["xy_abs"] = R.d_xy_abs[: wl.n].cpu().numpy()
     return out
 
 
