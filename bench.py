@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--impl", default="gs2d", choices=["gs2d", "reference"])
     ap.add_argument("--workload", default="image_768x512_50k")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
+    ap.add_argument("--path", choices=("fused", "separate"), default="fused",
+                    help="training step: the fused fwd+L2+bwd call, or the three separate calls")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -284,13 +286,21 @@ def run_gs2d(args):
     stream = torch.cuda.Stream(device=dev)
     flush_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
-    def step():
+    def step_separate():
         R.project(xy, chol, rgb, depth, opac)
         R.bin_and_sort(sync=False)
         R.render_fwd(bg)
         if not fwd_only:
             R.loss_l2(target)
             R.render_bwd()
+
+    def step_fused():
+        R.project(xy, chol, rgb, depth, opac)
+        R.bin_and_sort(sync=False)
+        R.render_fwd_bwd_l2(target, bg)
+
+    use_fused = args.path == "fused" and not fwd_only
+    step = step_fused if use_fused else step_separate
 
     def render():
         R.project(xy, chol, rgb, depth, opac)
@@ -353,13 +363,20 @@ def run_gs2d(args):
     k2 = max(20, min(args.steps, 400))
     render_ms = statistics.median(timed(run_render, k2, 5))
     cached_ms = statistics.median(timed(run_cached, k2, 5))
+    path_ms = {}
+    if not fwd_only:
+        other = step_separate if use_fused else step_fused
+        path_ms[args.path] = statistics.median(step_ms)
+        path_ms["separate" if use_fused else "fused"] = statistics.median(timed(graph_of(other), k2, 5))
     phases = {}
     if True:  # eager, one call per timing pair
-        names = ["project", "bin_and_sort", "render_fwd"] + ([] if fwd_only else ["loss_l2", "render_bwd"])
+        names = ["project", "bin_and_sort", "render_fwd"] + (
+            [] if fwd_only else ["loss_l2", "render_bwd", "render_fwd_bwd_l2"])
         fns = {"project": lambda: R.project(xy, chol, rgb, depth, opac),
                "bin_and_sort": lambda: R.bin_and_sort(sync=False),
                "render_fwd": lambda: R.render_fwd(bg),
-               "loss_l2": lambda: R.loss_l2(target), "render_bwd": lambda: R.render_bwd()}
+               "loss_l2": lambda: R.loss_l2(target), "render_bwd": lambda: R.render_bwd(),
+               "render_fwd_bwd_l2": lambda: R.render_fwd_bwd_l2(target, bg)}
         per = {k: [] for k in names}
         with torch.cuda.stream(stream):
             for _ in range(k2):
@@ -434,9 +451,7 @@ def run_gs2d(args):
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, args.cpu_seconds)
 
-    layout_passes = (R.num_tiles - 1).bit_length()
-    passes = (layout_passes + (32 if wl.mode == 1 else 0) + 7) // 8
-    per_step_kernels = 1 + (2 + passes) + 1 + (0 if fwd_only else 2 + 2)
+    per_step_kernels = kernels_per_step(R, wl, use_fused, fwd_only)
     unit = "iters/s" if not fwd_only else "frames/s"
     if rank == 0:
         line = {
@@ -446,8 +461,12 @@ def run_gs2d(args):
             "config": {"workload": describe(wl), "name": args.workload, "pairs": int(P),
                        "l2": "256 MiB buffer written before every timed step",
                        "graph": not args.no_graph,
+                       "path": ("fused fwd+L2+bwd call" if use_fused else
+                                "separate forward, loss and backward calls") if not fwd_only else
+                               "forward",
                        "replicas": "each rank renders its own independently seeded image"},
             "render_fps": 1e3 / render_ms, "cached_render_fps": 1e3 / cached_ms,
+            "paths_iters_s": {k: 1e3 / v for k, v in path_ms.items()},
             "phase_ms": phases,
             "roofline": dominant,
             "roofline_fwd": rl_fwd, "roofline_bwd": rl_bwd,
@@ -464,6 +483,25 @@ def run_gs2d(args):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def kernels_per_step(R, wl, fused: bool, fwd_only: bool) -> int:
+    """The library's kernel launches in one step (memsets not counted), from
+    the same rules the library uses to pick its kernels."""
+    comp = wl.mode == 1
+    T = R.num_tiles
+    if not comp and T <= 2048 and wl.n <= (1 << 20):
+        binning = 3  # tile histogram, tile scan, scatter
+    else:
+        passes = ((T - 1).bit_length() + (32 if comp else 0) + 7) // 8
+        partitions = (R.capacity + 2047) // 2048
+        binning = 2 + passes + (passes - 1) + (passes if partitions > 128 else 0) + 1
+    k = 1 + binning
+    if fwd_only:
+        return k + 1
+    if fused:
+        return k + (2 if comp else 3)  # (fused kernel | forward+loss, backward) + gather
+    return k + 1 + 2 + 2  # forward, loss (2), backward + gather
 
 
 def main():
