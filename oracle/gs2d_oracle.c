@@ -599,9 +599,10 @@ typedef struct {
  * Chain rule through one touching pair, given dL/dw (how the loss moves with
  * the weight w of this Gaussian at this pixel).  The pair's share of the mean
  * gradient is also added in absolute value (absgrad: DrawingWithGaussians
- * README, 3D fitting: gsplat-style absgrad, per-pixel absolute mean-gradient
- * contributions; the three colour channels are summed before the absolute
- * value, since dL/dw already holds all three).  With
+ * README, Fit 3D Gaussians and export to SuperSplat: gsplat-style absgrad,
+ * per-pixel absolute mean-gradient contributions; the three colour channels
+ * are summed before the absolute value, since dL/dw already holds all
+ * three).  With
  * q = A dx^2 + 2B dx dy + C dy^2, dx = px - mu_x, dy = py - mu_y and
  * w = exp(-q/2):  dw/dq = -w/2,  dq/dmu_x = -2(A dx + B dy),
  * dq/dmu_y = -2(B dx + C dy),  dq/dA = dx^2, dq/dB = 2 dx dy, dq/dC = dy^2.
