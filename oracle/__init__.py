@@ -55,7 +55,7 @@ class use_library:
 class RefCfg(C.Structure):
     _fields_ = [("width", C.c_int32), ("height", C.c_int32), ("tile", C.c_int32),
                 ("mode", C.c_int32), ("cutoff_sigma", C.c_float), ("t_min", C.c_float),
-                ("param", C.c_int32)]
+                ("param", C.c_int32), ("scale", C.c_float)]
 
 
 SUM, COMPOSITE = 0, 1
@@ -100,10 +100,11 @@ class Config:
     t_min: float = 1e-4
     tile: int = 16
     param: int = CHOLESKY
+    scale: float = 1.0  # output pixels per unit of xy and shape
 
     def c(self) -> RefCfg:
         return RefCfg(self.width, self.height, self.tile, self.mode, self.cutoff_sigma, self.t_min,
-                      self.param)
+                      self.param, self.scale)
 
     @property
     def tiles_x(self) -> int:

@@ -69,6 +69,7 @@ typedef struct {
   float cutoff_sigma;    /* k: the mask is q <= k*k */
   float t_min;           /* composite early-termination threshold */
   int32_t param;         /* 0: Cholesky factor (l11, l21, l22); 1: scale-rotation (s_x, s_y, theta) */
+  float scale;           /* output pixels per unit of xy and shape (any-resolution render); 0 means 1 */
 } ref_cfg;
 
 #define REF_MODE_SUM 0
@@ -80,6 +81,29 @@ static int32_t ref_tiles_x(const ref_cfg* cfg) { return (cfg->width + cfg->tile 
 static int32_t ref_tiles_y(const ref_cfg* cfg) { return (cfg->height + cfg->tile - 1) / cfg->tile; }
 
 int32_t gs2dref_num_tiles(const ref_cfg* cfg) { return ref_tiles_x(cfg) * ref_tiles_y(cfg); }
+
+/*
+ * Rendering at any resolution (FlashImgs README, Lifecycle / building-block
+ * API: render at any height): the parameters live in the units of the image they were fitted
+ * to, and the render scales them by s output pixels per unit.  The mean and
+ * every length of the shape (the whole Cholesky factor, or both scales) are
+ * multiplied by s, the rotation and the colour are unchanged, so Sigma is
+ * multiplied by s^2 and the peak value stays the colour.  In FP32 the mask
+ * data take the rounded products s * x as their inputs; s = 1 changes
+ * nothing.
+ */
+static float ref_scale(const ref_cfg* cfg) { return cfg->scale == 0.0f ? 1.0f : cfg->scale; }
+
+/* The scaled double-precision mean and shape of one Gaussian. */
+static void ref_scaled(const ref_cfg* cfg, const double* xy, const double* P, double xs[2],
+                       double Ps[3]) {
+  const double s = (double)ref_scale(cfg);
+  xs[0] = s * xy[0];
+  xs[1] = s * xy[1];
+  Ps[0] = s * P[0];
+  Ps[1] = s * P[1];
+  Ps[2] = (cfg->param == REF_PARAM_SCALE_ROT) ? P[2] : s * P[2];
+}
 
 /* ------------------------------------------------------------------------- */
 /* Projection: validity, FP32 inverse covariance, pixel box, tile rectangle.  */
@@ -256,11 +280,11 @@ int32_t gs2dref_project(const ref_cfg* cfg, int32_t n, const float* xy, const fl
     float cf[3];
     int32_t b4[4];
     const float* sh = chol + 3 * (int64_t)i;  /* shape parameters, per cfg->param */
+    const float sc = ref_scale(cfg);
+    const float mx = sc * xy[2 * (int64_t)i], my = sc * xy[2 * (int64_t)i + 1];
     const int kept = (cfg->param == REF_PARAM_SCALE_ROT)
-                         ? ref_mask_data_sr(cfg, xy[2 * (int64_t)i], xy[2 * (int64_t)i + 1], sh[0],
-                                            sh[1], sh[2], cf, b4)
-                         : ref_mask_data(cfg, xy[2 * (int64_t)i], xy[2 * (int64_t)i + 1], sh[0],
-                                         sh[1], sh[2], cf, b4);
+                         ? ref_mask_data_sr(cfg, mx, my, sc * sh[0], sc * sh[1], sh[2], cf, b4)
+                         : ref_mask_data(cfg, mx, my, sc * sh[0], sc * sh[1], sc * sh[2], cf, b4);
     if (!kept) continue;
     memcpy(cn, cf, sizeof cf);
     memcpy(bb, b4, sizeof b4);
@@ -347,8 +371,9 @@ static int ref_touches(const ref_cfg* cfg, const float* xy, const float* conic, 
                        int32_t i, int32_t j) {
   if (j < bb[0] || j > bb[2] || i < bb[1] || i > bb[3]) return 0;
   const float kk = cfg->cutoff_sigma * cfg->cutoff_sigma;
-  const float dx = ((float)j + 0.5f) - xy[0];
-  const float dy = ((float)i + 0.5f) - xy[1];
+  const float sc = ref_scale(cfg);
+  const float dx = ((float)j + 0.5f) - sc * xy[0];
+  const float dy = ((float)i + 0.5f) - sc * xy[1];
   const float q = fmaf(dx, fmaf(conic[0], dx, (2.0f * conic[1]) * dy), (conic[2] * dy) * dy);
   return q <= kk;
 }
@@ -377,9 +402,10 @@ static void ref_inverse_cov(const ref_cfg* cfg, const double* P, double* A, doub
 }
 
 /* One Gaussian at one pixel centre, in double: w = exp(-q/2), plus dx, dy. */
-static double ref_weight(const ref_cfg* cfg, const double* xy, const double* L, int32_t i,
+static double ref_weight(const ref_cfg* cfg, const double* xy0, const double* L0, int32_t i,
                          int32_t j, double* dx, double* dy) {
-  double A, B, C;
+  double xy[2], L[3], A, B, C;
+  ref_scaled(cfg, xy0, L0, xy, L);
   ref_inverse_cov(cfg, L, &A, &B, &C);
   *dx = ((double)j + 0.5) - xy[0];
   *dy = ((double)i + 0.5) - xy[1];
@@ -607,9 +633,11 @@ typedef struct {
  * w = exp(-q/2):  dw/dq = -w/2,  dq/dmu_x = -2(A dx + B dy),
  * dq/dmu_y = -2(B dx + C dy),  dq/dA = dx^2, dq/dB = 2 dx dy, dq/dC = dy^2.
  */
-static void ref_accumulate_w(const ref_cfg* cfg, ref_grad* g, const double* L, double w,
+static void ref_accumulate_w(const ref_cfg* cfg, ref_grad* g, const double* L0, double w,
                              double dLdw, double dx, double dy) {
-  double A, B, C;
+  double xy_unused[2], L[3], A, B, C;
+  const double zero[2] = {0.0, 0.0};
+  ref_scaled(cfg, zero, L0, xy_unused, L);
   ref_inverse_cov(cfg, L, &A, &B, &C);
   const double dq = dLdw * (-0.5 * w);
   const double gx = dq * (-2.0) * (A * dx + B * dy);
@@ -694,11 +722,16 @@ static void ref_pixel_bwd(const ref_scene* s, const int32_t* list, int64_t len, 
  *   d/du = (c^2, c s, s^2), d/dv = (s^2, -c s, c^2) on (A, B, C),
  *   du/ds_x = -2/s_x^3, dv/ds_y = -2/s_y^3,
  *   dA/dtheta = -2B, dB/dtheta = (c^2 - s^2)(u - v), dC/dtheta = 2B.
+ * These are taken at the scaled parameters; with a render scale s the
+ * gradients with respect to the unscaled ones are s times the mean, absgrad
+ * and length gradients (the rotation's is unchanged).
  * The position gradient is the mean gradient (xy is the mean).
  */
-static void ref_finish(const ref_cfg* cfg, const double* L, const ref_grad* g, double* dxy,
+static void ref_finish(const ref_cfg* cfg, const double* L0, const ref_grad* g, double* dxy,
                        double* dchol, double* drgb, double* dopac, double* dxy_abs) {
-  double A, B, C;
+  double xy_unused[2], L[3], A, B, C;
+  const double zero[2] = {0.0, 0.0};
+  ref_scaled(cfg, zero, L0, xy_unused, L);
   ref_inverse_cov(cfg, L, &A, &B, &C);
   const double dA = g->dconic[0], dB = g->dconic[1], dC = g->dconic[2];
   if (cfg->param == REF_PARAM_SCALE_ROT) {
@@ -714,11 +747,15 @@ static void ref_finish(const ref_cfg* cfg, const double* L, const ref_grad* g, d
     dchol[2] = dA * (-2.0 * b * b / (a * a * c * c * c)) + dB * (2.0 * b / (a * c * c * c)) +
                dC * (-2.0 / (c * c * c));
   }
-  dxy[0] = g->dmu[0];
-  dxy[1] = g->dmu[1];
+  const double sc = (double)ref_scale(cfg);
+  dchol[0] *= sc;
+  dchol[1] *= sc;
+  if (cfg->param != REF_PARAM_SCALE_ROT) dchol[2] *= sc;
+  dxy[0] = sc * g->dmu[0];
+  dxy[1] = sc * g->dmu[1];
   if (dxy_abs) {
-    dxy_abs[0] = g->dmu_abs[0];
-    dxy_abs[1] = g->dmu_abs[1];
+    dxy_abs[0] = sc * g->dmu_abs[0];
+    dxy_abs[1] = sc * g->dmu_abs[1];
   }
   for (int d = 0; d < 3; ++d) drgb[d] = g->drgb[d];
   if (dopac) *dopac = g->dopac;

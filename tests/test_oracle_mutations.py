@@ -15,6 +15,7 @@ from oracle import build as obuild
 import test_oracle_pins as pins
 import test_oracle_scale_rot as sr_pins
 import test_oracle_absgrad as abs_pins
+import test_oracle_render_scale as scale_pins
 
 # (name, text in the oracle source, replacement)
 MUTATIONS = [
@@ -47,6 +48,9 @@ MUTATIONS = [
     ("fp32 sincos: quadrant sign", "case 1: *sn = c; *cs = -s; break;", "case 1: *sn = c; *cs = s; break;"),
     ("absgrad: signed instead of absolute", "g->dmu_abs[0] += fabs(gx);", "g->dmu_abs[0] += gx;"),
     ("absgrad: y from x", "g->dmu_abs[1] += fabs(gy);", "g->dmu_abs[1] += fabs(gx);"),
+    ("render scale: mean not scaled in the mask", "const float dx = ((float)j + 0.5f) - sc * xy[0];",
+     "const float dx = ((float)j + 0.5f) - xy[0];"),
+    ("render scale: gradient not scaled back", "dxy[0] = sc * g->dmu[0];", "dxy[0] = g->dmu[0];"),
     ("composite lists not depth sorted", "if (cfg->mode == REF_MODE_COMPOSITE) {\n      g_sort_depth = depth;\n      for",
      "if (0) {\n      g_sort_depth = depth;\n      for"),
 ]
@@ -71,6 +75,9 @@ PINS = [
     sr_pins.test_sum_gradients_by_central_differences,
     lambda: abs_pins.test_absgrad_by_per_pixel_central_differences(oracle.SUM, oracle.CHOLESKY),
     abs_pins.test_triangle_inequality_and_culled_zero,
+    lambda: scale_pins.test_peak_keeps_the_colour(2.0),
+    lambda: scale_pins.test_same_as_prescaled_parameters(oracle.CHOLESKY),
+    lambda: scale_pins.test_gradients_by_central_differences(oracle.CHOLESKY, oracle.SUM),
 ]
 
 
