@@ -101,6 +101,12 @@ typedef struct gs2d_config {
                            while the transmittance in front of it is >= t_min;
                            1e-4 by default */
   int32_t param;        /* GS2D_PARAM_CHOLESKY (0, the default) or GS2D_PARAM_SCALE_ROT */
+  float scale;          /* render at any resolution: output pixels per unit of xy and
+                           shape (the mean and the shape's lengths are multiplied by it;
+                           rotation and colour unchanged; gradients are with respect to
+                           the unscaled parameters).  0 means 1; otherwise finite and
+                           > 0.  (FlashImgs README, Lifecycle / building-block API:
+                           render at any height.) */
 } gs2d_config;
 
 /*

@@ -21,6 +21,7 @@ bool config_ok(const gs2d_config* c) {
   if (c->tile != kTile) return false;
   if (c->mode != GS2D_MODE_SUM && c->mode != GS2D_MODE_COMPOSITE) return false;
   if (c->param != GS2D_PARAM_CHOLESKY && c->param != GS2D_PARAM_SCALE_ROT) return false;
+  if (!isfinite(c->scale) || c->scale < 0.0f) return false;
   if (!isfinite(c->cutoff_sigma) || !(c->cutoff_sigma > 0.0f)) return false;
   if (!isfinite(c->cutoff_sigma * c->cutoff_sigma)) return false;
   if (c->mode == GS2D_MODE_COMPOSITE && !(c->t_min >= 0.0f && c->t_min <= 1.0f)) return false;

@@ -66,6 +66,11 @@ inline int tiles_x(const gs2d_config& c) { return (c.width + kTile - 1) / kTile;
 inline int tiles_y(const gs2d_config& c) { return (c.height + kTile - 1) / kTile; }
 inline int num_tiles(const gs2d_config& c) { return tiles_x(c) * tiles_y(c); }
 
+// Render scale (output pixels per unit of xy and shape); 0 means 1.
+__host__ __device__ inline float render_scale(const gs2d_config& c) {
+  return c.scale == 0.0f ? 1.0f : c.scale;
+}
+
 // Streaming multiprocessors of the current device (148 if the query fails).
 inline int sm_count() {
   int dev = 0, sms = 148;

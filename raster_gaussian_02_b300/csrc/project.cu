@@ -21,8 +21,13 @@ k_project(gs2d_config c, int n, const float* __restrict__ xy, const float* __res
   pdl_enter();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
-  const float mx = xy[2 * i], my = xy[2 * i + 1];
-  const float a = chol[3 * i], b = chol[3 * i + 1], cc = chol[3 * i + 2];
+  // Render scale s: the mean and the shape's lengths enter as the rounded
+  // products s * x (the rotation angle unscaled); s = 1 changes nothing.
+  const float sc = render_scale(c);
+  const bool rot = c.param == GS2D_PARAM_SCALE_ROT;  // (a, b, cc) = (s_x, s_y, theta)
+  const float mx = __fmul_rn(sc, xy[2 * i]), my = __fmul_rn(sc, xy[2 * i + 1]);
+  const float a = __fmul_rn(sc, chol[3 * i]), b = __fmul_rn(sc, chol[3 * i + 1]);
+  const float cc = rot ? chol[3 * i + 2] : __fmul_rn(sc, chol[3 * i + 2]);
   const float r = rgb[3 * i], g = rgb[3 * i + 1], bl = rgb[3 * i + 2];
   const bool comp = c.mode == GS2D_MODE_COMPOSITE;
   float o = 0.0f, d = 0.0f;
@@ -30,7 +35,6 @@ k_project(gs2d_config c, int n, const float* __restrict__ xy, const float* __res
     o = opacity[i];
     d = depth[i];
   }
-  const bool rot = c.param == GS2D_PARAM_SCALE_ROT;  // (a, b, cc) = (s_x, s_y, theta)
   bool ok = isfinite(mx) && isfinite(my) && isfinite(a) && isfinite(b) && isfinite(cc) &&
             isfinite(r) && isfinite(g) && isfinite(bl);
   ok = ok && (rot ? (a != 0.0f && b != 0.0f && fabsf(cc) <= 65536.0f) : (a != 0.0f && cc != 0.0f));
@@ -129,7 +133,7 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
          float* __restrict__ d_xy, float* __restrict__ d_chol, float* __restrict__ d_rgb,
          float* __restrict__ d_opacity, int T, const float4* __restrict__ tile_partials,
          float* __restrict__ d_bg, const float* __restrict__ loss_partials, int loss_blocks,
-         float* __restrict__ loss, float m, int param, float* __restrict__ d_xy_abs) {
+         float* __restrict__ loss, float m, int param, float sc, float* __restrict__ d_xy_abs) {
   pdl_enter();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   const bool bad = (hdr->flags & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) != 0;
@@ -157,9 +161,12 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
     }
     float g0 = 0.f, g1 = 0.f, g2 = 0.f;
     if (cnt > 0 && !bad) {
-      const float a = chol[3 * i], b = chol[3 * i + 1], c = chol[3 * i + 2];
+      // derivatives at the scaled shape, then back to the unscaled one
+      const bool rot = param == GS2D_PARAM_SCALE_ROT;
+      const float a = sc * chol[3 * i], b = sc * chol[3 * i + 1];
+      const float c = rot ? chol[3 * i + 2] : sc * chol[3 * i + 2];
       const float dA = s[2], dB = s[3], dC = s[4];
-      if (param == GS2D_PARAM_SCALE_ROT) {
+      if (rot) {
         float sn, cs;
         sincos_fp32(c, &sn, &cs);
         const float isx = 1.0f / a, isy = 1.0f / b;
@@ -178,6 +185,13 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
         g2 = dA * (-2.0f * b * b * ia2ic2 * ic) + dB * (2.0f * b * ia * ic * ic * ic) +
              dC * (-2.0f * ic * ic * ic);
       }
+      g0 *= sc;
+      g1 *= sc;
+      if (!rot) g2 *= sc;
+      s[0] *= sc;
+      s[1] *= sc;
+      ax *= sc;
+      ay *= sc;
     } else {
       for (int k = 0; k < 9; ++k) s[k] = 0.f;
     }
@@ -260,7 +274,8 @@ cudaError_t launch_gather(const gs2d_config& c, int n, const float* chol, const 
   float* d_b = comp ? d_bg : nullptr;
   auto go = [&](auto kern) {
     return launch(kern, dim3(blocks), dim3(256), 0, s, n, chol, r, rc, offsets, partials, hdr, d_xy,
-                  d_chol, d_rgb, d_op, T, tp, d_b, lp, loss_blocks, loss, m, param, d_xy_abs);
+                  d_chol, d_rgb, d_op, T, tp, d_b, lp, loss_blocks, loss, m, param, render_scale(c),
+                  d_xy_abs);
   };
   if (comp)
     GS2D_TRY(d_xy_abs ? go(k_gather<true, true>) : go(k_gather<true, false>));

@@ -30,13 +30,15 @@ TILE = 16
 class gs2d_config(C.Structure):
     _fields_ = [("width", C.c_int32), ("height", C.c_int32), ("tile", C.c_int32),
                 ("mode", C.c_int32), ("cutoff_sigma", C.c_float), ("t_min", C.c_float),
-                ("param", C.c_int32)]
+                ("param", C.c_int32), ("scale", C.c_float)]
 
 
 def make_config(width: int, height: int, mode: int = GS2D_MODE_SUM, cutoff_sigma: float = 3.0,
-                t_min: float = 1e-4, param: int = GS2D_PARAM_CHOLESKY) -> gs2d_config:
+                t_min: float = 1e-4, param: int = GS2D_PARAM_CHOLESKY,
+                scale: float = 1.0) -> gs2d_config:
+    """scale: output pixels per unit of xy and shape (render at any resolution)."""
     return gs2d_config(int(width), int(height), TILE, int(mode), float(cutoff_sigma), float(t_min),
-                       int(param))
+                       int(param), float(scale))
 
 
 class Gs2dError(RuntimeError):
@@ -209,8 +211,8 @@ class Rasterizer:
     """
 
     def __init__(self, width, height, n, mode=GS2D_MODE_SUM, cutoff_sigma=3.0, t_min=1e-4,
-                 pair_capacity=None, device="cuda", param=GS2D_PARAM_CHOLESKY):
-        self.cfg = make_config(width, height, mode, cutoff_sigma, t_min, param)
+                 pair_capacity=None, device="cuda", param=GS2D_PARAM_CHOLESKY, scale=1.0):
+        self.cfg = make_config(width, height, mode, cutoff_sigma, t_min, param, scale)
         self.width, self.height, self.n, self.mode = int(width), int(height), int(n), int(mode)
         self.device = torch.device(device)
         self.num_tiles = ((width + TILE - 1) // TILE) * ((height + TILE - 1) // TILE)

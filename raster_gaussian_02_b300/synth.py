@@ -211,6 +211,7 @@ class Workload:
     cutoff_sigma: float = 3.0
     t_min: float = 1e-4
     param: int = CHOLESKY
+    scale: float = 1.0  # render scale: output pixels per unit of xy and shape
 
     @property
     def n(self) -> int:

@@ -34,13 +34,14 @@ def to_dev(a, dev="cuda"):
 
 
 def oracle_cfg(wl) -> oracle.Config:
-    return oracle.Config(wl.width, wl.height, wl.mode, wl.cutoff_sigma, wl.t_min, param=wl.param)
+    return oracle.Config(wl.width, wl.height, wl.mode, wl.cutoff_sigma, wl.t_min, param=wl.param,
+                         scale=wl.scale)
 
 
 def gpu_run(wl, d_image=None, capacity=None, sync=True, backward=True, absgrad=False):
     """Whole path on the GPU; returns numpy copies of every output."""
     R = gs2d.Rasterizer(wl.width, wl.height, wl.n, wl.mode, wl.cutoff_sigma, wl.t_min,
-                        pair_capacity=capacity, param=wl.param)
+                        pair_capacity=capacity, param=wl.param, scale=wl.scale)
     xy, chol, rgb = to_dev(wl.xy), to_dev(wl.chol), to_dev(wl.rgb)
     depth, opac, bg = to_dev(wl.depth), to_dev(wl.opacity), to_dev(wl.background)
     R.project(xy, chol, rgb, depth, opac)
@@ -167,6 +168,15 @@ def full_parity(wl, composite=None, check_chain=True):
     else:
         check_grads(g["grads"], gr, keys)
     return g, s, ref
+
+
+def _sampled_fwd_common(g, s: oracle.Scene, rng, m_pix=20000):
+    """Sampled pixels against the oracle's per-pixel forward (sum mode)."""
+    H, W = s.cfg.height, s.cfg.width
+    pix = rng.choice(H * W, size=min(m_pix, H * W), replace=False)
+    ref = s.render_pixels(pix)
+    err = image_errors(g["image"].reshape(3, -1)[:, pix].T, ref["rgb"])
+    assert err.max(initial=0) <= IMG_TOL, err.max()
 
 
 def _sampled_bwd_common(g, s: oracle.Scene, wl, rng, m_pix=20000, m_gauss=1500):

@@ -72,7 +72,9 @@ def test_workspace_size(gs2d):
            gs2d.gs2d_config(768, 512, 16, 0, float("nan"), 1e-4),
            gs2d.gs2d_config(40000, 512, 16, 0, 3.0, 1e-4),
            gs2d.gs2d_config(768, 512, 16, 1, 3.0, 2.0),
-           gs2d.gs2d_config(768, 512, 16, 0, 3.0, 1e-4, 2)]
+           gs2d.gs2d_config(768, 512, 16, 0, 3.0, 1e-4, 2),
+           gs2d.gs2d_config(768, 512, 16, 0, 3.0, 1e-4, 0, -1.0),
+           gs2d.gs2d_config(768, 512, 16, 0, 3.0, 1e-4, 0, float("inf"))]
     for c in bad:
         assert gs2d.gs2d_workspace_size(c, 10, 10) == 0
     assert gs2d.gs2d_workspace_size(cfg, -1, 10) == 0

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 def fused_run(wl, write_image=True, capacity=None, absgrad=False):
     R = gs2d.Rasterizer(wl.width, wl.height, wl.n, wl.mode, wl.cutoff_sigma, wl.t_min,
-                        pair_capacity=capacity, param=wl.param)
+                        pair_capacity=capacity, param=wl.param, scale=wl.scale)
     R.project(to_dev(wl.xy), to_dev(wl.chol), to_dev(wl.rgb), to_dev(wl.depth),
               to_dev(wl.opacity))
     R.bin_and_sort(sync=True)
