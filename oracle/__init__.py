@@ -81,6 +81,8 @@ def _declare(L):
     L.gs2dref_render_pixels.restype = None
     L.gs2dref_render_brute.argtypes = [cfgp, _i32] + [_p] * 12
     L.gs2dref_render_brute.restype = None
+    L.gs2dref_merge.argtypes = [cfgp, _i32] + [_p] * 6 + [_i32] + [_p] * 4
+    L.gs2dref_merge.restype = _i32
     L.gs2dref_sincos_f32.argtypes = [_i32, _p, _p, _p]
     L.gs2dref_sincos_f32.restype = None
     L.gs2dref_loss_l2.argtypes = [_i32, _i32, _p, _p, _p]
@@ -300,6 +302,28 @@ def loss_l2(image, target):
     d = np.zeros_like(image)
     loss = lib().gs2dref_loss_l2(h, w, _ptr(image), _ptr(target), _ptr(d))
     return float(loss), d
+
+
+def merge(cfg: Config, xy, shape, rgb, max_merges: int, with_partners: bool = False):
+    """One round of the moment-matching merge (sum mode).  Returns
+    (xy, shape, rgb) of the merged set (FP32) and the number of merges (and,
+    with_partners, each input's merged partner if it was the pair's lower
+    index, else -1)."""
+    if cfg.mode != SUM:
+        raise ValueError("the merge is defined for the accumulated sum")
+    n = int(np.asarray(xy).reshape(-1, 2).shape[0])
+    xy, shape, rgb = _f32(xy, (n, 2)), _f32(shape, (n, 3)), _f32(rgb, (n, 3))
+    proj = project(cfg, xy, shape, rgb)
+    ranges, sorted_gid = bin_tiles(cfg, proj)
+    sg = sorted_gid if sorted_gid.size else np.zeros(1, np.int32)
+    oxy, osh, orgb = np.zeros_like(xy), np.zeros_like(shape), np.zeros_like(rgb)
+    partner = np.zeros(max(n, 1), np.int32)
+    m = lib().gs2dref_merge(C.byref(cfg.c()), n, _ptr(xy), _ptr(shape), _ptr(rgb), _ptr(proj.count),
+                            _ptr(ranges), _ptr(sg), int(max_merges), _ptr(oxy), _ptr(osh), _ptr(orgb),
+                            _ptr(partner))
+    k = n - m
+    out = (oxy[:k], osh[:k], orgb[:k], int(m))
+    return out + (partner[:n],) if with_partners else out
 
 
 def step(cfg: Config, xy, chol, rgb, target, depth=None, opacity=None, background=None):

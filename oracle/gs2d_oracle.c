@@ -869,3 +869,187 @@ void gs2dref_render_bwd_gaussians(const ref_cfg* cfg, int32_t n, const double* x
   }
   free(scratch);
 }
+
+/* ------------------------------------------------------------------------- */
+/* Moment-matching merge (sum mode).                                          */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * FlashImgs merges an overcomplete fit down to a target count "via
+ * moment-matching", merging similar Gaussians (FlashImgs README, merge --
+ * Best quality pipeline; the CUDA library's merge_gaussians).  The pages do
+ * not say which Gaussians count as similar or how the moments are weighted;
+ * the readings here:
+ *   - Sigma of a Gaussian in double: Cholesky [[a^2, ab], [ab, b^2 + c^2]];
+ *     scale-rotation R diag(s_x^2, s_y^2) R^T with cos and sin from
+ *     ref_sincos_f32 (so that both sides form the same doubles);
+ *   - cost(i, j) = d^T M^-1 d, d = mu_i - mu_j, M = (Sigma_i + Sigma_j) / 2
+ *     (the Mahalanobis distance of the means under the average covariance);
+ *   - candidates of i: the other valid Gaussians in the tile list of the tile
+ *     holding i's rendered mean (clamped to the image); nn(i) = the candidate
+ *     of least cost, ties to the smaller index;
+ *   - i < j = nn(i) with nn(j) = i form a pair ("mutual nearest neighbours");
+ *   - at most max_merges pairs merge: ordered by the top 16 bits of the FP32
+ *     cost (sign, exponent, 7 mantissa bits), ties by index, the first ones;
+ *   - weights w = sqrt(det Sigma) (|r| + |g| + |b|) (the Gaussian's mass,
+ *     channels summed; 2 pi cancels), equal weights if both are 0; the merged
+ *     mean and covariance are the w-weighted first and second moments, and
+ *     each colour channel keeps its mass: c = (c_i sqrt(det Sigma_i) +
+ *     c_j sqrt(det Sigma_j)) / sqrt(det Sigma);
+ *   - the merged shape: Cholesky a = sqrt(Sxx), b = Sxy / a,
+ *     c = sqrt(Syy - b^2); scale-rotation theta = atan2(2 Sxy, Sxx - Syy) / 2,
+ *     s_x^2, s_y^2 the eigenvalues along theta and across it;
+ *   - output: the Gaussians in index order, a merged pair in the slot of its
+ *     lower index and its upper index dropped; culled Gaussians pass through.
+ * Every value of a decision is computed in double with the operations in the
+ * order written (the kernel evaluates the same sequence).
+ */
+static void ref_sigma_d(const ref_cfg* cfg, const float* P, double S[3]) {
+  if (cfg->param == REF_PARAM_SCALE_ROT) {
+    float sn, cs;
+    ref_sincos_f32(P[2], &sn, &cs);
+    const double c = (double)cs, s = (double)sn;
+    const double x2 = (double)P[0] * (double)P[0], y2 = (double)P[1] * (double)P[1];
+    S[0] = c * c * x2 + s * s * y2;
+    S[1] = c * s * (x2 - y2);
+    S[2] = s * s * x2 + c * c * y2;
+  } else {
+    const double a = P[0], b = P[1], c = P[2];
+    S[0] = a * a;
+    S[1] = a * b;
+    S[2] = b * b + c * c;
+  }
+}
+
+static double ref_merge_cost(const float* xi, const double* Si, const float* xj, const double* Sj) {
+  const double m0 = 0.5 * (Si[0] + Sj[0]), m1 = 0.5 * (Si[1] + Sj[1]), m2 = 0.5 * (Si[2] + Sj[2]);
+  const double dx = (double)xi[0] - (double)xj[0], dy = (double)xi[1] - (double)xj[1];
+  const double det = m0 * m2 - m1 * m1;
+  return (m2 * dx * dx - 2.0 * m1 * dx * dy + m0 * dy * dy) / det;
+}
+
+static int ref_cmp_u64(const void* pa, const void* pb) {
+  const uint64_t a = *(const uint64_t*)pa, b = *(const uint64_t*)pb;
+  return (a > b) - (a < b);
+}
+
+int32_t gs2dref_merge(const ref_cfg* cfg, int32_t n, const float* xy, const float* shape,
+                      const float* rgb, const int32_t* count, const int32_t* ranges,
+                      const int32_t* sorted_gid, int32_t max_merges, float* out_xy,
+                      float* out_shape, float* out_rgb, int32_t* partner) {
+  const int32_t tx = ref_tiles_x(cfg);
+  const float sc = ref_scale(cfg);
+  double* S = (double*)malloc(sizeof(double) * 3 * (size_t)(n > 0 ? n : 1));
+  int32_t* nn = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+  double* cost = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  for (int32_t i = 0; i < n; ++i) ref_sigma_d(cfg, shape + 3 * (int64_t)i, S + 3 * (int64_t)i);
+  for (int32_t i = 0; i < n; ++i) {
+    nn[i] = -1;
+    cost[i] = HUGE_VAL;
+    if (count[i] == 0) continue;
+    const float px = floorf(sc * xy[2 * (int64_t)i]), py = floorf(sc * xy[2 * (int64_t)i + 1]);
+    const int32_t col = px < 0.0f ? 0 : (px > (float)(cfg->width - 1) ? cfg->width - 1 : (int32_t)px);
+    const int32_t row = py < 0.0f ? 0 : (py > (float)(cfg->height - 1) ? cfg->height - 1 : (int32_t)py);
+    const int64_t t = (int64_t)(row / cfg->tile) * tx + col / cfg->tile;
+    for (int32_t k = ranges[2 * t]; k < ranges[2 * t + 1]; ++k) {
+      const int32_t j = sorted_gid[k];
+      if (j == i) continue;
+      const double c = ref_merge_cost(xy + 2 * (int64_t)i, S + 3 * (int64_t)i, xy + 2 * (int64_t)j,
+                                      S + 3 * (int64_t)j);
+      if (c < cost[i] || (c == cost[i] && j < nn[i])) {
+        cost[i] = c;
+        nn[i] = j;
+      }
+    }
+  }
+  /* mutual pairs (lower index), ordered by the top 16 bits of the FP32 cost, then index */
+  int32_t* pairs = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+  uint32_t* key = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(n > 0 ? n : 1));
+  int32_t np = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t j = nn[i];
+    if (j > i && nn[j] == i) {
+      const float cf = (float)cost[i];
+      uint32_t u;
+      memcpy(&u, &cf, sizeof u);
+      key[np] = u >> 16;
+      pairs[np++] = i;
+    }
+  }
+  /* the first max_merges pairs in (key, index) order */
+  uint64_t* order = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)(np > 0 ? np : 1));
+  for (int32_t q = 0; q < np; ++q) order[q] = ((uint64_t)key[q] << 32) | (uint32_t)pairs[q];
+  qsort(order, (size_t)np, sizeof(uint64_t), ref_cmp_u64);
+  char* take = (char*)calloc((size_t)(n > 0 ? n : 1), 1);
+  int32_t merges = 0;
+  for (int32_t q = 0; q < np && merges < max_merges; ++q, ++merges)
+    take[(int32_t)(order[q] & 0xFFFFFFFFu)] = 1;
+  free(order);
+  /* write the merged set */
+  char* dropped = (char*)calloc((size_t)(n > 0 ? n : 1), 1);
+  for (int32_t i = 0; i < n; ++i)
+    if (take[i]) dropped[nn[i]] = 1;
+  if (partner) /* for the tests: the merged partner of each lower index, else -1 */
+    for (int32_t i = 0; i < n; ++i) partner[i] = take[i] ? nn[i] : -1;
+  int32_t o = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    if (dropped[i]) continue;
+    float* X = out_xy + 2 * (int64_t)o;
+    float* P = out_shape + 3 * (int64_t)o;
+    float* Cc = out_rgb + 3 * (int64_t)o;
+    if (!take[i]) {
+      memcpy(X, xy + 2 * (int64_t)i, 2 * sizeof(float));
+      memcpy(P, shape + 3 * (int64_t)i, 3 * sizeof(float));
+      memcpy(Cc, rgb + 3 * (int64_t)i, 3 * sizeof(float));
+      ++o;
+      continue;
+    }
+    const int32_t j = nn[i];
+    const double* Si = S + 3 * (int64_t)i;
+    const double* Sj = S + 3 * (int64_t)j;
+    const double ri = sqrt(Si[0] * Si[2] - Si[1] * Si[1]);
+    const double rj = sqrt(Sj[0] * Sj[2] - Sj[1] * Sj[1]);
+    const float* ci = rgb + 3 * (int64_t)i;
+    const float* cj = rgb + 3 * (int64_t)j;
+    double wi = ri * (fabs((double)ci[0]) + fabs((double)ci[1]) + fabs((double)ci[2]));
+    double wj = rj * (fabs((double)cj[0]) + fabs((double)cj[1]) + fabs((double)cj[2]));
+    if (wi + wj == 0.0) wi = wj = 1.0;
+    const double W = wi + wj;
+    const double xi0 = xy[2 * (int64_t)i], xi1 = xy[2 * (int64_t)i + 1];
+    const double xj0 = xy[2 * (int64_t)j], xj1 = xy[2 * (int64_t)j + 1];
+    const double m0 = (wi * xi0 + wj * xj0) / W, m1 = (wi * xi1 + wj * xj1) / W;
+    const double di0 = xi0 - m0, di1 = xi1 - m1, dj0 = xj0 - m0, dj1 = xj1 - m1;
+    const double sxx = (wi * (Si[0] + di0 * di0) + wj * (Sj[0] + dj0 * dj0)) / W;
+    const double sxy = (wi * (Si[1] + di0 * di1) + wj * (Sj[1] + dj0 * dj1)) / W;
+    const double syy = (wi * (Si[2] + di1 * di1) + wj * (Sj[2] + dj1 * dj1)) / W;
+    const double r = sqrt(sxx * syy - sxy * sxy);
+    X[0] = (float)m0;
+    X[1] = (float)m1;
+    for (int d = 0; d < 3; ++d) Cc[d] = (float)(((double)ci[d] * ri + (double)cj[d] * rj) / r);
+    if (cfg->param == REF_PARAM_SCALE_ROT) {
+      const double th = 0.5 * atan2(2.0 * sxy, sxx - syy);
+      const double c = cos(th), s = sin(th);
+      /* eigenvalue along theta: the quadratic form of (cos, sin); the other
+         is the trace minus it */
+      const double l1 = c * c * sxx + 2.0 * c * s * sxy + s * s * syy;
+      const double l2 = (sxx + syy) - l1;
+      P[0] = (float)sqrt(l1);
+      P[1] = (float)sqrt(l2 > 0.0 ? l2 : 0.0);
+      P[2] = (float)th;
+    } else {
+      const double a = sqrt(sxx), b = sxy / a;
+      P[0] = (float)a;
+      P[1] = (float)b;
+      P[2] = (float)sqrt(syy - b * b);
+    }
+    ++o;
+  }
+  free(S);
+  free(nn);
+  free(cost);
+  free(pairs);
+  free(key);
+  free(take);
+  free(dropped);
+  return merges;
+}

@@ -16,6 +16,7 @@ import test_oracle_pins as pins
 import test_oracle_scale_rot as sr_pins
 import test_oracle_absgrad as abs_pins
 import test_oracle_render_scale as scale_pins
+import test_oracle_merge as merge_pins
 
 # (name, text in the oracle source, replacement)
 MUTATIONS = [
@@ -51,6 +52,11 @@ MUTATIONS = [
     ("render scale: mean not scaled in the mask", "const float dx = ((float)j + 0.5f) - sc * xy[0];",
      "const float dx = ((float)j + 0.5f) - xy[0];"),
     ("render scale: gradient not scaled back", "dxy[0] = sc * g->dmu[0];", "dxy[0] = g->dmu[0];"),
+    ("merge: weight from the partner's area", "double wi = ri * (fabs", "double wi = rj * (fabs"),
+    ("merge: spread term transposed", "(wi * (Si[0] + di0 * di0)", "(wi * (Si[0] + di0 * di1)"),
+    ("merge: colour mass over the wrong area", "(double)cj[d] * rj) / r);", "(double)cj[d] * rj) / ri);"),
+    ("merge: cost cross-term sign", "(m2 * dx * dx - 2.0 * m1 * dx * dy", "(m2 * dx * dx + 2.0 * m1 * dx * dy"),
+    ("merge: pairs not mutual", "if (j > i && nn[j] == i) {", "if (j > i) {"),
     ("composite lists not depth sorted", "if (cfg->mode == REF_MODE_COMPOSITE) {\n      g_sort_depth = depth;\n      for",
      "if (0) {\n      g_sort_depth = depth;\n      for"),
 ]
@@ -78,6 +84,10 @@ PINS = [
     lambda: scale_pins.test_peak_keeps_the_colour(2.0),
     lambda: scale_pins.test_same_as_prescaled_parameters(oracle.CHOLESKY),
     lambda: scale_pins.test_gradients_by_central_differences(oracle.CHOLESKY, oracle.SUM),
+    merge_pins.test_identical_twins,
+    lambda: merge_pins.test_moments_of_the_image_are_kept(oracle.CHOLESKY),
+    merge_pins.test_channel_masses_are_kept,
+    lambda: merge_pins.test_pairs_are_mutual_nearest_neighbours(oracle.CHOLESKY),
 ]
 
 
