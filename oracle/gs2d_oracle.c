@@ -880,11 +880,14 @@ void gs2dref_render_bwd_gaussians(const ref_cfg* cfg, int32_t n, const double* x
  * Best quality pipeline; the CUDA library's merge_gaussians).  The pages do
  * not say which Gaussians count as similar or how the moments are weighted;
  * the readings here:
- *   - Sigma of a Gaussian in double: Cholesky [[a^2, ab], [ab, b^2 + c^2]];
+ *   - Sigma of a Gaussian: Cholesky [[a^2, ab], [ab, b^2 + c^2]];
  *     scale-rotation R diag(s_x^2, s_y^2) R^T with cos and sin from
- *     ref_sincos_f32 (so that both sides form the same doubles);
+ *     ref_sincos_f32;
  *   - cost(i, j) = d^T M^-1 d, d = mu_i - mu_j, M = (Sigma_i + Sigma_j) / 2
- *     (the Mahalanobis distance of the means under the average covariance);
+ *     (the Mahalanobis distance of the means under the average covariance),
+ *     taken in FP32 in the order of ref_merge_cost (a decision: the kernel
+ *     evaluates the same sequence), +inf when det M <= 0, the quadratic form
+ *     clamped at 0;
  *   - candidates of i: the other valid Gaussians in the tile list of the tile
  *     holding i's rendered mean (clamped to the image); nn(i) = the candidate
  *     of least cost, ties to the smaller index;
@@ -901,8 +904,7 @@ void gs2dref_render_bwd_gaussians(const ref_cfg* cfg, int32_t n, const double* x
  *     s_x^2, s_y^2 the eigenvalues along theta and across it;
  *   - output: the Gaussians in index order, a merged pair in the slot of its
  *     lower index and its upper index dropped; culled Gaussians pass through.
- * Every value of a decision is computed in double with the operations in the
- * order written (the kernel evaluates the same sequence).
+ * The merged values are computed in double.
  */
 static void ref_sigma_d(const ref_cfg* cfg, const float* P, double S[3]) {
   if (cfg->param == REF_PARAM_SCALE_ROT) {
@@ -921,11 +923,30 @@ static void ref_sigma_d(const ref_cfg* cfg, const float* P, double S[3]) {
   }
 }
 
-static double ref_merge_cost(const float* xi, const double* Si, const float* xj, const double* Sj) {
-  const double m0 = 0.5 * (Si[0] + Sj[0]), m1 = 0.5 * (Si[1] + Sj[1]), m2 = 0.5 * (Si[2] + Sj[2]);
-  const double dx = (double)xi[0] - (double)xj[0], dy = (double)xi[1] - (double)xj[1];
-  const double det = m0 * m2 - m1 * m1;
-  return (m2 * dx * dx - 2.0 * m1 * dx * dy + m0 * dy * dy) / det;
+/* Sigma in FP32 for the pairing decision: the same products as
+ * ref_sigma_d, each rounded to FP32. */
+static void ref_sigma_f(const ref_cfg* cfg, const float* P, float S[3]) {
+  if (cfg->param == REF_PARAM_SCALE_ROT) {
+    float sn, cs;
+    ref_sincos_f32(P[2], &sn, &cs);
+    const float x2 = P[0] * P[0], y2 = P[1] * P[1];
+    S[0] = (cs * cs) * x2 + (sn * sn) * y2;
+    S[1] = (cs * sn) * (x2 - y2);
+    S[2] = (sn * sn) * x2 + (cs * cs) * y2;
+  } else {
+    S[0] = P[0] * P[0];
+    S[1] = P[0] * P[1];
+    S[2] = P[1] * P[1] + P[2] * P[2];
+  }
+}
+
+static float ref_merge_cost(const float* xi, const float* Si, const float* xj, const float* Sj) {
+  const float m0 = 0.5f * (Si[0] + Sj[0]), m1 = 0.5f * (Si[1] + Sj[1]), m2 = 0.5f * (Si[2] + Sj[2]);
+  const float dx = xi[0] - xj[0], dy = xi[1] - xj[1];
+  const float det = m0 * m2 - m1 * m1;
+  if (!(det > 0.0f)) return HUGE_VALF;
+  const float num = ((m2 * dx) * dx - ((2.0f * m1) * dx) * dy) + (m0 * dy) * dy;
+  return fmaxf(num, 0.0f) / det;
 }
 
 static int ref_cmp_u64(const void* pa, const void* pb) {
@@ -940,12 +961,16 @@ int32_t gs2dref_merge(const ref_cfg* cfg, int32_t n, const float* xy, const floa
   const int32_t tx = ref_tiles_x(cfg);
   const float sc = ref_scale(cfg);
   double* S = (double*)malloc(sizeof(double) * 3 * (size_t)(n > 0 ? n : 1));
+  float* Sf = (float*)malloc(sizeof(float) * 3 * (size_t)(n > 0 ? n : 1));
   int32_t* nn = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
-  double* cost = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
-  for (int32_t i = 0; i < n; ++i) ref_sigma_d(cfg, shape + 3 * (int64_t)i, S + 3 * (int64_t)i);
+  float* cost = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+  for (int32_t i = 0; i < n; ++i) {
+    ref_sigma_d(cfg, shape + 3 * (int64_t)i, S + 3 * (int64_t)i);
+    ref_sigma_f(cfg, shape + 3 * (int64_t)i, Sf + 3 * (int64_t)i);
+  }
   for (int32_t i = 0; i < n; ++i) {
     nn[i] = -1;
-    cost[i] = HUGE_VAL;
+    cost[i] = HUGE_VALF;
     if (count[i] == 0) continue;
     const float px = floorf(sc * xy[2 * (int64_t)i]), py = floorf(sc * xy[2 * (int64_t)i + 1]);
     const int32_t col = px < 0.0f ? 0 : (px > (float)(cfg->width - 1) ? cfg->width - 1 : (int32_t)px);
@@ -954,8 +979,8 @@ int32_t gs2dref_merge(const ref_cfg* cfg, int32_t n, const float* xy, const floa
     for (int32_t k = ranges[2 * t]; k < ranges[2 * t + 1]; ++k) {
       const int32_t j = sorted_gid[k];
       if (j == i) continue;
-      const double c = ref_merge_cost(xy + 2 * (int64_t)i, S + 3 * (int64_t)i, xy + 2 * (int64_t)j,
-                                      S + 3 * (int64_t)j);
+      const float c = ref_merge_cost(xy + 2 * (int64_t)i, Sf + 3 * (int64_t)i, xy + 2 * (int64_t)j,
+                                     Sf + 3 * (int64_t)j);
       if (c < cost[i] || (c == cost[i] && j < nn[i])) {
         cost[i] = c;
         nn[i] = j;
@@ -969,9 +994,8 @@ int32_t gs2dref_merge(const ref_cfg* cfg, int32_t n, const float* xy, const floa
   for (int32_t i = 0; i < n; ++i) {
     const int32_t j = nn[i];
     if (j > i && nn[j] == i) {
-      const float cf = (float)cost[i];
       uint32_t u;
-      memcpy(&u, &cf, sizeof u);
+      memcpy(&u, &cost[i], sizeof u);
       key[np] = u >> 16;
       pairs[np++] = i;
     }
@@ -1045,6 +1069,7 @@ int32_t gs2dref_merge(const ref_cfg* cfg, int32_t n, const float* xy, const floa
     ++o;
   }
   free(S);
+  free(Sf);
   free(nn);
   free(cost);
   free(pairs);

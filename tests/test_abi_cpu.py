@@ -144,6 +144,15 @@ def test_host_checks_reject_bad_arguments(gs2d):
     args[3] = odd  # tile_ranges
     assert L.gs2d_render_fwd_bwd_l2(C.byref(good), 4, *args, null) == INVALID
     assert L.gs2d_render_fwd_bwd_l2(C.byref(bad), 4, *([fake] * 16), null) == INVALID
+    # merge: sum mode only, max_merges >= 0, a 256-byte aligned workspace
+    margs = [fake] * 7
+    assert L.gs2d_merge(C.byref(comp), 4, *margs, 1, fake, fake, fake, None, fake, null) == INVALID
+    assert L.gs2d_merge(C.byref(good), 4, *margs, -1, fake, fake, fake, None, fake, null) == INVALID
+    assert L.gs2d_merge(C.byref(good), 4, *margs, 1, fake, fake, fake, None, C.c_void_p(0x10010),
+                        null) == INVALID
+    assert L.gs2d_merge(C.byref(good), 4, *margs, 1, null, fake, fake, None, fake, null) == INVALID
+    assert gs2d.gs2d_merge_workspace_size(-1) == 0
+    assert gs2d.gs2d_merge_workspace_size(1000) > gs2d.gs2d_merge_workspace_size(10) > 0
     # read_status
     assert L.gs2d_read_status(None, None, None, None) == INVALID
     assert L.gs2d_read_status(odd, None, None, None) == INVALID

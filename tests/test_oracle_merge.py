@@ -73,6 +73,19 @@ def test_channel_masses_are_kept():
                                render(cfg, xy, sh, rgb).sum((1, 2)), rtol=1e-5)
 
 
+def sigma32(param, sh):
+    """Sigma in FP32 (each product rounded), as the pairing cost uses it."""
+    f = np.float32
+    sh = sh.astype(np.float32)
+    if param == oracle.SCALE_ROT:
+        sn, cs = oracle.sincos_f32(sh[:, 2])
+        x2, y2 = sh[:, 0] * sh[:, 0], sh[:, 1] * sh[:, 1]
+        return np.stack([(cs * cs) * x2 + (sn * sn) * y2, (cs * sn) * (x2 - y2),
+                         (sn * sn) * x2 + (cs * cs) * y2], 1).astype(f)
+    a, b, c = sh.T
+    return np.stack([a * a, a * b, b * b + c * c], 1).astype(f)
+
+
 def sigma(param, sh):
     sh = sh.astype(np.float64)
     if param == oracle.SCALE_ROT:
@@ -89,13 +102,19 @@ def test_pairs_are_mutual_nearest_neighbours(param):
     wl = synth.random_scene(64, 48, 500, seed=131, diag=(0.5, 4.0), margin=3, param=param)
     cfg = oracle.Config(64, 48, param=param)
     s = oracle.Scene(cfg, wl.xy, wl.chol, wl.rgb)
-    S = sigma(param, wl.chol)
+    S = sigma32(param, wl.chol)
     valid = s.proj.count > 0
+    f = np.float32
 
     def cost(i, j):
-        M = 0.5 * (S[i] + S[j])
-        d = wl.xy[i].astype(np.float64) - wl.xy[j].astype(np.float64)
-        return (M[2] * d[0] ** 2 - 2 * M[1] * d[0] * d[1] + M[0] * d[1] ** 2) / (M[0] * M[2] - M[1] ** 2)
+        # the stated reading, in FP32 operation by operation
+        m0, m1, m2 = f(0.5) * (S[i, 0] + S[j, 0]), f(0.5) * (S[i, 1] + S[j, 1]), f(0.5) * (S[i, 2] + S[j, 2])
+        dx, dy = wl.xy[i, 0] - wl.xy[j, 0], wl.xy[i, 1] - wl.xy[j, 1]
+        det = m0 * m2 - m1 * m1
+        if not det > 0:
+            return np.inf
+        num = ((m2 * dx) * dx - ((f(2) * m1) * dx) * dy) + (m0 * dy) * dy
+        return max(num, f(0)) / det
 
     nn = np.full(wl.n, -1)
     for i in np.nonzero(valid)[0]:

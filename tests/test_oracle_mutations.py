@@ -55,7 +55,8 @@ MUTATIONS = [
     ("merge: weight from the partner's area", "double wi = ri * (fabs", "double wi = rj * (fabs"),
     ("merge: spread term transposed", "(wi * (Si[0] + di0 * di0)", "(wi * (Si[0] + di0 * di1)"),
     ("merge: colour mass over the wrong area", "(double)cj[d] * rj) / r);", "(double)cj[d] * rj) / ri);"),
-    ("merge: cost cross-term sign", "(m2 * dx * dx - 2.0 * m1 * dx * dy", "(m2 * dx * dx + 2.0 * m1 * dx * dy"),
+    ("merge: cost cross-term sign", "((m2 * dx) * dx - ((2.0f * m1) * dx) * dy)",
+     "((m2 * dx) * dx + ((2.0f * m1) * dx) * dy)"),
     ("merge: pairs not mutual", "if (j > i && nn[j] == i) {", "if (j > i) {"),
     ("composite lists not depth sorted", "if (cfg->mode == REF_MODE_COMPOSITE) {\n      g_sort_depth = depth;\n      for",
      "if (0) {\n      g_sort_depth = depth;\n      for"),
