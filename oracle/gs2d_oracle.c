@@ -946,7 +946,7 @@ static float ref_merge_cost(const float* xi, const float* Si, const float* xj, c
   const float det = m0 * m2 - m1 * m1;
   if (!(det > 0.0f)) return HUGE_VALF;
   const float num = ((m2 * dx) * dx - ((2.0f * m1) * dx) * dy) + (m0 * dy) * dy;
-  return fmaxf(num, 0.0f) / det;
+  return (num > 0.0f ? num : 0.0f) / det; /* -0 and NaN clamp to +0 */
 }
 
 static int ref_cmp_u64(const void* pa, const void* pb) {

@@ -114,7 +114,7 @@ def test_pairs_are_mutual_nearest_neighbours(param):
         if not det > 0:
             return np.inf
         num = ((m2 * dx) * dx - ((f(2) * m1) * dx) * dy) + (m0 * dy) * dy
-        return max(num, f(0)) / det
+        return (num if num > 0 else f(0)) / det
 
     nn = np.full(wl.n, -1)
     for i in np.nonzero(valid)[0]:
