@@ -281,6 +281,35 @@ GS2D_API gs2d_status gs2d_render_fwd_bwd_l2(const gs2d_config* cfg, int32_t n, c
                                             float* d_xy_abs, void* workspace, gs2d_stream_t stream);
 
 /*
+ * Moment-matching merge, one round, sum mode (FlashImgs README, merge --
+ * Best quality pipeline: an overcomplete fit merged down via moment
+ * matching).  Each valid Gaussian's most similar neighbour is the one of
+ * least cost d^T M^-1 d (d = difference of the means, M = the mean of the two
+ * covariances) among the Gaussians listed in the tile of its rendered mean;
+ * mutual pairs merge, cheapest first (ordered by the top 16 bits of the FP32
+ * cost, ties by index), at most max_merges of them.  A pair becomes one
+ * Gaussian with the mass-weighted mean and covariance of the two (weight =
+ * sqrt(det Sigma) * (|r| + |g| + |b|)) and each colour channel's mass kept.
+ *   xy, shape, rgb       the parameters (cfg->param; cfg->scale is the render
+ *                        scale the lists were binned at)
+ *   rec, count, tile_ranges, sorted_gid   from gs2d_project and
+ *                        gs2d_bin_and_sort of the same parameters and cfg
+ *   out_xy[n,2], out_shape[n,3], out_rgb[n,3]   out: the merged set, in index
+ *                        order (a pair in the slot of its lower index), its
+ *                        first n - merges rows valid; must not alias the inputs
+ *   merges_out           host, may be NULL: waits for the stream and stores
+ *                        the number of pairs merged
+ *   merge_workspace      gs2d_merge_workspace_size(n) bytes, 256-byte aligned
+ * Errors: GS2D_ERR_INVALID_ARG for composite mode or bad arguments.
+ */
+GS2D_API size_t gs2d_merge_workspace_size(int32_t n);
+GS2D_API gs2d_status gs2d_merge(const gs2d_config* cfg, int32_t n, const float* xy, const float* shape,
+                                const float* rgb, const gs2d_record* rec, const int32_t* count,
+                                const int32_t* tile_ranges, const int32_t* sorted_gid,
+                                int32_t max_merges, float* out_xy, float* out_shape, float* out_rgb,
+                                int32_t* merges_out, void* merge_workspace, gs2d_stream_t stream);
+
+/*
  * The L2 loss of gs2d_loss_l2 for callers that cannot supply a workspace.
  * (This call has no counterpart in the method's pages; it serves callers.)
  * Some callers cannot hand the library device memory beyond the image,

@@ -1,6 +1,7 @@
 // The C ABI (include/gs2d.h): host-side argument checks, workspace sizing,
 // and the launches of each call on the caller's stream.  Every check runs
 // before anything is enqueued; no call aborts, throws or traps.
+#include <cstddef>
 #include <math.h>
 #include <stdint.h>
 
@@ -168,6 +169,43 @@ gs2d_status gs2d_render_fwd_bwd_l2(const gs2d_config* cfg, int32_t n, const floa
                                           comp ? d_background : nullptr, n > 0 ? d_xy_abs : nullptr,
                                           static_cast<unsigned char*>(workspace),
                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t gs2d_merge_workspace_size(int32_t n) {
+  if (n < 0) return 0;
+  return merge_workspace_size(n);
+}
+
+gs2d_status gs2d_merge(const gs2d_config* cfg, int32_t n, const float* xy, const float* shape,
+                       const float* rgb, const gs2d_record* rec, const int32_t* count,
+                       const int32_t* tile_ranges, const int32_t* sorted_gid, int32_t max_merges,
+                       float* out_xy, float* out_shape, float* out_rgb, int32_t* merges_out,
+                       void* merge_workspace, gs2d_stream_t stream) {
+  if (!config_ok(cfg) || n < 0 || max_merges < 0) return GS2D_ERR_INVALID_ARG;
+  if (cfg->mode != GS2D_MODE_SUM) return GS2D_ERR_INVALID_ARG;
+  if (!merge_workspace || !aligned(merge_workspace, 256)) return GS2D_ERR_INVALID_ARG;
+  if (n > 0 && (!xy || !shape || !rgb || !rec || !count || !tile_ranges || !sorted_gid ||
+                !out_xy || !out_shape || !out_rgb || !aligned(rec, 16) ||
+                !aligned(tile_ranges, 8) || !aligned(xy, 4) || !aligned(shape, 4) ||
+                !aligned(rgb, 4) || !aligned(count, 4) || !aligned(sorted_gid, 4) ||
+                !aligned(out_xy, 4) || !aligned(out_shape, 4) || !aligned(out_rgb, 4)))
+    return GS2D_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned char* ws = static_cast<unsigned char*>(merge_workspace);
+  cudaError_t e = launch_merge(*cfg, n, xy, shape, rgb, rec, count, tile_ranges, sorted_gid,
+                               max_merges, out_xy, out_shape, out_rgb, ws, nullptr, s);
+  if (e != cudaSuccess) return GS2D_ERR_CUDA;
+  if (merges_out) {
+    int m = 0;
+    if (n > 0) {
+      e = cudaMemcpyAsync(&m, ws + offsetof(MergeHeader, merges), sizeof(int),
+                          cudaMemcpyDeviceToHost, s);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+      if (e != cudaSuccess) return GS2D_ERR_CUDA;
+    }
+    *merges_out = m;
+  }
+  return GS2D_OK;
 }
 
 gs2d_status gs2d_read_status(const void* workspace, int64_t* pairs, uint32_t* flags,

@@ -305,4 +305,21 @@ cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* cho
                                    float* d_rgb, float* d_opacity, float* d_bg, float* d_xy_abs,
                                    unsigned char* ws, cudaStream_t s);
 
+// Start of the merge workspace.
+struct MergeHeader {
+  int boundary;     // key bin at which the selection stops
+  int need;         // pairs to take from the boundary bin, in index order
+  int pairs;        // mutual pairs found
+  int merges;       // pairs merged
+  unsigned int done_a, done_b;
+};
+
+size_t merge_workspace_size(long long n);
+
+cudaError_t launch_merge(const gs2d_config& c, int n, const float* xy, const float* shape,
+                         const float* rgb, const gs2d_record* rec, const int* count,
+                         const int* ranges, const int* sorted_gid, int max_merges, float* out_xy,
+                         float* out_shape, float* out_rgb, unsigned char* ws, int* merges_dev,
+                         cudaStream_t s);
+
 }  // namespace gs2d

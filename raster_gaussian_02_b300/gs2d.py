@@ -75,6 +75,10 @@ def lib() -> C.CDLL:
         L.gs2d_render_bwd.restype = C.c_int
         L.gs2d_render_fwd_bwd_l2.argtypes = [_cfgp, C.c_int32] + [_p] * 16 + [_p]
         L.gs2d_render_fwd_bwd_l2.restype = C.c_int
+        L.gs2d_merge_workspace_size.argtypes = [C.c_int32]
+        L.gs2d_merge_workspace_size.restype = C.c_size_t
+        L.gs2d_merge.argtypes = [_cfgp, C.c_int32] + [_p] * 7 + [C.c_int32] + [_p] * 5 + [_p]
+        L.gs2d_merge.restype = C.c_int
         L.gs2d_loss_l2_noalloc.argtypes = [C.c_int32, C.c_int32] + [_p] * 4 + [_p]
         L.gs2d_loss_l2_noalloc.restype = C.c_int
         L.gs2d_read_status.argtypes = [_p, C.POINTER(C.c_int64), C.POINTER(C.c_uint32), _p]
@@ -190,6 +194,21 @@ def gs2d_render_fwd_bwd_l2(cfg, n, shape, rec, rect, tile_ranges, sorted_gid, ba
         _ptr(d_xy, _f32, "d_xy"), _ptr(d_shape, _f32, "d_shape"), _ptr(d_rgb, _f32, "d_rgb"),
         _ptr(d_opacity, _f32, "d_opacity"), _ptr(d_background, _f32, "d_background"),
         _ptr(d_xy_abs, _f32, "d_xy_abs"), _ptr(workspace, None, "workspace"), _stream(stream))
+
+
+def gs2d_merge_workspace_size(n: int) -> int:
+    return int(lib().gs2d_merge_workspace_size(int(n)))
+
+
+def gs2d_merge(cfg, n, xy, shape, rgb, rec, count, tile_ranges, sorted_gid, max_merges, out_xy,
+               out_shape, out_rgb, merges_out, merge_workspace, stream=None) -> int:
+    return lib().gs2d_merge(
+        C.byref(cfg), int(n), _ptr(xy, _f32, "xy"), _ptr(shape, _f32, "shape"), _ptr(rgb, _f32, "rgb"),
+        _ptr(rec, None, "rec"), _ptr(count, _i32, "count"), _ptr(tile_ranges, _i32, "tile_ranges"),
+        _ptr(sorted_gid, _i32, "sorted_gid"), int(max_merges), _ptr(out_xy, _f32, "out_xy"),
+        _ptr(out_shape, _f32, "out_shape"), _ptr(out_rgb, _f32, "out_rgb"),
+        None if merges_out is None else C.byref(merges_out),
+        _ptr(merge_workspace, None, "merge_workspace"), _stream(stream))
 
 
 def gs2d_read_status(workspace, stream=None):
@@ -321,6 +340,23 @@ class Rasterizer:
         self.loss_l2(target)
         self.render_bwd()
         return self.loss
+
+    def merge(self, max_merges: int):
+        """One round of the moment-matching merge of the parameters last
+        projected and binned (sum mode).  Returns (xy, shape, rgb) of the
+        merged set as new tensors and the number of pairs merged."""
+        n = self.n
+        d = self.device
+        out_xy = torch.empty((max(n, 1), 2), dtype=_f32, device=d)
+        out_shape = torch.empty((max(n, 1), 3), dtype=_f32, device=d)
+        out_rgb = torch.empty((max(n, 1), 3), dtype=_f32, device=d)
+        ws = torch.empty(gs2d_merge_workspace_size(n), dtype=_u8, device=d)
+        m = C.c_int32(0)
+        check(gs2d_merge(self.cfg, n, self.xy, self.shape, self.rgb, self.rec, self.count,
+                         self.tile_ranges, self.sorted_gid, max_merges, out_xy, out_shape, out_rgb,
+                         m, ws), "gs2d_merge")
+        k = n - m.value
+        return out_xy[:k], out_shape[:k], out_rgb[:k], m.value
 
     def records(self):
         """The projected records decoded into named tensors (for tests)."""
