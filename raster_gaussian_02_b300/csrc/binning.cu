@@ -179,7 +179,7 @@ k_tile_hist(int n, int T, int tiles_x, long long cap, const int4* __restrict__ r
 
 __global__ void __launch_bounds__(256)
 k_tile_scan(int T, int B, long long cap, Header* hdr, unsigned int* __restrict__ H,
-            unsigned int* __restrict__ R, int2* __restrict__ ranges) {
+            unsigned int* __restrict__ R, int2* __restrict__ ranges, int* __restrict__ order) {
   pdl_enter();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t = blockIdx.x * 8 + warp;
@@ -244,6 +244,34 @@ k_tile_scan(int T, int B, long long cap, Header* hdr, unsigned int* __restrict__
       const unsigned int start = before + ex[j];
       ranges[u] = (ok && v[j]) ? make_int2(int(start), int(start + v[j])) : make_int2(0, 0);
     }
+  }
+  // Launch order for the raster: tiles bucketed by floor(log2(list length)),
+  // longest first, so that the heaviest tiles start early instead of
+  // finishing last.  The order within a bucket does not matter (it only
+  // affects scheduling; every tile's result is the same).
+  __shared__ unsigned int s_cnt[33], s_pos[33];
+  if (tid < 33) s_cnt[tid] = 0u;
+  __syncthreads();
+  int bk[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int u = tid * 8 + j;
+    bk[j] = (u < T && ok && v[j]) ? 32 - __clz(v[j]) : 0;
+    if (u < T) atomicAdd(&s_cnt[bk[j]], 1u);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    unsigned int run = 0;
+    for (int b = 32; b >= 0; --b) {
+      s_pos[b] = run;
+      run += s_cnt[b];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int u = tid * 8 + j;
+    if (u < T) order[atomicAdd(&s_pos[bk[j]], 1u)] = u;
   }
 }
 
@@ -582,7 +610,7 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
                       reinterpret_cast<const int4*>(rect), count, hdr, block_off, H,
                       (unsigned long long)L.keys_a));
       GS2D_TRY(launch(k_tile_scan, dim3((T + 7) / 8), dim3(256), 0, s, T, blocks, cap, hdr, H, R,
-                      reinterpret_cast<int2*>(tile_ranges)));
+                      reinterpret_cast<int2*>(tile_ranges), reinterpret_cast<int*>(ws + L.tile_order)));
       const size_t smem = size_t(T) * 8 * sizeof(unsigned int);
       GS2D_TRY(cudaFuncSetAttribute(k_tile_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     int(size_t(kCountSortMaxTiles) * 8 * sizeof(unsigned int))));

@@ -113,7 +113,10 @@ cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* cho
   }
   float* d_image = reinterpret_cast<float*>(ws + L.dimage);
   int blocks = 0;
-  GS2D_TRY(launch_render_fwd_loss(c, rec, ranges, sorted_gid, target, scale, image, d_image, lp, &blocks, s));
+  // the counting sort leaves a longest-first launch order of the tiles
+  const int* order = L.count_sort ? reinterpret_cast<const int*>(ws + L.tile_order) : nullptr;
+  GS2D_TRY(launch_render_fwd_loss(c, rec, ranges, sorted_gid, target, scale, image, d_image, lp, &blocks,
+                                  order, s));
   return launch_render_bwd(c, n, chol, rec, rect, ranges, sorted_gid, nullptr, nullptr, nullptr, d_image,
                            d_xy, d_chol, d_rgb, nullptr, nullptr, d_xy_abs, ws, s, loss, blocks);
 }

@@ -54,7 +54,7 @@ constexpr int kCountSortMaxTiles = 2048;
 constexpr long long kCountSortMaxGaussians = 1 << 20;
 
 struct Layout {
-  size_t block_off, offsets, tile_partials, loss_partials, dimage, tile_hist, partials, tables, keys_a, keys_b, vals_tmp, total;
+  size_t block_off, offsets, tile_partials, loss_partials, dimage, tile_order, tile_hist, partials, tables, keys_a, keys_b, vals_tmp, total;
   int passes, digit_bits, tile_bits, key_bits, key_bytes, partial_floats, radix_per_thread;
   bool count_sort;  // sum mode with few tiles: counting sort by tile instead of radix passes
   long long partitions, partitions4;  // radix partitions, and rounded up to a multiple of 4
@@ -119,6 +119,8 @@ inline Layout layout_of(const gs2d_config& c, long long n, long long cap) {
   o = align256(o + 8 * size_t(T));
   L.dimage = o;  // fused pass, sum mode: dL/dC [3,H,W]
   if (!comp) o = align256(o + 12 * size_t(c.width) * size_t(c.height));
+  L.tile_order = o;  // counting sort: tiles by descending list length (launch order)
+  o = align256(o + 4 * size_t(T));
   L.tile_hist = o;  // counting sort by tile: [T][blocks] counts, then row totals [T]
   L.count_sort = !comp && T <= kCountSortMaxTiles && n <= kCountSortMaxGaussians;
   if (L.count_sort) {
@@ -292,11 +294,12 @@ cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
 
 // Sum forward that also takes the L2 loss: writes image (if non-NULL),
 // dL/dC = scale (C - target) to d_image and one loss partial per block to
-// loss_partials; returns the number of blocks in *blocks.
+// loss_partials; returns the number of blocks in *blocks.  order (may be
+// NULL): the tiles in the order their blocks are launched.
 cudaError_t launch_render_fwd_loss(const gs2d_config& c, const gs2d_record* rec, const int* ranges,
                                    const int* sorted_gid, const float* target, float scale,
                                    float* image, float* d_image, float* loss_partials, int* blocks,
-                                   cudaStream_t s);
+                                   const int* order, cudaStream_t s);
 
 cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* chol,
                                    const gs2d_record* rec, const int* rect, const int* ranges,

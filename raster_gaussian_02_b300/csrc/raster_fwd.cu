@@ -27,12 +27,13 @@ __global__ void __launch_bounds__(kWarps * 32, kWarps == 8 ? 8 : 10)
 k_render_fwd_sum(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
                  const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
                  float* __restrict__ image, const float* __restrict__ target, float scale,
-                 float* __restrict__ d_image, float* __restrict__ loss_partials) {
+                 float* __restrict__ d_image, float* __restrict__ loss_partials,
+                 const int* __restrict__ order) {
   constexpr int kParts = 8 / kWarps;
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SumSmem<kWarps>& sm = *reinterpret_cast<SumSmem<kWarps>*>(smem_raw);
-  const int tile = blockIdx.x / kParts;
+  const int tile = order ? order[blockIdx.x / kParts] : int(blockIdx.x / kParts);
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = (blockIdx.x % kParts) * kWarps + warp;  // 8x4 sub-block 0..7 of the tile
@@ -61,7 +62,8 @@ k_render_fwd_sum(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
       d_image[2 * HW + p] = eb * scale;
     }
     const float l = block_sum_ordered<kWarps>(fmaf(eb, eb, fmaf(eg, eg, er * er)), sm.red);
-    if (threadIdx.x == 0) loss_partials[blockIdx.x] = l;
+    // indexed by tile (not by block) so that the launch order cannot change the sum
+    if (threadIdx.x == 0) loss_partials[tile * kParts + int(blockIdx.x % kParts)] = l;
   }
 }
 
@@ -102,12 +104,12 @@ k_render_fwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
 template <int kWarps, bool kLoss>
 cudaError_t launch_fwd_sum(const gs2d_config& c, const float4* r, const int2* rg, const int* sorted_gid,
                            float* image, const float* target, float scale, float* d_image,
-                           float* loss_partials, cudaStream_t s) {
+                           float* loss_partials, const int* order, cudaStream_t s) {
   const size_t smem = sizeof(SumSmem<kWarps>);
   auto kern = k_render_fwd_sum<kWarps, kLoss>;
   GS2D_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
   GS2D_TRY(launch(kern, dim3(num_tiles(c) * (8 / kWarps)), dim3(kWarps * 32), smem, s, c, tiles_x(c), r,
-                  rg, sorted_gid, image, target, scale, d_image, loss_partials));
+                  rg, sorted_gid, image, target, scale, d_image, loss_partials, order));
   return cudaSuccess;
 }
 
@@ -130,9 +132,11 @@ cudaError_t launch_render_fwd(const gs2d_config& c, const gs2d_record* rec, cons
     GS2D_TRY(launch(k_render_fwd_comp, dim3(T), dim3(256), 0, s, c, tiles_x(c), r, rg, sorted_gid, bg, image, t_final, last));
   } else {
     if (half_tile_blocks(T))
-      GS2D_TRY((launch_fwd_sum<4, false>(c, r, rg, sorted_gid, image, nullptr, 0.f, nullptr, nullptr, s)));
+      GS2D_TRY((launch_fwd_sum<4, false>(c, r, rg, sorted_gid, image, nullptr, 0.f, nullptr, nullptr,
+                                         nullptr, s)));
     else
-      GS2D_TRY((launch_fwd_sum<8, false>(c, r, rg, sorted_gid, image, nullptr, 0.f, nullptr, nullptr, s)));
+      GS2D_TRY((launch_fwd_sum<8, false>(c, r, rg, sorted_gid, image, nullptr, 0.f, nullptr, nullptr,
+                                         nullptr, s)));
   }
   return cudaGetLastError();
 }
@@ -140,16 +144,18 @@ cudaError_t launch_render_fwd(const gs2d_config& c, const gs2d_record* rec, cons
 cudaError_t launch_render_fwd_loss(const gs2d_config& c, const gs2d_record* rec, const int* ranges,
                                    const int* sorted_gid, const float* target, float scale,
                                    float* image, float* d_image, float* loss_partials, int* blocks,
-                                   cudaStream_t s) {
+                                   const int* order, cudaStream_t s) {
   const int T = num_tiles(c);
   const float4* r = reinterpret_cast<const float4*>(rec);
   const int2* rg = reinterpret_cast<const int2*>(ranges);
   if (half_tile_blocks(T)) {
     *blocks = 2 * T;
-    GS2D_TRY((launch_fwd_sum<4, true>(c, r, rg, sorted_gid, image, target, scale, d_image, loss_partials, s)));
+    GS2D_TRY((launch_fwd_sum<4, true>(c, r, rg, sorted_gid, image, target, scale, d_image, loss_partials,
+                                      order, s)));
   } else {
     *blocks = T;
-    GS2D_TRY((launch_fwd_sum<8, true>(c, r, rg, sorted_gid, image, target, scale, d_image, loss_partials, s)));
+    GS2D_TRY((launch_fwd_sum<8, true>(c, r, rg, sorted_gid, image, target, scale, d_image, loss_partials,
+                                      order, s)));
   }
   return cudaGetLastError();
 }
