@@ -61,7 +61,7 @@ __device__ __forceinline__ int block_inclusive_count_256(int flag, int* total, i
 // pair's pixels of |t (A dx + B dy)| and |t (B dx + C dy)| (each pixel's
 // share of dL/dmu in absolute value), in a third float4 of the pair's slot.
 template <bool kAbs>
-__global__ void __launch_bounds__(kChunkPairs)
+__global__ void __launch_bounds__(kChunkPairs, 4)  // 4 per SM: measured best (5 or 6 spill and lose)
 k_render_bwd_sum(gs2d_config c, int tiles_x, const Header* __restrict__ hdr,
                  const unsigned char* __restrict__ ws, const float4* __restrict__ rec,
                  const int4* __restrict__ rect, const int* __restrict__ sorted_gid,
