@@ -1,6 +1,6 @@
 // Tile binning and sort, as reduce-then-scan steps that never wait on
-// another block.  Sum mode with few tiles takes the counting sort further
-// down; otherwise:
+// another block.  With few tiles the counting sort further down is taken
+// (composite: then a per-tile depth sort); otherwise:
 //
 //   k_count_scan   sum of the tile counts of every 256-Gaussian block; the
 //                  last block to finish scans the block sums into block
@@ -575,6 +575,61 @@ k_tile_bounds(long long cap, const Header* __restrict__ hdr, const Key* __restri
   }
 }
 
+constexpr int kSegSmem = 4096;  // tile lists up to this long are depth-sorted in shared memory
+
+// Composite: each tile's list, in ascending index after the counting sort,
+// into ascending (depth, index).  The keys (depth_key << 32 | index) are
+// unique, so any sorting network gives the order of a stable sort by depth
+// (ties by index).  The network is the bitonic merge sort with every
+// comparator ascending -- the first step of each merge compares mirrored
+// positions -- so positions past the list's end act as +inf and their
+// comparators are skipped.  Lists longer than kSegSmem are sorted in place in
+// a workspace buffer.
+__global__ void __launch_bounds__(256)
+k_tile_depth_sort(long long cap, const Header* __restrict__ hdr, const int2* __restrict__ ranges,
+                  const float4* __restrict__ rec, int* __restrict__ sorted_gid,
+                  unsigned long long* __restrict__ temp) {
+  pdl_enter();
+  extern __shared__ __align__(16) unsigned long long s_key[];  // kSegSmem
+  if (usable_pairs(hdr, cap) == 0) return;
+  const int2 rg = ranges[blockIdx.x];
+  const int len = rg.y - rg.x;
+  if (len <= 1) return;
+  unsigned long long* key = len <= kSegSmem ? s_key : temp + rg.x;
+  for (int k = threadIdx.x; k < len; k += blockDim.x) {
+    const int g = sorted_gid[rg.x + k];
+    key[k] = ((unsigned long long)depth_key(rec[3 * size_t(g) + 2].w) << 32) | unsigned(g);
+  }
+  __syncthreads();
+  int n2 = 2;
+  while (n2 < len) n2 <<= 1;
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < (n2 >> 1); i += blockDim.x) {
+        int lo, hi;
+        if (j == (k >> 1)) {  // mirrored: merge two ascending runs of length j
+          const int blk = i / j, off = i % j;
+          lo = blk * k + off;
+          hi = blk * k + k - 1 - off;
+        } else {
+          lo = (i / j) * 2 * j + (i % j);
+          hi = lo + j;
+        }
+        if (hi < len) {
+          const unsigned long long a = key[lo], b = key[hi];
+          if (a > b) {
+            key[lo] = b;
+            key[hi] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int k = threadIdx.x; k < len; k += blockDim.x)
+    sorted_gid[rg.x + k] = int(unsigned(key[k] & 0xFFFFFFFFull));
+}
+
 template <bool kComposite>
 cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec, const int* rect,
                              const int* count, long long cap, int* tile_ranges, int* sorted_gid,
@@ -601,7 +656,7 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
   Key* kb = reinterpret_cast<Key*>(ws + L.keys_b);
   const size_t keys_final = (L.passes % 2 == 0) ? L.keys_a : L.keys_b;
   const int blocks = n > 0 ? (n + kScanItems - 1) / kScanItems : 1;
-  if constexpr (!kComposite) {
+  {
     if (L.count_sort) {
       unsigned int* H = reinterpret_cast<unsigned int*>(ws + L.tile_hist);
       unsigned int* R = H + size_t(T) * size_t(blocks);
@@ -618,6 +673,14 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
                       static_cast<const Header*>(hdr), reinterpret_cast<const int4*>(rect), count,
                       static_cast<const long long*>(block_off), static_cast<const unsigned int*>(H), rg,
                       offsets, sorted_gid, reinterpret_cast<unsigned int*>(ws + L.keys_a)));
+      if (kComposite) {
+        const size_t dsmem = size_t(kSegSmem) * sizeof(unsigned long long);
+        GS2D_TRY(cudaFuncSetAttribute(k_tile_depth_sort, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      int(dsmem)));
+        GS2D_TRY(launch(k_tile_depth_sort, dim3(T), dim3(256), dsmem, s, cap,
+                        static_cast<const Header*>(hdr), rg, reinterpret_cast<const float4*>(rec),
+                        sorted_gid, reinterpret_cast<unsigned long long*>(ws + L.keys_b)));
+      }
       return cudaGetLastError();
     }
   }

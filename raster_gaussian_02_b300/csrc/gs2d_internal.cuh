@@ -47,7 +47,7 @@ constexpr int kScanThreads = 256;
 constexpr int kScanItems = kScanThreads;  // Gaussians per scan block, one per thread
 
 constexpr int kRadixThreads = 256;
-// Sum mode with at most this many tiles (and Gaussians) sorts by counting:
+// With at most this many tiles (and Gaussians) the lists are sorted by counting:
 // the per-tile Gaussian masks of one 256-Gaussian block take 32 bytes per
 // tile of shared memory.
 constexpr int kCountSortMaxTiles = 2048;
@@ -56,7 +56,7 @@ constexpr long long kCountSortMaxGaussians = 1 << 20;
 struct Layout {
   size_t block_off, offsets, tile_partials, loss_partials, dimage, tile_order, tile_hist, partials, tables, keys_a, keys_b, vals_tmp, total;
   int passes, digit_bits, tile_bits, key_bits, key_bytes, partial_floats, radix_per_thread;
-  bool count_sort;  // sum mode with few tiles: counting sort by tile instead of radix passes
+  bool count_sort;  // few tiles: counting sort by tile (composite: then by depth per tile)
   long long partitions, partitions4;  // radix partitions, and rounded up to a multiple of 4
 };
 
@@ -122,7 +122,7 @@ inline Layout layout_of(const gs2d_config& c, long long n, long long cap) {
   L.tile_order = o;  // counting sort: tiles by descending list length (launch order)
   o = align256(o + 4 * size_t(T));
   L.tile_hist = o;  // counting sort by tile: [T][blocks] counts, then row totals [T]
-  L.count_sort = !comp && T <= kCountSortMaxTiles && n <= kCountSortMaxGaussians;
+  L.count_sort = T <= kCountSortMaxTiles && n <= kCountSortMaxGaussians;
   if (L.count_sort) {
     const long long B = n > 0 ? (n + kScanItems - 1) / kScanItems : 1;
     o = align256(o + 4 * size_t(T) * size_t(B) + 4 * size_t(T));

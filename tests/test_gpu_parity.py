@@ -73,6 +73,28 @@ def test_sum_sort_paths_near_the_tile_limit(w, h, n):
     check_lists(g, s)
 
 
+def test_composite_list_longer_than_shared_memory_sort():
+    """One tile with more than 4096 Gaussians: its depth sort runs in the
+    workspace instead of shared memory."""
+    wl = synth.random_scene(48, 32, 7000, seed=19, mode=synth.COMPOSITE, diag=(0.5, 2.0))
+    wl.xy[:6000] = np.random.default_rng(1).uniform(18, 30, (6000, 2)).astype(np.float32)
+    wl.opacity[:] = np.minimum(wl.opacity, 0.001)  # no pixel reaches t_min: the test is about the sort
+    wl.depth = (np.round(wl.depth * 50) / 50).astype(np.float32)  # many equal depths: ties by index
+    g, s, _ = full_parity(wl)
+    assert (s.ranges[:, 1] - s.ranges[:, 0]).max() > 4096
+
+
+@pytest.mark.parametrize("w,h,n", [(1024, 512, 8000), (1040, 512, 8000)])
+def test_composite_sort_paths_near_the_tile_limit(w, h, n):
+    """2048 and 2080 tiles: counting sort + per-tile depth sort, and the radix
+    passes, give the oracle's (depth, index) lists."""
+    wl = synth.random_scene(w, h, n, seed=w + n + 1, mode=synth.COMPOSITE, diag=(0.5, 12.0))
+    g = gpu_run(wl)
+    s = oracle_scene(wl)
+    check_projection(g, s)
+    check_lists(g, s)
+
+
 def test_composite_early_termination_dense():
     wl = synth.random_scene(96, 80, 4000, seed=12, mode=synth.COMPOSITE, diag=(1.0, 4.0))
     wl.opacity[:] = 0.95
