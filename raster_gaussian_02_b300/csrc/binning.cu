@@ -601,20 +601,20 @@ k_tile_depth_sort(long long cap, const Header* __restrict__ hdr, const int2* __r
     key[k] = ((unsigned long long)depth_key(rec[3 * size_t(g) + 2].w) << 32) | unsigned(g);
   }
   __syncthreads();
-  int n2 = 2;
-  while (n2 < len) n2 <<= 1;
-  for (int k = 2; k <= n2; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
+  int n2 = 2, l2 = 1;
+  while (n2 < len) {
+    n2 <<= 1;
+    ++l2;
+  }
+  for (int lk = 1; lk <= l2; ++lk) {  // merge size k = 2^lk
+    const int k = 1 << lk;
+    for (int lj = lk - 1; lj >= 0; --lj) {  // comparator distance j = 2^lj
+      const int j = 1 << lj;
       for (int i = threadIdx.x; i < (n2 >> 1); i += blockDim.x) {
-        int lo, hi;
-        if (j == (k >> 1)) {  // mirrored: merge two ascending runs of length j
-          const int blk = i / j, off = i % j;
-          lo = blk * k + off;
-          hi = blk * k + k - 1 - off;
-        } else {
-          lo = (i / j) * 2 * j + (i % j);
-          hi = lo + j;
-        }
+        // comparator i: block i >> lj of width 2j, offset i & (j - 1)
+        const int lo = ((i >> lj) << (lj + 1)) + (i & (j - 1));
+        // first step of a merge: mirrored partner (merges two ascending runs)
+        const int hi = (lj == lk - 1) ? (lo ^ (k - 1)) : (lo + j);
         if (hi < len) {
           const unsigned long long a = key[lo], b = key[hi];
           if (a > b) {
