@@ -36,11 +36,12 @@ k_fused_comp(gs2d_config c, int tiles_x, float scale, const float4* __restrict__
              const int* __restrict__ sorted_gid, const int* __restrict__ offsets,
              const float* __restrict__ bg, const float* __restrict__ target,
              float* __restrict__ image, float4* __restrict__ partials,
-             float4* __restrict__ tile_partials, float* __restrict__ loss_partials) {
+             float4* __restrict__ tile_partials, float* __restrict__ loss_partials,
+             const int* __restrict__ order) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   FusedCompSmem<kAbs>& sm = *reinterpret_cast<FusedCompSmem<kAbs>*>(smem_raw);
-  const int tile = blockIdx.x;
+  const int tile = order ? order[blockIdx.x] : int(blockIdx.x);  // longest lists first when known
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bx0 = tx * kTile + (warp & 1) * 8;
@@ -102,7 +103,8 @@ cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* cho
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
       if (e != cudaSuccess) return e;
       return launch(kern, dim3(T), dim3(256), smem, s, c, tiles_x(c), scale, r, rc, rg, sorted_gid,
-                    offsets, bg, target, image, reinterpret_cast<float4*>(ws + L.partials), tp, lp);
+                    offsets, bg, target, image, reinterpret_cast<float4*>(ws + L.partials), tp, lp,
+                    L.count_sort ? reinterpret_cast<const int*>(ws + L.tile_order) : nullptr);
     };
     if (d_xy_abs)
       GS2D_TRY(go(k_fused_comp<true>, sizeof(FusedCompSmem<true>)));

@@ -222,11 +222,12 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
                   const int* __restrict__ sorted_gid, const int* __restrict__ offsets,
                   const float* __restrict__ bg, const float* __restrict__ t_final,
                   const int* __restrict__ last, const float* __restrict__ d_image,
-                  float4* __restrict__ partials, float4* __restrict__ tile_partials) {
+                  float4* __restrict__ partials, float4* __restrict__ tile_partials,
+                  const int* __restrict__ order) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   CompStage<kAbs>& sm = *reinterpret_cast<CompStage<kAbs>*>(smem_raw);
-  const int tile = blockIdx.x;
+  const int tile = order ? order[blockIdx.x] : int(blockIdx.x);  // longest lists first when known
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bx0 = tx * kTile + (warp & 1) * 8;
@@ -268,7 +269,8 @@ cudaError_t launch_bwd_pairs(const gs2d_config& c, const Layout& L, const float4
     GS2D_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
     GS2D_TRY(launch(kern, dim3(T), dim3(kBwdCompThreads), smem, s, c, tiles_x(c), r, rc, rg, sorted_gid,
                     offsets, bg, t_final, last, d_image, partials,
-                    reinterpret_cast<float4*>(ws + L.tile_partials)));
+                    reinterpret_cast<float4*>(ws + L.tile_partials),
+                    L.count_sort ? reinterpret_cast<const int*>(ws + L.tile_order) : nullptr));
   } else {
     const size_t smem = sizeof(BwdSumSmem);
     auto kern = k_render_bwd_sum<kAbs>;
