@@ -68,7 +68,8 @@ typedef enum gs2d_status {
   GS2D_ERR_CAPACITY = 2,    /* the (tile, Gaussian) pairs exceed pair_capacity */
   GS2D_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
   GS2D_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (results invalid) */
-  GS2D_ERR_OVERFLOW = 5     /* the pair count reached 2^30 */
+  GS2D_ERR_OVERFLOW = 5,    /* the pair count reached 2^30 */
+  GS2D_ERR_UNSUPPORTED = 6  /* the call needs the bounds-checked build of the library */
 } gs2d_status;
 
 enum { GS2D_MODE_SUM = 0, GS2D_MODE_COMPOSITE = 1 };
@@ -345,6 +346,24 @@ GS2D_API gs2d_status gs2d_read_status(const void* workspace, int64_t* pairs, uin
 
 /* A static, human-readable name for a status code. */
 GS2D_API const char* gs2d_status_string(gs2d_status status);
+
+/*
+ * Bounds-check word of the checked build (libgs2d_checked.so, compiled with
+ * GS2D_CHECKS).  In that build every index the kernels take from data -- a
+ * tile id, a list range, a Gaussian index from a tile list, a pair's
+ * destination or partial-gradient slot, a merge partner -- is tested before
+ * the memory access it guards; a failed test skips the access and sets one
+ * bit in a device word instead of faulting.  Bits: 1 tile id, 2 pair
+ * destination, 3 list range, 4 Gaussian index, 5 partial slot, 6 merge
+ * index, 7 shared-memory index.
+ *   word   host out: the OR of the bits set since the last clear (0: every
+ *          checked access stayed in bounds)
+ *   clear  nonzero: zero the bits after reading them
+ * Synchronizes the device.  Returns GS2D_ERR_UNSUPPORTED (and *word = 0) in
+ * the normal build, whose kernels carry no checks; GS2D_ERR_INVALID_ARG for
+ * a NULL word; GS2D_ERR_CUDA if a copy fails.
+ */
+GS2D_API gs2d_status gs2d_debug_check_word(uint32_t* word, int32_t clear);
 
 #ifdef __cplusplus
 }

@@ -170,7 +170,8 @@ k_tile_hist(int n, int T, int tiles_x, long long cap, const int4* __restrict__ r
   block_exclusive_scan_256<long long>(cnt, &total);  // its barriers order the clears
   if (cnt > 0)
     for (int y = r.y; y <= r.w; ++y)
-      for (int x = r.x; x <= r.z; ++x) atomicAdd(&s_h[y * tiles_x + x], 1u);
+      for (int x = r.x; x <= r.z; ++x)
+        if (check_ok(y * tiles_x + x < T, kCheckTile)) atomicAdd(&s_h[y * tiles_x + x], 1u);
   __syncthreads();
   const size_t B = gridDim.x;
   for (int t = tid; t < T; t += blockDim.x) H[size_t(t) * B + blockIdx.x] = s_h[t];
@@ -304,7 +305,9 @@ k_tile_scatter(int n, int T, int tiles_x, long long cap, const Header* __restric
   if (cnt > 0) {
     const unsigned int bit = 1u << (tid & 31);
     for (int y = r.y; y <= r.w; ++y)
-      for (int x = r.x; x <= r.z; ++x) atomicOr(&s_mask[(y * tiles_x + x) * 8 + (tid >> 5)], bit);
+      for (int x = r.x; x <= r.z; ++x)
+        if (check_ok(y * tiles_x + x < T, kCheckTile))
+          atomicOr(&s_mask[(y * tiles_x + x) * 8 + (tid >> 5)], bit);
   }
   const size_t B = gridDim.x;
   {
@@ -333,10 +336,12 @@ k_tile_scatter(int n, int T, int tiles_x, long long cap, const Header* __restric
     const int4 q = s_rect[lo];
     const int rw = q.z - q.x + 1;
     const int t = (q.y + k / rw) * tiles_x + q.x + k % rw;
+    if (!check_ok(t >= 0 && t < T, kCheckTile)) continue;
     const unsigned int* m = s_mask + t * 8;
     unsigned int rank = __popc(m[lo >> 5] & ((1u << (lo & 31)) - 1u));
     for (int j = 0; j < (lo >> 5); ++j) rank += __popc(m[j]);
     const long long dst = (long long)s_base[t] + rank;
+    if (!check_ok(dst >= 0 && dst < cap, kCheckPairSlot)) continue;
     sorted_gid[dst] = int(g0 + lo);
     keys_out[dst] = unsigned(t);
   }
@@ -529,8 +534,10 @@ k_radix_scatter(int pass, long long cap, long long partitions4, bool own_offsets
   for (int j = 0; j < kPerThread; ++j) {
     if (d[j] < 256u) {
       const unsigned int dst = s_base[d[j]] + s_whist[warp][d[j]] + rank[j];
-      keys_out[dst] = k[j];
-      vals_out[dst] = v[j];
+      if (check_ok((long long)dst < cap, kCheckPairSlot)) {
+        keys_out[dst] = k[j];
+        vals_out[dst] = v[j];
+      }
     }
   }
 }
@@ -563,13 +570,14 @@ k_radix_count(int pass, long long cap, long long partitions4, const Header* __re
 template <typename Key>
 __global__ void __launch_bounds__(256)
 k_tile_bounds(long long cap, const Header* __restrict__ hdr, const Key* __restrict__ keys,
-              int2* __restrict__ ranges, int tile_shift) {
+              int2* __restrict__ ranges, int tile_shift, int T) {
   pdl_enter();
   const long long n = usable_pairs(hdr, cap);
   int* rg = reinterpret_cast<int*>(ranges);
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const unsigned int t = unsigned(keys[i] >> tile_shift);
+    if (!check_ok(t < unsigned(T), kCheckTile)) continue;
     if (i == 0 || unsigned(keys[i - 1] >> tile_shift) != t) rg[2 * size_t(t)] = int(i);
     if (i == n - 1 || unsigned(keys[i + 1] >> tile_shift) != t) rg[2 * size_t(t) + 1] = int(i + 1);
   }
@@ -586,18 +594,21 @@ constexpr int kSegSmem = 4096;  // tile lists up to this long are depth-sorted i
 // comparators are skipped.  Lists longer than kSegSmem are sorted in place in
 // a workspace buffer.
 __global__ void __launch_bounds__(256)
-k_tile_depth_sort(long long cap, const Header* __restrict__ hdr, const int2* __restrict__ ranges,
-                  const float4* __restrict__ rec, int* __restrict__ sorted_gid,
-                  unsigned long long* __restrict__ temp) {
+k_tile_depth_sort(int n, long long cap, const Header* __restrict__ hdr,
+                  const int2* __restrict__ ranges, const float4* __restrict__ rec,
+                  int* __restrict__ sorted_gid, unsigned long long* __restrict__ temp) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned long long s_key[];  // kSegSmem
-  if (usable_pairs(hdr, cap) == 0) return;
+  const long long P = usable_pairs(hdr, cap);
+  if (P == 0) return;
   const int2 rg = ranges[blockIdx.x];
   const int len = rg.y - rg.x;
   if (len <= 1) return;
+  if (!check_ok(rg.x >= 0 && rg.y <= P, kCheckRange)) return;
   unsigned long long* key = len <= kSegSmem ? s_key : temp + rg.x;
   for (int k = threadIdx.x; k < len; k += blockDim.x) {
-    const int g = sorted_gid[rg.x + k];
+    int g = sorted_gid[rg.x + k];
+    if (!check_ok(g >= 0 && g < n, kCheckGaussian)) g = 0;
     key[k] = ((unsigned long long)depth_key(rec[3 * size_t(g) + 2].w) << 32) | unsigned(g);
   }
   __syncthreads();
@@ -677,7 +688,7 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
         const size_t dsmem = size_t(kSegSmem) * sizeof(unsigned long long);
         GS2D_TRY(cudaFuncSetAttribute(k_tile_depth_sort, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       int(dsmem)));
-        GS2D_TRY(launch(k_tile_depth_sort, dim3(T), dim3(256), dsmem, s, cap,
+        GS2D_TRY(launch(k_tile_depth_sort, dim3(T), dim3(256), dsmem, s, n, cap,
                         static_cast<const Header*>(hdr), rg, reinterpret_cast<const float4*>(rec),
                         sorted_gid, reinterpret_cast<unsigned long long*>(ws + L.keys_b)));
       }
@@ -709,7 +720,7 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
     if (tb > 148 * 16) tb = 148 * 16;
     GS2D_TRY(launch(k_tile_bounds<Key>, dim3(int(tb)), dim3(256), 0, s, cap, hdr, reinterpret_cast<const Key*>(ws + keys_final),
                                               reinterpret_cast<int2*>(tile_ranges),
-                                              kComposite ? 32 : 0));
+                                              kComposite ? 32 : 0, T));
   }
   return cudaGetLastError();
 }
@@ -724,4 +735,8 @@ cudaError_t launch_binning(const gs2d_config& c, int n, const gs2d_record* rec, 
   return launch_binning_t<false>(c, n, rec, rect, count, cap, tile_ranges, sorted_gid, ws, s);
 }
 
+}  // namespace gs2d
+
+namespace gs2d {
+GS2D_CHECK_WORD_READER(binning)
 }  // namespace gs2d

@@ -31,7 +31,8 @@ struct FusedCompSmem {
 
 template <bool kAbs>
 __global__ void __launch_bounds__(256)
-k_fused_comp(gs2d_config c, int tiles_x, float scale, const float4* __restrict__ rec,
+k_fused_comp(gs2d_config c, int tiles_x, int n, const Header* __restrict__ hdr, float scale,
+             const float4* __restrict__ rec,
              const int4* __restrict__ rect, const int2* __restrict__ ranges,
              const int* __restrict__ sorted_gid, const int* __restrict__ offsets,
              const float* __restrict__ bg, const float* __restrict__ target,
@@ -42,6 +43,7 @@ k_fused_comp(gs2d_config c, int tiles_x, float scale, const float4* __restrict__
   extern __shared__ __align__(16) unsigned char smem_raw[];
   FusedCompSmem<kAbs>& sm = *reinterpret_cast<FusedCompSmem<kAbs>*>(smem_raw);
   const int tile = order ? order[blockIdx.x] : int(blockIdx.x);  // longest lists first when known
+  if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile)) return;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bx0 = tx * kTile + (warp & 1) * 8;
@@ -50,10 +52,13 @@ k_fused_comp(gs2d_config c, int tiles_x, float scale, const float4* __restrict__
   const float pxf = float(px) + 0.5f, pyf = float(py) + 0.5f;
   const bool inside = px < c.width && py < c.height;
   const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
-  const int2 rg = ranges[tile];
+  const long long pairs = hdr->pairs;
+  int2 rg = ranges[tile];
+  if (!check_ok(rg.x >= 0 && rg.x <= rg.y && rg.y <= pairs, kCheckRange)) rg = make_int2(0, 0);
   // every thread has passed its last read of the forward's staging area when
   // comp_tile_forward returns (each round ends at a block barrier)
-  const CompFwdOut o = comp_tile_forward(sm.u.f, c, rg, bx0, by0, pxf, pyf, inside, kk, rec, sorted_gid);
+  const CompFwdOut o = comp_tile_forward(sm.u.f, c, rg, bx0, by0, pxf, pyf, inside, kk, n, rec,
+                                         sorted_gid);
   float er = 0.f, eg = 0.f, eb = 0.f;
   if (inside) {
     const size_t HW = size_t(c.width) * c.height;
@@ -76,8 +81,8 @@ k_fused_comp(gs2d_config c, int tiles_x, float scale, const float4* __restrict__
   const float tl = block_sum_ordered<8>(fmaf(eb, eb, fmaf(eg, eg, er * er)), sm.red);
   if (threadIdx.x == 0) loss_partials[tile] = tl;
   comp_tile_backward<kAbs>(sm.u.b, c, tile, tx, ty, rg, bx0, by0, pxf, pyf, inside, kk, o.T, o.last,
-                     er * scale, eg * scale, eb * scale, bg, rec, rect, sorted_gid, offsets, partials,
-                     tile_partials);
+                           er * scale, eg * scale, eb * scale, n, pairs, bg, rec, rect, sorted_gid,
+                           offsets, partials, tile_partials);
 }
 
 }  // namespace
@@ -102,7 +107,8 @@ cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* cho
     auto go = [&](auto kern, size_t smem) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
       if (e != cudaSuccess) return e;
-      return launch(kern, dim3(T), dim3(256), smem, s, c, tiles_x(c), scale, r, rc, rg, sorted_gid,
+      return launch(kern, dim3(T), dim3(256), smem, s, c, tiles_x(c), n,
+                    reinterpret_cast<const Header*>(ws), scale, r, rc, rg, sorted_gid,
                     offsets, bg, target, image, reinterpret_cast<float4*>(ws + L.partials), tp, lp,
                     L.count_sort ? reinterpret_cast<const int*>(ws + L.tile_order) : nullptr);
     };
@@ -117,10 +123,12 @@ cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* cho
   int blocks = 0;
   // the counting sort leaves a longest-first launch order of the tiles
   const int* order = L.count_sort ? reinterpret_cast<const int*>(ws + L.tile_order) : nullptr;
-  GS2D_TRY(launch_render_fwd_loss(c, rec, ranges, sorted_gid, target, scale, image, d_image, lp, &blocks,
+  GS2D_TRY(launch_render_fwd_loss(c, n, rec, ranges, sorted_gid, target, scale, image, d_image, lp, &blocks,
                                   order, s));
   return launch_render_bwd(c, n, chol, rec, rect, ranges, sorted_gid, nullptr, nullptr, nullptr, d_image,
                            d_xy, d_chol, d_rgb, nullptr, nullptr, d_xy_abs, ws, s, loss, blocks);
 }
+
+GS2D_CHECK_WORD_READER(fused)
 
 }  // namespace gs2d

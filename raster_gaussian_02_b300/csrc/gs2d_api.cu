@@ -96,7 +96,7 @@ gs2d_status gs2d_render_fwd(const gs2d_config* cfg, int32_t n, const gs2d_record
   if ((t_final && !aligned(t_final, 4)) || (last && !aligned(last, 4)) ||
       (background && !aligned(background, 4)))
     return GS2D_ERR_INVALID_ARG;
-  return from_cuda(launch_render_fwd(*cfg, rec, tile_ranges, sorted_gid, background, image, t_final,
+  return from_cuda(launch_render_fwd(*cfg, n, rec, tile_ranges, sorted_gid, background, image, t_final,
                                      last, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -229,8 +229,30 @@ const char* gs2d_status_string(gs2d_status status) {
     case GS2D_ERR_CUDA: return "CUDA error";
     case GS2D_ERR_TIMEOUT: return "device wait timed out";
     case GS2D_ERR_OVERFLOW: return "pair count overflow";
+    case GS2D_ERR_UNSUPPORTED: return "not supported by this build";
   }
   return "unknown status";
+}
+
+gs2d_status gs2d_debug_check_word(uint32_t* word, int32_t clear) {
+  if (!word) return GS2D_ERR_INVALID_ARG;
+  *word = 0;
+#ifdef GS2D_CHECKS
+  cudaError_t (*const readers[])(unsigned int*, bool) = {
+      gs2d::check_word_project, gs2d::check_word_binning, gs2d::check_word_raster_fwd,
+      gs2d::check_word_raster_bwd, gs2d::check_word_fused, gs2d::check_word_merge};
+  unsigned int all = 0;
+  for (auto read : readers) {
+    unsigned int w = 0;
+    if (read(&w, clear != 0) != cudaSuccess) return GS2D_ERR_CUDA;
+    all |= w;
+  }
+  *word = all;
+  return GS2D_OK;
+#else
+  (void)clear;
+  return GS2D_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // extern "C"

@@ -211,6 +211,47 @@ __device__ __forceinline__ void sincos_fp32(float th, float* sn, float* cs) {
   }
 }
 
+// ------------------------------------------------------- checked build --
+// Built with -DGS2D_CHECKS (libgs2d_checked.so), every index that comes from
+// data -- a list entry, an offset, a tile id, a destination slot -- is tested
+// before the access it guards.  A failed test sets bit `site` of its
+// translation unit's check word and the access is skipped: nothing traps, and
+// gs2d_debug_check_word() reads the bits back.  The normal build compiles the
+// tests away.  Sites:
+enum CheckSite {
+  kCheckTile = 1,      // tile id outside [0, T)
+  kCheckPairSlot = 2,  // pair destination outside [0, capacity)
+  kCheckRange = 3,     // a tile's list range outside [0, pairs]
+  kCheckGaussian = 4,  // Gaussian index outside [0, n)
+  kCheckPartial = 5,   // partial-gradient slot outside [0, pairs)
+  kCheckMerge = 6,     // merge index outside [0, n)
+  kCheckShared = 7,    // shared-memory index outside its array
+};
+#ifdef GS2D_CHECKS
+static __device__ unsigned int g_check_word;
+__device__ __forceinline__ bool check_ok(bool cond, int site) {
+  if (!cond) atomicOr(&g_check_word, 1u << site);
+  return cond;
+}
+// Defines check_word_<name>(): reads (and with clear, zeroes) this
+// translation unit's check word.
+#define GS2D_CHECK_WORD_READER(name)                                                   \
+  cudaError_t check_word_##name(unsigned int* out, bool clear) {                      \
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_check_word, sizeof(unsigned int));    \
+    if (e == cudaSuccess && clear) {                                                   \
+      const unsigned int zero = 0u;                                                    \
+      e = cudaMemcpyToSymbol(g_check_word, &zero, sizeof(unsigned int));              \
+    }                                                                                  \
+    return e;                                                                          \
+  }
+#else
+__device__ __forceinline__ bool check_ok(bool cond, int) {
+  (void)cond;
+  return true;
+}
+#define GS2D_CHECK_WORD_READER(name)
+#endif
+
 // Monotone map of a finite float to uint32 (IEEE order, -0 mapped as +0).
 __device__ __forceinline__ unsigned int depth_key(float d) {
   unsigned int u = __float_as_uint(d);
@@ -270,7 +311,7 @@ cudaError_t launch_binning(const gs2d_config& c, int n, const gs2d_record* rec, 
                            const int* count, long long cap, int* tile_ranges, int* sorted_gid,
                            unsigned char* ws, cudaStream_t s);
 
-cudaError_t launch_render_fwd(const gs2d_config& c, const gs2d_record* rec, const int* ranges,
+cudaError_t launch_render_fwd(const gs2d_config& c, int n, const gs2d_record* rec, const int* ranges,
                               const int* sorted_gid, const float* bg, float* image, float* t_final,
                               int* last, cudaStream_t s);
 
@@ -296,7 +337,7 @@ cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
 // dL/dC = scale (C - target) to d_image and one loss partial per block to
 // loss_partials; returns the number of blocks in *blocks.  order (may be
 // NULL): the tiles in the order their blocks are launched.
-cudaError_t launch_render_fwd_loss(const gs2d_config& c, const gs2d_record* rec, const int* ranges,
+cudaError_t launch_render_fwd_loss(const gs2d_config& c, int n, const gs2d_record* rec, const int* ranges,
                                    const int* sorted_gid, const float* target, float scale,
                                    float* image, float* d_image, float* loss_partials, int* blocks,
                                    const int* order, cudaStream_t s);
@@ -316,6 +357,15 @@ struct MergeHeader {
   int merges;       // pairs merged
   unsigned int done_a, done_b;
 };
+
+#ifdef GS2D_CHECKS
+cudaError_t check_word_project(unsigned int* out, bool clear);
+cudaError_t check_word_binning(unsigned int* out, bool clear);
+cudaError_t check_word_raster_fwd(unsigned int* out, bool clear);
+cudaError_t check_word_raster_bwd(unsigned int* out, bool clear);
+cudaError_t check_word_fused(unsigned int* out, bool clear);
+cudaError_t check_word_merge(unsigned int* out, bool clear);
+#endif
 
 size_t merge_workspace_size(long long n);
 

@@ -136,17 +136,19 @@ __device__ __forceinline__ float merge_cost(float4 a, float ayy, float4 b, float
 // listed in its mean's tile: its box holds the pixel nearest its mean), and
 // finds its least-cost candidate over the whole list, staged 256 at a time.
 __global__ void __launch_bounds__(kMergeThreads)
-k_merge_nn(const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
+k_merge_nn(int n, const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
            const float4* __restrict__ mrec, const float* __restrict__ msyy,
            const int* __restrict__ mtile, int* __restrict__ nn, float* __restrict__ cost) {
   __shared__ float4 s_rec[kMergeThreads];
   __shared__ float s_syy[kMergeThreads];
   __shared__ int s_gid[kMergeThreads];
   const int t = blockIdx.x, tid = threadIdx.x;
-  const int2 rg = ranges[t];
+  int2 rg = ranges[t];
+  if (!check_ok(rg.x >= 0 && rg.x <= rg.y, kCheckRange)) rg = make_int2(0, 0);
   for (int mc = rg.x; mc < rg.y; mc += kMergeThreads) {
     const int k = mc + tid;
-    const int g = k < rg.y ? sorted_gid[k] : -1;
+    int g = k < rg.y ? sorted_gid[k] : -1;
+    if (g >= 0 && !check_ok(g < n, kCheckMerge)) g = -1;
     const bool member = g >= 0 && mtile[g] == t;
     float4 me = make_float4(0.f, 0.f, 0.f, 0.f);
     float myy = 0.f;
@@ -160,7 +162,8 @@ k_merge_nn(const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
       const int cnt = min(kMergeThreads, rg.y - cc);
       __syncthreads();  // the previous chunk is no longer read
       if (tid < cnt) {
-        const int j = sorted_gid[cc + tid];
+        int j = sorted_gid[cc + tid];
+        if (!check_ok(j >= 0 && j < n, kCheckMerge)) j = 0;
         s_rec[tid] = mrec[j];
         s_syy[tid] = msyy[j];
         s_gid[tid] = j;
@@ -193,7 +196,7 @@ k_merge_pairs(int n, const int* __restrict__ nn, const float* __restrict__ cost,
   if (i >= n) return;
   const int j = nn[i];
   unsigned int k = kKeyBins;
-  if (j > i && nn[j] == i) {
+  if (j > i && check_ok(j < n, kCheckMerge) && nn[j] == i) {
     k = __float_as_uint(cost[i]) >> 16;
     atomicAdd(&hist[k], 1u);
   }
@@ -322,7 +325,7 @@ k_merge_take(int n, const MergeHeader* __restrict__ hdr, const unsigned int* __r
   const unsigned int b = unsigned(hdr->boundary);
   const bool t = k < unsigned(kKeyBins) && (k < b || (k == b && rank < hdr->need));
   take[i] = t ? 1 : 0;
-  if (t) drop[nn[i]] = 1;  // pairs are disjoint: every partner is dropped once
+  if (t && check_ok(nn[i] >= 0 && nn[i] < n, kCheckMerge)) drop[nn[i]] = 1;  // pairs are disjoint: every partner is dropped once
 }
 
 // Sigma in double from the shape, in the order the merged values use it.
@@ -353,7 +356,7 @@ k_merge_write(int n, int param, const float* __restrict__ xy, const float* __res
   int total;
   const int keep = (i < n && !drop[i]) ? 1 : 0;
   const int o = block_off[blockIdx.x] + block_excl_scan_int(keep, &total);
-  if (!keep) return;
+  if (!keep || !check_ok(o >= 0 && o < n, kCheckMerge)) return;
   if (!take[i]) {
     out_xy[2 * o] = xy[2 * i];
     out_xy[2 * o + 1] = xy[2 * i + 1];
@@ -364,6 +367,7 @@ k_merge_write(int n, int param, const float* __restrict__ xy, const float* __res
     return;
   }
   const int j = nn[i];
+  if (!check_ok(j >= 0 && j < n, kCheckMerge)) return;
   double Si[3], Sj[3];
   sigma_double(param, shape + 3 * i, Si);
   sigma_double(param, shape + 3 * j, Sj);
@@ -436,7 +440,7 @@ cudaError_t launch_merge(const gs2d_config& c, int n, const float* xy, const flo
   const dim3 g(blocks), b(kMergeThreads);
   GS2D_TRY(launch(k_merge_prep, g, b, 0, s, c, n, tiles_x(c), xy, shape,
                   reinterpret_cast<const float4*>(rec), count, mrec, msyy, mtile, nn, cost));
-  GS2D_TRY(launch(k_merge_nn, dim3(num_tiles(c)), b, 0, s, reinterpret_cast<const int2*>(ranges),
+  GS2D_TRY(launch(k_merge_nn, dim3(num_tiles(c)), b, 0, s, n, reinterpret_cast<const int2*>(ranges),
                   sorted_gid, static_cast<const float4*>(mrec), static_cast<const float*>(msyy),
                   static_cast<const int*>(mtile), nn, cost));
   GS2D_TRY(launch(k_merge_pairs, g, b, 0, s, n, static_cast<const int*>(nn),
@@ -458,5 +462,7 @@ cudaError_t launch_merge(const gs2d_config& c, int n, const float* xy, const flo
     GS2D_TRY(cudaMemcpyAsync(merges_dev, &hdr->merges, sizeof(int), cudaMemcpyDeviceToDevice, s));
   return cudaGetLastError();
 }
+
+GS2D_CHECK_WORD_READER(merge)
 
 }  // namespace gs2d

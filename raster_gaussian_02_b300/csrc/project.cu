@@ -142,9 +142,10 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
     const int cnt = (rc.z >= rc.x) ? (rc.z - rc.x + 1) * (rc.w - rc.y + 1) : 0;
     float s[9] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float ax = 0.f, ay = 0.f;
-    if (!bad && cnt > 0) {
+    const int off = (!bad && cnt > 0) ? offsets[i] : 0;
+    if (!bad && cnt > 0 && check_ok(off >= 0 && off + (long long)cnt <= hdr->pairs, kCheckPartial)) {
       constexpr int kStride = (kComposite || kAbs) ? 3 : 2;
-      const float4* p = partials + size_t(offsets[i]) * kStride;
+      const float4* p = partials + size_t(off) * kStride;
       for (int k = 0; k < cnt; ++k, p += kStride) {
         const float4 u = p[0], v = p[1];
         s[0] += u.x; s[1] += u.y; s[2] += u.z; s[3] += u.w;
@@ -283,5 +284,7 @@ cudaError_t launch_gather(const gs2d_config& c, int n, const float* chol, const 
     GS2D_TRY(d_xy_abs ? go(k_gather<false, true>) : go(k_gather<false, false>));
   return cudaGetLastError();
 }
+
+GS2D_CHECK_WORD_READER(project)
 
 }  // namespace gs2d

@@ -62,7 +62,7 @@ __device__ __forceinline__ int block_inclusive_count_256(int flag, int* total, i
 // share of dL/dmu in absolute value), in a third float4 of the pair's slot.
 template <bool kAbs>
 __global__ void __launch_bounds__(kChunkPairs, 4)  // 4 per SM: measured best (5 or 6 spill and lose)
-k_render_bwd_sum(gs2d_config c, int tiles_x, const Header* __restrict__ hdr,
+k_render_bwd_sum(gs2d_config c, int tiles_x, int n_gauss, const Header* __restrict__ hdr,
                  const unsigned char* __restrict__ ws, const float4* __restrict__ rec,
                  const int4* __restrict__ rect, const int* __restrict__ sorted_gid,
                  const int* __restrict__ offsets, const float* __restrict__ d_image,
@@ -80,7 +80,9 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, const Header* __restrict__ hdr,
        k0 += (long long)gridDim.x * kChunkPairs) {
     const long long k = k0 + tid;
     const bool valid = k < n;
-    const int tile = valid ? int(keys[k]) : -1;
+    int tile = valid ? int(keys[k]) : -1;
+    if (valid && !check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile))
+      tile = 0;
     const int prev = (valid && tid > 0) ? int(keys[k - 1]) : -2;
     int ntiles;
     const int slot = block_inclusive_count_256(valid && tile != prev, &ntiles, warp_tot) - 1;
@@ -89,6 +91,7 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, const Header* __restrict__ hdr,
     int key = 255;  // sort key: boxes of the same shape (h, w) side by side, largest first
     if (valid) {
       gid = sorted_gid[k];
+      if (!check_ok(gid >= 0 && gid < n_gauss, kCheckGaussian)) gid = 0;
       const float4* r = rec + 3 * size_t(gid);
       const float4 p0 = r[0], p1 = r[1], p2 = r[2];
       sm.rec[tid][0] = p0;
@@ -200,10 +203,12 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, const Header* __restrict__ hdr,
         const int gid_me = sm.gid[me];
         const int4 rc = rect[gid_me];
         const int pslot = offsets[gid_me] + (ty - rc.y) * (rc.z - rc.x + 1) + (tx - rc.x);
-        float4* out = partials + (kAbs ? 3 : 2) * size_t(pslot);
-        out[0] = make_float4(fmaf(A, Sx, B * Sy), fmaf(B, Sx, C * Sy), -0.5f * Sxx, -Sxy);
-        out[1] = make_float4(-0.5f * Syy, sr, sg, sb);
-        if constexpr (kAbs) out[2] = make_float4(0.f, ax, ay, 0.f);
+        if (check_ok(pslot >= 0 && pslot < n, kCheckPartial)) {
+          float4* out = partials + (kAbs ? 3 : 2) * size_t(pslot);
+          out[0] = make_float4(fmaf(A, Sx, B * Sy), fmaf(B, Sx, C * Sy), -0.5f * Sxx, -Sxy);
+          out[1] = make_float4(-0.5f * Syy, sr, sg, sb);
+          if constexpr (kAbs) out[2] = make_float4(0.f, ax, ay, 0.f);
+        }
       }
       __syncthreads();
     }
@@ -217,7 +222,8 @@ constexpr int kBwdCompThreads = 256;
 // pixel's last contributor (comp_tile_backward).
 template <bool kAbs>
 __global__ void __launch_bounds__(kBwdCompThreads)
-k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
+k_render_bwd_comp(gs2d_config c, int tiles_x, int n, const Header* __restrict__ hdr,
+                  const float4* __restrict__ rec,
                   const int4* __restrict__ rect, const int2* __restrict__ ranges,
                   const int* __restrict__ sorted_gid, const int* __restrict__ offsets,
                   const float* __restrict__ bg, const float* __restrict__ t_final,
@@ -228,6 +234,10 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
   extern __shared__ __align__(16) unsigned char smem_raw[];
   CompStage<kAbs>& sm = *reinterpret_cast<CompStage<kAbs>*>(smem_raw);
   const int tile = order ? order[blockIdx.x] : int(blockIdx.x);  // longest lists first when known
+  if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile)) return;
+  const long long pairs = hdr->pairs;
+  int2 rg = ranges[tile];
+  if (!check_ok(rg.x >= 0 && rg.x <= rg.y && rg.y <= pairs, kCheckRange)) rg = make_int2(0, 0);
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bx0 = tx * kTile + (warp & 1) * 8;
@@ -246,8 +256,8 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
     gg = d_image[HW + p];
     gb = d_image[2 * HW + p];
   }
-  comp_tile_backward<kAbs>(sm, c, tile, tx, ty, ranges[tile], bx0, by0, float(px) + 0.5f,
-                           float(py) + 0.5f, inside, kk, T, lst, gr, gg, gb, bg, rec, rect, sorted_gid,
+  comp_tile_backward<kAbs>(sm, c, tile, tx, ty, rg, bx0, by0, float(px) + 0.5f, float(py) + 0.5f,
+                           inside, kk, T, lst, gr, gg, gb, n, pairs, bg, rec, rect, sorted_gid,
                            offsets, partials, tile_partials);
 }
 
@@ -256,7 +266,7 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
 namespace {
 
 template <bool kAbs>
-cudaError_t launch_bwd_pairs(const gs2d_config& c, const Layout& L, const float4* r, const int4* rc,
+cudaError_t launch_bwd_pairs(const gs2d_config& c, int n, const Layout& L, const float4* r, const int4* rc,
                              const int2* rg, const int* sorted_gid, const float* bg,
                              const float* t_final, const int* last, const float* d_image,
                              unsigned char* ws, cudaStream_t s) {
@@ -267,15 +277,15 @@ cudaError_t launch_bwd_pairs(const gs2d_config& c, const Layout& L, const float4
     const size_t smem = sizeof(CompStage<kAbs>);
     auto kern = k_render_bwd_comp<kAbs>;
     GS2D_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-    GS2D_TRY(launch(kern, dim3(T), dim3(kBwdCompThreads), smem, s, c, tiles_x(c), r, rc, rg, sorted_gid,
-                    offsets, bg, t_final, last, d_image, partials,
+    GS2D_TRY(launch(kern, dim3(T), dim3(kBwdCompThreads), smem, s, c, tiles_x(c), n,
+                    reinterpret_cast<const Header*>(ws), r, rc, rg, sorted_gid, offsets, bg, t_final, last, d_image, partials,
                     reinterpret_cast<float4*>(ws + L.tile_partials),
                     L.count_sort ? reinterpret_cast<const int*>(ws + L.tile_order) : nullptr));
   } else {
     const size_t smem = sizeof(BwdSumSmem);
     auto kern = k_render_bwd_sum<kAbs>;
     GS2D_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-    GS2D_TRY(launch(kern, dim3(4 * sm_count()), dim3(kChunkPairs), smem, s, c, tiles_x(c),
+    GS2D_TRY(launch(kern, dim3(4 * sm_count()), dim3(kChunkPairs), smem, s, c, tiles_x(c), n,
                     reinterpret_cast<const Header*>(ws), static_cast<const unsigned char*>(ws), r, rc,
                     sorted_gid, offsets, d_image, partials));
   }
@@ -295,11 +305,13 @@ cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
   const int4* rc = reinterpret_cast<const int4*>(rect);
   const int2* rg = reinterpret_cast<const int2*>(ranges);
   if (d_xy_abs)
-    GS2D_TRY(launch_bwd_pairs<true>(c, L, r, rc, rg, sorted_gid, bg, t_final, last, d_image, ws, s));
+    GS2D_TRY(launch_bwd_pairs<true>(c, n, L, r, rc, rg, sorted_gid, bg, t_final, last, d_image, ws, s));
   else
-    GS2D_TRY(launch_bwd_pairs<false>(c, L, r, rc, rg, sorted_gid, bg, t_final, last, d_image, ws, s));
+    GS2D_TRY(launch_bwd_pairs<false>(c, n, L, r, rc, rg, sorted_gid, bg, t_final, last, d_image, ws, s));
   return launch_gather(c, n, chol, rec, rect, ws, d_xy, d_chol, d_rgb, d_opacity, d_bg, d_xy_abs,
                        loss, loss_blocks, s);
 }
+
+GS2D_CHECK_WORD_READER(raster_bwd)
 
 }  // namespace gs2d

@@ -24,7 +24,7 @@ namespace {
 // is then optional (NULL: not written).
 template <int kWarps, bool kLoss>
 __global__ void __launch_bounds__(kWarps * 32, kWarps == 8 ? 8 : 10)
-k_render_fwd_sum(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
+k_render_fwd_sum(gs2d_config c, int tiles_x, int n, const float4* __restrict__ rec,
                  const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
                  float* __restrict__ image, const float* __restrict__ target, float scale,
                  float* __restrict__ d_image, float* __restrict__ loss_partials,
@@ -34,6 +34,7 @@ k_render_fwd_sum(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SumSmem<kWarps>& sm = *reinterpret_cast<SumSmem<kWarps>*>(smem_raw);
   const int tile = order ? order[blockIdx.x / kParts] : int(blockIdx.x / kParts);
+  if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile)) return;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = (blockIdx.x % kParts) * kWarps + warp;  // 8x4 sub-block 0..7 of the tile
@@ -41,8 +42,10 @@ k_render_fwd_sum(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
   const int by0 = ty * kTile + (sub >> 1) * 4;
   const int px = bx0 + (lane & 7), py = by0 + (lane >> 3);
   const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
-  const float3 a = sum_tile_forward<kWarps>(sm, ranges[tile], bx0, by0, float(px) + 0.5f,
-                                            float(py) + 0.5f, kk, rec, sorted_gid);
+  int2 rg = ranges[tile];
+  if (!check_ok(rg.x >= 0 && rg.x <= rg.y, kCheckRange)) rg = make_int2(0, 0);
+  const float3 a = sum_tile_forward<kWarps>(sm, rg, bx0, by0, float(px) + 0.5f, float(py) + 0.5f, kk,
+                                            n, rec, sorted_gid);
   const bool inside = px < c.width && py < c.height;
   const size_t HW = size_t(c.width) * c.height;
   const size_t p = size_t(py) * c.width + px;
@@ -68,7 +71,7 @@ k_render_fwd_sum(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
 }
 
 __global__ void __launch_bounds__(256)
-k_render_fwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
+k_render_fwd_comp(gs2d_config c, int tiles_x, int n, const float4* __restrict__ rec,
                   const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
                   const float* __restrict__ bg, float* __restrict__ image,
                   float* __restrict__ t_final, int* __restrict__ last) {
@@ -82,8 +85,10 @@ k_render_fwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
   const int px = bx0 + (lane & 7), py = by0 + (lane >> 3);
   const bool inside = px < c.width && py < c.height;
   const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
-  const CompFwdOut o = comp_tile_forward(sm, c, ranges[tile], bx0, by0, float(px) + 0.5f,
-                                         float(py) + 0.5f, inside, kk, rec, sorted_gid);
+  int2 rg = ranges[tile];
+  if (!check_ok(rg.x >= 0 && rg.x <= rg.y, kCheckRange)) rg = make_int2(0, 0);
+  const CompFwdOut o = comp_tile_forward(sm, c, rg, bx0, by0, float(px) + 0.5f, float(py) + 0.5f,
+                                         inside, kk, n, rec, sorted_gid);
   if (inside) {
     const size_t HW = size_t(c.width) * c.height;
     const size_t p = size_t(py) * c.width + px;
@@ -102,14 +107,14 @@ k_render_fwd_comp(gs2d_config c, int tiles_x, const float4* __restrict__ rec,
 }
 
 template <int kWarps, bool kLoss>
-cudaError_t launch_fwd_sum(const gs2d_config& c, const float4* r, const int2* rg, const int* sorted_gid,
+cudaError_t launch_fwd_sum(const gs2d_config& c, int n, const float4* r, const int2* rg, const int* sorted_gid,
                            float* image, const float* target, float scale, float* d_image,
                            float* loss_partials, const int* order, cudaStream_t s) {
   const size_t smem = sizeof(SumSmem<kWarps>);
   auto kern = k_render_fwd_sum<kWarps, kLoss>;
   GS2D_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-  GS2D_TRY(launch(kern, dim3(num_tiles(c) * (8 / kWarps)), dim3(kWarps * 32), smem, s, c, tiles_x(c), r,
-                  rg, sorted_gid, image, target, scale, d_image, loss_partials, order));
+  GS2D_TRY(launch(kern, dim3(num_tiles(c) * (8 / kWarps)), dim3(kWarps * 32), smem, s, c, tiles_x(c), n,
+                  r, rg, sorted_gid, image, target, scale, d_image, loss_partials, order));
   return cudaSuccess;
 }
 
@@ -122,26 +127,26 @@ bool half_tile_blocks(int T) { return T <= 2 * 8 * sm_count(); }
 
 }  // namespace
 
-cudaError_t launch_render_fwd(const gs2d_config& c, const gs2d_record* rec, const int* ranges,
+cudaError_t launch_render_fwd(const gs2d_config& c, int n, const gs2d_record* rec, const int* ranges,
                               const int* sorted_gid, const float* bg, float* image, float* t_final,
                               int* last, cudaStream_t s) {
   const int T = num_tiles(c);
   const float4* r = reinterpret_cast<const float4*>(rec);
   const int2* rg = reinterpret_cast<const int2*>(ranges);
   if (c.mode == GS2D_MODE_COMPOSITE) {
-    GS2D_TRY(launch(k_render_fwd_comp, dim3(T), dim3(256), 0, s, c, tiles_x(c), r, rg, sorted_gid, bg, image, t_final, last));
+    GS2D_TRY(launch(k_render_fwd_comp, dim3(T), dim3(256), 0, s, c, tiles_x(c), n, r, rg, sorted_gid, bg, image, t_final, last));
   } else {
     if (half_tile_blocks(T))
-      GS2D_TRY((launch_fwd_sum<4, false>(c, r, rg, sorted_gid, image, nullptr, 0.f, nullptr, nullptr,
+      GS2D_TRY((launch_fwd_sum<4, false>(c, n, r, rg, sorted_gid, image, nullptr, 0.f, nullptr, nullptr,
                                          nullptr, s)));
     else
-      GS2D_TRY((launch_fwd_sum<8, false>(c, r, rg, sorted_gid, image, nullptr, 0.f, nullptr, nullptr,
+      GS2D_TRY((launch_fwd_sum<8, false>(c, n, r, rg, sorted_gid, image, nullptr, 0.f, nullptr, nullptr,
                                          nullptr, s)));
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_render_fwd_loss(const gs2d_config& c, const gs2d_record* rec, const int* ranges,
+cudaError_t launch_render_fwd_loss(const gs2d_config& c, int n, const gs2d_record* rec, const int* ranges,
                                    const int* sorted_gid, const float* target, float scale,
                                    float* image, float* d_image, float* loss_partials, int* blocks,
                                    const int* order, cudaStream_t s) {
@@ -150,14 +155,16 @@ cudaError_t launch_render_fwd_loss(const gs2d_config& c, const gs2d_record* rec,
   const int2* rg = reinterpret_cast<const int2*>(ranges);
   if (half_tile_blocks(T)) {
     *blocks = 2 * T;
-    GS2D_TRY((launch_fwd_sum<4, true>(c, r, rg, sorted_gid, image, target, scale, d_image, loss_partials,
+    GS2D_TRY((launch_fwd_sum<4, true>(c, n, r, rg, sorted_gid, image, target, scale, d_image, loss_partials,
                                       order, s)));
   } else {
     *blocks = T;
-    GS2D_TRY((launch_fwd_sum<8, true>(c, r, rg, sorted_gid, image, target, scale, d_image, loss_partials,
+    GS2D_TRY((launch_fwd_sum<8, true>(c, n, r, rg, sorted_gid, image, target, scale, d_image, loss_partials,
                                       order, s)));
   }
   return cudaGetLastError();
 }
+
+GS2D_CHECK_WORD_READER(raster_fwd)
 
 }  // namespace gs2d

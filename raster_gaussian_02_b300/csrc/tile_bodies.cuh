@@ -32,11 +32,13 @@ struct SumSmem {
 
 // Loads records sorted_gid[rb .. rb + cnt) into the staging area (cnt <= 256).
 template <typename Smem>
-__device__ __forceinline__ void stage_records(Smem& sm, int rb, int cnt, int tid, int nthreads,
+__device__ __forceinline__ void stage_records(Smem& sm, int rb, int cnt, int tid, int nthreads, int n,
                                               const float4* __restrict__ rec,
                                               const int* __restrict__ sorted_gid) {
   for (int k = tid; k < cnt; k += nthreads) {
-    const float4* r = rec + 3 * size_t(sorted_gid[rb + k]);
+    int g = sorted_gid[rb + k];
+    if (!check_ok(g >= 0 && g < n, kCheckGaussian)) g = 0;
+    const float4* r = rec + 3 * size_t(g);
     const float4 p0 = r[0], p1 = r[1], p2 = r[2];
     sm.g[k].mc = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
     sm.g[k].cr = p1;
@@ -52,7 +54,7 @@ __device__ __forceinline__ void stage_records(Smem& sm, int rb, int cnt, int tid
 // block must call it.
 template <int kWarps>
 __device__ __forceinline__ float3 sum_tile_forward(SumSmem<kWarps>& sm, int2 rg, int bx0, int by0,
-                                                   float pxf, float pyf, float kk,
+                                                   float pxf, float pyf, float kk, int n,
                                                    const float4* __restrict__ rec,
                                                    const int* __restrict__ sorted_gid) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -62,7 +64,7 @@ __device__ __forceinline__ float3 sum_tile_forward(SumSmem<kWarps>& sm, int2 rg,
   for (int rb = rg.x; rb < rg.y; rb += 256) {
     const int cnt = min(256, rg.y - rb);
     if (rb != rg.x) __syncthreads();  // the previous round is no longer read
-    stage_records(sm, rb, cnt, tid, kWarps * 32, rec, sorted_gid);
+    stage_records(sm, rb, cnt, tid, kWarps * 32, n, rec, sorted_gid);
     __syncthreads();
     for (int wb = 0; wb < cnt; wb += kWindow) {
       const int wend = min(wb + kWindow, cnt);
@@ -130,7 +132,7 @@ struct CompFwdOut {
 // The caller adds T * background.  Every thread of the block must call it.
 __device__ __forceinline__ CompFwdOut comp_tile_forward(CompSmem& sm, const gs2d_config& c, int2 rg,
                                                         int bx0, int by0, float pxf, float pyf,
-                                                        bool inside, float kk,
+                                                        bool inside, float kk, int n,
                                                         const float4* __restrict__ rec,
                                                         const int* __restrict__ sorted_gid) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -143,7 +145,9 @@ __device__ __forceinline__ CompFwdOut comp_tile_forward(CompSmem& sm, const gs2d
     if (__syncthreads_and(done)) break;
     const int cnt = min(256, rg.y - rb);
     if (tid < cnt) {
-      const float4* r = rec + 3 * size_t(sorted_gid[rb + tid]);
+      int g = sorted_gid[rb + tid];
+      if (!check_ok(g >= 0 && g < n, kCheckGaussian)) g = 0;
+      const float4* r = rec + 3 * size_t(g);
       const float4 p0 = r[0], p1 = r[1], p2 = r[2];
       sm.g[tid].mc = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
       sm.g[tid].cr = p1;
@@ -267,7 +271,7 @@ template <bool kAbs>
 __device__ __forceinline__ void comp_tile_backward(
     CompStage<kAbs>& sm, const gs2d_config& c, int tile, int tx, int ty, int2 rg, int bx0, int by0,
     float pxf, float pyf, bool inside, float kk, float T, int lst, float gr, float gg, float gb,
-    const float* __restrict__ bg, const float4* __restrict__ rec,
+    int n, long long pairs, const float* __restrict__ bg, const float4* __restrict__ rec,
     const int4* __restrict__ rect, const int* __restrict__ sorted_gid,
     const int* __restrict__ offsets, float4* __restrict__ partials,
     float4* __restrict__ tile_partials) {
@@ -303,7 +307,8 @@ __device__ __forceinline__ void comp_tile_backward(
     const int cb = rg.x + ci * kCompChunk;
     const int cnt = min(kCompChunk, rg.y - cb);
     if (tid < cnt) {
-      const int gid = sorted_gid[cb + tid];
+      int gid = sorted_gid[cb + tid];
+      if (!check_ok(gid >= 0 && gid < n, kCheckGaussian)) gid = 0;
       const float4* r = rec + 3 * size_t(gid);
       const float4 p0 = r[0], p1 = r[1], p2 = r[2];
       sm.mc[tid] = make_float4(p0.x, p0.y, p0.z, 2.0f * p0.w);
@@ -401,16 +406,18 @@ __device__ __forceinline__ void comp_tile_backward(
       const float A = sm.mc[tid].z, B = 0.5f * sm.mc[tid].w, C = sm.cr[tid].x;
       const int4 rc = rect[gid];
       const int slot = offsets[gid] + (ty - rc.y) * (rc.z - rc.x + 1) + (tx - rc.x);
-      float4* out = partials + 3 * size_t(slot);
       float ax = 0.f, ay = 0.f;
       if constexpr (kAbs)
         for (int w = 0; w < 8; ++w) {
           ax += sm.acc_abs[w][tid][0];
           ay += sm.acc_abs[w][tid][1];
         }
-      out[0] = make_float4(fmaf(A, s[0], B * s[1]), fmaf(B, s[0], C * s[1]), -0.5f * s[2], -s[3]);
-      out[1] = make_float4(-0.5f * s[4], s[5], s[6], s[7]);
-      out[2] = make_float4(s[8], ax, ay, 0.f);
+      if (check_ok(slot >= 0 && slot < pairs, kCheckPartial)) {
+        float4* out = partials + 3 * size_t(slot);
+        out[0] = make_float4(fmaf(A, s[0], B * s[1]), fmaf(B, s[0], C * s[1]), -0.5f * s[2], -s[3]);
+        out[1] = make_float4(-0.5f * s[4], s[5], s[6], s[7]);
+        out[2] = make_float4(s[8], ax, ay, 0.f);
+      }
     }
     __syncthreads();
   }

@@ -17,9 +17,13 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libgs2d.so")
+# GS2D_CHECKED=1 loads the bounds-checked build instead (same ABI; see
+# gs2d_debug_check_word), for debugging and the checked-build tests.
+CHECKED = os.environ.get("GS2D_CHECKED", "0") == "1"
+LIB_PATH = os.path.join(_HERE, "libgs2d_checked.so" if CHECKED else "libgs2d.so")
 
-GS2D_OK, GS2D_ERR_INVALID_ARG, GS2D_ERR_CAPACITY, GS2D_ERR_CUDA, GS2D_ERR_TIMEOUT, GS2D_ERR_OVERFLOW = range(6)
+(GS2D_OK, GS2D_ERR_INVALID_ARG, GS2D_ERR_CAPACITY, GS2D_ERR_CUDA, GS2D_ERR_TIMEOUT, GS2D_ERR_OVERFLOW,
+ GS2D_ERR_UNSUPPORTED) = range(7)
 GS2D_MODE_SUM, GS2D_MODE_COMPOSITE = 0, 1
 GS2D_PARAM_CHOLESKY, GS2D_PARAM_SCALE_ROT = 0, 1
 GS2D_FLAG_CAPACITY, GS2D_FLAG_OVERFLOW, GS2D_FLAG_TIMEOUT = 1, 2, 4
@@ -58,7 +62,8 @@ def lib() -> C.CDLL:
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"gs2d CUDA library not built: {LIB_PATH} is missing "
-                               "(run raster_gaussian_02_b300/build.py)")
+                               "(run raster_gaussian_02_b300/build.py"
+                               + (" --checked)" if CHECKED else ")"))
         L = C.CDLL(LIB_PATH)
         L.gs2d_workspace_size.argtypes = [_cfgp, C.c_int32, C.c_int64]
         L.gs2d_workspace_size.restype = C.c_size_t
@@ -85,6 +90,8 @@ def lib() -> C.CDLL:
         L.gs2d_read_status.restype = C.c_int
         L.gs2d_status_string.argtypes = [C.c_int]
         L.gs2d_status_string.restype = C.c_char_p
+        L.gs2d_debug_check_word.argtypes = [C.POINTER(C.c_uint32), C.c_int32]
+        L.gs2d_debug_check_word.restype = C.c_int
         _lib = L
     return _lib
 
@@ -217,6 +224,14 @@ def gs2d_read_status(workspace, stream=None):
     st = lib().gs2d_read_status(_ptr(workspace, None, "workspace"), C.byref(pairs),
                                 C.byref(flags), _stream(stream))
     return st, pairs.value, flags.value
+
+
+def gs2d_debug_check_word(clear: bool = True):
+    """Synchronizes the device; returns (status, word): the bounds-check bits
+    set since the last clear (checked build), or GS2D_ERR_UNSUPPORTED."""
+    w = C.c_uint32(0)
+    st = lib().gs2d_debug_check_word(C.byref(w), 1 if clear else 0)
+    return st, w.value
 
 
 # ------------------------------------------------------------- convenience

@@ -34,3 +34,19 @@ def pytest_collection_modifyitems(config, items):
 def oracle_lib():
     import oracle
     return oracle.lib()
+
+
+@pytest.fixture(autouse=True)
+def _bounds_check_word(request):
+    """With GS2D_CHECKED=1 (the bounds-checked library), every GPU test must
+    leave the device check word at zero: no index taken from data fell
+    outside the buffer it addresses."""
+    yield
+    if os.environ.get("GS2D_CHECKED") != "1" or request.node.get_closest_marker("gpu") is None:
+        return
+    from raster_gaussian_02_b300 import gs2d
+    if gs2d._lib is None:
+        return
+    st, word = gs2d.gs2d_debug_check_word(clear=True)
+    assert st == gs2d.GS2D_OK, gs2d.status_string(st)
+    assert word == 0, f"bounds checks failed: word {word:#x}"

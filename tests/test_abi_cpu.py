@@ -51,9 +51,24 @@ def test_nm_shows_only_the_abi(gs2d):
     assert gs == set(declared_functions())
 
 
+def test_checked_build_exports_the_same_abi(gs2d):
+    """libgs2d_checked.so (GS2D_CHECKS) builds and exports exactly the
+    declared functions; the normal build answers the check-word call with
+    GS2D_ERR_UNSUPPORTED without touching CUDA."""
+    import subprocess
+    path = lib_build.build(checked=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l and " gs2d_" in l}
+    assert exported == set(declared_functions())
+    st, word = gs2d.gs2d_debug_check_word()
+    assert (st, word) == (gs2d.GS2D_ERR_UNSUPPORTED, 0)
+    assert gs2d.lib().gs2d_debug_check_word(None, 0) == gs2d.GS2D_ERR_INVALID_ARG
+
+
 def test_status_strings(gs2d):
-    for s in range(6):
-        assert gs2d.status_string(s)
+    for s in range(7):
+        assert gs2d.status_string(s) != "unknown status"
     assert gs2d.status_string(99) == "unknown status"
 
 
