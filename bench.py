@@ -500,8 +500,8 @@ def kernels_per_step(R, wl, fused: bool, fwd_only: bool) -> int:
     the same rules the library uses to pick its kernels."""
     comp = wl.mode == 1
     T = R.num_tiles
-    if not comp and T <= 2048 and wl.n <= (1 << 20):
-        binning = 3  # tile histogram, tile scan, scatter
+    if T <= 2048 and wl.n <= (1 << 20):
+        binning = 3 + (1 if comp else 0)  # tile histogram, tile scan, scatter (+ depth sort)
     else:
         passes = ((T - 1).bit_length() + (32 if comp else 0) + 7) // 8
         partitions = (R.capacity + 2047) // 2048
