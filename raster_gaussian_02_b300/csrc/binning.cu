@@ -139,26 +139,28 @@ k_count_scan(int n, long long cap, const int* __restrict__ count, Header* hdr,
 }
 
 // ---------------------------------------------------------------------------
-// Sum mode with at most kCountSortMaxTiles tiles: a counting sort by tile in
-// three kernels, writing the final lists directly.
+// With at most kCountSortMaxTiles tiles: a counting sort by tile in three
+// kernels, writing the final lists directly.  No block waits for another or
+// finishes for the others: what every block needs is recomputed by each.
 //   k_tile_hist     per 256-Gaussian block b: H[t][b] = how many of the
 //                   block's Gaussians cover tile t, and the block's pair
-//                   total; the last block scans the totals (block offsets, P).
+//                   total.
 //   k_tile_scan     per tile t (one warp): exclusive scan of H[t][.] over the
-//                   blocks, in place, and the row total R[t]; the last block
-//                   scans the totals into the tile ranges.  (Ranges of empty
-//                   tiles are [0, 0), as the radix path leaves them.)
-//   k_tile_scatter  per block: the pair (Gaussian g, tile t) goes to
-//                   start(t) + H[t][b] + the number of the block's Gaussians
-//                   before g that cover t, read off a per-tile 256-bit mask of
-//                   the block's Gaussians.
+//                   blocks, in place, and the row total R[t].
+//   k_tile_scatter  per block: the block's pair offset (sum of the totals of
+//                   the blocks before it) and the tile starts (exclusive scan
+//                   of R); the pair (Gaussian g, tile t) goes to start(t) +
+//                   H[t][b] + the number of the block's Gaussians before g
+//                   that cover t, read off a per-tile 256-bit mask of the
+//                   block's Gaussians.  Block 0 also writes the tile ranges
+//                   (empty tiles [0, 0), as the radix path leaves them), the
+//                   tiles' launch order, P and the flags.
 // Within a tile the list comes out in ascending index, as the radix passes
 // give it; the sorted tile ids are written too (the backward reads them).
 
 __global__ void __launch_bounds__(kScanThreads)
-k_tile_hist(int n, int T, int tiles_x, long long cap, const int4* __restrict__ rect,
-            const int* __restrict__ count, Header* hdr, long long* __restrict__ block_off,
-            unsigned int* __restrict__ H, unsigned long long keys_final) {
+k_tile_hist(int n, int T, int tiles_x, const int4* __restrict__ rect, const int* __restrict__ count,
+            long long* __restrict__ block_tot, unsigned int* __restrict__ H) {
   pdl_enter();
   __shared__ unsigned int s_h[kCountSortMaxTiles];
   const int tid = threadIdx.x;
@@ -175,16 +177,14 @@ k_tile_hist(int n, int T, int tiles_x, long long cap, const int4* __restrict__ r
   __syncthreads();
   const size_t B = gridDim.x;
   for (int t = tid; t < T; t += blockDim.x) H[size_t(t) * B + blockIdx.x] = s_h[t];
-  finish_block_totals(total, hdr, block_off, cap, keys_final);
+  if (tid == 0) block_tot[blockIdx.x] = total;
 }
 
 __global__ void __launch_bounds__(256)
-k_tile_scan(int T, int B, long long cap, Header* hdr, unsigned int* __restrict__ H,
-            unsigned int* __restrict__ R, int2* __restrict__ ranges, int* __restrict__ order) {
+k_tile_scan(int T, int B, unsigned int* __restrict__ H, unsigned int* __restrict__ R) {
   pdl_enter();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t = blockIdx.x * 8 + warp;
-  __shared__ bool last;
   if (t < T) {
     unsigned int* row = H + size_t(t) * B;
     unsigned int carry = 0;
@@ -216,90 +216,66 @@ k_tile_scan(int T, int B, long long cap, Header* hdr, unsigned int* __restrict__
     }
     if (lane == 0) R[t] = carry;
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) last = atomicAdd(&hdr->blocks_done2, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!last) return;
-  // The last block: tile starts = exclusive scan of the row totals (thread
-  // i takes tiles 8i .. 8i+7; T <= 2048), then the ranges.
-  __threadfence();
-  const bool ok = (*reinterpret_cast<const volatile unsigned int*>(&hdr->flags) & kBadFlags) == 0;
-  unsigned int v[8], ex[8], sum = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int u = tid * 8 + j;
-    v[j] = u < T ? __ldcg(R + u) : 0u;
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    ex[j] = sum;
-    sum += v[j];
-  }
-  unsigned int total;
-  const unsigned int before = block_exclusive_scan_256<unsigned int>(sum, &total);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int u = tid * 8 + j;
-    if (u < T) {
-      const unsigned int start = before + ex[j];
-      ranges[u] = (ok && v[j]) ? make_int2(int(start), int(start + v[j])) : make_int2(0, 0);
-    }
-  }
-  // Launch order for the raster: tiles bucketed by floor(log2(list length)),
-  // longest first, so that the heaviest tiles start early instead of
-  // finishing last.  The order within a bucket does not matter (it only
-  // affects scheduling; every tile's result is the same).
-  __shared__ unsigned int s_cnt[33], s_pos[33];
-  if (tid < 33) s_cnt[tid] = 0u;
-  __syncthreads();
-  int bk[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int u = tid * 8 + j;
-    bk[j] = (u < T && ok && v[j]) ? 32 - __clz(v[j]) : 0;
-    if (u < T) atomicAdd(&s_cnt[bk[j]], 1u);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    unsigned int run = 0;
-    for (int b = 32; b >= 0; --b) {
-      s_pos[b] = run;
-      run += s_cnt[b];
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int u = tid * 8 + j;
-    if (u < T) order[atomicAdd(&s_pos[bk[j]], 1u)] = u;
-  }
 }
 
 __global__ void __launch_bounds__(kScanThreads)
-k_tile_scatter(int n, int T, int tiles_x, long long cap, const Header* __restrict__ hdr,
+k_tile_scatter(int n, int T, int tiles_x, long long cap, Header* __restrict__ hdr,
                const int4* __restrict__ rect, const int* __restrict__ count,
-               const long long* __restrict__ block_off, const unsigned int* __restrict__ H,
-               const int2* __restrict__ ranges, int* __restrict__ offsets,
-               int* __restrict__ sorted_gid, unsigned int* __restrict__ keys_out) {
+               const long long* __restrict__ block_tot, const unsigned int* __restrict__ H,
+               const unsigned int* __restrict__ R, int2* __restrict__ ranges, int* __restrict__ order,
+               int* __restrict__ offsets, int* __restrict__ sorted_gid,
+               unsigned int* __restrict__ keys_out, unsigned long long keys_final) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned int s_mask[];  // [T][8]: bit i = local Gaussian i covers t
   __shared__ long long s_excl[kScanItems + 1];
   __shared__ int4 s_rect[kScanItems];
   __shared__ unsigned int s_base[kCountSortMaxTiles];  // where the block's part of list t starts
+  constexpr int kTilesPer = kCountSortMaxTiles / kScanThreads;  // tiles per thread, consecutive
   const int tid = threadIdx.x;
+  const size_t B = gridDim.x;
   for (int k = tid; k < T * 8; k += blockDim.x) s_mask[k] = 0u;
   const long long g0 = (long long)blockIdx.x * kScanItems;
   const long long g = g0 + tid;
   const int cnt = g < n ? count[g] : 0;
   const int4 r = g < n ? rect[g] : make_int4(0, 0, -1, -1);
+  // this thread's tiles: row totals and the block's offsets within them
+  unsigned int v[kTilesPer], hb[kTilesPer];
+#pragma unroll
+  for (int j = 0; j < kTilesPer; ++j) {
+    const int u = tid * kTilesPer + j;
+    v[j] = u < T ? R[u] : 0u;
+    hb[j] = u < T ? H[size_t(u) * B + blockIdx.x] : 0u;
+  }
+  long long before_blocks = 0;  // pairs of the blocks before this one
+  for (int k = tid; k < int(blockIdx.x); k += blockDim.x) before_blocks += block_tot[k];
   s_rect[tid] = r;
   long long total;
   const long long excl = block_exclusive_scan_256<long long>(cnt, &total);  // orders the clears
   s_excl[tid] = excl;
   if (tid == 0) s_excl[kScanItems] = total;
+  long long boff;
+  block_exclusive_scan_256<long long>(before_blocks, &boff);
+  // tile starts: exclusive scan of the row totals (P fits 32 bits: n <= 2^20, T <= 2^11)
+  unsigned int ex[kTilesPer], sum = 0;
+#pragma unroll
+  for (int j = 0; j < kTilesPer; ++j) {
+    ex[j] = sum;
+    sum += v[j];
+  }
+  unsigned int P32;
+  const unsigned int before = block_exclusive_scan_256<unsigned int>(sum, &P32);
+  const long long P = P32;
+  unsigned int flags = 0;
+  if (P > cap) flags |= GS2D_FLAG_CAPACITY;
+  if (P >= (1ll << 30)) flags |= GS2D_FLAG_OVERFLOW;
+  const bool ok = flags == 0;
+#pragma unroll
+  for (int j = 0; j < kTilesPer; ++j) {
+    const int u = tid * kTilesPer + j;
+    if (u < T) s_base[u] = before + ex[j] + hb[j];
+  }
   if (g < n) {
-    const long long o = block_off[blockIdx.x] + excl;
+    const long long o = boff + excl;
     offsets[g] = o < (1ll << 31) ? int(o) : 0x7fffffff;
   }
   if (cnt > 0) {
@@ -309,23 +285,53 @@ k_tile_scatter(int n, int T, int tiles_x, long long cap, const Header* __restric
         if (check_ok(y * tiles_x + x < T, kCheckTile))
           atomicOr(&s_mask[(y * tiles_x + x) * 8 + (tid >> 5)], bit);
   }
-  const size_t B = gridDim.x;
-  {
-    unsigned int st[kCountSortMaxTiles / kScanThreads], hb[kCountSortMaxTiles / kScanThreads];
+  if (blockIdx.x == 0) {
 #pragma unroll
-    for (int j = 0; j < kCountSortMaxTiles / kScanThreads; ++j) {
-      const int u = tid + j * kScanThreads;
-      st[j] = u < T ? unsigned(ranges[u].x) : 0u;
-      hb[j] = u < T ? H[size_t(u) * B + blockIdx.x] : 0u;
+    for (int j = 0; j < kTilesPer; ++j) {
+      const int u = tid * kTilesPer + j;
+      if (u < T) {
+        const unsigned int start = before + ex[j];
+        ranges[u] = (ok && v[j]) ? make_int2(int(start), int(start + v[j])) : make_int2(0, 0);
+      }
     }
+    if (tid == 0) {
+      hdr->pairs = P;
+      hdr->flags = flags;
+      hdr->blocks_done = 0u;
+      hdr->blocks_done2 = 0u;
+      hdr->keys_final = keys_final;
+    }
+    // Launch order for the raster: tiles bucketed by floor(log2(list
+    // length)), longest first, so that the heaviest tiles start early
+    // instead of finishing last.  The order within a bucket does not matter
+    // (it only affects scheduling; every tile's result is the same).
+    __shared__ unsigned int s_cnt[33], s_pos[33];
+    if (tid < 33) s_cnt[tid] = 0u;
+    __syncthreads();
+    int bk[kTilesPer];
 #pragma unroll
-    for (int j = 0; j < kCountSortMaxTiles / kScanThreads; ++j) {
-      const int u = tid + j * kScanThreads;
-      if (u < T) s_base[u] = st[j] + hb[j];
+    for (int j = 0; j < kTilesPer; ++j) {
+      const int u = tid * kTilesPer + j;
+      bk[j] = (u < T && ok && v[j]) ? 32 - __clz(v[j]) : 0;
+      if (u < T) atomicAdd(&s_cnt[bk[j]], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      unsigned int run = 0;
+      for (int k = 32; k >= 0; --k) {
+        s_pos[k] = run;
+        run += s_cnt[k];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kTilesPer; ++j) {
+      const int u = tid * kTilesPer + j;
+      if (u < T) order[atomicAdd(&s_pos[bk[j]], 1u)] = u;
     }
   }
   __syncthreads();
-  if (usable_pairs(hdr, cap) == 0) return;  // P > capacity, overflow, or no pairs
+  if (!ok || P == 0) return;  // P > capacity, overflow, or no pairs
   for (long long e = tid; e < total; e += blockDim.x) {
     int lo = 0, hi = kScanItems - 1;  // the local Gaussian of pair e (as in k_emit)
     while (lo < hi) {
@@ -652,8 +658,6 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
     return cudaErrorInvalidConfiguration;
   const int T = num_tiles(c);
   Header* hdr = reinterpret_cast<Header*>(ws);
-  cudaError_t e = cudaMemsetAsync(ws, 0, kOffScan, s);  // header and histograms
-  if (e != cudaSuccess) return e;
   unsigned int* hist = reinterpret_cast<unsigned int*>(ws + kOffHist);
   long long* block_off = reinterpret_cast<long long*>(ws + L.block_off);
   int* offsets = reinterpret_cast<int*>(ws + L.offsets);
@@ -672,18 +676,19 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
       unsigned int* H = reinterpret_cast<unsigned int*>(ws + L.tile_hist);
       unsigned int* R = H + size_t(T) * size_t(blocks);
       const int2* rg = reinterpret_cast<const int2*>(tile_ranges);
-      GS2D_TRY(launch(k_tile_hist, dim3(blocks), dim3(kScanThreads), 0, s, n, T, tiles_x(c), cap,
-                      reinterpret_cast<const int4*>(rect), count, hdr, block_off, H,
-                      (unsigned long long)L.keys_a));
-      GS2D_TRY(launch(k_tile_scan, dim3((T + 7) / 8), dim3(256), 0, s, T, blocks, cap, hdr, H, R,
-                      reinterpret_cast<int2*>(tile_ranges), reinterpret_cast<int*>(ws + L.tile_order)));
+      // every header field is written by the scatter: no clearing pass
+      GS2D_TRY(launch(k_tile_hist, dim3(blocks), dim3(kScanThreads), 0, s, n, T, tiles_x(c),
+                      reinterpret_cast<const int4*>(rect), count, block_off, H));
+      GS2D_TRY(launch(k_tile_scan, dim3((T + 7) / 8), dim3(256), 0, s, T, blocks, H, R));
       const size_t smem = size_t(T) * 8 * sizeof(unsigned int);
       GS2D_TRY(cudaFuncSetAttribute(k_tile_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     int(size_t(kCountSortMaxTiles) * 8 * sizeof(unsigned int))));
       GS2D_TRY(launch(k_tile_scatter, dim3(blocks), dim3(kScanThreads), smem, s, n, T, tiles_x(c), cap,
-                      static_cast<const Header*>(hdr), reinterpret_cast<const int4*>(rect), count,
-                      static_cast<const long long*>(block_off), static_cast<const unsigned int*>(H), rg,
-                      offsets, sorted_gid, reinterpret_cast<unsigned int*>(ws + L.keys_a)));
+                      hdr, reinterpret_cast<const int4*>(rect), count,
+                      static_cast<const long long*>(block_off), static_cast<const unsigned int*>(H),
+                      static_cast<const unsigned int*>(R), reinterpret_cast<int2*>(tile_ranges),
+                      reinterpret_cast<int*>(ws + L.tile_order), offsets, sorted_gid,
+                      reinterpret_cast<unsigned int*>(ws + L.keys_a), (unsigned long long)L.keys_a));
       if (kComposite) {
         const size_t dsmem = size_t(kSegSmem) * sizeof(unsigned long long);
         GS2D_TRY(cudaFuncSetAttribute(k_tile_depth_sort, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -695,6 +700,7 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
       return cudaGetLastError();
     }
   }
+  GS2D_TRY(cudaMemsetAsync(ws, 0, kOffScan, s));  // header and histograms
   GS2D_TRY(launch(k_count_scan, dim3(blocks), dim3(kScanThreads), 0, s, n, cap, count, hdr, block_off, tables,
                                                L.passes * table_words,
                                                reinterpret_cast<unsigned int*>(tile_ranges), 2ll * T,
