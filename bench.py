@@ -307,16 +307,14 @@ def run_gs2d(args):
             R.render_bwd()
 
     def step_fused():
-        R.project(xy, chol, rgb, depth, opac)
-        R.bin_and_sort(sync=False)
+        R.project_bin_and_sort(xy, chol, rgb, depth, opac, sync=False)
         R.render_fwd_bwd_l2(target, bg)
 
     use_fused = args.path == "fused" and not fwd_only
     step = step_fused if use_fused else step_separate
 
     def render():
-        R.project(xy, chol, rgb, depth, opac)
-        R.bin_and_sort(sync=False)
+        R.project_bin_and_sort(xy, chol, rgb, depth, opac, sync=False)
         R.render_fwd(bg)
 
     def cached():
@@ -500,13 +498,15 @@ def kernels_per_step(R, wl, fused: bool, fwd_only: bool) -> int:
     the same rules the library uses to pick its kernels."""
     comp = wl.mode == 1
     T = R.num_tiles
-    if T <= 2048 and wl.n <= (1 << 20):
+    count_sort = T <= 2048 and wl.n <= (1 << 20)
+    if count_sort:
         binning = 3 + (1 if comp else 0)  # tile histogram, tile scan, scatter (+ depth sort)
     else:
         passes = ((T - 1).bit_length() + (32 if comp else 0) + 7) // 8
         partitions = (R.capacity + 2047) // 2048
         binning = 2 + passes + (passes - 1) + (passes if partitions > 128 else 0) + 1
-    k = 1 + binning
+    # the fused step projects inside the counting sort's histogram kernel
+    k = (0 if fused and count_sort else 1) + binning
     if fwd_only:
         return k + 1
     if fused:

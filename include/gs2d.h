@@ -192,6 +192,22 @@ GS2D_API gs2d_status gs2d_bin_and_sort(const gs2d_config* cfg, int32_t n, const 
                               void* workspace, gs2d_stream_t stream);
 
 /*
+ * gs2d_project followed by gs2d_bin_and_sort, with the same arguments and
+ * results as the two calls (the outputs are bit-identical).  With few tiles
+ * (the counting sort: at most 2048 tiles and 2^20 Gaussians) each block of
+ * the sort's histogram kernel projects its own Gaussians first, so the
+ * projection costs no launch of its own and its outputs are not read back.
+ * Argument checks and errors are those of the two calls.
+ */
+GS2D_API gs2d_status gs2d_project_bin_and_sort(const gs2d_config* cfg, int32_t n, const float* xy,
+                                               const float* shape, const float* rgb,
+                                               const float* depth, const float* opacity,
+                                               gs2d_record* rec, int32_t* rect, int32_t* count,
+                                               int64_t pair_capacity, int64_t* pairs_out,
+                                               int32_t* tile_ranges, int32_t* sorted_gid,
+                                               void* workspace, gs2d_stream_t stream);
+
+/*
  * Forward render, one thread block per 16x16 tile.
  * Sum:        C(p) = sum over touching i of rgb_i * w_i(p), w = exp(-q/2).
  * Composite:  T = 1; for the touching Gaussians in list order, while

@@ -29,7 +29,7 @@
 // README, Overview: gsplat-style projection/rasterization).
 #include <type_traits>
 
-#include "gs2d_internal.cuh"
+#include "project_body.cuh"
 
 namespace gs2d {
 
@@ -158,16 +158,29 @@ k_count_scan(int n, long long cap, const int* __restrict__ count, Header* hdr,
 // Within a tile the list comes out in ascending index, as the radix passes
 // give it; the sorted tile ids are written too (the backward reads them).
 
+// kProject: the block first projects its Gaussians (project_one), so the
+// projection and the histogram are one launch.
+template <bool kProject>
 __global__ void __launch_bounds__(kScanThreads)
-k_tile_hist(int n, int T, int tiles_x, const int4* __restrict__ rect, const int* __restrict__ count,
-            long long* __restrict__ block_tot, unsigned int* __restrict__ H) {
+k_tile_hist(int n, int T, int tiles_x, gs2d_config c, ProjectIn in, float4* __restrict__ rec,
+            int4* __restrict__ rect, int* __restrict__ count, long long* __restrict__ block_tot,
+            unsigned int* __restrict__ H) {
   pdl_enter();
   __shared__ unsigned int s_h[kCountSortMaxTiles];
   const int tid = threadIdx.x;
   for (int t = tid; t < T; t += blockDim.x) s_h[t] = 0u;
   const long long g = (long long)blockIdx.x * kScanItems + tid;
-  const int cnt = g < n ? count[g] : 0;
-  const int4 r = g < n ? rect[g] : make_int4(0, 0, -1, -1);
+  int cnt = 0;
+  int4 r = make_int4(0, 0, -1, -1);
+  if (g < n) {
+    if constexpr (kProject) {
+      r = project_one(c, int(g), in.xy, in.shape, in.rgb, in.depth, in.opacity, rec, rect, count);
+      cnt = r.z >= r.x ? (r.z - r.x + 1) * (r.w - r.y + 1) : 0;
+    } else {
+      cnt = count[g];
+      r = rect[g];
+    }
+  }
   long long total;
   block_exclusive_scan_256<long long>(cnt, &total);  // its barriers order the clears
   if (cnt > 0)
@@ -648,8 +661,8 @@ k_tile_depth_sort(int n, long long cap, const Header* __restrict__ hdr,
 }
 
 template <bool kComposite>
-cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec, const int* rect,
-                             const int* count, long long cap, int* tile_ranges, int* sorted_gid,
+cudaError_t launch_binning_t(const gs2d_config& c, int n, const ProjectIn* proj, gs2d_record* rec,
+                             int* rect, int* count, long long cap, int* tile_ranges, int* sorted_gid,
                              unsigned char* ws, cudaStream_t s) {
   using Key = KeyOf<kComposite>;
   const Layout L = layout_of(c, n, cap);
@@ -677,8 +690,11 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
       unsigned int* R = H + size_t(T) * size_t(blocks);
       const int2* rg = reinterpret_cast<const int2*>(tile_ranges);
       // every header field is written by the scatter: no clearing pass
-      GS2D_TRY(launch(k_tile_hist, dim3(blocks), dim3(kScanThreads), 0, s, n, T, tiles_x(c),
-                      reinterpret_cast<const int4*>(rect), count, block_off, H));
+      // with proj the projection runs inside the histogram kernel
+      GS2D_TRY(launch(proj ? k_tile_hist<true> : k_tile_hist<false>, dim3(blocks), dim3(kScanThreads), 0,
+                      s, n, T, tiles_x(c), c, proj ? *proj : ProjectIn{},
+                      reinterpret_cast<float4*>(rec), reinterpret_cast<int4*>(rect), count, block_off,
+                      H));
       GS2D_TRY(launch(k_tile_scan, dim3((T + 7) / 8), dim3(256), 0, s, T, blocks, H, R));
       const size_t smem = size_t(T) * 8 * sizeof(unsigned int);
       GS2D_TRY(cudaFuncSetAttribute(k_tile_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -700,6 +716,9 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
       return cudaGetLastError();
     }
   }
+  if (proj)
+    GS2D_TRY(launch_project(c, n, proj->xy, proj->shape, proj->rgb, proj->depth, proj->opacity, rec,
+                            rect, count, s));
   GS2D_TRY(cudaMemsetAsync(ws, 0, kOffScan, s));  // header and histograms
   GS2D_TRY(launch(k_count_scan, dim3(blocks), dim3(kScanThreads), 0, s, n, cap, count, hdr, block_off, tables,
                                                L.passes * table_words,
@@ -736,9 +755,21 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const gs2d_record* rec
 cudaError_t launch_binning(const gs2d_config& c, int n, const gs2d_record* rec, const int* rect,
                            const int* count, long long cap, int* tile_ranges, int* sorted_gid,
                            unsigned char* ws, cudaStream_t s) {
+  // without a projection the kernels only read rec, rect and count
+  gs2d_record* r = const_cast<gs2d_record*>(rec);
+  int* rc = const_cast<int*>(rect);
+  int* ct = const_cast<int*>(count);
   if (c.mode == GS2D_MODE_COMPOSITE)
-    return launch_binning_t<true>(c, n, rec, rect, count, cap, tile_ranges, sorted_gid, ws, s);
-  return launch_binning_t<false>(c, n, rec, rect, count, cap, tile_ranges, sorted_gid, ws, s);
+    return launch_binning_t<true>(c, n, nullptr, r, rc, ct, cap, tile_ranges, sorted_gid, ws, s);
+  return launch_binning_t<false>(c, n, nullptr, r, rc, ct, cap, tile_ranges, sorted_gid, ws, s);
+}
+
+cudaError_t launch_project_binning(const gs2d_config& c, int n, const ProjectIn& in, gs2d_record* rec,
+                                   int* rect, int* count, long long cap, int* tile_ranges,
+                                   int* sorted_gid, unsigned char* ws, cudaStream_t s) {
+  if (c.mode == GS2D_MODE_COMPOSITE)
+    return launch_binning_t<true>(c, n, &in, rec, rect, count, cap, tile_ranges, sorted_gid, ws, s);
+  return launch_binning_t<false>(c, n, &in, rec, rect, count, cap, tile_ranges, sorted_gid, ws, s);
 }
 
 }  // namespace gs2d

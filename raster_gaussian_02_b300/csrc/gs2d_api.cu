@@ -84,6 +84,35 @@ gs2d_status gs2d_bin_and_sort(const gs2d_config* cfg, int32_t n, const gs2d_reco
   return st;
 }
 
+gs2d_status gs2d_project_bin_and_sort(const gs2d_config* cfg, int32_t n, const float* xy,
+                                      const float* shape, const float* rgb, const float* depth,
+                                      const float* opacity, gs2d_record* rec, int32_t* rect,
+                                      int32_t* count, int64_t pair_capacity, int64_t* pairs_out,
+                                      int32_t* tile_ranges, int32_t* sorted_gid, void* workspace,
+                                      gs2d_stream_t stream) {
+  if (!config_ok(cfg) || n < 0) return GS2D_ERR_INVALID_ARG;
+  if (pair_capacity < 0 || pair_capacity > kMaxCapacity) return GS2D_ERR_INVALID_ARG;
+  if (!tile_ranges || !workspace || !aligned(tile_ranges, 16) || !aligned(workspace, 16))
+    return GS2D_ERR_INVALID_ARG;
+  if (pair_capacity > 0 && (!sorted_gid || !aligned(sorted_gid, 4))) return GS2D_ERR_INVALID_ARG;
+  if (n > 0) {
+    if (!xy || !shape || !rgb || !rec || !rect || !count) return GS2D_ERR_INVALID_ARG;
+    if (cfg->mode == GS2D_MODE_COMPOSITE && (!depth || !opacity)) return GS2D_ERR_INVALID_ARG;
+    if (!aligned(rec, 16) || !aligned(rect, 16) || !aligned(xy, 4) || !aligned(shape, 4) ||
+        !aligned(rgb, 4) || !aligned(count, 4) || (depth && !aligned(depth, 4)) ||
+        (opacity && !aligned(opacity, 4)))
+      return GS2D_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const ProjectIn in{xy, shape, rgb, depth, opacity};
+  cudaError_t e = launch_project_binning(*cfg, n, in, rec, rect, count, pair_capacity, tile_ranges,
+                                         sorted_gid, static_cast<unsigned char*>(workspace), s);
+  if (e != cudaSuccess) return GS2D_ERR_CUDA;
+  if (!pairs_out) return GS2D_OK;
+  uint32_t flags = 0;
+  return gs2d_read_status(workspace, pairs_out, &flags, stream);
+}
+
 gs2d_status gs2d_render_fwd(const gs2d_config* cfg, int32_t n, const gs2d_record* rec,
                             const int32_t* tile_ranges, const int32_t* sorted_gid,
                             const float* background, float* image, float* t_final, int32_t* last,

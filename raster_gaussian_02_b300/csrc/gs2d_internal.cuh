@@ -252,6 +252,114 @@ __device__ __forceinline__ bool check_ok(bool cond, int) {
 #define GS2D_CHECK_WORD_READER(name)
 #endif
 
+// Sums a Gaussian's cnt per-pair partial slots (kStride float4 each, in
+// emission order) starting at p: s[0..7] from the first two float4, s[8]
+// (kOpacity) from the third's .x, the absgrad sums (kAbs) from its .y, .z.
+// The loads of four slots are issued before their adds, which keep the slot
+// order.
+template <int kStride, bool kOpacity, bool kAbs>
+__device__ __forceinline__ void sum_pair_partials(const float4* __restrict__ p, int cnt,
+                                                  float (&s)[9], float& ax, float& ay) {
+  constexpr int kBatch = 4;  // slots whose loads are issued together; the adds stay in slot order
+  constexpr int kUsed = (kOpacity || kAbs) ? 3 : 2;
+  for (int k0 = 0; k0 < cnt; k0 += kBatch, p += kBatch * kStride) {
+    float4 q[kBatch][kUsed];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      if (k0 + j < cnt)
+#pragma unroll
+        for (int u = 0; u < kUsed; ++u) q[j][u] = p[j * kStride + u];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (k0 + j >= cnt) break;
+      const float4 u = q[j][0], v = q[j][1];
+      s[0] += u.x; s[1] += u.y; s[2] += u.z; s[3] += u.w;
+      s[4] += v.x; s[5] += v.y; s[6] += v.z; s[7] += v.w;
+      if constexpr (kOpacity || kAbs) {
+        const float4 x = q[j][kUsed - 1];
+        if (kOpacity) s[8] += x.x;
+        if (kAbs) {
+          ax += x.y;
+          ay += x.z;
+        }
+      }
+    }
+  }
+}
+
+// Writes Gaussian i's gradients with respect to the caller's parameters,
+// given its derivatives at the rendered (scaled) values: s[0..1] the mean,
+// s[2..4] the inverse covariance (A, B, C), s[5..7] the colour, s[8] the
+// opacity, and (ax, ay) its absgrad sums.  A is the record's A.  ok false
+// (a culled Gaussian, or no valid binning): zeros.  d_opacity and d_xy_abs
+// may be NULL (not written).  The chain rule to the shape parameters:
+// Cholesky:
+//   dA/da = -2A/a,        dA/db = 2b/(a^2 c^2),  dA/dc = -2b^2/(a^2 c^3)
+//   dB/da = b/(a^2 c^2),  dB/db = -1/(a c^2),    dB/dc = 2b/(a c^3)
+//   dC/dc = -2/c^3.
+// Scale-rotation (u = 1/s_x^2, v = 1/s_y^2, c = cos theta, s = sin theta):
+//   d(A, B, C)/du = (c^2, c s, s^2),  d(A, B, C)/dv = (s^2, -c s, c^2),
+//   du/ds_x = -2/s_x^3,  dv/ds_y = -2/s_y^3,
+//   d(A, B, C)/dtheta = (-2B, (c^2 - s^2)(u - v), 2B).
+// d(xy) = d(mean).  With render scale sc the derivatives are taken at the
+// scaled shape and multiplied back by sc (lengths and the mean only).
+__device__ __forceinline__ void write_gaussian_grads(int i, bool ok, float (&s)[9], float ax, float ay,
+                                                     float A, const float* __restrict__ shape,
+                                                     int param, float sc, float* __restrict__ d_xy,
+                                                     float* __restrict__ d_shape,
+                                                     float* __restrict__ d_rgb,
+                                                     float* __restrict__ d_opacity,
+                                                     float* __restrict__ d_xy_abs) {
+  float g0 = 0.f, g1 = 0.f, g2 = 0.f;
+  if (ok) {
+    const bool rot = param == GS2D_PARAM_SCALE_ROT;
+    const float a = sc * shape[3 * i], b = sc * shape[3 * i + 1];
+    const float c = rot ? shape[3 * i + 2] : sc * shape[3 * i + 2];
+    const float dA = s[2], dB = s[3], dC = s[4];
+    if (rot) {
+      float sn, cs;
+      sincos_fp32(c, &sn, &cs);
+      const float isx = 1.0f / a, isy = 1.0f / b;
+      const float u = isx * isx, v = isy * isy;
+      const float c2 = cs * cs, s2 = sn * sn, csn = cs * sn;
+      const float Bv = csn * (u - v);
+      g0 = (dA * c2 + dB * csn + dC * s2) * (-2.0f * u * isx);
+      g1 = (dA * s2 - dB * csn + dC * c2) * (-2.0f * v * isy);
+      g2 = 2.0f * Bv * (dC - dA) + dB * (c2 - s2) * (u - v);
+    } else {
+      const float ia = 1.0f / a, ic = 1.0f / c;
+      const float ia2ic2 = ia * ia * ic * ic;
+      g0 = dA * (-2.0f * A * ia) + dB * (b * ia2ic2);
+      g1 = dA * (2.0f * b * ia2ic2) + dB * (-ia * ic * ic);
+      g2 = dA * (-2.0f * b * b * ia2ic2 * ic) + dB * (2.0f * b * ia * ic * ic * ic) +
+           dC * (-2.0f * ic * ic * ic);
+    }
+    g0 *= sc;
+    g1 *= sc;
+    if (!rot) g2 *= sc;
+    s[0] *= sc;
+    s[1] *= sc;
+    ax *= sc;
+    ay *= sc;
+  } else {
+    for (int k = 0; k < 9; ++k) s[k] = 0.f;
+    ax = ay = 0.f;
+  }
+  d_xy[2 * i] = s[0];
+  d_xy[2 * i + 1] = s[1];
+  d_shape[3 * i] = g0;
+  d_shape[3 * i + 1] = g1;
+  d_shape[3 * i + 2] = g2;
+  d_rgb[3 * i] = s[5];
+  d_rgb[3 * i + 1] = s[6];
+  d_rgb[3 * i + 2] = s[7];
+  if (d_opacity) d_opacity[i] = s[8];
+  if (d_xy_abs) {
+    d_xy_abs[2 * i] = ax;
+    d_xy_abs[2 * i + 1] = ay;
+  }
+}
+
 // Monotone map of a finite float to uint32 (IEEE order, -0 mapped as +0).
 __device__ __forceinline__ unsigned int depth_key(float d) {
   unsigned int u = __float_as_uint(d);
@@ -310,6 +418,17 @@ cudaError_t launch_project(const gs2d_config& c, int n, const float* xy, const f
 cudaError_t launch_binning(const gs2d_config& c, int n, const gs2d_record* rec, const int* rect,
                            const int* count, long long cap, int* tile_ranges, int* sorted_gid,
                            unsigned char* ws, cudaStream_t s);
+
+// The projection's inputs, for the fused projection + binning.
+struct ProjectIn {
+  const float *xy, *shape, *rgb, *depth, *opacity;
+};
+
+// launch_project followed by launch_binning, with the projection folded into
+// the counting sort's histogram kernel where that sort is used.
+cudaError_t launch_project_binning(const gs2d_config& c, int n, const ProjectIn& in, gs2d_record* rec,
+                                   int* rect, int* count, long long cap, int* tile_ranges,
+                                   int* sorted_gid, unsigned char* ws, cudaStream_t s);
 
 cudaError_t launch_render_fwd(const gs2d_config& c, int n, const gs2d_record* rec, const int* ranges,
                               const int* sorted_gid, const float* bg, float* image, float* t_final,

@@ -72,6 +72,9 @@ def lib() -> C.CDLL:
         L.gs2d_bin_and_sort.argtypes = [_cfgp, C.c_int32, _p, _p, _p, C.c_int64,
                                         C.POINTER(C.c_int64), _p, _p, _p, _p]
         L.gs2d_bin_and_sort.restype = C.c_int
+        L.gs2d_project_bin_and_sort.argtypes = ([_cfgp, C.c_int32] + [_p] * 8 +
+                                                [C.c_int64, C.POINTER(C.c_int64)] + [_p] * 3 + [_p])
+        L.gs2d_project_bin_and_sort.restype = C.c_int
         L.gs2d_render_fwd.argtypes = [_cfgp, C.c_int32] + [_p] * 7 + [_p]
         L.gs2d_render_fwd.restype = C.c_int
         L.gs2d_loss_l2.argtypes = [C.c_int32, C.c_int32] + [_p] * 5 + [_p]
@@ -149,6 +152,19 @@ def gs2d_bin_and_sort(cfg, n, rec, rect, count, pair_capacity, pairs_out, tile_r
                                    int(pair_capacity), po, _ptr(tile_ranges, _i32, "tile_ranges"),
                                    _ptr(sorted_gid, _i32, "sorted_gid"),
                                    _ptr(workspace, None, "workspace"), _stream(stream))
+
+
+def gs2d_project_bin_and_sort(cfg, n, xy, shape, rgb, depth, opacity, rec, rect, count,
+                              pair_capacity, pairs_out, tile_ranges, sorted_gid, workspace,
+                              stream=None) -> int:
+    """gs2d_project then gs2d_bin_and_sort in one call (pairs_out as there)."""
+    po = C.byref(pairs_out) if pairs_out is not None else None
+    return lib().gs2d_project_bin_and_sort(
+        C.byref(cfg), int(n), _ptr(xy, _f32, "xy"), _ptr(shape, _f32, "shape"),
+        _ptr(rgb, _f32, "rgb"), _ptr(depth, _f32, "depth"), _ptr(opacity, _f32, "opacity"),
+        _ptr(rec, None, "rec"), _ptr(rect, _i32, "rect"), _ptr(count, _i32, "count"),
+        int(pair_capacity), po, _ptr(tile_ranges, _i32, "tile_ranges"),
+        _ptr(sorted_gid, _i32, "sorted_gid"), _ptr(workspace, None, "workspace"), _stream(stream))
 
 
 def gs2d_render_fwd(cfg, n, rec, tile_ranges, sorted_gid, background, image, t_final, last,
@@ -303,6 +319,24 @@ class Rasterizer:
             self.pairs = int(P.value)
             return self.pairs
 
+    def project_bin_and_sort(self, xy, shape, rgb, depth=None, opacity=None, sync: bool = True,
+                             grow: bool = True):
+        """project() and bin_and_sort() in one library call (same results)."""
+        self.xy, self.shape, self.rgb, self.depth, self.opacity = xy, shape, rgb, depth, opacity
+        while True:
+            P = C.c_int64(0) if sync else None
+            st = gs2d_project_bin_and_sort(self.cfg, self.n, xy, shape, rgb, depth, opacity,
+                                           self.rec, self.rect, self.count, self.capacity, P,
+                                           self.tile_ranges, self.sorted_gid, self.workspace)
+            if sync and st == GS2D_ERR_CAPACITY and grow:
+                self._alloc_pairs(int(P.value * 1.25) + 1024)
+                continue
+            check(st, "gs2d_project_bin_and_sort")
+            if sync:
+                self.pairs = int(P.value)
+                return self.pairs
+            return None
+
     def render_fwd(self, background=None):
         self.background = background
         check(gs2d_render_fwd(self.cfg, self.n, self.rec, self.tile_ranges, self.sorted_gid,
@@ -345,12 +379,14 @@ class Rasterizer:
     def step(self, xy, shape, rgb, target, depth=None, opacity=None, background=None, sync=False,
              fused=False):
         """One pass of the whole path: project, bin and sort, forward, L2
-        loss, backward (fused=True: the last three in one fused call).
-        Returns the device loss tensor."""
+        loss, backward (fused=True: projection and binning in one call, and
+        forward, loss and backward in another).  Returns the device loss
+        tensor."""
+        if fused:
+            self.project_bin_and_sort(xy, shape, rgb, depth, opacity, sync=sync)
+            return self.render_fwd_bwd_l2(target, background)
         self.project(xy, shape, rgb, depth, opacity)
         self.bin_and_sort(sync=sync)
-        if fused:
-            return self.render_fwd_bwd_l2(target, background)
         self.render_fwd(background)
         self.loss_l2(target)
         self.render_bwd()

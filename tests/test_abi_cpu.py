@@ -125,6 +125,15 @@ def test_host_checks_reject_bad_arguments(gs2d):
     assert L.gs2d_bin_and_sort(C.byref(good), 4, fake, fake, fake, 10, None, odd, fake, fake, null) == INVALID
     assert L.gs2d_bin_and_sort(C.byref(good), 4, fake, fake, fake, 10, None, fake, null, fake, null) == INVALID
     assert L.gs2d_bin_and_sort(C.byref(good), 4, null, fake, fake, 10, None, fake, fake, fake, null) == INVALID
+    # project_bin_and_sort: (xy shape rgb depth opacity rec rect count) cap pairs_out (ranges gid ws)
+    pb = L.gs2d_project_bin_and_sort
+    assert pb(C.byref(bad), 4, fake, fake, fake, null, null, fake, fake, fake, 10, None, fake, fake, fake, null) == INVALID
+    assert pb(C.byref(good), 4, null, fake, fake, null, null, fake, fake, fake, 10, None, fake, fake, fake, null) == INVALID
+    assert pb(C.byref(good), 4, fake, fake, fake, null, null, odd, fake, fake, 10, None, fake, fake, fake, null) == INVALID
+    assert pb(C.byref(comp), 4, fake, fake, fake, null, fake, fake, fake, fake, 10, None, fake, fake, fake, null) == INVALID
+    assert pb(C.byref(good), 4, fake, fake, fake, null, null, fake, fake, fake, -1, None, fake, fake, fake, null) == INVALID
+    assert pb(C.byref(good), 4, fake, fake, fake, null, null, fake, fake, fake, 10, None, fake, fake, odd, null) == INVALID
+    assert pb(C.byref(good), 4, fake, fake, fake, null, null, fake, fake, fake, 10, None, fake, null, fake, null) == INVALID
     # render_fwd
     assert L.gs2d_render_fwd(C.byref(good), 4, fake, fake, fake, null, null, null, null, null) == INVALID
     assert L.gs2d_render_fwd(C.byref(good), 4, odd, fake, fake, null, fake, null, null, null) == INVALID
