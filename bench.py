@@ -43,7 +43,10 @@ CSRC = os.path.join(ROOT, "raster_gaussian_02_b300", "csrc")
 #            + dL/dw = g.rgb (5) + t = w dL/dw (1) + 4 moment sums (5) = 27
 # plus one SFU exp2 per pair in both.
 FLOPS_FWD, FLOPS_BWD = 16, 27
-SM_FP32_LANES, SM_SFU_LANES = 128, 16
+# Per-SM rates per clock: 128 FP32 FMA lanes; 32 ex2 results from the SFU
+# (the probe in libgs2d_probe.so measures 9.0e12 ex2/s on 148 SMs at 2032
+# MHz, i.e. 30 per SM per clock, twice the 16 of earlier parts).
+SM_FP32_LANES, SM_SFU_LANES = 128, 32
 
 
 def parse():
@@ -190,6 +193,46 @@ def oracle_step(wl):
     oracle.step(cfg, wl.xy, wl.chol, wl.rgb, wl.target, wl.depth, wl.opacity, wl.background)
 
 
+def probe_peaks(dev, sms: int):
+    """Measured FP32 FMA and SFU ex2 throughput (libgs2d_probe.so), a
+    cross-check of the derived peaks: median of 10 timed launches of each
+    probe after 3 warm-up launches, 8 blocks of 256 threads per SM."""
+    import ctypes as C
+
+    import torch
+
+    from raster_gaussian_02_b300 import build as lib_build
+    L = C.CDLL(lib_build.build_probe())
+    L.gs2d_probe_fp32_fma.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_float, C.c_float, C.c_void_p]
+    L.gs2d_probe_ex2.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]
+    blocks = 8 * sms
+    out = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream(dev)
+
+    def rate(launch, work):
+        for _ in range(3):
+            if launch() != 0:
+                raise RuntimeError("probe launch failed")
+        ms = []
+        for _ in range(10):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            launch()
+            b.record(s)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return work / (statistics.median(ms) * 1e-3)
+
+    fma_iters, ex2_iters = 4096, 512
+    fma = rate(lambda: L.gs2d_probe_fp32_fma(out.data_ptr(), blocks, fma_iters, 0.999, 1e-3, s.cuda_stream),
+               2.0 * blocks * 256 * 8 * fma_iters)
+    ex2 = rate(lambda: L.gs2d_probe_ex2(out.data_ptr(), blocks, ex2_iters, s.cuda_stream),
+               1.0 * blocks * 256 * 8 * ex2_iters)
+    return {"fp32_tflops": fma / 1e12, "ex2_per_s": ex2,
+            "method": f"{blocks} blocks x 256 threads x 8 independent chains; "
+                      f"{fma_iters} FMAs / {ex2_iters} ex2.approx per chain; median of 10"}
+
+
 def cpu_baseline(wl, budget_s: float, min_steps: int = 2):
     """The CPU oracle as it stands, single-threaded, full steps of the same
     workload for about budget_s seconds (at least min_steps)."""
@@ -320,9 +363,10 @@ def run_gs2d(args):
     def cached():
         R.render_fwd(bg)
 
-    def graph_of(fn):
-        if args.no_graph:
-            return fn
+    if fwd_only and args.path == "fused":
+        step = render  # the render step through the combined projection + binning call
+
+    def graph_of_forced(fn):
         with torch.cuda.stream(stream):
             fn()
             fn()
@@ -331,6 +375,9 @@ def run_gs2d(args):
         with torch.cuda.graph(g, stream=stream):
             fn()
         return g.replay
+
+    def graph_of(fn):
+        return fn if args.no_graph else graph_of_forced(fn)
 
     run_step, run_render, run_cached = graph_of(step), graph_of(render), graph_of(cached)
 
@@ -373,6 +420,14 @@ def run_gs2d(args):
     k2 = max(20, min(args.steps, 400))
     render_ms = statistics.median(timed(run_render, k2, 5))
     cached_ms = statistics.median(timed(run_cached, k2, 5))
+    # the same step launched eagerly (no CUDA graph), or through a graph when
+    # the headline ran eagerly
+    if args.no_graph:
+        alt_graph_ms = statistics.median(timed(graph_of_forced(step), k2, 5))
+        eager_ms = statistics.median(step_ms)
+    else:
+        alt_graph_ms = statistics.median(step_ms)
+        eager_ms = statistics.median(timed(step, k2, 5))
     path_ms = {}
     if not fwd_only:
         other = step_separate if use_fused else step_fused
@@ -407,6 +462,9 @@ def run_gs2d(args):
     sm_max = float(peaks.get("sm_max_mhz") or clocks.get("sm_max_mhz") or 2032.0)
     fp32_peak = props.multi_processor_count * SM_FP32_LANES * 2 * sm_max * 1e6 / 1e12  # TFLOP/s
     sfu_peak = props.multi_processor_count * SM_SFU_LANES * sm_max * 1e6  # exp2 / s
+    probe = probe_peaks(dev, props.multi_processor_count)
+    probe["fp32_of_derived"] = probe["fp32_tflops"] / fp32_peak
+    probe["ex2_of_derived"] = probe["ex2_per_s"] / sfu_peak
     traffic_db = load_json(TRAFFIC) or {}
     src_hash = kernel_source_hash()
     seed_mismatch = rank != 0  # the stored counts are for rank 0's seed
@@ -426,6 +484,16 @@ def run_gs2d(args):
                               f"{sm_max:.0f} MHz (max SM clock; fraction of measured-clock peak = "
                               f"frac x {sm_max:.0f}/median MHz)"}
 
+    # Gaussian-pixel evaluations: the touching pairs (algorithmic) and the
+    # tile-level candidates, 256 pixels for every (tile, Gaussian) pair
+    evals = None
+    if counts and not seed_mismatch:
+        tp, cand = counts["touching_pairs"], 256 * int(P)
+        evals = {"touching_pairs": tp, "tile_candidates": cand, "touching_fraction": tp / cand,
+                 "fwd_touching_per_s": tp / (phases["render_fwd"] * 1e-3),
+                 "fwd_candidates_per_s": cand / (phases["render_fwd"] * 1e-3)}
+        if not fwd_only:
+            evals["bwd_touching_per_s"] = tp / (phases["render_bwd"] * 1e-3)
     rl_fwd = roofline("render_fwd", phases["render_fwd"], FLOPS_FWD)
     rl_bwd = None if fwd_only else roofline("render_bwd", phases["render_bwd"], FLOPS_BWD)
     dominant = rl_fwd
@@ -458,7 +526,7 @@ def run_gs2d(args):
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, args.cpu_seconds)
 
-    per_step_kernels = kernels_per_step(R, wl, use_fused, fwd_only)
+    per_step_kernels = kernels_per_step(R, wl, args.path == "fused", fwd_only)
     unit = "iters/s" if not fwd_only else "frames/s"
     if rank == 0:
         line = {
@@ -474,6 +542,10 @@ def run_gs2d(args):
                        "replicas": "each rank renders its own independently seeded image"},
             "render_fps": 1e3 / render_ms, "cached_render_fps": 1e3 / cached_ms,
             "paths_iters_s": {k: 1e3 / v for k, v in path_ms.items()},
+            "graph_vs_eager": {"graph_iters_s": 1e3 / alt_graph_ms, "eager_iters_s": 1e3 / eager_ms,
+                               "note": "median step, same L2 flush; eager = one launch per kernel"},
+            "gaussian_pixel_evals": evals,
+            "peak_probe": probe,
             "phase_ms": phases,
             "roofline": dominant,
             "roofline_fwd": rl_fwd, "roofline_bwd": rl_bwd,

@@ -23,6 +23,11 @@ LIB = os.path.join(HERE, "libgs2d.so")
 OBJDIR_CHECKED = os.path.join(ROOT, "_build", "gs2d_checked")
 LIB_CHECKED = os.path.join(HERE, "libgs2d_checked.so")
 
+# The FP32 / SFU throughput probes behind the roofline's peaks
+# (include/gs2d_probe.h): a separate library, not part of the rasterizer.
+PROBE_SRC = os.path.join(HERE, "probe", "peak_probe.cu")
+LIB_PROBE = os.path.join(HERE, "libgs2d_probe.so")
+
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]
@@ -77,6 +82,23 @@ def build(force: bool = False, verbose: bool = False, checked: bool = False) -> 
     return lib
 
 
+def build_probe(force: bool = False) -> str:
+    deps = [PROBE_SRC, os.path.join(INCLUDE, "gs2d_probe.h")]
+    if (not force and os.path.exists(LIB_PROBE) and
+            all(os.path.getmtime(p) <= os.path.getmtime(LIB_PROBE) for p in deps)):
+        return LIB_PROBE
+    tmp = LIB_PROBE + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-shared", "-cudart", "static", PROBE_SRC, "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"probe build failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB_PROBE)
+    return LIB_PROBE
+
+
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                checked="--checked" in sys.argv))
+    if "--probe" in sys.argv:
+        print(build_probe(force="--force" in sys.argv))
+    else:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                    checked="--checked" in sys.argv))

@@ -180,3 +180,26 @@ def test_host_checks_reject_bad_arguments(gs2d):
     # read_status
     assert L.gs2d_read_status(None, None, None, None) == INVALID
     assert L.gs2d_read_status(odd, None, None, None) == INVALID
+
+
+def test_probe_library_builds_and_checks_arguments():
+    """libgs2d_probe.so (the FP32 / SFU throughput probes behind the
+    roofline's peaks) exports exactly what include/gs2d_probe.h declares and
+    rejects bad arguments on the host (status 1, nothing launched)."""
+    import subprocess
+    path = lib_build.build_probe()
+    text = open(os.path.join(ROOT, "include", "gs2d_probe.h")).read()
+    declared = set(re.findall(r"GS2D_PROBE_API\s+[\w\s\*]+?\b(gs2d_\w+)\s*\(", text))
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l and " gs2d_" in l}
+    assert exported == declared == {"gs2d_probe_fp32_fma", "gs2d_probe_ex2"}
+    L = C.CDLL(path)
+    L.gs2d_probe_fp32_fma.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_float, C.c_float, C.c_void_p]
+    L.gs2d_probe_ex2.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]
+    fake = C.c_void_p(0x10000)
+    assert L.gs2d_probe_fp32_fma(None, 8, 16, 1.0, 0.0, None) == 1
+    assert L.gs2d_probe_fp32_fma(fake, 0, 16, 1.0, 0.0, None) == 1
+    assert L.gs2d_probe_fp32_fma(fake, 8, 0, 1.0, 0.0, None) == 1
+    assert L.gs2d_probe_ex2(fake, 70000, 16, None) == 1
+    assert L.gs2d_probe_ex2(fake, 8, (1 << 20) + 1, None) == 1
