@@ -21,16 +21,16 @@ namespace gs2d {
 
 namespace {
 
-constexpr int kChunkPairs = 256;   // pairs per block, one per thread
+constexpr int kBwdThreads = 256;  // threads per block; pairs per block round: 256 / kSplit
 constexpr int kStageTiles = 8;     // tiles of dL/dC staged at a time
 
 struct BwdSumSmem {
   float4 g[kStageTiles][kTilePixels];  // dL/dC of the staged tiles (r, g, b, 0)
-  float4 rec[kChunkPairs][3];          // the chunk's records
-  int gid[kChunkPairs];
-  int slot[kChunkPairs];               // index of the pair's tile among the chunk's tiles
-  int tiles[kChunkPairs];              // the chunk's distinct tiles, in order
-  int perm[kChunkPairs];               // processing order (similar boxes side by side)
+  float4 rec[kBwdThreads][3];          // the chunk's records
+  int gid[kBwdThreads];
+  int slot[kBwdThreads];               // index of the pair's tile among the chunk's tiles
+  int tiles[kBwdThreads];              // the chunk's distinct tiles, in order
+  int perm[kBwdThreads];               // processing order (similar boxes side by side)
   unsigned int bucket[256];
   int ntiles;
 };
@@ -53,33 +53,26 @@ __device__ __forceinline__ int block_inclusive_count_256(int flag, int* total, i
   return before + in_warp;
 }
 
-// Sum mode: one thread per (tile, Gaussian) pair, walking exactly the pixels
-// of the Gaussian's box inside the tile.  Blocks take fixed chunks of the
-// sorted pair list, whatever the tile boundaries, so heavy tiles spread over
-// many blocks; inside a block the pairs are reordered so that lanes of a
-// warp walk boxes of the same shape.  kAbs: also the absgrad sums over the
-// pair's pixels of |t (A dx + B dy)| and |t (B dx + C dy)| (each pixel's
-// share of dL/dmu in absolute value), in a third float4 of the pair's slot.
-template <bool kAbs>
-__global__ void __launch_bounds__(kChunkPairs, 4)  // 4 per SM: measured best (5 or 6 spill and lose)
-k_render_bwd_sum(gs2d_config c, int tiles_x, int n_gauss, const Header* __restrict__ hdr,
-                 const unsigned char* __restrict__ ws, const float4* __restrict__ rec,
-                 const int4* __restrict__ rect, const int* __restrict__ sorted_gid,
-                 const int* __restrict__ offsets, const float* __restrict__ d_image,
-                 float4* __restrict__ partials) {
-  pdl_enter();
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  BwdSumSmem& sm = *reinterpret_cast<BwdSumSmem*>(smem_raw);
-  __shared__ int warp_tot[8];
+// One block's rounds of the sum backward (k_render_bwd_sum), kSplit threads
+// per (tile, Gaussian) pair: chunks of 256 / kSplit consecutive pairs.
+template <bool kAbs, int kSplit>
+__device__ __forceinline__ void bwd_sum_rounds(BwdSumSmem& sm, int* warp_tot, const gs2d_config& c,
+                                               int tiles_x, int n_gauss, long long n,
+                                               const Header* __restrict__ hdr,
+                                               const unsigned char* __restrict__ ws,
+                                               const float4* __restrict__ rec,
+                                               const int4* __restrict__ rect,
+                                               const int* __restrict__ sorted_gid,
+                                               const int* __restrict__ offsets,
+                                               const float* __restrict__ d_image,
+                                               float4* __restrict__ partials) {
+  constexpr int kChunkPairs = kBwdThreads / kSplit;
   const int tid = threadIdx.x;
-  const unsigned int f = hdr->flags;
-  const long long n = (f & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) ? 0
-                      : hdr->pairs;
   const unsigned int* keys = reinterpret_cast<const unsigned int*>(ws + hdr->keys_final);
   for (long long k0 = (long long)blockIdx.x * kChunkPairs; k0 < n;
        k0 += (long long)gridDim.x * kChunkPairs) {
     const long long k = k0 + tid;
-    const bool valid = k < n;
+    const bool valid = tid < kChunkPairs && k < n;
     int tile = valid ? int(keys[k]) : -1;
     if (valid && !check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile))
       tile = 0;
@@ -103,12 +96,14 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, int n_gauss, const Header* __restri
       const int h = min(int(box_hi(by)), Y0 + kTile - 1) - max(int(box_lo(by)), Y0) + 1;
       key = (kTile - h) * kTile + (kTile - w);
     }
-    sm.gid[tid] = gid;
-    sm.slot[tid] = slot;
+    if (tid < kChunkPairs) {
+      sm.gid[tid] = gid;
+      sm.slot[tid] = slot;
+    }
     sm.bucket[tid] = 0u;
     __syncthreads();
     if (ntiles <= kStageTiles) {
-      atomicAdd(&sm.bucket[key], 1u);
+      if (tid < kChunkPairs) atomicAdd(&sm.bucket[key], 1u);
       __syncthreads();
       // exclusive scan of the 256 bucket counts, one per thread
       const unsigned int cnt = sm.bucket[tid];
@@ -128,20 +123,22 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, int n_gauss, const Header* __restri
       __syncthreads();
       sm.bucket[tid] = before + incl - cnt;
       __syncthreads();
-      const unsigned int pos = atomicAdd(&sm.bucket[key], 1u);
-      sm.perm[pos] = tid;
+      if (tid < kChunkPairs) {
+        const unsigned int pos = atomicAdd(&sm.bucket[key], 1u);
+        sm.perm[pos] = tid;
+      }
     } else {
-      sm.perm[tid] = tid;
+      if (tid < kChunkPairs) sm.perm[tid] = tid;
     }
     __syncthreads();
 
     const size_t HW = size_t(c.width) * c.height;
     const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
-    const int me = sm.perm[tid];
+    const int me = sm.perm[tid / kSplit], half = tid % kSplit;
     const bool mine_valid = (k0 + me) < n;
     for (int t0 = 0; t0 < ntiles; t0 += kStageTiles) {
       const int nst = min(kStageTiles, ntiles - t0);
-      for (int q = tid; q < nst * kTilePixels; q += kChunkPairs) {
+      for (int q = tid; q < nst * kTilePixels; q += kBwdThreads) {
         const int s = q >> 8, pp = q & 255;
         const int t = sm.tiles[t0 + s];
         const int x = (t % tiles_x) * kTile + (pp & 15), y = (t / tiles_x) * kTile + (pp >> 4);
@@ -154,19 +151,23 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, int n_gauss, const Header* __restri
       }
       __syncthreads();
       const int ms = sm.slot[me] - t0;
-      if (mine_valid && ms >= 0 && ms < nst) {
+      const bool act = mine_valid && ms >= 0 && ms < nst;
+      float sr = 0.f, sg = 0.f, sb = 0.f, Sx = 0.f, Sy = 0.f, Sxx = 0.f, Sxy = 0.f, Syy = 0.f;
+      float ax = 0.f, ay = 0.f;
+      int tx = 0, ty = 0;
+      float A = 0.f, B = 0.f, C = 0.f;
+      if (act) {
         const int t = sm.tiles[t0 + ms];
-        const int tx = t % tiles_x, ty = t / tiles_x;
+        tx = t % tiles_x; ty = t / tiles_x;
         const int X0 = tx * kTile, Y0 = ty * kTile;
         const float4 p0 = sm.rec[me][0], p1 = sm.rec[me][1], p2 = sm.rec[me][2];
-        const float mx = p0.x, my = p0.y, A = p0.z, B = p0.w, B2 = 2.0f * p0.w, C = p1.x;
+        const float mx = p0.x, my = p0.y, B2 = 2.0f * p0.w;
+        A = p0.z; B = p0.w; C = p1.x;
         const unsigned int bx = __float_as_uint(p2.x), by = __float_as_uint(p2.y);
         const int xa = max(int(box_lo(bx)), X0), xb = min(int(box_hi(bx)), X0 + kTile - 1);
         const int ya = max(int(box_lo(by)), Y0), yb = min(int(box_hi(by)), Y0 + kTile - 1);
         const float4* gt = sm.g[ms];
-        float sr = 0.f, sg = 0.f, sb = 0.f, Sx = 0.f, Sy = 0.f, Sxx = 0.f, Sxy = 0.f, Syy = 0.f;
-        float ax = 0.f, ay = 0.f;
-        for (int y = ya; y <= yb; ++y) {
+        for (int y = ya + half; y <= yb; y += kSplit) {
           const float dy = __fsub_rn(float(y) + 0.5f, my);
           const float b2dy = __fmul_rn(B2, dy);
           const float cdydy = __fmul_rn(__fmul_rn(C, dy), dy);
@@ -200,6 +201,13 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, int n_gauss, const Header* __restri
           Sxy = fmaf(rx, dy, Sxy);
           Syy = fmaf(r0 * dy, dy, Syy);
         }
+      }
+      if constexpr (kSplit == 2) {  // the two halves' sums, even rows + odd rows
+        float* vv[10] = {&sr, &sg, &sb, &Sx, &Sy, &Sxx, &Sxy, &Syy, &ax, &ay};
+#pragma unroll
+        for (int u = 0; u < (kAbs ? 10 : 8); ++u) *vv[u] += __shfl_xor_sync(0xffffffffu, *vv[u], 1);
+      }
+      if (act && half == 0) {
         const int gid_me = sm.gid[me];
         const int4 rc = rect[gid_me];
         const int pslot = offsets[gid_me] + (ty - rc.y) * (rc.z - rc.x + 1) + (tx - rc.x);
@@ -213,6 +221,39 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, int n_gauss, const Header* __restri
       __syncthreads();
     }
   }
+}
+
+// Sum mode: one thread per (tile, Gaussian) pair (or two, see below),
+// walking exactly the pixels of the Gaussian's box inside the tile.  Blocks
+// take fixed chunks of the sorted pair list, whatever the tile boundaries,
+// so heavy tiles spread over many blocks; inside a block the pairs are
+// reordered so that lanes of a warp walk boxes of the same shape.  When the
+// pairs would not give every resident block a full chunk, two adjacent
+// threads share each pair, one taking its even rows and one its odd rows,
+// and add their sums with one shuffle (fixed order), so the chunks are half
+// as long and twice as many.  kAbs: also the absgrad sums over the pair's
+// pixels of |t (A dx + B dy)| and |t (B dx + C dy)| (each pixel's share of
+// dL/dmu in absolute value), in a third float4 of the pair's slot.
+template <bool kAbs>
+__global__ void __launch_bounds__(kBwdThreads, 4)  // 4 per SM: measured best (5 or 6 spill and lose)
+k_render_bwd_sum(gs2d_config c, int tiles_x, int n_gauss, const Header* __restrict__ hdr,
+                 const unsigned char* __restrict__ ws, const float4* __restrict__ rec,
+                 const int4* __restrict__ rect, const int* __restrict__ sorted_gid,
+                 const int* __restrict__ offsets, const float* __restrict__ d_image,
+                 float4* __restrict__ partials) {
+  pdl_enter();
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  BwdSumSmem& sm = *reinterpret_cast<BwdSumSmem*>(smem_raw);
+  __shared__ int warp_tot[8];
+  const unsigned int f = hdr->flags;
+  const long long n = (f & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) ? 0
+                      : hdr->pairs;
+  if (n <= (long long)gridDim.x * kBwdThreads)
+    bwd_sum_rounds<kAbs, 2>(sm, warp_tot, c, tiles_x, n_gauss, n, hdr, ws, rec, rect, sorted_gid,
+                            offsets, d_image, partials);
+  else
+    bwd_sum_rounds<kAbs, 1>(sm, warp_tot, c, tiles_x, n_gauss, n, hdr, ws, rec, rect, sorted_gid,
+                            offsets, d_image, partials);
 }
 
 constexpr int kBwdCompThreads = 256;
@@ -285,7 +326,7 @@ cudaError_t launch_bwd_pairs(const gs2d_config& c, int n, const Layout& L, const
     const size_t smem = sizeof(BwdSumSmem);
     auto kern = k_render_bwd_sum<kAbs>;
     GS2D_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-    GS2D_TRY(launch(kern, dim3(4 * sm_count()), dim3(kChunkPairs), smem, s, c, tiles_x(c), n,
+    GS2D_TRY(launch(kern, dim3(4 * sm_count()), dim3(kBwdThreads), smem, s, c, tiles_x(c), n,
                     reinterpret_cast<const Header*>(ws), static_cast<const unsigned char*>(ws), r, rc,
                     sorted_gid, offsets, d_image, partials));
   }
