@@ -290,7 +290,9 @@ __device__ __forceinline__ void sum_pair_partials(const float4* __restrict__ p, 
 // Writes Gaussian i's gradients with respect to the caller's parameters,
 // given its derivatives at the rendered (scaled) values: s[0..1] the mean,
 // s[2..4] the inverse covariance (A, B, C), s[5..7] the colour, s[8] the
-// opacity, and (ax, ay) its absgrad sums.  A is the record's A.  ok false
+// opacity, and (ax, ay) its absgrad sums.  A is the record's A and shp the
+// caller's three shape parameters of Gaussian i (loaded by the caller, so
+// that its loads can be issued early).  ok false
 // (a culled Gaussian, or no valid binning): zeros.  d_opacity and d_xy_abs
 // may be NULL (not written).  The chain rule to the shape parameters:
 // Cholesky:
@@ -304,8 +306,8 @@ __device__ __forceinline__ void sum_pair_partials(const float4* __restrict__ p, 
 // d(xy) = d(mean).  With render scale sc the derivatives are taken at the
 // scaled shape and multiplied back by sc (lengths and the mean only).
 __device__ __forceinline__ void write_gaussian_grads(int i, bool ok, float (&s)[9], float ax, float ay,
-                                                     float A, const float* __restrict__ shape,
-                                                     int param, float sc, float* __restrict__ d_xy,
+                                                     float A, float3 shp, int param, float sc,
+                                                     float* __restrict__ d_xy,
                                                      float* __restrict__ d_shape,
                                                      float* __restrict__ d_rgb,
                                                      float* __restrict__ d_opacity,
@@ -313,8 +315,8 @@ __device__ __forceinline__ void write_gaussian_grads(int i, bool ok, float (&s)[
   float g0 = 0.f, g1 = 0.f, g2 = 0.f;
   if (ok) {
     const bool rot = param == GS2D_PARAM_SCALE_ROT;
-    const float a = sc * shape[3 * i], b = sc * shape[3 * i + 1];
-    const float c = rot ? shape[3 * i + 2] : sc * shape[3 * i + 2];
+    const float a = sc * shp.x, b = sc * shp.y;
+    const float c = rot ? shp.z : sc * shp.z;
     const float dA = s[2], dB = s[3], dC = s[4];
     if (rot) {
       float sn, cs;

@@ -44,11 +44,15 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   const bool bad = (hdr->flags & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) != 0;
   if (i < n) {
+    // every per-Gaussian load is issued up front, so one round trip precedes
+    // the partial slots' reads
     const int4 rc = rect[i];
+    const int off = offsets[i];
+    const float A = rec[3 * size_t(i)].z;
+    const float3 shp = make_float3(chol[3 * i], chol[3 * i + 1], chol[3 * i + 2]);
     const int cnt = (rc.z >= rc.x) ? (rc.z - rc.x + 1) * (rc.w - rc.y + 1) : 0;
     float s[9] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float ax = 0.f, ay = 0.f;
-    const int off = (!bad && cnt > 0) ? offsets[i] : 0;
     const bool ok = !bad && cnt > 0 && check_ok(off >= 0 && off + (long long)cnt <= hdr->pairs, kCheckPartial);
     if (ok) {
       if constexpr (kComposite || kAbs)
@@ -56,7 +60,7 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
       else
         sum_pair_partials<2, false, false>(partials + size_t(off) * 2, cnt, s, ax, ay);
     }
-    write_gaussian_grads(i, ok, s, ax, ay, rec[3 * size_t(i)].z, chol, param, sc, d_xy, d_chol, d_rgb,
+    write_gaussian_grads(i, ok, s, ax, ay, A, shp, param, sc, d_xy, d_chol, d_rgb,
                          kComposite ? d_opacity : nullptr, kAbs ? d_xy_abs : nullptr);
   }
   if ((d_bg || loss) && blockIdx.x == 0) {  // the first block: its extra work overlaps the rest
