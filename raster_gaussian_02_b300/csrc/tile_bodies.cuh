@@ -15,6 +15,7 @@
 namespace gs2d {
 
 constexpr int kWindow = 64;  // entries culled per warp at a time
+constexpr int kCompBatch = 4;  // composite backward: list entries per warp reduction
 
 struct Staged {
   float4 mc;  // mean_x, mean_y, A, 2B
@@ -201,25 +202,26 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Butterfly reduce-scatter of eight per-lane values over the warp: returns,
-// in every lane, the warp total of value ((lane >> 2) & 7) in the order
-// v[0..7] (lane bit 4 picks values 4-7, bit 3 values +2, bit 2 values +1).
-__device__ __forceinline__ float warp_reduce_scatter8(const float (&v)[8], int lane) {
-  float a[4], b[2];
-  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4;
+// Butterfly reduce-scatter of N = 2^m (m <= 5) per-lane values over the
+// warp: returns, in lane L, the warp total of value L >> (5 - m), each value
+// summed in the same fixed order on every run.  The first m steps halve the
+// values a lane carries (lane bit 4 picks the upper half first, then bit 3,
+// ...); the remaining steps add whole totals.
+template <int N>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[N], int lane) {
+  static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "N must be a power of two <= 32");
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float keep = u16 ? v[i + 4] : v[i], send = u16 ? v[i] : v[i + 4];
-    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
+  for (int half = N / 2, o = 16; half >= 1; half >>= 1, o >>= 1) {
+    const bool up = lane & o;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float keep = u8 ? a[i + 2] : a[i], send = u8 ? a[i] : a[i + 2];
-    b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    for (int i = 0; i < half; ++i) {
+      const float keep = up ? v[i + half] : v[i], send = up ? v[i] : v[i + half];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
   }
-  float c = (u4 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, u4 ? b[0] : b[1], 4);
-  c += __shfl_xor_sync(0xffffffffu, c, 2);
-  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  float c = v[0];
+#pragma unroll
+  for (int o = 16 / N; o >= 1; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
   return c;
 }
 
@@ -335,63 +337,83 @@ __device__ __forceinline__ void comp_tile_backward(
       nl += __popc(hits);
     }
     __syncwarp();
-    for (int e = nl - 1; e >= 0; --e) {
-      const uint2 u = list[e];
-      const int j = int(u.x);
-      const int idx = cb - rg.x + j;  // position in the tile's list
-      const float4 mc = sm.mc[j];
-      const float4 cr = sm.cr[j];
-      const float dx = __fsub_rn(pxf, mc.x);
-      const float dy = __fsub_rn(pyf, mc.y);
-      const float q = touch_q(dx, dy, mc.z, mc.w, cr.x);
-      const bool act = inside && (u.y & bit) && idx < lst && q <= kk;
-      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float v8 = 0.f, gxa = 0.f, gya = 0.f;
-      if (act) {
-        const float o = sm.op[j];
-        const float w = ex2_approx(q * kNegHalfLog2e);
-        const float alpha = o * w;
-        const float inv = 1.0f / (1.0f - alpha);
-        const float Tb = T * inv;  // transmittance in front of this Gaussian
-        const float aT = alpha * Tb;
-        const float dal = gr * (cr.y * Tb - Sr * inv) + gg * (cr.z * Tb - Sg * inv) +
-                          gb * (cr.w * Tb - Sb * inv);
-        const float t = w * o * dal;
-        v[0] = t * dx;
-        v[1] = t * dy;
-        v[2] = v[0] * dx;
-        v[3] = v[0] * dy;
-        v[4] = v[1] * dy;
-        v[5] = gr * aT;
-        v[6] = gg * aT;
-        v[7] = gb * aT;
-        v8 = dal * w;
-        if constexpr (kAbs) {
-          const float Bh = 0.5f * mc.w;
-          gxa = fabsf(fmaf(mc.z, v[0], Bh * v[1]));
-          gya = fabsf(fmaf(Bh, v[0], cr.x * v[1]));
-        }
-        Sr = fmaf(cr.y, aT, Sr);
-        Sg = fmaf(cr.z, aT, Sg);
-        Sb = fmaf(cr.w, aT, Sb);
-        T = Tb;
-      }
-      if (__any_sync(0xffffffffu, act)) {
-        const float tot = warp_reduce_scatter8(v, lane);
-        const float tot8 = warp_sum(v8);
-        if ((lane & 3) == 0) sm.acc[warp][j][(lane >> 2) & 7] = tot;
-        if (lane == 0) sm.acc[warp][j][8] = tot8;
-        if constexpr (kAbs) {
-          const float tx_ = warp_sum(gxa), ty_ = warp_sum(gya);
-          if (lane == 0) {
-            sm.acc_abs[warp][j][0] = tx_;
-            sm.acc_abs[warp][j][1] = ty_;
+    // Four list entries at a time, back to front: each lane's transmittance
+    // and colour-behind chain runs through them in order, then the warp
+    // reduces the four entries' values together (one reduce-scatter of 32
+    // values and one of the rest) instead of one reduction chain per entry.
+    for (int e0 = nl - 1; e0 >= 0; e0 -= kCompBatch) {
+      float v[kCompBatch * 8];
+      float x[kCompBatch * (kAbs ? 4 : 1)];  // v8 per entry, then (kAbs) absgrad x, y per entry
+      int jj[kCompBatch];
+#pragma unroll
+      for (int k = 0; k < kCompBatch; ++k) {
+        const int e = e0 - k;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) v[k * 8 + c8] = 0.f;
+        x[k] = 0.f;
+        if constexpr (kAbs) x[kCompBatch + 2 * k] = x[kCompBatch + 2 * k + 1] = 0.f;
+        jj[k] = -1;
+        if (e < 0) continue;  // warp-uniform
+        const uint2 u = list[e];
+        const int j = int(u.x);
+        jj[k] = j;
+        const int idx = cb - rg.x + j;  // position in the tile's list
+        const float4 mc = sm.mc[j];
+        const float4 cr = sm.cr[j];
+        const float dx = __fsub_rn(pxf, mc.x);
+        const float dy = __fsub_rn(pyf, mc.y);
+        const float q = touch_q(dx, dy, mc.z, mc.w, cr.x);
+        const bool act = inside && (u.y & bit) && idx < lst && q <= kk;
+        if (act) {
+          const float o = sm.op[j];
+          const float w = ex2_approx(q * kNegHalfLog2e);
+          const float alpha = o * w;
+          const float inv = 1.0f / (1.0f - alpha);
+          const float Tb = T * inv;  // transmittance in front of this Gaussian
+          const float aT = alpha * Tb;
+          const float dal = gr * (cr.y * Tb - Sr * inv) + gg * (cr.z * Tb - Sg * inv) +
+                            gb * (cr.w * Tb - Sb * inv);
+          const float t = w * o * dal;
+          const float t0x = t * dx, t0y = t * dy;
+          v[k * 8 + 0] = t0x;
+          v[k * 8 + 1] = t0y;
+          v[k * 8 + 2] = t0x * dx;
+          v[k * 8 + 3] = t0x * dy;
+          v[k * 8 + 4] = t0y * dy;
+          v[k * 8 + 5] = gr * aT;
+          v[k * 8 + 6] = gg * aT;
+          v[k * 8 + 7] = gb * aT;
+          x[k] = dal * w;
+          if constexpr (kAbs) {
+            const float Bh = 0.5f * mc.w;
+            x[kCompBatch + 2 * k] = fabsf(fmaf(mc.z, t0x, Bh * t0y));
+            x[kCompBatch + 2 * k + 1] = fabsf(fmaf(Bh, t0x, cr.x * t0y));
           }
+          Sr = fmaf(cr.y, aT, Sr);
+          Sg = fmaf(cr.z, aT, Sg);
+          Sb = fmaf(cr.w, aT, Sb);
+          T = Tb;
         }
-      } else {
-        if (lane < kCompVals) sm.acc[warp][j][lane] = 0.f;
-        if constexpr (kAbs)
-          if (lane < 2) sm.acc_abs[warp][j][lane] = 0.f;
+      }
+      // lane L: the total of v[L] = entry L / 8, value L % 8
+      const float tot = warp_reduce_scatter<kCompBatch * 8>(v, lane);
+      {
+        const int k = lane >> 3;
+        const int j = k == 0 ? jj[0] : k == 1 ? jj[1] : k == 2 ? jj[2] : jj[3];
+        if (j >= 0) sm.acc[warp][j][lane & 7] = tot;
+      }
+      constexpr int kX = kCompBatch * (kAbs ? 4 : 1);
+      const float totx = warp_reduce_scatter<kX>(x, lane);  // lane L: x[L >> (5 - log2 kX)]
+      if ((lane & (32 / kX - 1)) == 0) {
+        const int m = lane / (32 / kX);
+        const int k = m < kCompBatch ? m : (m - kCompBatch) >> 1;
+        const int j = k == 0 ? jj[0] : k == 1 ? jj[1] : k == 2 ? jj[2] : jj[3];
+        if (j >= 0) {
+          if (m < kCompBatch)
+            sm.acc[warp][j][8] = totx;
+          else if constexpr (kAbs)
+            sm.acc_abs[warp][j][(m - kCompBatch) & 1] = totx;
+        }
       }
     }
     __syncthreads();
