@@ -161,6 +161,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 1/x with the hardware approximation (the PTX rcp.approx instruction, about
+// one ulp); used only in gradient arithmetic, never in a touch or
+// termination decision.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // exp(-q/2) = 2^(q * (-log2(e)/2)).
 constexpr float kNegHalfLog2e = -0.72134752044448170368f;
 

@@ -368,7 +368,7 @@ __device__ __forceinline__ void comp_tile_backward(
           const float o = sm.op[j];
           const float w = ex2_approx(q * kNegHalfLog2e);
           const float alpha = o * w;
-          const float inv = 1.0f / (1.0f - alpha);
+          const float inv = rcp_approx(1.0f - alpha);
           const float Tb = T * inv;  // transmittance in front of this Gaussian
           const float aT = alpha * Tb;
           const float dal = gr * (cr.y * Tb - Sr * inv) + gg * (cr.z * Tb - Sg * inv) +
