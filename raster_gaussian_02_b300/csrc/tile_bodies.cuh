@@ -170,15 +170,13 @@ __device__ __forceinline__ CompFwdOut comp_tile_forward(CompSmem& sm, const gs2d
         nl += __popc(hits);
       }
       __syncwarp();
-      for (int e = 0; e < nl; ++e) {
-        const uint2 u = list[e];
-        const Staged s = sm.g[u.x];
-        const float q = touch_q(__fsub_rn(pxf, s.mc.x), __fsub_rn(pyf, s.mc.y), s.mc.z, s.mc.w, s.cr.x);
+      // front to back; the weights of two entries are formed together (they
+      // do not depend on T), then the transmittance steps run in order
+      auto step = [&](uint2 u, const Staged& s, float q, float w) {
         if (q <= kk && (u.y & bit) && !done) {
           if (T < c.t_min) {
             done = true;
           } else {
-            const float w = ex2_approx(q * kNegHalfLog2e);
             const float alpha = sm.op[u.x] * w;
             const float aT = alpha * T;
             ar = fmaf(s.cr.y, aT, ar);
@@ -188,6 +186,22 @@ __device__ __forceinline__ CompFwdOut comp_tile_forward(CompSmem& sm, const gs2d
             lst = rb - rg.x + int(u.x) + 1;
           }
         }
+      };
+      int e = 0;
+      for (; e + 1 < nl; e += 2) {
+        const uint2 u0 = list[e], u1 = list[e + 1];
+        const Staged s0 = sm.g[u0.x], s1 = sm.g[u1.x];
+        const float q0 = touch_q(__fsub_rn(pxf, s0.mc.x), __fsub_rn(pyf, s0.mc.y), s0.mc.z, s0.mc.w, s0.cr.x);
+        const float q1 = touch_q(__fsub_rn(pxf, s1.mc.x), __fsub_rn(pyf, s1.mc.y), s1.mc.z, s1.mc.w, s1.cr.x);
+        const float w0 = ex2_approx(q0 * kNegHalfLog2e), w1 = ex2_approx(q1 * kNegHalfLog2e);
+        step(u0, s0, q0, w0);
+        step(u1, s1, q1, w1);
+      }
+      if (e < nl) {
+        const uint2 u = list[e];
+        const Staged s = sm.g[u.x];
+        const float q = touch_q(__fsub_rn(pxf, s.mc.x), __fsub_rn(pyf, s.mc.y), s.mc.z, s.mc.w, s.cr.x);
+        step(u, s, q, ex2_approx(q * kNegHalfLog2e));
       }
       __syncwarp();
     }
