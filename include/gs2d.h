@@ -67,7 +67,8 @@ typedef enum gs2d_status {
   GS2D_ERR_INVALID_ARG = 1, /* a host-side argument check failed; nothing was enqueued */
   GS2D_ERR_CAPACITY = 2,    /* the (tile, Gaussian) pairs exceed pair_capacity */
   GS2D_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
-  GS2D_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (results invalid) */
+  GS2D_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (results invalid); reserved:
+                               no kernel of this version waits on another block */
   GS2D_ERR_OVERFLOW = 5,    /* the pair count reached 2^30 */
   GS2D_ERR_UNSUPPORTED = 6  /* the call needs the bounds-checked build of the library */
 } gs2d_status;
