@@ -26,7 +26,8 @@
  *    operation order, so the decision is reproducible bit for bit.
  *  Memory: every pointer argument is DEVICE memory unless marked "host".
  *    The caller owns every buffer; the library allocates nothing and keeps
- *    no state between calls (all per-call state lives in `workspace`).
+ *    no state between calls (all per-call state lives in `workspace`; the
+ *    one exception is gs2d_loss_l2_noalloc's fixed device array, below).
  *    Buffers are contiguous and element-aligned; gs2d_record arrays, rect,
  *    tile_ranges and the workspace must be 16-byte aligned (cudaMalloc and
  *    torch allocations are 256-byte aligned).  Calls that share a workspace
