@@ -364,9 +364,11 @@ class Rasterizer:
                               d_xy_abs=self._absgrad_out(absgrad)), "gs2d_render_bwd")
 
     def render_fwd_bwd_l2(self, target, background=None, write_image=True, absgrad=False):
-        """Fused forward + L2 loss + backward (one per-tile kernel and the
-        gather).  Fills loss and the d_* gradients, and the image unless
-        write_image is False; d_image, t_final and last are not written."""
+        """Fused forward + L2 loss + backward: composite, one per-tile kernel
+        and the gather; sum, the forward with the loss folded in, the pair
+        backward and the gather.  Fills loss and the d_* gradients, and the
+        image unless write_image is False; d_image (sum mode: kept in the
+        workspace instead), t_final and last are not written."""
         self.background = background
         check(gs2d_render_fwd_bwd_l2(self.cfg, self.n, self.shape, self.rec, self.rect,
                                      self.tile_ranges, self.sorted_gid, background, target,
