@@ -62,6 +62,8 @@ extern "C" {
 
 /* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
 typedef struct CUstream_st* gs2d_stream_t;
+/* A CUDA event (cudaEvent_t). */
+typedef struct CUevent_st* gs2d_event_t;
 
 typedef enum gs2d_status {
   GS2D_OK = 0,
@@ -364,6 +366,39 @@ GS2D_API gs2d_status gs2d_read_status(const void* workspace, int64_t* pairs, uin
 
 /* A static, human-readable name for a status code. */
 GS2D_API const char* gs2d_status_string(gs2d_status status);
+
+/*
+ * Kernel trace: the device time of each kernel the library enqueues, for
+ * profiling a pass from inside the program that runs it.  (No counterpart in
+ * the method's pages, which time whole renders -- FlashImgs README, Python
+ * API: benchmark_render; the trace splits such a time by kernel.)  While a
+ * trace is active on the calling
+ * host thread, every kernel any gs2d call launches from that thread is
+ * bracketed on its stream by two of the caller's events: events[2k] is
+ * recorded just before the k-th traced kernel and events[2k + 1] just after
+ * it, so cudaEventElapsedTime(events[2k], events[2k + 1]) is that kernel's
+ * duration.  During a stream capture the records are captured as event
+ * nodes of the graph (cudaEventRecordExternal) and are recorded again on
+ * every replay, so the durations are the last replay's.  Kernels, results
+ * and the other calls' behaviour are unchanged; memory copies and sets are
+ * not traced.
+ *   events        host array of 2 * max_kernels events, created by the
+ *                 caller with timing enabled and owned by it; it must stay
+ *                 valid until gs2d_trace_end
+ *   max_kernels   1 .. 4096: kernels that get events; later launches are
+ *                 counted but not bracketed
+ * gs2d_trace_begin returns GS2D_ERR_INVALID_ARG for a NULL array, a NULL
+ * event or max_kernels out of range, and starts a new trace otherwise (an
+ * active one is discarded).  gs2d_trace_end stops the trace and returns the
+ * number of kernels launched while it was active (0 if none was).
+ * gs2d_trace_kernel_name(k) returns the k-th traced kernel's name with its
+ * template arguments (e.g. "k_render_bwd_sum<false>") in a per-thread
+ * buffer valid until the next call, or NULL when k was not traced or a
+ * trace is active.
+ */
+GS2D_API gs2d_status gs2d_trace_begin(const gs2d_event_t* events, int32_t max_kernels);
+GS2D_API int32_t gs2d_trace_end(void);
+GS2D_API const char* gs2d_trace_kernel_name(int32_t k);
 
 /*
  * Bounds-check word of the checked build (libgs2d_checked.so, compiled with

@@ -397,9 +397,33 @@ __device__ __forceinline__ void pdl_enter() {
 // +-1.5 % of plain stream order, so it is left off.
 constexpr bool kDependentLaunch = false;
 
+// ------------------------------------------------------------- tracing --
+// Kernel trace (gs2d_trace_begin / gs2d_trace_end, csrc/trace.cu): while a
+// trace is active on the calling host thread, launch() records one of the
+// caller's events just before each kernel and one just after it on the
+// kernel's stream, so the pair brackets that kernel alone.  During a stream
+// capture the records become event nodes of the graph and are re-recorded on
+// every replay.
+struct Trace {
+  const cudaEvent_t* events = nullptr;  // 2 per kernel: before, after
+  int capacity = 0;                     // kernels that can be bracketed
+  int launched = 0;                     // kernels launched while active
+  bool active = false;
+};
+constexpr int kTraceMaxKernels = 4096;
+Trace& trace_state();                              // this host thread's trace
+void trace_set_kernel(int i, const void* kernel);  // the i-th traced kernel's host stub
+cudaError_t trace_record(cudaEvent_t e, cudaStream_t s);
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                           cudaStream_t s, Args... args) {
+  Trace& tr = trace_state();
+  const bool traced = tr.active && tr.launched < tr.capacity;
+  if (traced) {
+    const cudaError_t e = trace_record(tr.events[2 * tr.launched], s);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -410,7 +434,15 @@ inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   attr.val.programmaticStreamSerializationAllowed = kDependentLaunch ? 1 : 0;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  if (e != cudaSuccess || !tr.active) return e;
+  if (traced) {
+    trace_set_kernel(tr.launched, reinterpret_cast<const void*>(kernel));
+    const cudaError_t e2 = trace_record(tr.events[2 * tr.launched + 1], s);
+    if (e2 != cudaSuccess) return e2;
+  }
+  ++tr.launched;
+  return cudaSuccess;
 }
 
 #define GS2D_TRY(expr)                    \

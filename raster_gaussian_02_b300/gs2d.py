@@ -95,6 +95,12 @@ def lib() -> C.CDLL:
         L.gs2d_status_string.restype = C.c_char_p
         L.gs2d_debug_check_word.argtypes = [C.POINTER(C.c_uint32), C.c_int32]
         L.gs2d_debug_check_word.restype = C.c_int
+        L.gs2d_trace_begin.argtypes = [C.POINTER(C.c_void_p), C.c_int32]
+        L.gs2d_trace_begin.restype = C.c_int
+        L.gs2d_trace_end.argtypes = []
+        L.gs2d_trace_end.restype = C.c_int32
+        L.gs2d_trace_kernel_name.argtypes = [C.c_int32]
+        L.gs2d_trace_kernel_name.restype = C.c_char_p
         _lib = L
     return _lib
 
@@ -248,6 +254,63 @@ def gs2d_debug_check_word(clear: bool = True):
     w = C.c_uint32(0)
     st = lib().gs2d_debug_check_word(C.byref(w), 1 if clear else 0)
     return st, w.value
+
+
+def gs2d_trace_begin(events, max_kernels: int) -> int:
+    """events: a ctypes array of 2 * max_kernels cudaEvent_t handles."""
+    return lib().gs2d_trace_begin(events, int(max_kernels))
+
+
+def gs2d_trace_end() -> int:
+    return int(lib().gs2d_trace_end())
+
+
+def gs2d_trace_kernel_name(k: int):
+    name = lib().gs2d_trace_kernel_name(int(k))
+    return None if name is None else name.decode()
+
+
+class KernelTrace:
+    """Per-kernel device times of the library calls made inside a `with`
+    block (gs2d_trace_begin / gs2d_trace_end), on `device`.  Works eagerly
+    and under CUDA-graph capture; after a graph replay, durations() gives
+    that replay's times.
+
+        tr = KernelTrace(64)
+        with tr:
+            ...library calls...
+        torch.cuda.synchronize()
+        tr.durations()   # [(kernel name, ms), ...] in launch order
+    """
+
+    def __init__(self, max_kernels: int = 256, device=None):
+        self.max_kernels = int(max_kernels)
+        self.events = []
+        with torch.cuda.device(device):
+            s = torch.cuda.current_stream()
+            for _ in range(2 * self.max_kernels):
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(s)  # creates the underlying CUDA event
+                self.events.append(e)
+            torch.cuda.synchronize()
+        self._arr = (C.c_void_p * len(self.events))(*[e.cuda_event for e in self.events])
+        self.names = []
+        self.launched = 0
+
+    def __enter__(self):
+        check(gs2d_trace_begin(self._arr, self.max_kernels), "gs2d_trace_begin")
+        return self
+
+    def __exit__(self, *exc):
+        self.launched = gs2d_trace_end()
+        k = min(self.launched, self.max_kernels)
+        self.names = [gs2d_trace_kernel_name(i) for i in range(k)]
+        return False
+
+    def durations(self):
+        """[(name, ms)] of the traced kernels; synchronize first."""
+        return [(n, self.events[2 * i].elapsed_time(self.events[2 * i + 1]))
+                for i, n in enumerate(self.names)]
 
 
 # ------------------------------------------------------------- convenience

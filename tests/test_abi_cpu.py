@@ -203,3 +203,19 @@ def test_probe_library_builds_and_checks_arguments():
     assert L.gs2d_probe_fp32_fma(fake, 8, 0, 1.0, 0.0, None) == 1
     assert L.gs2d_probe_ex2(fake, 70000, 16, None) == 1
     assert L.gs2d_probe_ex2(fake, 8, (1 << 20) + 1, None) == 1
+
+
+def test_trace_rejects_bad_arguments_on_the_host(gs2d):
+    """gs2d_trace_begin checks its arguments before anything else; with no
+    trace active gs2d_trace_end returns 0 and no kernel has a name.  None of
+    this reaches CUDA."""
+    L = gs2d.lib()
+    assert L.gs2d_trace_begin(None, 1) == gs2d.GS2D_ERR_INVALID_ARG
+    fake = (C.c_void_p * 4)(1, 2, 3, 4)  # never dereferenced: rejected first
+    assert L.gs2d_trace_begin(fake, 0) == gs2d.GS2D_ERR_INVALID_ARG
+    assert L.gs2d_trace_begin(fake, 4097) == gs2d.GS2D_ERR_INVALID_ARG
+    holes = (C.c_void_p * 4)(1, None, 3, 4)
+    assert L.gs2d_trace_begin(holes, 2) == gs2d.GS2D_ERR_INVALID_ARG
+    assert gs2d.gs2d_trace_end() == 0
+    assert gs2d.gs2d_trace_kernel_name(0) is None
+    assert gs2d.gs2d_trace_kernel_name(-1) is None
