@@ -37,16 +37,28 @@ TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 CSRC = os.path.join(ROOT, "raster_gaussian_02_b300", "csrc")
 
-# Algorithmic FP32 work per touching (pixel, Gaussian) pair, FMA = 2 flops:
-#   forward  dx, dy (2) + q (7) + exponent scale (1) + 3 colour FMAs (6) = 16
-#   backward dx, dy (2) + q (7) + scale (1) + 3 colour-gradient FMAs (6)
-#            + dL/dw = g.rgb (5) + t = w dL/dw (1) + 4 moment sums (5) = 27
-# plus one SFU exp2 per pair in both.
-FLOPS_FWD, FLOPS_BWD = 16, 27
+# Algorithmic work per touching (pixel, Gaussian) pair, the unit of work:
+# FP32 flops (FMA = 2) of the per-pixel formulation of each pass, and SFU
+# exp2 evaluations.  Sum forward: dx, dy (2), q (7), exponent scale (1),
+# 3 colour FMAs (6) = 16.  Sum backward, every pixel forming its own share
+# of each gradient: the recomputed weight (10), 3 colour-gradient FMAs (6),
+# g.rgb (5), dL/dq (2), the mean's two terms (11) and the inverse
+# covariance's three (10): 44 by this count, about 40 as the unit is quoted,
+# and 40 is taken.  Composite adds about 6 (forward) and 10 (backward).
+FLOPS = {"fwd_sum": 16, "bwd_sum": 40, "fwd_comp": 22, "bwd_comp": 50, "fused_comp": 72}
+EX2 = {"fwd_sum": 1, "bwd_sum": 1, "fwd_comp": 1, "bwd_comp": 1, "fused_comp": 2}
+# What the kernels execute per touching pair after factoring (for
+# comparison): the sum backward takes the inverse covariance out of its
+# pixel sums and the row offset dy out of each row's, 23 flops per pixel
+# plus about 3 per pixel of row work.
+FLOPS_EXECUTED = {"fwd_sum": 16, "bwd_sum": 26, "fwd_comp": 22, "bwd_comp": 38, "fused_comp": 60}
 # Per-SM rates per clock: 128 FP32 FMA lanes; 32 ex2 results from the SFU
-# (the probe in libgs2d_probe.so measures 9.0e12 ex2/s on 148 SMs at 2032
-# MHz, i.e. 30 per SM per clock, twice the 16 of earlier parts).
+# (the probe in libgs2d_probe.so measures 28-30 per SM per clock on 148 SMs
+# at 2032 MHz, more than 16 could give).
 SM_FP32_LANES, SM_SFU_LANES = 128, 32
+# The workloads measured after the headline one in the same run.
+EXTRA_CONFIGS = ["heavy_2048x1360_300k", "composite_768x512_50k", "render_4096x4096_2m",
+                 "sweep_768x512_10k", "sweep_768x512_50k", "sweep_768x512_200k", "sweep_768x512_1m"]
 
 
 def parse():
@@ -61,6 +73,9 @@ def parse():
                     help="training step: the fused fwd+L2+bwd call, or the three separate calls")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (heavy, composite, 4096x4096, N sweep)")
+    ap.add_argument("--config-steps", type=int, default=30, help="timed steps per other workload")
     return ap.parse_args()
 
 
@@ -183,14 +198,14 @@ def aggregate_replicas(local_ms: float, steps: int, world: int, device=None):
 
 # ------------------------------------------------------------ reference ---
 
-def oracle_step(wl):
+def oracle_step(wl, omp: bool = False):
     import oracle
     cfg = oracle.Config(wl.width, wl.height, wl.mode, wl.cutoff_sigma, wl.t_min, param=wl.param)
     if wl.target is None:
         s = oracle.Scene(cfg, wl.xy, wl.chol, wl.rgb, wl.depth, wl.opacity, wl.background)
-        s.render()
+        s.render(omp=omp)
         return
-    oracle.step(cfg, wl.xy, wl.chol, wl.rgb, wl.target, wl.depth, wl.opacity, wl.background)
+    oracle.step(cfg, wl.xy, wl.chol, wl.rgb, wl.target, wl.depth, wl.opacity, wl.background, omp=omp)
 
 
 def probe_peaks(dev, sms: int):
@@ -234,18 +249,47 @@ def probe_peaks(dev, sms: int):
 
 
 def cpu_baseline(wl, budget_s: float, min_steps: int = 2):
-    """The CPU oracle as it stands, single-threaded, full steps of the same
-    workload for about budget_s seconds (at least min_steps)."""
-    oracle_step(wl)  # builds the oracle library, warms caches
+    """The CPU oracle timed on this machine's host cores: as it stands,
+    single-threaded, full steps of the same workload for about budget_s
+    seconds (at least min_steps); then the same steps through its OpenMP
+    timing driver (the same per-pixel functions, tile rows over all host
+    threads) for about a third of that."""
+    import oracle
+    unit = "iters/s" if wl.target is not None else "frames/s"
+
+    def run(omp, budget, least):
+        oracle_step(wl, omp)  # builds the library, warms caches
+        t0 = time.perf_counter()
+        k = 0
+        while k < least or time.perf_counter() - t0 < budget:
+            oracle_step(wl, omp)
+            k += 1
+        return k, time.perf_counter() - t0
+
+    k, dt = run(False, budget_s, min_steps)
+    threads = oracle.omp_threads(0)
+    k2, dt2 = run(True, budget_s / 3, min_steps)
+    single = {"value": k / dt, "unit": unit, "cores": 1,
+              "sample": f"{k} full steps of the same workload, single-threaded C oracle, {dt:.1f} s"}
+    omp = {"value": k2 / dt2, "unit": unit, "cores": threads, "nproc": os.cpu_count(),
+           "sample": f"{k2} full steps of the same workload, the oracle's per-pixel functions over "
+                     f"{threads} OpenMP threads (tile rows), {dt2:.1f} s"}
+    return {"value": single["value"], "unit": unit, "cores": 1, "kind": "oracle",
+            "sample": single["sample"], "single": single, "omp": omp}
+
+
+def cpu_config(wl):
+    """One full step of a workload through the oracle's OpenMP driver on all
+    host threads (the larger workloads: one step is the sample)."""
+    import oracle
+    threads = oracle.omp_threads(0)
     t0 = time.perf_counter()
-    k = 0
-    while k < min_steps or time.perf_counter() - t0 < budget_s:
-        oracle_step(wl)
-        k += 1
+    oracle_step(wl, omp=True)
     dt = time.perf_counter() - t0
-    return {"value": k / dt, "unit": "iters/s" if wl.target is not None else "frames/s",
-            "cores": 1, "kind": "oracle",
-            "sample": f"{k} full steps of the same workload, single-threaded C oracle, {dt:.1f} s"}
+    return {"value": 1.0 / dt, "unit": "iters/s" if wl.target is not None else "frames/s",
+            "cores": threads, "kind": "oracle",
+            "sample": f"one full step, the oracle's per-pixel functions over {threads} OpenMP "
+                      f"threads, {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -294,8 +338,328 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def kernel_kind(name: str):
+    """The raster work a kernel does (a key of FLOPS), or None."""
+    for prefix, kind in (("k_render_bwd_sum", "bwd_sum"), ("k_render_fwd_sum", "fwd_sum"),
+                         ("k_render_bwd_comp", "bwd_comp"), ("k_render_fwd_comp", "fwd_comp"),
+                         ("k_fused_comp", "fused_comp")):
+        if name.startswith(prefix):
+            return kind
+    return None
+
+
+class Peaks:
+    """FP32 and SFU peaks for the ALU roofline, derived from the SM count and
+    the maximum SM clock."""
+
+    def __init__(self, props, clocks):
+        peaks = load_json(PEAKS) or {}
+        self.sms = props.multi_processor_count
+        self.sm_max = float(peaks.get("sm_max_mhz") or clocks.get("sm_max_mhz") or 2032.0)
+        self.fp32 = self.sms * SM_FP32_LANES * 2 * self.sm_max * 1e6 / 1e12  # TFLOP/s
+        self.sfu = self.sms * SM_SFU_LANES * self.sm_max * 1e6  # ex2 / s
+        self.basis = (f"{self.sms} SMs x {SM_FP32_LANES} FP32 lanes x 2 x {self.sm_max:.0f} MHz; "
+                      f"SFU {self.sms} x {SM_SFU_LANES} ex2/clock x {self.sm_max:.0f} MHz (max SM "
+                      f"clock; at the sampled clock the fraction is frac x {self.sm_max:.0f}/median MHz)")
+
+
+def roofline(peaks: Peaks, kernel: str, ms: float, touching_pairs, traffic=None, step_ms=None):
+    """ALU roofline of one raster kernel: algorithmic FP32 work (touching
+    pairs x FLOPS per pair) and SFU work (touching pairs x EX2 per pair) over
+    the kernel's device time `ms`.  frac = max(FP32 fraction, SFU fraction)."""
+    kind = kernel_kind(kernel)
+    if kind is None or not touching_pairs or not ms:
+        return None
+    flops = FLOPS[kind]
+    achieved = touching_pairs * flops / (ms * 1e-3) / 1e12
+    fp32_frac = achieved / peaks.fp32
+    sfu_frac = touching_pairs * EX2[kind] / (ms * 1e-3) / peaks.sfu
+    out = {"bound": "alu", "achieved": achieved, "peak": peaks.fp32, "unit": "TFLOP/s",
+           "frac": max(fp32_frac, sfu_frac), "fp32_frac": fp32_frac, "sfu_frac": sfu_frac,
+           "traffic": traffic, "kernel": kernel, "ms": ms, "touching_pairs": touching_pairs,
+           "flops_per_pair": flops, "ex2_per_pair": EX2[kind],
+           "flops_per_pair_executed": FLOPS_EXECUTED[kind],
+           "fp32_frac_executed": touching_pairs * FLOPS_EXECUTED[kind] / (ms * 1e-3) / 1e12 / peaks.fp32,
+           "peak_basis": peaks.basis,
+           "time_basis": "median device time of this kernel over traced CUDA-graph replays of the "
+                         "step, each after an L2 flush (CUDA events recorded just before and just "
+                         "after the kernel on its stream)"}
+    if step_ms is not None:
+        out["kernel_ms_le_step_ms"] = bool(ms <= step_ms)
+    return out
+
+
+class WorkloadRun:
+    """One workload on one GPU: inputs resident in HBM, a Rasterizer with pair
+    headroom, and the calls of a step, replayable as CUDA graphs."""
+
+    def __init__(self, name, dev, stream, flush_buf, rank=0, path="fused", use_graph=True):
+        import numpy as np
+        import torch
+
+        from raster_gaussian_02_b300 import gs2d
+
+        self.name, self.dev, self.stream, self.flush_buf = name, dev, stream, flush_buf
+        self.use_graph = use_graph
+        self._graphs = []
+        wl = self.wl = make_workload(name, seed_offset=rank)
+        self.fwd_only = wl.target is None
+        # The step's inputs live in one device buffer (each part 16-byte
+        # aligned), so that the end-to-end leg moves them with one copy.
+        parts = [wl.xy, wl.chol, wl.rgb, wl.depth, wl.opacity, wl.background, wl.target]
+        offs, total = [], 0
+        for a in parts:
+            offs.append(total)
+            if a is not None:
+                total += (a.size + 3) // 4 * 4
+        self.host_pack = np.zeros(max(total, 4), np.float32)
+        for a, o in zip(parts, offs):
+            if a is not None:
+                self.host_pack[o:o + a.size] = np.ascontiguousarray(a, np.float32).ravel()
+        self.d_pack = torch.from_numpy(self.host_pack).to(dev)
+        views = [None if a is None else self.d_pack[o:o + a.size].view(a.shape)
+                 for a, o in zip(parts, offs)]
+        self.xy, self.chol, self.rgb, self.depth, self.opac, self.bg, self.target = views
+        R = self.R = gs2d.Rasterizer(wl.width, wl.height, wl.n, wl.mode, wl.cutoff_sigma, wl.t_min,
+                                     device=dev, param=wl.param)
+        R.project(self.xy, self.chol, self.rgb, self.depth, self.opac)
+        self.P = R.bin_and_sort(sync=True)
+        R._alloc_pairs(int(self.P * 1.25) + 4096)  # headroom, as a fitting loop would keep
+        self.fused = path == "fused"
+
+    def calls(self, kind):
+        """The library calls of one step of `kind`, as (call name, callable):
+        fused (the two fused calls), separate (the five calls), render
+        (projection + binning, forward) or cached (forward only)."""
+        R = self.R
+        a = (self.xy, self.chol, self.rgb, self.depth, self.opac)
+        pbs = ("project_bin_and_sort", lambda: R.project_bin_and_sort(*a, sync=False))
+        fwd = ("render_fwd", lambda: R.render_fwd(self.bg))
+        if kind == "cached":
+            return [fwd]
+        if kind == "render":
+            return [pbs, fwd]
+        if kind == "fused":
+            return [pbs, ("render_fwd_bwd_l2", lambda: R.render_fwd_bwd_l2(self.target, self.bg))]
+        out = [("project", lambda: R.project(*a)),
+               ("bin_and_sort", lambda: R.bin_and_sort(sync=False)), fwd]
+        if not self.fwd_only:
+            out += [("loss_l2", lambda: R.loss_l2(self.target)), ("render_bwd", R.render_bwd)]
+        return out
+
+    def step_kind(self):
+        if self.fwd_only:
+            return "render"
+        return "fused" if self.fused else "separate"
+
+    def fn(self, kind):
+        cs = self.calls(kind)
+
+        def run():
+            for _, f in cs:
+                f()
+        return run
+
+    def graph(self, fn, force=False):
+        """A replay callable of fn captured as one CUDA graph (fn itself when
+        graphs are off, unless force)."""
+        import torch
+        if not self.use_graph and not force:
+            return fn
+        with torch.cuda.stream(self.stream):
+            fn()
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            fn()
+        self._graphs.append(g)
+        return g.replay
+
+    def timed(self, fn, steps, warm, flush=True):
+        """Per-step device time (ms), the L2 flushed before each step."""
+        import torch
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        with torch.cuda.stream(self.stream):
+            for _ in range(warm):
+                fn()
+            torch.cuda.synchronize()
+            for a, b in ev:
+                if flush:
+                    self.flush_buf.fill_(1.0)
+                a.record(self.stream)
+                fn()
+                b.record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    def traced(self, kind, reps):
+        """Device time of every kernel and of every call of one step, from a
+        CUDA graph of the step whose calls each run under a kernel trace,
+        replayed `reps` times, each after an L2 flush.  Returns (kernels,
+        calls, launches): kernels = [(name, median ms)] in launch order,
+        calls = {call: median ms from its first kernel's start to its last
+        kernel's end}, launches = kernels launched per step."""
+        import torch
+
+        from raster_gaussian_02_b300 import gs2d
+        cs = self.calls(kind)
+        traces = [gs2d.KernelTrace(64, device=self.dev) for _ in cs]
+
+        def run():
+            for (_, f), tr in zip(cs, traces):
+                with tr:
+                    f()
+        with torch.cuda.stream(self.stream):
+            run()
+            run()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            run()
+        per_kernel, per_call = None, {c: [] for c, _ in cs}
+        with torch.cuda.stream(self.stream):
+            for r in range(reps + 2):
+                self.flush_buf.fill_(1.0)
+                g.replay()
+                torch.cuda.synchronize()
+                if r < 2:
+                    continue  # warm-up replays
+                flat = [d for tr in traces for d in tr.durations()]
+                if per_kernel is None:
+                    per_kernel = [(n, []) for n, _ in flat]
+                for (_, lst), (_, ms) in zip(per_kernel, flat):
+                    lst.append(ms)
+                for (c, _), tr in zip(cs, traces):
+                    k = len(tr.names)
+                    if k:
+                        per_call[c].append(tr.events[0].elapsed_time(tr.events[2 * k - 1]))
+        kernels = [(n, statistics.median(v)) for n, v in (per_kernel or [])]
+        calls = {c: statistics.median(v) for c, v in per_call.items() if v}
+        launches = sum(tr.launched for tr in traces)
+        del g
+        return kernels, calls, launches
+
+    def call_ms(self, kind, repeats=10, reps=20):
+        """Device time of each call of a `kind` step on its own: the call
+        captured `repeats` times back to back in one CUDA graph, replayed
+        `reps` times (each after an L2 flush); median replay time / repeats."""
+        out = {}
+        for name, f in self.calls(kind):
+            def rep(f=f):
+                for _ in range(repeats):
+                    f()
+            out[name] = statistics.median(self.timed(self.graph(rep, force=True), reps, 3)) / repeats
+        self._graphs = []
+        return out
+
+    def release(self):
+        """Frees this workload's device memory."""
+        import torch
+        self._graphs = []
+        for k in ("R", "d_pack", "xy", "chol", "rgb", "depth", "opac", "bg", "target"):
+            setattr(self, k, None)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def trace_floor(dev, stream, reps=50):
+    """The kernel trace's floor: the traced interval (median over graph
+    replays) of the smallest kernels the library launches, the L2 loss of a
+    1x1 image (one block each).  Every traced kernel time includes about
+    this much of launch and event overhead."""
+    import torch
+
+    from raster_gaussian_02_b300 import gs2d
+    z = lambda *sh: torch.zeros(*sh, dtype=torch.float32, device=dev)
+    img, tgt, loss, dimg = z(3, 1, 1), z(3, 1, 1), z(1), z(3, 1, 1)
+    ws = torch.zeros(16384, dtype=torch.uint8, device=dev)
+    tr = gs2d.KernelTrace(4, device=dev)
+
+    def run():
+        with tr:
+            gs2d.check(gs2d.gs2d_loss_l2(1, 1, img, tgt, loss, dimg, ws, stream), "gs2d_loss_l2")
+    with torch.cuda.stream(stream):
+        run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run()
+    per = {}
+    for _ in range(reps):
+        g.replay()
+        torch.cuda.synchronize()
+        for n, ms in tr.durations():
+            per.setdefault(n, []).append(ms)
+    return min(statistics.median(v) for v in per.values())
+
+
+def kernel_table(kernels, step_ms=None):
+    """Per kernel name: launches per step, summed median ms, share of the
+    traced kernels' total (and of the step)."""
+    agg = {}
+    for n, ms in kernels:
+        a = agg.setdefault(n, {"launches": 0, "ms": 0.0})
+        a["launches"] += 1
+        a["ms"] += ms
+    tot = sum(a["ms"] for a in agg.values()) or 1.0
+    for a in agg.values():
+        a["share"] = a["ms"] / tot
+        if step_ms:
+            a["share_of_step"] = a["ms"] / step_ms
+    return dict(sorted(agg.items(), key=lambda kv: -kv[1]["ms"]))
+
+
+def dominant_raster(kernels):
+    """The raster kernel with the largest median time: (name, ms)."""
+    best = None
+    for n, ms in kernels:
+        if kernel_kind(n) and (best is None or ms > best[1]):
+            best = (n, ms)
+    return best
+
+
+def first_of(kernels, kinds):
+    for n, ms in kernels:
+        if kernel_kind(n) in kinds:
+            return n, ms
+    return None
+
+
+def measure_config(name, dev, stream, flush_buf, peaks, counts, steps, warm, reps, cpu=False):
+    """Graph-replayed throughput and a kernel-time roofline of one workload."""
+    t0 = time.perf_counter()
+    w = WorkloadRun(name, dev, stream, flush_buf)
+    kind = w.step_kind()
+    step_ms = statistics.median(w.timed(w.graph(w.fn(kind)), steps, warm))
+    kernels, calls, launches = w.traced(kind, reps)
+    out = {"workload": describe(w.wl), "pairs": int(w.P),
+           "unit": "frames/s" if w.fwd_only else "iters/s", "value": 1e3 / step_ms,
+           "ms_per_step": step_ms, "steps": steps, "call_ms": calls,
+           "kernels": kernel_table(kernels, step_ms), "gpu_launches_per_step": launches}
+    render_ms = step_ms
+    if not w.fwd_only:
+        render_ms = statistics.median(w.timed(w.graph(w.fn("render")), steps, warm))
+        out["render_fps"] = 1e3 / render_ms
+    out["cached_render_fps"] = 1e3 / statistics.median(w.timed(w.graph(w.fn("cached")), steps, warm))
+    tp = (counts.get(name) or {}).get("touching_pairs")
+    dom = dominant_raster(kernels)
+    if dom:
+        out["roofline"] = roofline(peaks, dom[0], dom[1], tp, step_ms=step_ms)
+    if not w.fwd_only:
+        rk, _, _ = w.traced("render", reps)
+        f = first_of(rk, ("fwd_sum", "fwd_comp"))
+        if f:
+            out["roofline_fwd"] = roofline(peaks, f[0], f[1], tp, step_ms=render_ms)
+    w.release()
+    if cpu:
+        out["cpu_baseline"] = cpu_config(w.wl)
+    out["wall_s"] = time.perf_counter() - t0
+    return out
+
+
 def run_gs2d(args):
-    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -315,88 +679,12 @@ def run_gs2d(args):
         dist.barrier()
     gs2d.lib()
 
-    wl = make_workload(args.workload, seed_offset=rank)
-    fwd_only = wl.target is None
-    # The step's inputs live in one device buffer (each part 16-byte aligned),
-    # so that the end-to-end leg moves them with one host-to-device copy.
-    parts = [wl.xy, wl.chol, wl.rgb, wl.depth, wl.opacity, wl.background, wl.target]
-    offs, total = [], 0
-    for a in parts:
-        offs.append(total)
-        if a is not None:
-            total += (a.size + 3) // 4 * 4
-    host_pack = np.zeros(max(total, 4), np.float32)
-    for a, o in zip(parts, offs):
-        if a is not None:
-            host_pack[o:o + a.size] = np.ascontiguousarray(a, np.float32).ravel()
-    d_pack = torch.from_numpy(host_pack).to(dev)
-    views = [None if a is None else d_pack[o:o + a.size].view(a.shape) for a, o in zip(parts, offs)]
-    xy, chol, rgb, depth, opac, bg, target = views
-
-    R = gs2d.Rasterizer(wl.width, wl.height, wl.n, wl.mode, wl.cutoff_sigma, wl.t_min, device=dev,
-                        param=wl.param)
-    R.project(xy, chol, rgb, depth, opac)
-    P = R.bin_and_sort(sync=True)
-    R._alloc_pairs(int(P * 1.25) + 4096)  # headroom, as a fitting loop would keep
     stream = torch.cuda.Stream(device=dev)
     flush_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-
-    def step_separate():
-        R.project(xy, chol, rgb, depth, opac)
-        R.bin_and_sort(sync=False)
-        R.render_fwd(bg)
-        if not fwd_only:
-            R.loss_l2(target)
-            R.render_bwd()
-
-    def step_fused():
-        R.project_bin_and_sort(xy, chol, rgb, depth, opac, sync=False)
-        R.render_fwd_bwd_l2(target, bg)
-
-    use_fused = args.path == "fused" and not fwd_only
-    step = step_fused if use_fused else step_separate
-
-    def render():
-        R.project_bin_and_sort(xy, chol, rgb, depth, opac, sync=False)
-        R.render_fwd(bg)
-
-    def cached():
-        R.render_fwd(bg)
-
-    if fwd_only and args.path == "fused":
-        step = render  # the render step through the combined projection + binning call
-
-    def graph_of_forced(fn):
-        with torch.cuda.stream(stream):
-            fn()
-            fn()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            fn()
-        return g.replay
-
-    def graph_of(fn):
-        return fn if args.no_graph else graph_of_forced(fn)
-
-    run_step, run_render, run_cached = graph_of(step), graph_of(render), graph_of(cached)
-
-    def timed(fn, steps, warm, flush=True):
-        """Per-step device time (ms) with the L2 flushed before each step."""
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
-        with torch.cuda.stream(stream):
-            for _ in range(warm):
-                fn()
-            torch.cuda.synchronize()
-            for a, b in ev:
-                if flush:
-                    flush_buf.fill_(1.0)
-                a.record(stream)
-                fn()
-                b.record(stream)
-        torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in ev]
+    w = WorkloadRun(args.workload, dev, stream, flush_buf, rank=rank, path=args.path,
+                    use_graph=not args.no_graph)
+    R, fwd_only, kind = w.R, w.fwd_only, w.step_kind()
+    run_step = w.graph(w.fn(kind))
 
     # ---- headline: K steps, max over ranks
     sampler = ClockSampler(local)
@@ -405,138 +693,131 @@ def run_gs2d(args):
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     with sampler:
-        step_ms = timed(run_step, args.steps, args.warmup)
+        step_ms = w.timed(run_step, args.steps, args.warmup)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    st, pairs_now, flags = gs2d.gs2d_read_status(R.workspace)
+    st, _, _ = gs2d.gs2d_read_status(R.workspace)
     if st != gs2d.GS2D_OK:
         raise RuntimeError(f"device status after the timed region: {gs2d.status_string(st)}")
     value, total_ms = aggregate_replicas(sum(step_ms), args.steps, world, dev)
     clocks = sampler.summary()
+    med_step = statistics.median(step_ms)
 
-    # ---- secondary numbers (each after an L2 flush, same stream)
-    k2 = max(20, min(args.steps, 400))
-    render_ms = statistics.median(timed(run_render, k2, 5))
-    cached_ms = statistics.median(timed(run_cached, k2, 5))
+    # ---- per-kernel and per-call device times of the same step (traced
+    # graph replays, L2 flushed before each), of the separate calls, and of
+    # the render-only step
+    k2 = max(20, min(args.steps, 200))
+    kernels, calls, launches = w.traced(kind, k2)
+    _, phases_traced, _ = w.traced("separate", k2)
+    render_kernels, render_calls, _ = w.traced("render", k2)
+    phases = w.call_ms("separate")
+    phases.update({k: v for k, v in w.call_ms("fused" if not fwd_only else "render").items()
+                   if k not in phases})
+    floor_ms = trace_floor(dev, stream)
+    k3 = max(20, min(args.steps, 400))
+    path_ms = {}
+    if not fwd_only:
+        other = "separate" if kind == "fused" else "fused"
+        path_ms[kind] = med_step
+        path_ms[other] = statistics.median(w.timed(w.graph(w.fn(other)), k3, 5))
+    render_ms = statistics.median(w.timed(w.graph(w.fn("render")), k3, 5))
+    cached_ms = statistics.median(w.timed(w.graph(w.fn("cached")), k3, 5))
     # the same step launched eagerly (no CUDA graph), or through a graph when
     # the headline ran eagerly
     if args.no_graph:
-        alt_graph_ms = statistics.median(timed(graph_of_forced(step), k2, 5))
-        eager_ms = statistics.median(step_ms)
+        alt_graph_ms = statistics.median(w.timed(w.graph(w.fn(kind), force=True), k3, 5))
+        eager_ms = med_step
     else:
-        alt_graph_ms = statistics.median(step_ms)
-        eager_ms = statistics.median(timed(step, k2, 5))
-    path_ms = {}
-    if not fwd_only:
-        other = step_separate if use_fused else step_fused
-        path_ms[args.path] = statistics.median(step_ms)
-        path_ms["separate" if use_fused else "fused"] = statistics.median(timed(graph_of(other), k2, 5))
-    phases = {}
-    if True:  # eager, one call per timing pair
-        names = ["project", "bin_and_sort", "render_fwd"] + (
-            [] if fwd_only else ["loss_l2", "render_bwd", "render_fwd_bwd_l2"])
-        fns = {"project": lambda: R.project(xy, chol, rgb, depth, opac),
-               "bin_and_sort": lambda: R.bin_and_sort(sync=False),
-               "render_fwd": lambda: R.render_fwd(bg),
-               "loss_l2": lambda: R.loss_l2(target), "render_bwd": lambda: R.render_bwd(),
-               "render_fwd_bwd_l2": lambda: R.render_fwd_bwd_l2(target, bg)}
-        per = {k: [] for k in names}
-        with torch.cuda.stream(stream):
-            for _ in range(k2):
-                for k in names:
-                    flush_buf.fill_(1.0)
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    fns[k]()
-                    b.record(stream)
-                    per[k].append((a, b))
-        torch.cuda.synchronize()
-        phases = {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in per.items()}
+        alt_graph_ms = med_step
+        eager_ms = statistics.median(w.timed(w.fn(kind), k3, 5))
 
     # ---- roofline of the dominant raster kernel (FP32/SFU bound)
-    counts = (load_json(COUNTS) or {}).get(args.workload)
+    counts = load_json(COUNTS) or {}
     props = torch.cuda.get_device_properties(dev)
-    peaks = load_json(PEAKS) or {}
-    sm_max = float(peaks.get("sm_max_mhz") or clocks.get("sm_max_mhz") or 2032.0)
-    fp32_peak = props.multi_processor_count * SM_FP32_LANES * 2 * sm_max * 1e6 / 1e12  # TFLOP/s
-    sfu_peak = props.multi_processor_count * SM_SFU_LANES * sm_max * 1e6  # exp2 / s
+    peaks = Peaks(props, clocks)
     probe = probe_peaks(dev, props.multi_processor_count)
-    probe["fp32_of_derived"] = probe["fp32_tflops"] / fp32_peak
-    probe["ex2_of_derived"] = probe["ex2_per_s"] / sfu_peak
+    probe["fp32_of_derived"] = probe["fp32_tflops"] / peaks.fp32
+    probe["ex2_of_derived"] = probe["ex2_per_s"] / peaks.sfu
     traffic_db = load_json(TRAFFIC) or {}
     src_hash = kernel_source_hash()
-    seed_mismatch = rank != 0  # the stored counts are for rank 0's seed
+    # the stored counts are for rank 0's seed
+    tp = (counts.get(args.workload) or {}).get("touching_pairs") if rank == 0 else None
 
-    def roofline(kernel, ms, flops_per_pair):
-        if not counts or seed_mismatch:
-            return None
-        tp = counts["touching_pairs"]
-        achieved = tp * flops_per_pair / (ms * 1e-3) / 1e12
-        sfu_frac = tp / (ms * 1e-3) / sfu_peak
+    def traffic(kernel):
         tr = traffic_db.get(f"{kernel}:{args.workload}")
-        traffic = tr["bytes"] if tr and tr.get("source_hash") == src_hash else None
-        return {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp32_peak, "sfu_frac": sfu_frac, "traffic": traffic,
-                "kernel": kernel, "ms": ms, "touching_pairs": tp, "flops_per_pair": flops_per_pair,
-                "peak_basis": f"{props.multi_processor_count} SMs x {SM_FP32_LANES} FP32 lanes x 2 x "
-                              f"{sm_max:.0f} MHz (max SM clock; fraction of measured-clock peak = "
-                              f"frac x {sm_max:.0f}/median MHz)"}
+        return tr["bytes"] if tr and tr.get("source_hash") == src_hash else None
+
+    dom = dominant_raster(kernels)
+    rl = roofline(peaks, dom[0], dom[1], tp, traffic(dom[0]), step_ms=med_step) if dom else None
+    f = first_of(render_kernels, ("fwd_sum", "fwd_comp"))
+    rl_fwd = roofline(peaks, f[0], f[1], tp, traffic(f[0]), step_ms=render_ms) if f else None
+    b = first_of(kernels, ("bwd_sum", "bwd_comp", "fused_comp"))
+    rl_bwd = roofline(peaks, b[0], b[1], tp, traffic(b[0]), step_ms=med_step) if b else None
 
     # Gaussian-pixel evaluations: the touching pairs (algorithmic) and the
     # tile-level candidates, 256 pixels for every (tile, Gaussian) pair
     evals = None
-    if counts and not seed_mismatch:
-        tp, cand = counts["touching_pairs"], 256 * int(P)
-        evals = {"touching_pairs": tp, "tile_candidates": cand, "touching_fraction": tp / cand,
-                 "fwd_touching_per_s": tp / (phases["render_fwd"] * 1e-3),
-                 "fwd_candidates_per_s": cand / (phases["render_fwd"] * 1e-3)}
-        if not fwd_only:
-            evals["bwd_touching_per_s"] = tp / (phases["render_bwd"] * 1e-3)
-    rl_fwd = roofline("render_fwd", phases["render_fwd"], FLOPS_FWD)
-    rl_bwd = None if fwd_only else roofline("render_bwd", phases["render_bwd"], FLOPS_BWD)
-    dominant = rl_fwd
-    if rl_bwd and phases["render_bwd"] >= phases["render_fwd"]:
-        dominant = rl_bwd
+    if tp:
+        cand = 256 * int(w.P)
+        evals = {"touching_pairs": tp, "tile_candidates": cand, "touching_fraction": tp / cand}
+        if f:
+            evals["fwd_touching_per_s"] = tp / (f[1] * 1e-3)
+            evals["fwd_candidates_per_s"] = cand / (f[1] * 1e-3)
+        if b:
+            evals["bwd_touching_per_s"] = tp / (b[1] * 1e-3)
 
     # ---- end to end through the same calls, host buffers, copies inside:
     # every step copies its inputs (parameters and target, one pinned buffer)
     # to the device and reads its result back (the loss; the image when the
     # workload renders only)
-    h_pack = torch.from_numpy(host_pack).pin_memory()
+    h_pack = torch.from_numpy(w.host_pack).pin_memory()
     out = R.image if fwd_only else R.loss
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = h_pack.numel() * h_pack.element_size()  # the bytes copied (parts padded to 16 B)
     d2h = h_out.numel() * h_out.element_size()
+    d_pack = w.d_pack
 
     def e2e_step():
         d_pack.copy_(h_pack, non_blocking=True)
         run_step()
         h_out.copy_(out, non_blocking=True)
 
-    k3 = max(20, min(args.steps, 500))
-    e2e_ms = timed(e2e_step, k3, 5)
-    e2e_val, _ = aggregate_replicas(sum(e2e_ms), k3, world, dev)
+    k4 = max(20, min(args.steps, 500))
+    e2e_ms = w.timed(e2e_step, k4, 5)
+    e2e_val, _ = aggregate_replicas(sum(e2e_ms), k4, world, dev)
     # the host link alone: the same input copy without the step
-    copy_ms = statistics.median(timed(lambda: d_pack.copy_(h_pack, non_blocking=True), k3, 5))
+    copy_ms = statistics.median(w.timed(lambda: d_pack.copy_(h_pack, non_blocking=True), k4, 5))
 
-    # ---- CPU baseline (rank 0, one GPU only)
+    # ---- the other workloads (one GPU only): graph-replayed throughput and
+    # kernel-time rooflines
+    configs = None
+    if world == 1 and not args.no_configs:
+        R = out = d_pack = run_step = e2e_step = None  # drop the headline's device buffers
+        w.release()
+        configs = {}
+        for name in EXTRA_CONFIGS:
+            if name != args.workload:
+                configs[name] = measure_config(name, dev, stream, flush_buf, peaks, counts,
+                                               args.config_steps, 3, 10,
+                                               cpu=not args.no_cpu_baseline)
+
+    # ---- CPU baseline (one GPU only)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, args.cpu_seconds)
+        cpu = cpu_baseline(w.wl, args.cpu_seconds)
 
-    per_step_kernels = kernels_per_step(R, wl, args.path == "fused", fwd_only)
     unit = "iters/s" if not fwd_only else "frames/s"
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": describe(wl), "name": args.workload, "pairs": int(P),
+            "config": {"workload": describe(w.wl), "name": args.workload, "pairs": int(w.P),
                        "l2": "256 MiB buffer written before every timed step",
                        "graph": not args.no_graph,
-                       "path": ("fused fwd+L2+bwd call" if use_fused else
+                       "path": ("fused fwd+L2+bwd call" if kind == "fused" else
                                 "separate forward, loss and backward calls") if not fwd_only else
                                "forward",
                        "replicas": "each rank renders its own independently seeded image"},
@@ -546,15 +827,29 @@ def run_gs2d(args):
                                "note": "median step, same L2 flush; eager = one launch per kernel"},
             "gaussian_pixel_evals": evals,
             "peak_probe": probe,
+            "kernels": kernel_table(kernels, med_step),
+            "step_call_ms": calls,
             "phase_ms": phases,
-            "roofline": dominant,
+            "phase_basis": "device time of each call on its own: the call captured 10 times back "
+                           "to back in one CUDA graph, median of 20 replays (each after an L2 "
+                           "flush) / 10",
+            "phase_ms_traced": phases_traced,
+            "trace_floor_ms": floor_ms,
+            "trace_note": "kernel times come from CUDA events recorded just before and just after "
+                          "each kernel in a graph of the step; each includes about trace_floor_ms "
+                          "of launch and event overhead, so the fractions derived from them are "
+                          "lower bounds",
+            "render_kernels": kernel_table(render_kernels, render_ms),
+            "render_call_ms": render_calls,
+            "roofline": rl,
             "roofline_fwd": rl_fwd, "roofline_bwd": rl_bwd,
             "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "h2d_copy_ms": copy_ms,
                     "h2d_gbs": h2d / (copy_ms * 1e-3) / 1e9},
-            "gpu_launches": per_step_kernels * args.steps,
+            "gpu_launches": launches * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "configs": configs,
             "wall_s": wall,
             "gpu": props.name,
         }
@@ -563,27 +858,6 @@ def run_gs2d(args):
         dist.barrier()
         dist.destroy_process_group()
     return 0
-
-
-def kernels_per_step(R, wl, fused: bool, fwd_only: bool) -> int:
-    """The library's kernel launches in one step (memsets not counted), from
-    the same rules the library uses to pick its kernels."""
-    comp = wl.mode == 1
-    T = R.num_tiles
-    count_sort = T <= 2048 and wl.n <= (1 << 20)
-    if count_sort:
-        binning = 3 + (1 if comp else 0)  # tile histogram, tile scan, scatter (+ depth sort)
-    else:
-        passes = ((T - 1).bit_length() + (32 if comp else 0) + 7) // 8
-        partitions = (R.capacity + 2047) // 2048
-        binning = 2 + passes + (passes - 1) + (passes if partitions > 128 else 0) + 1
-    # the fused step projects inside the counting sort's histogram kernel
-    k = (0 if fused and count_sort else 1) + binning
-    if fwd_only:
-        return k + 1
-    if fused:
-        return k + (2 if comp else 3)  # (fused kernel | forward+loss, backward) + gather
-    return k + 1 + 2 + 2  # forward, loss (2), backward + gather
 
 
 def main():

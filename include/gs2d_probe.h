@@ -4,9 +4,11 @@
  * The raster kernels are bound by FP32 arithmetic and by the special-function
  * unit's 2^x (the Gaussian weight exp(-q/2) is one ex2.approx per touching
  * pixel).  The FP32/SFU peaks used for their roofline are derived from the
- * SM count, the per-SM lane counts (128 FP32 FMA lanes, 16 SFU lanes) and
- * the SM clock.  These two kernels measure what the GPU actually delivers,
- * as a cross-check of that derivation.  They are separate from libgs2d.so
+ * SM count, the per-SM rates per clock (128 FP32 FMAs; 32 ex2 results, the
+ * figure the ex2 probe below supports on a B300: it measures 28 to 30 per
+ * SM per clock, more than 16 could give) and the SM clock.  These two
+ * kernels measure what the GPU actually delivers, as a cross-check of that
+ * derivation.  They are separate from libgs2d.so
  * (built as libgs2d_probe.so) and take no part in the rasterizer.
  *
  * Both calls only enqueue one kernel on `stream`; the caller times them
