@@ -5,7 +5,10 @@ Tolerances (derived from FP32 arithmetic, see the design notes):
   * projection (conic, box, rect, count), tile ranges and sorted lists:
     bit-exact (the touch rule and the lists are integer outcomes of the
     same FP32 operation sequence);
-  * image: |gpu - ref| <= 1e-4 * max(1, |ref|);
+  * image: |gpu - ref| <= 1e-4 * max(1, |ref| / 10): absolute 1e-4 for every
+    value up to 10 (every [0, 1] image, and most pixels of the sum images),
+    relative 1e-5 above, where FP32's accumulation error grows with the sum
+    (a pixel summing 2500 Gaussians on one tile misses a pure 1e-4 bound);
   * loss: relative 1e-5; d_image elementwise to FP32 rounding;
   * gradients, per tensor: ||gpu - ref|| / ||ref|| <= 1e-3 and
     max |gpu - ref| <= 1e-3 * max |ref|.
@@ -106,8 +109,14 @@ def check_lists(g, s: oracle.Scene):
     assert np.array_equal(g["sorted_gid"], s.sorted_gid)
 
 
+IMG_REL_FROM = 10.0  # values above this get the relative bound IMG_TOL / IMG_REL_FROM
+
+
 def image_errors(gpu, ref):
-    return np.abs(gpu.astype(np.float64) - ref) / np.maximum(1.0, np.abs(ref))
+    """Error of each image value in units of its bound: the absolute error
+    for values up to IMG_REL_FROM, the error relative to |ref| / IMG_REL_FROM
+    above (so the check is `<= IMG_TOL` either way)."""
+    return np.abs(gpu.astype(np.float64) - ref) / np.maximum(1.0, np.abs(ref) / IMG_REL_FROM)
 
 
 def check_image(g, ref_fwd, composite: bool, max_ambiguous_frac=1e-3):
@@ -121,7 +130,10 @@ def check_image(g, ref_fwd, composite: bool, max_ambiguous_frac=1e-3):
         tf = np.abs(g["t_final"][ok].astype(np.float64) - tref)
         assert np.all(tf <= 1e-6 + 1e-4 * tref), tf.max(initial=0)
     err = image_errors(g["image"], ref_fwd["image"])[:, ok]
-    assert err.max(initial=0) <= IMG_TOL, err.max()
+    if err.size and err.max() > IMG_TOL:
+        k = np.unravel_index(np.argmax(err), err.shape)
+        raise AssertionError(f"image error {err.max():.3g} at a pixel of value "
+                             f"{ref_fwd['image'][:, ok][k]:.4g}")
     return ok
 
 
