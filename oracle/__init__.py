@@ -32,6 +32,31 @@ def lib():
     return _lib
 
 
+_omp = None
+
+
+def omp_lib():
+    """The multi-threaded timing driver (libgs2d_oracle_omp.so): the same
+    per-pixel functions, tile rows spread over OpenMP threads."""
+    global _omp
+    if _omp is None:
+        _omp = C.CDLL(_build.build_omp())
+        _declare(_omp)
+        cfgp = C.POINTER(RefCfg)
+        _omp.gs2dref_omp_threads.argtypes = [_i32]
+        _omp.gs2dref_omp_threads.restype = _i32
+        _omp.gs2dref_omp_render_fwd.argtypes = [cfgp] + [_p] * 14
+        _omp.gs2dref_omp_render_fwd.restype = _i64
+        _omp.gs2dref_omp_render_bwd.argtypes = [cfgp, _i32] + [_p] * 19 + [_i64]
+        _omp.gs2dref_omp_render_bwd.restype = None
+    return _omp
+
+
+def omp_threads(want: int = 0) -> int:
+    """Sets (want > 0) and returns the thread count of the OpenMP driver."""
+    return int(omp_lib().gs2dref_omp_threads(int(want)))
+
+
 class use_library:
     """Context manager that points this module at another build of the
     oracle source (the mutation tests plant mistakes in copies of it)."""
@@ -83,6 +108,8 @@ def _declare(L):
     L.gs2dref_render_brute.restype = None
     L.gs2dref_merge.argtypes = [cfgp, _i32] + [_p] * 6 + [_i32] + [_p] * 4
     L.gs2dref_merge.restype = _i32
+    L.gs2dref_merge_cost.argtypes = [cfgp, _i32] + [_p] * 5
+    L.gs2dref_merge_cost.restype = None
     L.gs2dref_sincos_f32.argtypes = [_i32, _p, _p, _p]
     L.gs2dref_sincos_f32.restype = None
     L.gs2dref_loss_l2.argtypes = [_i32, _i32, _p, _p, _p]
@@ -231,16 +258,18 @@ class Scene:
             return _ptr(self.ranges), _ptr(self._sg_keep)
         return _ptr(self.ranges), _ptr(self.sorted_gid)
 
-    def render(self):
-        """Full image: returns dict(image[3,H,W], t_final[H,W], last[H,W], margin[H,W], masked)."""
+    def render(self, omp: bool = False):
+        """Full image: returns dict(image[3,H,W], t_final[H,W], last[H,W], margin[H,W], masked).
+        omp: through the OpenMP timing driver (same per-pixel functions)."""
         H, W = self.cfg.height, self.cfg.width
         img = np.zeros((3, H, W), np.float64)
         tf = np.zeros((H, W), np.float64)
         last = np.zeros((H, W), np.int32)
         margin = np.zeros((H, W), np.float64)
         c = self.cfg.c()
-        masked = lib().gs2dref_render_fwd(C.byref(c), *self._common(), *self._lists(), _ptr(img),
-                                          _ptr(tf), _ptr(last), _ptr(margin))
+        fn = omp_lib().gs2dref_omp_render_fwd if omp else lib().gs2dref_render_fwd
+        masked = fn(C.byref(c), *self._common(), *self._lists(), _ptr(img), _ptr(tf), _ptr(last),
+                    _ptr(margin))
         return dict(image=img, t_final=tf, last=last, margin=margin, masked=int(masked))
 
     def render_pixels(self, pix):
@@ -266,15 +295,20 @@ class Scene:
                                    _ptr(depth), _ptr(img), _ptr(tf))
         return dict(image=img, t_final=tf)
 
-    def render_bwd(self, d_image):
+    def render_bwd(self, d_image, omp: bool = False):
+        """omp: through the OpenMP timing driver (same per-pixel functions,
+        per-thread accumulators summed in thread order)."""
         d_image = _f64(d_image, (3, self.cfg.height, self.cfg.width))
         n = self.n
         dxy = np.zeros((n, 2)); dchol = np.zeros((n, 3)); drgb = np.zeros((n, 3))
         dop = np.zeros(n); dbg = np.zeros(3); dconic = np.zeros((n, 3)); dabs = np.zeros((n, 2))
         c = self.cfg.c()
-        lib().gs2dref_render_bwd(C.byref(c), n, *self._common(), _ptr(self.proj.count),
-                                 *self._lists(), _ptr(d_image), _ptr(dxy), _ptr(dchol), _ptr(drgb),
-                                 _ptr(dop), _ptr(dbg), _ptr(dconic), _ptr(dabs))
+        args = (C.byref(c), n, *self._common(), _ptr(self.proj.count), *self._lists(), _ptr(d_image),
+                _ptr(dxy), _ptr(dchol), _ptr(drgb), _ptr(dop), _ptr(dbg), _ptr(dconic), _ptr(dabs))
+        if omp:
+            omp_lib().gs2dref_omp_render_bwd(*args, 0)
+        else:
+            lib().gs2dref_render_bwd(*args)
         return dict(xy=dxy, chol=dchol, rgb=drgb, opacity=dop, background=dbg, conic=dconic,
                     xy_abs=dabs)
 
@@ -326,11 +360,24 @@ def merge(cfg: Config, xy, shape, rgb, max_merges: int, with_partners: bool = Fa
     return out + (partner[:n],) if with_partners else out
 
 
-def step(cfg: Config, xy, chol, rgb, target, depth=None, opacity=None, background=None):
+def merge_cost(cfg: Config, xa, sha, xb, shb):
+    """The merge's pairing cost (FP32) of the k-th Gaussian of (xa, sha)
+    against the k-th of (xb, shb), shapes in cfg.param's parameters."""
+    xa = _f32(xa, (-1, 2))
+    m = xa.shape[0]
+    xb, sha, shb = _f32(xb, (m, 2)), _f32(sha, (m, 3)), _f32(shb, (m, 3))
+    out = np.zeros(max(m, 1), np.float32)
+    lib().gs2dref_merge_cost(C.byref(cfg.c()), m, _ptr(xa), _ptr(sha), _ptr(xb), _ptr(shb), _ptr(out))
+    return out[:m]
+
+
+def step(cfg: Config, xy, chol, rgb, target, depth=None, opacity=None, background=None,
+         omp: bool = False):
     """One pass of the whole path on the CPU: project, bin, render, L2 loss,
-    backward.  Returns (scene, forward dict, loss, d_image, gradient dict)."""
+    backward.  Returns (scene, forward dict, loss, d_image, gradient dict).
+    omp: render and backward through the OpenMP timing driver."""
     s = Scene(cfg, xy, chol, rgb, depth, opacity, background)
-    fwd = s.render()
+    fwd = s.render(omp=omp)
     loss, dimg = loss_l2(fwd["image"], target)
-    grads = s.render_bwd(dimg)
+    grads = s.render_bwd(dimg, omp=omp)
     return s, fwd, loss, dimg, grads

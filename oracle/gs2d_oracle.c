@@ -949,6 +949,23 @@ static float ref_merge_cost(const float* xi, const float* Si, const float* xj, c
   return (num > 0.0f ? num : 0.0f) / det; /* -0 and NaN clamp to +0 */
 }
 
+/*
+ * The pairing cost of m pairs, the k-th of (xa, sha) against the k-th of
+ * (xb, shb), each Sigma from its shape parameters as the merge forms it
+ * (FP32 products): out[k] = cost in the sequence of ref_merge_cost.  The
+ * merge itself calls the same function; this entry point exposes it so that
+ * its values can be pinned.
+ */
+void gs2dref_merge_cost(const ref_cfg* cfg, int32_t m, const float* xa, const float* sha,
+                        const float* xb, const float* shb, float* out) {
+  for (int32_t k = 0; k < m; ++k) {
+    float Sa[3], Sb[3];
+    ref_sigma_f(cfg, sha + 3 * (int64_t)k, Sa);
+    ref_sigma_f(cfg, shb + 3 * (int64_t)k, Sb);
+    out[k] = ref_merge_cost(xa + 2 * (int64_t)k, Sa, xb + 2 * (int64_t)k, Sb);
+  }
+}
+
 static int ref_cmp_u64(const void* pa, const void* pb) {
   const uint64_t a = *(const uint64_t*)pa, b = *(const uint64_t*)pb;
   return (a > b) - (a < b);

@@ -7,6 +7,9 @@ per-channel masses preserved for coloured pairs; every merged pair being a
 mutual nearest-neighbour pair under the stated cost (brute force over the
 candidate lists); the merge count; both parameterizations giving the same
 merged covariance; pass-through of culled Gaussians and of max_merges = 0.
+The pairing cost itself is pinned by its closed forms (isotropic and
+axis-aligned pairs, a rotated pair along and across its axes) and by
+double-precision linear algebra on random pairs.
 """
 import numpy as np
 import pytest
@@ -73,19 +76,6 @@ def test_channel_masses_are_kept():
                                render(cfg, xy, sh, rgb).sum((1, 2)), rtol=1e-5)
 
 
-def sigma32(param, sh):
-    """Sigma in FP32 (each product rounded), as the pairing cost uses it."""
-    f = np.float32
-    sh = sh.astype(np.float32)
-    if param == oracle.SCALE_ROT:
-        sn, cs = oracle.sincos_f32(sh[:, 2])
-        x2, y2 = sh[:, 0] * sh[:, 0], sh[:, 1] * sh[:, 1]
-        return np.stack([(cs * cs) * x2 + (sn * sn) * y2, (cs * sn) * (x2 - y2),
-                         (sn * sn) * x2 + (cs * cs) * y2], 1).astype(f)
-    a, b, c = sh.T
-    return np.stack([a * a, a * b, b * b + c * c], 1).astype(f)
-
-
 def sigma(param, sh):
     sh = sh.astype(np.float64)
     if param == oracle.SCALE_ROT:
@@ -97,24 +87,85 @@ def sigma(param, sh):
     return np.stack([a * a, a * b, b * b + c * c], 1)
 
 
+def test_merge_cost_closed_forms():
+    """The pairing cost d^T M^-1 d with M the mean of the two covariances,
+    against its closed forms: two isotropic Gaussians of scale s at distance
+    d give d^2/s^2 in any direction; scales s1 and s2 give 2 d^2/(s1^2 + s2^2);
+    two axis-aligned Gaussians diag(sx^2, sy^2) give dx^2/sx^2 + dy^2/sy^2;
+    a rotated pair gives d^2/sx^2 along its major axis and d^2/sy^2 across
+    it; coincident means cost 0."""
+    ch = oracle.Config(64, 64)
+    cases = []  # (xa, shape a, xb, shape b, expected)
+    for s, d, ang in ((1.0, 2.0, 0.0), (2.5, 3.0, 0.7), (0.8, 0.5, 2.0), (4.0, 10.0, -1.2)):
+        dx, dy = d * np.cos(ang), d * np.sin(ang)
+        cases.append(((10.0, 20.0), (s, 0.0, s), (10.0 + dx, 20.0 + dy), (s, 0.0, s), d * d / (s * s)))
+    for s1, s2, d in ((1.0, 3.0, 2.0), (0.6, 2.2, 1.3)):
+        cases.append(((5.0, 5.0), (s1, 0.0, s1), (5.0, 5.0 + d), (s2, 0.0, s2),
+                      2 * d * d / (s1 * s1 + s2 * s2)))
+    for sx, sy, dx, dy in ((2.0, 0.5, 1.5, 0.25), (1.2, 3.1, -2.0, 4.0)):
+        cases.append(((30.0, 30.0), (sx, 0.0, sy), (30.0 + dx, 30.0 + dy), (sx, 0.0, sy),
+                      dx * dx / (sx * sx) + dy * dy / (sy * sy)))
+    cases.append(((7.0, 9.0), (1.5, 0.4, 2.0), (7.0, 9.0), (0.9, -0.3, 1.1), 0.0))
+    xa, sa, xb, sb, want = (np.array(v, np.float64) for v in zip(*cases))
+    got = oracle.merge_cost(ch, xa, sa, xb, sb).astype(np.float64)
+    np.testing.assert_allclose(got, want, rtol=2e-6, atol=0)
+    # rotated pair (scale-rotation shapes): along the major axis, then across it
+    sr = oracle.Config(64, 64, param=oracle.SCALE_ROT)
+    th, sx, sy, d = 0.6, 3.0, 1.0, 2.0
+    sn, cs = (float(v[0]) for v in oracle.sincos_f32(np.array([th], np.float32)))
+    xa = np.array([[20.0, 20.0], [20.0, 20.0]])
+    xb = xa + d * np.array([[cs, sn], [-sn, cs]])
+    shp = np.array([[sx, sy, th], [sx, sy, th]])
+    got = oracle.merge_cost(sr, xa, shp, xb, shp).astype(np.float64)
+    np.testing.assert_allclose(got, [d * d / (sx * sx), d * d / (sy * sy)], rtol=1e-5)
+
+
+def test_merge_cost_against_linear_algebra():
+    """Random pairs: the FP32 cost against d^T M^-1 d solved in double by
+    numpy, M = (Sigma_a + Sigma_b) / 2 with Sigma = L L^T (Cholesky) or
+    R diag(s^2) R^T (scale-rotation), within FP32 rounding of the inputs."""
+    rng = np.random.default_rng(12)
+    m = 400
+    for param in (oracle.CHOLESKY, oracle.SCALE_ROT):
+        cfg = oracle.Config(64, 64, param=param)
+        xa = rng.uniform(0, 64, (m, 2))
+        xb = xa + rng.normal(0, 3, (m, 2))
+        if param == oracle.CHOLESKY:
+            sa = np.stack([rng.uniform(0.5, 3, m), rng.normal(0, 0.5, m), rng.uniform(0.5, 3, m)], 1)
+            sb = np.stack([rng.uniform(0.5, 3, m), rng.normal(0, 0.5, m), rng.uniform(0.5, 3, m)], 1)
+        else:
+            sa = np.stack([rng.uniform(0.5, 3, m), rng.uniform(0.5, 3, m), rng.uniform(-3, 3, m)], 1)
+            sb = np.stack([rng.uniform(0.5, 3, m), rng.uniform(0.5, 3, m), rng.uniform(-3, 3, m)], 1)
+        sa, sb = sa.astype(np.float32), sb.astype(np.float32)
+        got = oracle.merge_cost(cfg, xa, sa, xb, sb).astype(np.float64)
+
+        def cov(sh):
+            sh = sh.astype(np.float64)
+            if param == oracle.CHOLESKY:
+                L = np.zeros((m, 2, 2))
+                L[:, 0, 0], L[:, 1, 0], L[:, 1, 1] = sh[:, 0], sh[:, 1], sh[:, 2]
+                return L @ np.transpose(L, (0, 2, 1))
+            c, s = np.cos(sh[:, 2]), np.sin(sh[:, 2])
+            R = np.stack([np.stack([c, -s], -1), np.stack([s, c], -1)], -2)
+            D = np.zeros((m, 2, 2))
+            D[:, 0, 0], D[:, 1, 1] = sh[:, 0] ** 2, sh[:, 1] ** 2
+            return R @ D @ np.transpose(R, (0, 2, 1))
+        M = 0.5 * (cov(sa) + cov(sb))
+        d = (xa.astype(np.float32) - xb.astype(np.float32)).astype(np.float64)
+        want = np.einsum("ki,ki->k", d, np.linalg.solve(M, d[..., None])[..., 0])
+        np.testing.assert_allclose(got, want, rtol=2e-4, atol=1e-5)
+
+
 @pytest.mark.parametrize("param", [oracle.CHOLESKY, oracle.SCALE_ROT])
 def test_pairs_are_mutual_nearest_neighbours(param):
     wl = synth.random_scene(64, 48, 500, seed=131, diag=(0.5, 4.0), margin=3, param=param)
     cfg = oracle.Config(64, 48, param=param)
     s = oracle.Scene(cfg, wl.xy, wl.chol, wl.rgb)
-    S = sigma32(param, wl.chol)
     valid = s.proj.count > 0
-    f = np.float32
 
     def cost(i, j):
-        # the stated reading, in FP32 operation by operation
-        m0, m1, m2 = f(0.5) * (S[i, 0] + S[j, 0]), f(0.5) * (S[i, 1] + S[j, 1]), f(0.5) * (S[i, 2] + S[j, 2])
-        dx, dy = wl.xy[i, 0] - wl.xy[j, 0], wl.xy[i, 1] - wl.xy[j, 1]
-        det = m0 * m2 - m1 * m1
-        if not det > 0:
-            return np.inf
-        num = ((m2 * dx) * dx - ((f(2) * m1) * dx) * dy) + (m0 * dy) * dy
-        return (num if num > 0 else f(0)) / det
+        # the pairing cost, pinned by test_merge_cost_closed_forms
+        return float(oracle.merge_cost(cfg, wl.xy[[i]], wl.chol[[i]], wl.xy[[j]], wl.chol[[j]])[0])
 
     nn = np.full(wl.n, -1)
     for i in np.nonzero(valid)[0]:

@@ -58,6 +58,12 @@ MUTATIONS = [
     ("merge: cost cross-term sign", "((m2 * dx) * dx - ((2.0f * m1) * dx) * dy)",
      "((m2 * dx) * dx + ((2.0f * m1) * dx) * dy)"),
     ("merge: pairs not mutual", "if (j > i && nn[j] == i) {", "if (j > i) {"),
+    ("merge: cost with the sum of the covariances, not their mean",
+     "const float m0 = 0.5f * (Si[0] + Sj[0]), m1 = 0.5f * (Si[1] + Sj[1]), m2 = 0.5f * (Si[2] + Sj[2]);",
+     "const float m0 = (Si[0] + Sj[0]), m1 = (Si[1] + Sj[1]), m2 = (Si[2] + Sj[2]);"),
+    ("merge: cost with one Gaussian's covariance only",
+     "const float m0 = 0.5f * (Si[0] + Sj[0]), m1 = 0.5f * (Si[1] + Sj[1]), m2 = 0.5f * (Si[2] + Sj[2]);",
+     "const float m0 = Si[0], m1 = Si[1], m2 = Si[2];"),
     ("composite lists not depth sorted", "if (cfg->mode == REF_MODE_COMPOSITE) {\n      g_sort_depth = depth;\n      for",
      "if (0) {\n      g_sort_depth = depth;\n      for"),
 ]
@@ -89,6 +95,8 @@ PINS = [
     lambda: merge_pins.test_moments_of_the_image_are_kept(oracle.CHOLESKY),
     merge_pins.test_channel_masses_are_kept,
     lambda: merge_pins.test_pairs_are_mutual_nearest_neighbours(oracle.CHOLESKY),
+    merge_pins.test_merge_cost_closed_forms,
+    merge_pins.test_merge_cost_against_linear_algebra,
 ]
 
 
