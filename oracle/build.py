@@ -23,5 +23,24 @@ def build(force: bool = False) -> str:
     return LIB
 
 
+# The multi-threaded timing driver: the same source compiled with OpenMP
+# around its per-pixel functions (gs2d_oracle_omp.c includes gs2d_oracle.c).
+SRC_OMP = os.path.join(HERE, "gs2d_oracle_omp.c")
+LIB_OMP = os.path.join(HERE, "libgs2d_oracle_omp.so")
+
+
+def build_omp(force: bool = False) -> str:
+    t = os.path.getmtime(LIB_OMP) if os.path.exists(LIB_OMP) else -1.0
+    if not force and t >= max(os.path.getmtime(SRC), os.path.getmtime(SRC_OMP)):
+        return LIB_OMP
+    tmp = LIB_OMP + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC",
+           "-shared", "-Wall", "-Wextra", "-I", HERE, "-o", tmp, SRC_OMP, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB_OMP)
+    return LIB_OMP
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv))
+    print(build_omp(force="--force" in sys.argv))
