@@ -259,8 +259,17 @@ k_tile_scatter(int n, int T, int tiles_x, long long cap, Header* __restrict__ hd
     v[j] = u < T ? R[u] : 0u;
     hb[j] = u < T ? H[size_t(u) * B + blockIdx.x] : 0u;
   }
-  long long before_blocks = 0;  // pairs of the blocks before this one
-  for (int k = tid; k < int(blockIdx.x); k += blockDim.x) before_blocks += block_tot[k];
+  long long before_blocks = 0;  // pairs of the blocks before this one (loads issued 4 at a time)
+  for (int k0 = tid; k0 < int(blockIdx.x); k0 += 4 * blockDim.x) {
+    long long v4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int k = k0 + j * int(blockDim.x);
+      v4[j] = k < int(blockIdx.x) ? block_tot[k] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) before_blocks += v4[j];
+  }
   s_rect[tid] = r;
   long long total;
   const long long excl = block_exclusive_scan_256<long long>(cnt, &total);  // orders the clears

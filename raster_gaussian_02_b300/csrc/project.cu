@@ -65,15 +65,38 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
   }
   if ((d_bg || loss) && blockIdx.x == 0) {  // the first block: its extra work overlaps the rest
     // fixed-order reduction of the per-tile partials
+    // Each thread adds entries tid, tid + 256, ... in that order; the loads of
+    // kBatch entries are issued before their adds, so one round trip serves
+    // kBatch of them.
+    constexpr int kBatch = 8;
     __shared__ float red[4][256];
     float x = 0.f, y = 0.f, z = 0.f, l = 0.f;
     if (d_bg)
-      for (int t = threadIdx.x; t < T; t += blockDim.x) {
-        const float4 v = tile_partials[t];
-        x += v.x; y += v.y; z += v.z;
+      for (int t0 = threadIdx.x; t0 < T; t0 += kBatch * blockDim.x) {
+        float4 v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const int t = t0 + j * blockDim.x;
+          if (t < T) v[j] = tile_partials[t];
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+          if (t0 + j * int(blockDim.x) < T) {
+            x += v[j].x; y += v[j].y; z += v[j].z;
+          }
       }
     if (loss)
-      for (int t = threadIdx.x; t < loss_blocks; t += blockDim.x) l += loss_partials[t];
+      for (int t0 = threadIdx.x; t0 < loss_blocks; t0 += kBatch * blockDim.x) {
+        float v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const int t = t0 + j * blockDim.x;
+          if (t < loss_blocks) v[j] = loss_partials[t];
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+          if (t0 + j * int(blockDim.x) < loss_blocks) l += v[j];
+      }
     red[0][threadIdx.x] = x;
     red[1][threadIdx.x] = y;
     red[2][threadIdx.x] = z;
