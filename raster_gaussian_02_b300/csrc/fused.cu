@@ -29,6 +29,23 @@ struct FusedCompSmem {
   float red[8];
 };
 
+// A tile whose list is longer than kCompSegLen entries gets a second block.
+// Both render the tile (the forward, and with it every touch and termination
+// decision, is the same in each); then block 0 back-propagates the back
+// half of the list and block 1 the front half, starting from the
+// transmittance and colour its forward recorded at the midpoint.  The
+// longest lists' serial chains, which set this kernel's length, lose half
+// their backward part.  Each block writes the pair slots of its own half;
+// block 0 also writes the image, the loss and the background partial.
+// Measured on a B300 at 768x512 / 50K Gaussians (lists up to ~500 entries):
+// 129.9 us unsplit; split above 96 / 128 / 192 / 256 / 320 / 384 entries:
+// 121.7 / 119.6 / 113.5 / 109.4 / 111.4 / 125.8 us; three or four parts per
+// long list were slower (the extra forwards cost more than the shorter
+// backward chains save).  The code takes K = ceil(len / kCompSegLen) parts,
+// at most kCompMaxParts.
+constexpr int kCompSegLen = 256;
+constexpr int kCompMaxParts = 2;
+
 template <bool kAbs>
 __global__ void __launch_bounds__(256)
 k_fused_comp(gs2d_config c, int tiles_x, int n, const Header* __restrict__ hdr, float scale,
@@ -42,7 +59,10 @@ k_fused_comp(gs2d_config c, int tiles_x, int n, const Header* __restrict__ hdr, 
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   FusedCompSmem<kAbs>& sm = *reinterpret_cast<FusedCompSmem<kAbs>*>(smem_raw);
-  const int tile = order ? order[blockIdx.x] : int(blockIdx.x);  // longest lists first when known
+  // kCompMaxParts blocks per tile (its parts), longest lists first when known;
+  // the parts of one tile have adjacent block indices
+  const int part = int(blockIdx.x % kCompMaxParts);
+  const int tile = order ? order[blockIdx.x / kCompMaxParts] : int(blockIdx.x / kCompMaxParts);
   if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile)) return;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -55,10 +75,16 @@ k_fused_comp(gs2d_config c, int tiles_x, int n, const Header* __restrict__ hdr, 
   const long long pairs = hdr->pairs;
   int2 rg = ranges[tile];
   if (!check_ok(rg.x >= 0 && rg.x <= rg.y && rg.y <= pairs, kCheckRange)) rg = make_int2(0, 0);
+  const int len = rg.y - rg.x;
+  const int parts = min(kCompMaxParts, max(1, (len + kCompSegLen - 1) / kCompSegLen));
+  if (part >= parts) return;  // the whole block: no barrier reached yet
+  // this block's segment [lo, hi) of the list, segments counted from the back
+  const int lo = int((long long)(parts - 1 - part) * len / parts);
+  const int hi = int((long long)(parts - part) * len / parts);
   // every thread has passed its last read of the forward's staging area when
   // comp_tile_forward returns (each round ends at a block barrier)
-  const CompFwdOut o = comp_tile_forward(sm.u.f, c, rg, bx0, by0, pxf, pyf, inside, kk, n, rec,
-                                         sorted_gid);
+  const CompFwdOut o = comp_tile_forward<true>(sm.u.f, c, rg, bx0, by0, pxf, pyf, inside, kk, n, rec,
+                                               sorted_gid, part > 0 ? hi : 0x7fffffff);
   float er = 0.f, eg = 0.f, eb = 0.f;
   if (inside) {
     const size_t HW = size_t(c.width) * c.height;
@@ -69,7 +95,7 @@ k_fused_comp(gs2d_config c, int tiles_x, int n, const Header* __restrict__ hdr, 
       ag = fmaf(o.T, bg[1], ag);
       ab = fmaf(o.T, bg[2], ab);
     }
-    if (image) {
+    if (image && part == 0) {
       image[p] = ar;
       image[HW + p] = ag;
       image[2 * HW + p] = ab;
@@ -78,11 +104,28 @@ k_fused_comp(gs2d_config c, int tiles_x, int n, const Header* __restrict__ hdr, 
     eg = ag - target[HW + p];
     eb = ab - target[2 * HW + p];
   }
-  const float tl = block_sum_ordered<8>(fmaf(eb, eb, fmaf(eg, eg, er * er)), sm.red);
-  if (threadIdx.x == 0) loss_partials[tile] = tl;
-  comp_tile_backward<kAbs>(sm.u.b, c, tile, tx, ty, rg, bx0, by0, pxf, pyf, inside, kk, o.T, o.last,
-                           er * scale, eg * scale, eb * scale, n, pairs, bg, rec, rect, sorted_gid,
-                           offsets, partials, tile_partials);
+  if (part == 0) {
+    const float tl = block_sum_ordered<8>(fmaf(eb, eb, fmaf(eg, eg, er * er)), sm.red);
+    if (threadIdx.x == 0) loss_partials[tile] = tl;
+    // the whole list, or its back segment [lo, len)
+    comp_tile_backward<kAbs>(sm.u.b, c, tile, tx, ty, rg, bx0, by0, pxf, pyf, inside, kk, o.T, o.last,
+                             er * scale, eg * scale, eb * scale, n, pairs, bg, rec, rect, sorted_gid,
+                             offsets, partials, tile_partials, lo);
+  } else {
+    // an earlier segment [lo, hi): behind it lie the transmittance the forward
+    // recorded at hi and the colour the later segments and the background add
+    float Sr = 0.f, Sg = 0.f, Sb = 0.f;
+    if (inside) {
+      const float fr = bg ? fmaf(o.T, bg[0], o.r) : o.r, fg = bg ? fmaf(o.T, bg[1], o.g) : o.g,
+                  fb = bg ? fmaf(o.T, bg[2], o.b) : o.b;
+      Sr = fr - o.mr;
+      Sg = fg - o.mg;
+      Sb = fb - o.mb;
+    }
+    comp_tile_backward<kAbs>(sm.u.b, c, tile, tx, ty, rg, bx0, by0, pxf, pyf, inside, kk, o.Tm, o.last,
+                             er * scale, eg * scale, eb * scale, n, pairs, bg, rec, rect, sorted_gid,
+                             offsets, partials, tile_partials, lo, hi, false, Sr, Sg, Sb);
+  }
 }
 
 }  // namespace
@@ -107,7 +150,7 @@ cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* cho
     auto go = [&](auto kern, size_t smem) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
       if (e != cudaSuccess) return e;
-      return launch(kern, dim3(T), dim3(256), smem, s, c, tiles_x(c), n,
+      return launch(kern, dim3(kCompMaxParts * T), dim3(256), smem, s, c, tiles_x(c), n,
                     reinterpret_cast<const Header*>(ws), scale, r, rc, rg, sorted_gid,
                     offsets, bg, target, image, reinterpret_cast<float4*>(ws + L.partials), tp, lp,
                     L.count_sort ? reinterpret_cast<const int*>(ws + L.tile_order) : nullptr);

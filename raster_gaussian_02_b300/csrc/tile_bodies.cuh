@@ -124,22 +124,31 @@ struct CompFwdOut {
   float r, g, b;  // colour before the background term
   float T;        // transmittance after the last contributor
   int last;       // 1 + list position of the last contributor (0: none)
+  // kMid: the state in front of list position `mid` (after every entry
+  // before it): transmittance and colour so far
+  float Tm, mr, mg, mb;
 };
 
 // Composite forward for the calling thread's pixel (256 threads), front to
 // back in list (depth) order (DrawingWithGaussians README, Overview: alpha
 // compositing over a trainable background):
 //     while T >= t_min: alpha = o_i exp(-q/2); C += rgb_i alpha T; T *= 1 - alpha
-// The caller adds T * background.  Every thread of the block must call it.
+// The caller adds T * background.  kMid: also records the state in front of
+// list position `mid` (CompFwdOut::Tm, mr, mg, mb).  Every thread of the
+// block must call it.
+template <bool kMid = false>
 __device__ __forceinline__ CompFwdOut comp_tile_forward(CompSmem& sm, const gs2d_config& c, int2 rg,
                                                         int bx0, int by0, float pxf, float pyf,
                                                         bool inside, float kk, int n,
                                                         const float4* __restrict__ rec,
-                                                        const int* __restrict__ sorted_gid) {
+                                                        const int* __restrict__ sorted_gid,
+                                                        int mid = 0) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const unsigned int lt = (1u << lane) - 1u, bit = 1u << lane;
   uint2* list = sm.list[warp];
   float ar = 0.f, ag = 0.f, ab = 0.f, T = 1.f;
+  float Tm = 1.f, mr = 0.f, mg = 0.f, mb = 0.f;
+  bool have_mid = false;
   int lst = 0;
   bool done = !inside;
   for (int rb = rg.x; rb < rg.y; rb += 256) {
@@ -173,6 +182,15 @@ __device__ __forceinline__ CompFwdOut comp_tile_forward(CompSmem& sm, const gs2d
       // front to back; the weights of two entries are formed together (they
       // do not depend on T), then the transmittance steps run in order
       auto step = [&](uint2 u, const Staged& s, float q, float w) {
+        if constexpr (kMid) {
+          if (!have_mid && rb - rg.x + int(u.x) >= mid) {  // entries from here on are at or past mid
+            have_mid = true;
+            Tm = T;
+            mr = ar;
+            mg = ag;
+            mb = ab;
+          }
+        }
         if (q <= kk && (u.y & bit) && !done) {
           if (T < c.t_min) {
             done = true;
@@ -207,7 +225,13 @@ __device__ __forceinline__ CompFwdOut comp_tile_forward(CompSmem& sm, const gs2d
     }
     __syncthreads();
   }
-  return CompFwdOut{ar, ag, ab, T, lst};
+  if (kMid && !have_mid) {  // no entry at or past mid reached this pixel's warp
+    Tm = T;
+    mr = ar;
+    mg = ag;
+    mb = ab;
+  }
+  return CompFwdOut{ar, ag, ab, T, lst, Tm, mr, mg, mb};
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -270,9 +294,13 @@ struct CompStage {
 };
 
 // Composite backward for the calling thread's pixel (256 threads), walking
-// the tile's list back to front from the pixel's last contributor.  T is the
-// pixel's final transmittance, lst its last contributor, (gr, gg, gb) its
-// dL/dC.  With alpha = o w, T_i the transmittance in front of Gaussian i and
+// the tile's list back to front from the pixel's last contributor, over the
+// list positions [lo, hi) only (the whole list by default).  T is the
+// transmittance behind position hi - 1 (the pixel's final transmittance when
+// hi is the list's end), (Sr0, Sg0, Sb0) the colour accumulated behind it
+// including T_final * bg (T * bg when hi is the end), lst the pixel's last
+// contributor, (gr, gg, gb) its dL/dC.  with_bg: also write the tile's
+// background partial (T is then the final transmittance).  With alpha = o w, T_i the transmittance in front of Gaussian i and
 // S the colour accumulated behind it (including T_final * bg):
 //     dL/dalpha = sum_k g_k (rgb_k T_i - S_k / (1 - alpha)),
 //     dL/do = w dL/dalpha,  dL/dw = o dL/dalpha,  dL/drgb_k = g_k alpha T_i,
@@ -290,13 +318,14 @@ __device__ __forceinline__ void comp_tile_backward(
     int n, long long pairs, const float* __restrict__ bg, const float4* __restrict__ rec,
     const int4* __restrict__ rect, const int* __restrict__ sorted_gid,
     const int* __restrict__ offsets, float4* __restrict__ partials,
-    float4* __restrict__ tile_partials) {
+    float4* __restrict__ tile_partials, int lo = 0, int hi = 0x7fffffff, bool with_bg = true,
+    float Sr0 = 0.f, float Sg0 = 0.f, float Sb0 = 0.f) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const unsigned int lt = (1u << lane) - 1u, bit = 1u << lane;
   const float bgr = bg ? bg[0] : 0.f, bgg = bg ? bg[1] : 0.f, bgb = bg ? bg[2] : 0.f;
   uint2* list = sm.list[warp];
   // background gradient: T_final * g summed over the tile, fixed order
-  {
+  if (with_bg) {
     const float vr = warp_sum(inside ? T * gr : 0.f);
     const float vg = warp_sum(inside ? T * gg : 0.f);
     const float vb = warp_sum(inside ? T * gb : 0.f);
@@ -316,13 +345,16 @@ __device__ __forceinline__ void comp_tile_backward(
       tile_partials[tile] = make_float4(x, y, z, 0.f);
     }
   }
-  float Sr = T * bgr, Sg = T * bgg, Sb = T * bgb;
+  float Sr = with_bg ? T * bgr : Sr0, Sg = with_bg ? T * bgg : Sg0, Sb = with_bg ? T * bgb : Sb0;
   const int len = rg.y - rg.x;
-  const int nchunks = (len + kCompChunk - 1) / kCompChunk;
-  for (int ci = nchunks - 1; ci >= 0; --ci) {
+  hi = min(hi, len);
+  lo = max(lo, 0);
+  for (int ci = (hi - 1) / kCompChunk; lo < hi && ci >= lo / kCompChunk; --ci) {
     const int cb = rg.x + ci * kCompChunk;
     const int cnt = min(kCompChunk, rg.y - cb);
-    if (tid < cnt) {
+    // the chunk's entries in [lo, hi)
+    const int jlo = max(0, lo - ci * kCompChunk), jhi = min(cnt, hi - ci * kCompChunk);
+    if (tid >= jlo && tid < jhi) {
       int gid = sorted_gid[cb + tid];
       if (!check_ok(gid >= 0 && gid < n, kCheckGaussian)) gid = 0;
       const float4* r = rec + 3 * size_t(gid);
@@ -335,10 +367,10 @@ __device__ __forceinline__ void comp_tile_backward(
     }
     __syncthreads();
     int nl = 0;
-    for (int j0 = 0; j0 < cnt; j0 += 32) {
+    for (int j0 = jlo; j0 < jhi; j0 += 32) {
       const int j = j0 + lane;
       unsigned int m = 0;
-      if (j < cnt) {
+      if (j < jhi) {
         m = box_lanes(sm.box[j], bx0, by0);
         if (!m) {
 #pragma unroll
@@ -431,7 +463,7 @@ __device__ __forceinline__ void comp_tile_backward(
       }
     }
     __syncthreads();
-    if (tid < cnt) {
+    if (tid >= jlo && tid < jhi) {
       float s[kCompVals];
 #pragma unroll
       for (int u = 0; u < kCompVals; ++u) s[u] = 0.f;

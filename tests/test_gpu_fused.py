@@ -134,3 +134,18 @@ def test_heavy_2048x1360_full_size():
     gids = np.sort(rng.choice(valid, size=1500, replace=False)).astype(np.int32)
     ref = s.render_bwd_gaussians(dimg_ref, gids)
     check_grads({k: f["grads"][k][gids] for k in ("xy", "chol", "rgb")}, ref, ("xy", "chol", "rgb"))
+
+
+@pytest.mark.parametrize("k", [250, 262, 520])
+@pytest.mark.parametrize("opacity", [0.08, 0.9])
+def test_composite_long_lists_split_in_two(k, opacity):
+    """Lists around and above the length at which the fused composite kernel
+    splits a tile's backward between two blocks (256 entries): k small
+    Gaussians on one tile, with low opacity (nothing terminates, both halves
+    work) and high opacity (pixels terminate early, many in the front half)."""
+    wl = synth.random_scene(64, 48, k + 200, seed=30 + k, mode=synth.COMPOSITE, diag=(0.5, 1.5))
+    wl.xy[:k] = np.random.default_rng(k).uniform(17, 31, (k, 2)).astype(np.float32)
+    wl.opacity[:k] = opacity
+    f, g, s = fused_parity(wl)
+    lens = s.ranges[:, 1] - s.ranges[:, 0]
+    assert lens.max() >= k - 5  # the crowded tile's list
