@@ -344,8 +344,11 @@ GS2D_API gs2d_status gs2d_merge(const gs2d_config* cfg, int32_t n, const float* 
  *   Limits: 1 <= height, width <= 32768, else GS2D_ERR_INVALID_ARG (every
  *   such image fits the fixed array: the reduction uses at most 1024
  *   blocks).
- *   The first call on each device looks the array's address up
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   The first call on each device (and again the first after a device
+ *   reset, which ends the CUDA context that held the array) looks the
+ *   array's address up (cudaGetSymbolAddress); make that first call before
+ *   any stream capture.  Later calls only compare the current context with
+ *   the one the address belongs to.
  *   All calls on a device share the array: calls that overlap on the GPU
  *   (different streams, no ordering between them) race and give wrong
  *   losses.  Nothing in the array needs clearing between calls: every call

@@ -69,10 +69,14 @@ k_loss_final(int nb, const float* __restrict__ partials, float m, float* __restr
 
 }  // namespace
 
-cudaError_t launch_loss_l2(int h, int w, const float* image, const float* target, float* loss,
-                           float* d_image, unsigned char* ws, cudaStream_t s) {
+namespace {
+
+// The loss's two kernels with the block partial sums in `partials`
+// (kLossMaxBlocks floats): shared by the workspace and the fixed-array
+// entry points, so that both give the same loss bit for bit.
+cudaError_t launch_loss_l2_into(int h, int w, const float* image, const float* target, float* loss,
+                                float* d_image, float* partials, cudaStream_t s) {
   const long long m = 3ll * h * w;
-  float* partials = reinterpret_cast<float*>(ws + kOffLoss);
   const bool vec = (m % 4 == 0) && ((reinterpret_cast<uintptr_t>(image) |
                                      reinterpret_cast<uintptr_t>(target) |
                                      reinterpret_cast<uintptr_t>(d_image)) & 15) == 0;
@@ -87,6 +91,14 @@ cudaError_t launch_loss_l2(int h, int w, const float* image, const float* target
     GS2D_TRY(launch(k_loss_partial<false>, dim3(int(blocks)), dim3(kLossThreads), 0, s, m, image, target, scale, d_image, partials));
   GS2D_TRY(launch(k_loss_final, dim3(1), dim3(kLossThreads), 0, s, int(blocks), partials, float(m), loss));
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_loss_l2(int h, int w, const float* image, const float* target, float* loss,
+                           float* d_image, unsigned char* ws, cudaStream_t s) {
+  return launch_loss_l2_into(h, w, image, target, loss, d_image,
+                             reinterpret_cast<float*>(ws + kOffLoss), s);
 }
 
 }  // namespace gs2d
@@ -111,29 +123,61 @@ namespace gs2d {
 namespace {
 
 constexpr int kMaxDevices = 256;
-std::atomic<float*> g_loss_scratch_addr[kMaxDevices];  // per device, set once
+
+// The array's address is looked up once per device and CUDA context: a
+// device reset (cudaDeviceReset) ends the context that holds the array, and
+// the new context may hold it elsewhere, so a context change triggers a new
+// lookup.  The current context is read with the driver's cuCtxGetCurrent,
+// reached through the runtime (no link against the driver library); that
+// query is allowed during a stream capture, the lookup itself is not.
+struct ScratchSlot {
+  std::atomic<void*> ctx{nullptr};   // the context the address belongs to
+  std::atomic<float*> addr{nullptr};
+};
+ScratchSlot g_loss_scratch_slot[kMaxDevices];
 std::mutex g_loss_scratch_mu;
 
-// The device address of g_loss_scratch on the current device, looked up the
-// first time each device is seen.
+using CtxGetCurrent = int (*)(void**);  // cuCtxGetCurrent(CUcontext*), CUresult 0 = success
+
+CtxGetCurrent ctx_get_current() {
+  static const CtxGetCurrent fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return CtxGetCurrent(nullptr);
+    return reinterpret_cast<CtxGetCurrent>(p);
+  }();
+  return fn;
+}
+
+// The device address of g_loss_scratch in the current device's current context.
 cudaError_t loss_scratch_address(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  float* p = g_loss_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
+  const CtxGetCurrent get = ctx_get_current();
+  void* ctx = nullptr;
+  if (!get || get(&ctx) != 0) return cudaErrorDeviceUninitialized;
+  if (!ctx) {  // no context current yet (a first call, never inside a capture): make one
+    e = cudaFree(nullptr);
+    if (e != cudaSuccess) return e;
+    if (get(&ctx) != 0 || !ctx) return cudaErrorDeviceUninitialized;
+  }
+  ScratchSlot& slot = g_loss_scratch_slot[dev];
+  if (slot.ctx.load(std::memory_order_acquire) != ctx) {
     std::lock_guard<std::mutex> lock(g_loss_scratch_mu);
-    p = g_loss_scratch_addr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
+    if (slot.ctx.load(std::memory_order_acquire) != ctx) {
       void* addr = nullptr;
       e = cudaGetSymbolAddress(&addr, g_loss_scratch);
       if (e != cudaSuccess) return e;
-      p = static_cast<float*>(addr);
-      g_loss_scratch_addr[dev].store(p, std::memory_order_release);
+      slot.addr.store(static_cast<float*>(addr), std::memory_order_relaxed);
+      slot.ctx.store(ctx, std::memory_order_release);  // publishes addr
     }
   }
-  *out = p;
+  *out = slot.addr.load(std::memory_order_relaxed);
   return cudaSuccess;
 }
 
@@ -153,26 +197,8 @@ extern "C" gs2d_status gs2d_loss_l2_noalloc(int32_t height, int32_t width, const
   float* partials = nullptr;
   if (loss_scratch_address(&partials) != cudaSuccess) return GS2D_ERR_CUDA;
   // The same two kernels as gs2d_loss_l2, with the partials in the fixed array.
-  const long long m = 3ll * height * width;
-  const bool vec = (m % 4 == 0) && ((reinterpret_cast<uintptr_t>(image) |
-                                     reinterpret_cast<uintptr_t>(target) |
-                                     reinterpret_cast<uintptr_t>(d_image)) & 15) == 0;
-  const long long work = vec ? m / 4 : m;
-  long long blocks = (work + kLossThreads * 4 - 1) / (kLossThreads * 4);
-  if (blocks < 1) blocks = 1;
-  if (blocks > gs2d::kLossMaxBlocks) blocks = gs2d::kLossMaxBlocks;
-  const float scale = float(2.0 / double(m));
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (vec) {
-    e = launch(k_loss_partial<true>, dim3(int(blocks)), dim3(kLossThreads), 0, s, m, image, target,
-               scale, d_image, partials);
-  } else {
-    e = launch(k_loss_partial<false>, dim3(int(blocks)), dim3(kLossThreads), 0, s, m, image, target,
-               scale, d_image, partials);
-  }
-  if (e != cudaSuccess) return GS2D_ERR_CUDA;
-  e = launch(k_loss_final, dim3(1), dim3(kLossThreads), 0, s, int(blocks), partials, float(m), loss);
-  if (e != cudaSuccess) return GS2D_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? GS2D_OK : GS2D_ERR_CUDA;
+  return launch_loss_l2_into(height, width, image, target, loss, d_image, partials,
+                             reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GS2D_OK
+             : GS2D_ERR_CUDA;
 }
