@@ -417,15 +417,20 @@ class WorkloadRun:
             if a is not None:
                 self.host_pack[o:o + a.size] = np.ascontiguousarray(a, np.float32).ravel()
         self.d_pack = torch.from_numpy(self.host_pack).to(dev)
-        views = [None if a is None else self.d_pack[o:o + a.size].view(a.shape)
-                 for a, o in zip(parts, offs)]
-        self.xy, self.chol, self.rgb, self.depth, self.opac, self.bg, self.target = views
+        self._layout = [None if a is None else (o, a.size, a.shape) for a, o in zip(parts, offs)]
+        self.use_buffer(self.d_pack)
         R = self.R = gs2d.Rasterizer(wl.width, wl.height, wl.n, wl.mode, wl.cutoff_sigma, wl.t_min,
                                      device=dev, param=wl.param)
         R.project(self.xy, self.chol, self.rgb, self.depth, self.opac)
         self.P = R.bin_and_sort(sync=True)
         R._alloc_pairs(int(self.P * 1.25) + 4096)  # headroom, as a fitting loop would keep
         self.fused = path == "fused"
+
+    def use_buffer(self, d_pack):
+        """Points the step's inputs at views of a device buffer laid out like
+        host_pack (calls() made afterwards read from it)."""
+        views = [None if L is None else d_pack[L[0]:L[0] + L[1]].view(L[2]) for L in self._layout]
+        self.xy, self.chol, self.rgb, self.depth, self.opac, self.bg, self.target = views
 
     def calls(self, kind):
         """The library calls of one step of `kind`, as (call name, callable):
@@ -785,16 +790,55 @@ def run_gs2d(args):
         h_out.copy_(out, non_blocking=True)
 
     k4 = max(20, min(args.steps, 500))
-    e2e_ms = w.timed(e2e_step, k4, 5)
-    e2e_val, _ = aggregate_replicas(sum(e2e_ms), k4, world, dev)
+    serial_ms = w.timed(e2e_step, k4, 5)
     # the host link alone: the same input copy without the step
     copy_ms = statistics.median(w.timed(lambda: d_pack.copy_(h_pack, non_blocking=True), k4, 5))
+    # Pipelined, as a training loop runs: two device input buffers; step i's
+    # inputs are copied on a second stream into buffer i % 2 while step i - 1
+    # computes (the copy waits for step i - 2, the last reader of that
+    # buffer); the step waits for its copy, then its loss is read back.
+    d_packs = [d_pack, torch.empty_like(d_pack)]
+    pipe_graphs = []
+    for b in range(2):
+        d_packs[b].copy_(h_pack)
+        w.use_buffer(d_packs[b])
+        pipe_graphs.append(w.graph(w.fn(kind), force=True))
+    w.use_buffer(d_pack)
+    copy_stream = torch.cuda.Stream(device=dev)
+
+    def e2e_pipelined(K):
+        copied = [torch.cuda.Event() for _ in range(K)]
+        done = [torch.cuda.Event() for _ in range(K)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        copy_stream.wait_event(t0)
+        for i in range(K):
+            b = i % 2
+            if i >= 2:
+                copy_stream.wait_event(done[i - 2])
+            with torch.cuda.stream(copy_stream):
+                d_packs[b].copy_(h_pack, non_blocking=True)
+                copied[i].record(copy_stream)
+            stream.wait_event(copied[i])
+            with torch.cuda.stream(stream):
+                pipe_graphs[b]()
+                h_out.copy_(out, non_blocking=True)
+                done[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    e2e_pipelined(5)
+    e2e_total = e2e_pipelined(k4)
+    e2e_val, _ = aggregate_replicas(e2e_total, k4, world, dev)
+    serial_val, _ = aggregate_replicas(sum(serial_ms), k4, world, dev)
 
     # ---- the other workloads (one GPU only): graph-replayed throughput and
     # kernel-time rooflines
     configs = None
     if world == 1 and not args.no_configs:
-        R = out = d_pack = run_step = e2e_step = None  # drop the headline's device buffers
+        R = out = d_pack = d_packs = run_step = e2e_step = pipe_graphs = None  # drop the headline's buffers
         w.release()
         configs = {}
         for name in EXTRA_CONFIGS:
@@ -845,7 +889,12 @@ def run_gs2d(args):
             "roofline_fwd": rl_fwd, "roofline_bwd": rl_bwd,
             "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "h2d_copy_ms": copy_ms,
-                    "h2d_gbs": h2d / (copy_ms * 1e-3) / 1e9},
+                    "h2d_gbs": h2d / (copy_ms * 1e-3) / 1e9, "steps": k4,
+                    "how": "each step copies its inputs from pinned host memory (one buffer) and "
+                           "reads its result back; the copy of step i+1 runs on a second stream "
+                           "into a second device buffer while step i computes",
+                    "serial_value": serial_val,
+                    "serial_how": "copy, step and read-back one after the other on one stream"},
             "gpu_launches": launches * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
