@@ -32,6 +32,7 @@ struct BwdSumSmem {
   int tiles[kBwdThreads];              // the chunk's distinct tiles, in order
   int perm[kBwdThreads];               // processing order (similar boxes side by side)
   unsigned int bucket[256];
+  unsigned int split_end[8];           // per warp: the largest bucket end within the split budget
   int ntiles;
 };
 
@@ -53,9 +54,12 @@ __device__ __forceinline__ int block_inclusive_count_256(int flag, int* total, i
   return before + in_warp;
 }
 
-// One block's rounds of the sum backward (k_render_bwd_sum), kSplit threads
-// per (tile, Gaussian) pair: chunks of kChunkPairs <= 256 / kSplit
-// consecutive pairs.
+// One block's rounds of the sum backward (k_render_bwd_sum) over chunks of
+// kChunkPairs consecutive (tile, Gaussian) pairs.  kSplit: threads per pair
+// -- 1 (chunks of 256), 2 (chunks of 128), or kHybrid (one round, a chunk
+// of 128 < kChunkPairs <= 256 pairs: up to 256 - kChunkPairs of its largest
+// pairs get two threads each, the others one, so that few threads idle).
+constexpr int kHybrid = 3;
 template <bool kAbs, int kSplit>
 __device__ __forceinline__ void bwd_sum_rounds(BwdSumSmem& sm, int* warp_tot, const gs2d_config& c,
                                                int tiles_x, int n_gauss, long long n,
@@ -102,6 +106,11 @@ __device__ __forceinline__ void bwd_sum_rounds(BwdSumSmem& sm, int* warp_tot, co
     }
     sm.bucket[tid] = 0u;
     __syncthreads();
+    // kHybrid: how many of the sorted pairs get two threads.  At most
+    // 256 - chunk, and only whole shape buckets, so that the choice does not
+    // depend on the (atomic) order of the pairs inside a bucket: results stay
+    // bit-reproducible.
+    int nsplit = kSplit == kHybrid ? kBwdThreads - kChunkPairs : 0;
     if (ntiles <= kStageTiles) {
       if (tid < kChunkPairs) atomicAdd(&sm.bucket[key], 1u);
       __syncthreads();
@@ -122,7 +131,20 @@ __device__ __forceinline__ void bwd_sum_rounds(BwdSumSmem& sm, int* warp_tot, co
         if (w < warp) before += unsigned(warp_tot[w]);
       __syncthreads();
       sm.bucket[tid] = before + incl - cnt;
+      if constexpr (kSplit == kHybrid) {
+        const unsigned int end = before + incl;  // where bucket tid ends in sorted order
+        unsigned int e = end <= unsigned(nsplit) ? end : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) e = max(e, __shfl_xor_sync(0xffffffffu, e, o));
+        if (lane == 0) sm.split_end[warp] = e;
+      }
       __syncthreads();
+      if constexpr (kSplit == kHybrid) {
+        unsigned int e = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) e = max(e, sm.split_end[w]);
+        nsplit = int(e);
+      }
       if (tid < kChunkPairs) {
         const unsigned int pos = atomicAdd(&sm.bucket[key], 1u);
         sm.perm[pos] = tid;
@@ -134,8 +156,20 @@ __device__ __forceinline__ void bwd_sum_rounds(BwdSumSmem& sm, int* warp_tot, co
 
     const size_t HW = size_t(c.width) * c.height;
     const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
-    const bool in_chunk = tid / kSplit < kChunkPairs;
-    const int me = in_chunk ? sm.perm[tid / kSplit] : 0, half = tid % kSplit;
+    // the pair this thread walks (perm: the shape sort's order, largest
+    // boxes first), which of its rows (half), and the row step
+    int me = 0, half = 0, step = 1;
+    bool in_chunk = true;
+    if (kSplit == 1) {
+      me = sm.perm[tid];
+    } else if (kSplit == 2 || tid < 2 * nsplit) {
+      me = sm.perm[tid >> 1];
+      half = tid & 1;
+      step = 2;
+    } else {
+      in_chunk = tid - nsplit < kChunkPairs;  // the threads left over idle
+      me = in_chunk ? sm.perm[tid - nsplit] : 0;
+    }
     const bool mine_valid = in_chunk && (k0 + me) < n;
     for (int t0 = 0; t0 < ntiles; t0 += kStageTiles) {
       const int nst = min(kStageTiles, ntiles - t0);
@@ -168,7 +202,7 @@ __device__ __forceinline__ void bwd_sum_rounds(BwdSumSmem& sm, int* warp_tot, co
         const int xa = max(int(box_lo(bx)), X0), xb = min(int(box_hi(bx)), X0 + kTile - 1);
         const int ya = max(int(box_lo(by)), Y0), yb = min(int(box_hi(by)), Y0 + kTile - 1);
         const float4* gt = sm.g[ms];
-        for (int y = ya + half; y <= yb; y += kSplit) {
+        for (int y = ya + half; y <= yb; y += (kSplit == kHybrid ? step : kSplit)) {
           const float dy = __fsub_rn(float(y) + 0.5f, my);
           const float b2dy = __fmul_rn(B2, dy);
           const float cdydy = __fmul_rn(__fmul_rn(C, dy), dy);
@@ -203,10 +237,13 @@ __device__ __forceinline__ void bwd_sum_rounds(BwdSumSmem& sm, int* warp_tot, co
           Syy = fmaf(r0 * dy, dy, Syy);
         }
       }
-      if constexpr (kSplit == 2) {  // the two halves' sums, even rows + odd rows
+      if constexpr (kSplit != 1) {  // a split pair's two halves: even rows + odd rows
         float* vv[10] = {&sr, &sg, &sb, &Sx, &Sy, &Sxx, &Sxy, &Syy, &ax, &ay};
 #pragma unroll
-        for (int u = 0; u < (kAbs ? 10 : 8); ++u) *vv[u] += __shfl_xor_sync(0xffffffffu, *vv[u], 1);
+        for (int u = 0; u < (kAbs ? 10 : 8); ++u) {
+          const float o = __shfl_xor_sync(0xffffffffu, *vv[u], 1);
+          if (step == 2) *vv[u] += o;
+        }
       }
       if (act && half == 0) {
         const int gid_me = sm.gid[me];
@@ -233,10 +270,12 @@ __device__ __forceinline__ void bwd_sum_rounds(BwdSumSmem& sm, int* warp_tot, co
 //   P <= 128 G:  two adjacent threads share each pair, one taking its even
 //                rows and one its odd rows, and add their sums with one
 //                shuffle (fixed order); 128-pair chunks;
-//   P <= 256 G:  one thread per pair, chunks of ceil(P / G) pairs, so that
-//                every block has exactly one round (measured on a B300 at
-//                768x512 / 50K Gaussians, 117K pairs: 25.4 -> 23.4 us against
-//                two threads per pair in 1.55 rounds);
+//   P <= 256 G:  chunks of ceil(P / G) pairs, so that every block has
+//                exactly one round (measured on a B300 at 768x512 / 50K
+//                Gaussians, 117K pairs: 25.4 -> 23.4 us against two threads
+//                per pair in 1.55 rounds); up to 256 - chunk of the largest
+//                pairs (whole shape buckets) get two threads each and the
+//                rest one, so few threads idle (step 65.8 -> 64.1 us);
 //   otherwise:   one thread per pair, 256-pair chunks.  kAbs: also the absgrad sums over the pair's
 // pixels of |t (A dx + B dy)| and |t (B dx + C dy)| (each pixel's share of
 // dL/dmu in absolute value), in a third float4 of the pair's slot.
@@ -258,10 +297,12 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, int n_gauss, const Header* __restri
   if (n <= G * (kBwdThreads / 2))
     bwd_sum_rounds<kAbs, 2>(sm, warp_tot, c, tiles_x, n_gauss, n, hdr, ws, rec, rect, sorted_gid,
                             offsets, d_image, partials, kBwdThreads / 2);
+  else if (n <= G * kBwdThreads)
+    bwd_sum_rounds<kAbs, kHybrid>(sm, warp_tot, c, tiles_x, n_gauss, n, hdr, ws, rec, rect,
+                                  sorted_gid, offsets, d_image, partials, int((n + G - 1) / G));
   else
     bwd_sum_rounds<kAbs, 1>(sm, warp_tot, c, tiles_x, n_gauss, n, hdr, ws, rec, rect, sorted_gid,
-                            offsets, d_image, partials,
-                            n <= G * kBwdThreads ? int((n + G - 1) / G) : kBwdThreads);
+                            offsets, d_image, partials, kBwdThreads);
 }
 
 constexpr int kBwdCompThreads = 256;
