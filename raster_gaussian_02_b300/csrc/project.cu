@@ -31,6 +31,8 @@ k_project(gs2d_config c, int n, const float* __restrict__ xy, const float* __res
 // partials (composite, d_bg non-null) and the fused pass's per-block loss
 // partials (loss non-null; the total is divided by m, the number of image
 // values).
+constexpr int kWarpSlots = 32;
+
 template <bool kComposite, bool kAbs>
 __global__ void __launch_bounds__(256)
 k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
@@ -41,28 +43,76 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
          float* __restrict__ d_bg, const float* __restrict__ loss_partials, int loss_blocks,
          float* __restrict__ loss, float m, int param, float sc, float* __restrict__ d_xy_abs) {
   pdl_enter();
+  constexpr int kStride = (kComposite || kAbs) ? 3 : 2;  // float4 per pair slot
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
   const bool bad = (hdr->flags & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) != 0;
+  // every per-Gaussian load is issued up front, so one round trip precedes
+  // the partial slots' reads
+  int4 rc = make_int4(0, 0, -1, -1);
+  int off = 0;
+  float A = 0.f;
+  float3 shp = make_float3(0.f, 0.f, 0.f);
   if (i < n) {
-    // every per-Gaussian load is issued up front, so one round trip precedes
-    // the partial slots' reads
-    const int4 rc = rect[i];
-    const int off = offsets[i];
-    const float A = rec[3 * size_t(i)].z;
-    const float3 shp = make_float3(chol[3 * i], chol[3 * i + 1], chol[3 * i + 2]);
-    const int cnt = (rc.z >= rc.x) ? (rc.z - rc.x + 1) * (rc.w - rc.y + 1) : 0;
-    float s[9] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float ax = 0.f, ay = 0.f;
-    const bool ok = !bad && cnt > 0 && check_ok(off >= 0 && off + (long long)cnt <= hdr->pairs, kCheckPartial);
-    if (ok) {
-      if constexpr (kComposite || kAbs)
-        sum_pair_partials<3, kComposite, kAbs>(partials + size_t(off) * 3, cnt, s, ax, ay);
-      else
-        sum_pair_partials<2, false, false>(partials + size_t(off) * 2, cnt, s, ax, ay);
+    rc = rect[i];
+    off = offsets[i];
+    A = rec[3 * size_t(i)].z;
+    shp = make_float3(chol[3 * i], chol[3 * i + 1], chol[3 * i + 2]);
+  }
+  const int cnt = (rc.z >= rc.x) ? (rc.z - rc.x + 1) * (rc.w - rc.y + 1) : 0;
+  float s[9] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float ax = 0.f, ay = 0.f;
+  const bool ok = i < n && !bad && cnt > 0 &&
+                  check_ok(off >= 0 && off + (long long)cnt <= hdr->pairs, kCheckPartial);
+  // A Gaussian with more than kWarpSlots slots (a large one, over many tiles)
+  // is summed by its whole warp: lane l adds slots l, l + 32, ... in order,
+  // then the lanes' sums are added in a fixed butterfly.  Alone, one thread's
+  // chain through a few hundred slots set the kernel's length.
+  const bool big = ok && cnt > kWarpSlots;
+  if (ok && !big) sum_pair_partials<kStride, kComposite, kAbs>(partials + size_t(off) * kStride, cnt, s, ax, ay);
+  for (unsigned int todo = __ballot_sync(0xffffffffu, big); todo; todo &= todo - 1) {
+    const int src = __ffs(todo) - 1;
+    const int boff = __shfl_sync(0xffffffffu, off, src), bcnt = __shfl_sync(0xffffffffu, cnt, src);
+    float t[9] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float tx = 0.f, ty = 0.f;
+    for (int k0 = lane; k0 < bcnt; k0 += 4 * 32) {
+      float4 q[4][kStride];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (k0 + 32 * j < bcnt)
+#pragma unroll
+          for (int u = 0; u < kStride; ++u) q[j][u] = partials[size_t(boff + k0 + 32 * j) * kStride + u];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (k0 + 32 * j >= bcnt) break;
+        t[0] += q[j][0].x; t[1] += q[j][0].y; t[2] += q[j][0].z; t[3] += q[j][0].w;
+        t[4] += q[j][1].x; t[5] += q[j][1].y; t[6] += q[j][1].z; t[7] += q[j][1].w;
+        if constexpr (kComposite || kAbs) {
+          if (kComposite) t[8] += q[j][kStride - 1].x;
+          if (kAbs) {
+            tx += q[j][kStride - 1].y;
+            ty += q[j][kStride - 1].z;
+          }
+        }
+      }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int u = 0; u < 9; ++u) t[u] += __shfl_xor_sync(0xffffffffu, t[u], o);
+      tx += __shfl_xor_sync(0xffffffffu, tx, o);
+      ty += __shfl_xor_sync(0xffffffffu, ty, o);
+    }
+    if (lane == src) {
+#pragma unroll
+      for (int u = 0; u < 9; ++u) s[u] = t[u];
+      ax = tx;
+      ay = ty;
+    }
+  }
+  if (i < n)
     write_gaussian_grads(i, ok, s, ax, ay, A, shp, param, sc, d_xy, d_chol, d_rgb,
                          kComposite ? d_opacity : nullptr, kAbs ? d_xy_abs : nullptr);
-  }
   if ((d_bg || loss) && blockIdx.x == 0) {  // the first block: its extra work overlaps the rest
     // fixed-order reduction of the per-tile partials
     // Each thread adds entries tid, tid + 256, ... in that order; the loads of
