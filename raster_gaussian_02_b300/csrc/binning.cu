@@ -2,9 +2,10 @@
 // another block.  With few tiles the counting sort further down is taken
 // (composite: then a per-tile depth sort); otherwise:
 //
-//   k_count_scan   sum of the tile counts of every 256-Gaussian block; the
-//                  last block to finish scans the block sums into block
-//                  offsets and writes the pair count P (and the flags).
+//   k_count_scan   sum of the tile counts of every 256-Gaussian block (eight
+//                  such blocks per thread block); the last thread block to
+//                  finish scans the sums into block offsets and writes the
+//                  pair count P (and the flags).
 //   k_emit         per block: Gaussian pair offsets, then the (key, Gaussian
 //                  index) pairs of its Gaussians in index order -- key = tile
 //                  id (sum) or (tile id << 32 | depth key) (composite) -- plus
@@ -81,32 +82,52 @@ __device__ __forceinline__ long long usable_pairs(const Header* hdr, long long c
 template <bool kComposite>
 using KeyOf = typename std::conditional<kComposite, unsigned long long, unsigned int>::type;
 
-// Called by every thread of every block once the block's pair total is
-// known: the last block to arrive scans all block totals into block offsets
-// and writes P, the flags and the offset of the final keys.
-__device__ __forceinline__ void finish_block_totals(long long total, Header* hdr,
-                                                    long long* __restrict__ block_off, long long cap,
+// Called by every thread of every block once the block has written its
+// sub-block totals (each writer fenced its write): the last block to arrive
+// scans all nsub totals into exclusive offsets and writes P, the flags and the
+// offset of the final keys.
+__device__ __forceinline__ void finish_block_totals(Header* hdr, long long* __restrict__ block_off,
+                                                    long long nsub, long long cap,
                                                     unsigned long long keys_final) {
   const int tid = threadIdx.x;
   __shared__ bool last;
+  __syncthreads();
   if (tid == 0) {
-    block_off[blockIdx.x] = total;
     __threadfence();
     last = atomicAdd(&hdr->blocks_done, 1u) == gridDim.x - 1;
   }
   __syncthreads();
   if (!last) return;
-  // The last block: exclusive scan of all block sums, in chunks of 256.
+  // The last block: exclusive scan of all block sums.  Thread t takes the
+  // contiguous run [t per, (t + 1) per), loads it 8 at a time, and one block
+  // scan of the runs' sums gives every run's start (a scan per chunk of 256
+  // sums, each behind its own loads and barriers, made this block the
+  // kernel's tail at 2M Gaussians).
   __threadfence();
   const volatile long long* bo = block_off;
-  long long carry = 0;
-  for (long long b0 = 0; b0 < gridDim.x; b0 += kScanThreads) {
-    const long long b = b0 + tid;
-    const long long v = (b < gridDim.x) ? bo[b] : 0;
-    long long chunk;
-    const long long ex = block_exclusive_scan_256<long long>(v, &chunk);
-    if (b < gridDim.x) block_off[b] = carry + ex;
-    carry += chunk;
+  const long long B = nsub;
+  const long long per = (B + kScanThreads - 1) / kScanThreads;
+  const long long a = tid * per, b = a + per < B ? a + per : B;
+  long long sum = 0;
+  for (long long p0 = a; p0 < b; p0 += 8) {
+    long long v8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v8[j] = (p0 + j < b) ? bo[p0 + j] : 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sum += v8[j];
+  }
+  long long carry;
+  long long run = block_exclusive_scan_256<long long>(sum, &carry);
+  for (long long p0 = a; p0 < b; p0 += 8) {
+    long long v8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v8[j] = (p0 + j < b) ? bo[p0 + j] : 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (p0 + j < b) {
+        block_off[p0 + j] = run;
+        run += v8[j];
+      }
   }
   if (tid == 0) {
     hdr->pairs = carry;
@@ -118,24 +139,51 @@ __device__ __forceinline__ void finish_block_totals(long long total, Header* hdr
   }
 }
 
-// Block sums of the tile counts; the last block scans them.  Also clears the
-// count tables and the tile ranges for the kernels that follow.
+// Sums of the tile counts of every 256-Gaussian sub-block (kCountSubs of
+// them per block, so that only one block in kCountSubs takes a turn at the
+// arrival counter: with one block per sub-block, the 7,813 atomics of 2M
+// Gaussians on that one address set the kernel's length); the last block
+// scans them.  Also clears the count tables and the tile ranges for the
+// kernels that follow.
+constexpr int kCountSubs = 8;
+
 __global__ void __launch_bounds__(kScanThreads)
 k_count_scan(int n, long long cap, const int* __restrict__ count, Header* hdr,
              long long* __restrict__ block_off, unsigned int* __restrict__ zero_a,
              long long zero_a_words, unsigned int* __restrict__ zero_b, long long zero_b_words,
              unsigned long long keys_final) {
   pdl_enter();
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long gstride = (long long)gridDim.x * blockDim.x;
   for (long long k = (long long)blockIdx.x * blockDim.x + tid; k < zero_a_words; k += gstride)
     zero_a[k] = 0u;
   for (long long k = (long long)blockIdx.x * blockDim.x + tid; k < zero_b_words; k += gstride)
     zero_b[k] = 0u;
-  const long long g = (long long)blockIdx.x * kScanItems + tid;
-  long long total;
-  block_exclusive_scan_256<long long>((g < n) ? count[g] : 0, &total);
-  finish_block_totals(total, hdr, block_off, cap, keys_final);
+  __shared__ long long s_sum[kCountSubs][kScanThreads / 32];
+  const long long nsub = (n + kScanItems - 1) / kScanItems;
+  const long long sub0 = (long long)blockIdx.x * kCountSubs;
+  int c[kCountSubs];
+#pragma unroll
+  for (int j = 0; j < kCountSubs; ++j) {
+    const long long g = (sub0 + j) * kScanItems + tid;
+    c[j] = g < n ? count[g] : 0;
+  }
+#pragma unroll
+  for (int j = 0; j < kCountSubs; ++j) {
+    long long v = c[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) s_sum[j][warp] = v;
+  }
+  __syncthreads();
+  if (tid < kCountSubs && sub0 + tid < nsub) {
+    long long t = 0;
+#pragma unroll
+    for (int w = 0; w < kScanThreads / 32; ++w) t += s_sum[tid][w];
+    block_off[sub0 + tid] = t;
+    __threadfence();
+  }
+  finish_block_totals(hdr, block_off, nsub, cap, keys_final);
 }
 
 // ---------------------------------------------------------------------------
@@ -475,14 +523,27 @@ k_digit_offsets(int pass, long long cap, long long partitions, long long partiti
   const long long per = (partitions + blockDim.x - 1) / blockDim.x;
   const long long a = (long long)tid * per;
   const long long b = a + per < partitions ? a + per : partitions;
+  // the thread's run of counts, loaded 8 at a time (one round trip per 8)
   unsigned int sum = 0;
-  for (long long p = a; p < b; ++p) sum += row[p];
+  for (long long p0 = a; p0 < b; p0 += 8) {
+    unsigned int c8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) c8[j] = (p0 + j < b) ? row[p0 + j] : 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sum += c8[j];
+  }
   unsigned int tot;
   unsigned int run = dstart + block_exclusive_scan_256<unsigned int>(sum, &tot);
-  for (long long p = a; p < b; ++p) {
-    const unsigned int c = row[p];
-    row[p] = run;
-    run += c;
+  for (long long p0 = a; p0 < b; p0 += 8) {
+    unsigned int c8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) c8[j] = (p0 + j < b) ? row[p0 + j] : 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (p0 + j < b) {
+        row[p0 + j] = run;
+        run += c8[j];
+      }
   }
 }
 
@@ -739,7 +800,7 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const ProjectIn* proj,
     GS2D_TRY(launch_project(c, n, proj->xy, proj->shape, proj->rgb, proj->depth, proj->opacity, rec,
                             rect, count, s));
   GS2D_TRY(cudaMemsetAsync(ws, 0, kOffScan, s));  // header and histograms
-  GS2D_TRY(launch(k_count_scan, dim3(blocks), dim3(kScanThreads), 0, s, n, cap, count, hdr, block_off, tables,
+  GS2D_TRY(launch(k_count_scan, dim3((blocks + kCountSubs - 1) / kCountSubs), dim3(kScanThreads), 0, s, n, cap, count, hdr, block_off, tables,
                                                L.passes * table_words,
                                                reinterpret_cast<unsigned int*>(tile_ranges), 2ll * T,
                                                (unsigned long long)keys_final));
