@@ -23,6 +23,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import sys
 import threading
@@ -330,12 +331,23 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ gs2d ---
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources a kernel is compiled from: the .cu file that
+    defines it and every shared header.  A stored traffic figure is used only
+    while this matches, so editing one kernel voids only its own figures."""
+    base = kernel.split("<", 1)[0]
+    pat = re.compile(r"__global__[^;{]*?\b" + re.escape(base) + r"\s*\(", re.S)
     h = hashlib.sha256()
+    found = False
     for name in sorted(os.listdir(CSRC)):
         with open(os.path.join(CSRC, name), "rb") as f:
-            h.update(name.encode() + f.read())
-    return h.hexdigest()[:16]
+            text = f.read()
+        if name.endswith(".cuh"):
+            h.update(name.encode() + text)
+        elif name.endswith(".cu") and pat.search(text.decode()):
+            h.update(name.encode() + text)
+            found = True
+    return h.hexdigest()[:16] if found else ""
 
 
 def kernel_kind(name: str):
@@ -636,6 +648,13 @@ def first_of(kernels, kinds):
     return None
 
 
+def stored_traffic(db, kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from an ncu capture,
+    or None when none was taken or the kernel's sources changed since."""
+    tr = db.get(f"{kernel}:{workload}")
+    return tr["bytes"] if tr and tr.get("source_hash") == kernel_source_hash(kernel) else None
+
+
 def measure_config(name, dev, stream, flush_buf, peaks, counts, steps, warm, reps, cpu=False):
     """Graph-replayed throughput and a kernel-time roofline of one workload."""
     t0 = time.perf_counter()
@@ -653,14 +672,17 @@ def measure_config(name, dev, stream, flush_buf, peaks, counts, steps, warm, rep
         out["render_fps"] = 1e3 / render_ms
     out["cached_render_fps"] = 1e3 / statistics.median(w.timed(w.graph(w.fn("cached")), steps, warm))
     tp = (counts.get(name) or {}).get("touching_pairs")
+    traffic_db = load_json(TRAFFIC) or {}
     dom = dominant_raster(kernels)
     if dom:
-        out["roofline"] = roofline(peaks, dom[0], dom[1], tp, step_ms=step_ms)
+        out["roofline"] = roofline(peaks, dom[0], dom[1], tp, stored_traffic(traffic_db, dom[0], name),
+                                   step_ms=step_ms)
     if not w.fwd_only:
         rk, _, _ = w.traced("render", reps)
         f = first_of(rk, ("fwd_sum", "fwd_comp"))
         if f:
-            out["roofline_fwd"] = roofline(peaks, f[0], f[1], tp, step_ms=render_ms)
+            out["roofline_fwd"] = roofline(peaks, f[0], f[1], tp, stored_traffic(traffic_db, f[0], name),
+                                           step_ms=render_ms)
     w.release()
     if cpu:
         out["cpu_baseline"] = cpu_config(w.wl)
@@ -750,13 +772,11 @@ def run_gs2d(args):
     probe["fp32_of_derived"] = probe["fp32_tflops"] / peaks.fp32
     probe["ex2_of_derived"] = probe["ex2_per_s"] / peaks.sfu
     traffic_db = load_json(TRAFFIC) or {}
-    src_hash = kernel_source_hash()
     # the stored counts are for rank 0's seed
     tp = (counts.get(args.workload) or {}).get("touching_pairs") if rank == 0 else None
 
     def traffic(kernel):
-        tr = traffic_db.get(f"{kernel}:{args.workload}")
-        return tr["bytes"] if tr and tr.get("source_hash") == src_hash else None
+        return stored_traffic(traffic_db, kernel, args.workload)
 
     dom = dominant_raster(kernels)
     rl = roofline(peaks, dom[0], dom[1], tp, traffic(dom[0]), step_ms=med_step) if dom else None

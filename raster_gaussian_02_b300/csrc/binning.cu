@@ -17,8 +17,10 @@
 //                      output offset for that digit;
 //     k_radix_count    (passes after the first) digit counts of every
 //                      partition of the pass's input;
-//     k_radix_scatter  per partition: stable ranks within the partition (warp
-//                      match + per-warp counts) and the scatter.
+//     k_radix_scatter  per partition: stable ranks within the partition (lane
+//                      groups by digit from ballots + per-warp counts), the
+//                      keys reordered by digit in shared memory, and the
+//                      scatter from there in runs of consecutive slots.
 //   k_tile_bounds  [start, end) of every non-empty tile from the places where
 //                  the tile id changes along the sorted keys (empty tiles keep
 //                  the [0, 0) written by k_count_scan).
@@ -563,6 +565,9 @@ k_radix_scatter(int pass, long long cap, long long partitions4, bool own_offsets
   constexpr int kItems = kRadixThreads * kPerThread;
   __shared__ unsigned short s_whist[8][kMaxRadix];  // per-warp counts, then exclusive offsets
   __shared__ unsigned int s_base[kMaxRadix];
+  __shared__ Key s_k[kItems];            // the partition's keys in output order
+  __shared__ unsigned int s_v[kItems];
+  __shared__ unsigned int s_dstart[kMaxRadix];  // where each digit's run starts in s_k
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long n = usable_pairs(hdr, cap);
   const long long part = blockIdx.x;
@@ -621,24 +626,42 @@ k_radix_scatter(int pass, long long cap, long long partitions4, bool own_offsets
     rank[j] = prev + __popc(peers & lt);
   }
   __syncthreads();
+  // The keys are first placed in shared memory in their output order (digit
+  // by digit) and then written out from there, so that consecutive threads
+  // store consecutive slots of a digit's run: one slot per lane scattered over
+  // ~28 runs per store took 4096x4096 / 2M from 149.2 to 104.1 us for both
+  // passes.  Same positions as a direct scatter, so the lists are unchanged.
+  unsigned int dtot = 0;
   {  // per digit (one per thread): exclusive offsets across warps
-    unsigned int r = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
       const unsigned int c = s_whist[w][tid];
-      s_whist[w][tid] = (unsigned short)r;
-      r += c;
+      s_whist[w][tid] = (unsigned short)dtot;
+      dtot += c;
     }
   }
+  unsigned int all;
+  s_dstart[tid] = block_exclusive_scan_256<unsigned int>(dtot, &all);
   __syncthreads();
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
     if (d[j] < 256u) {
-      const unsigned int dst = s_base[d[j]] + s_whist[warp][d[j]] + rank[j];
-      if (check_ok((long long)dst < cap, kCheckPairSlot)) {
-        keys_out[dst] = k[j];
-        vals_out[dst] = v[j];
+      const unsigned int lpos = s_dstart[d[j]] + s_whist[warp][d[j]] + rank[j];
+      if (check_ok(lpos < unsigned(kItems), kCheckPairSlot)) {
+        s_k[lpos] = k[j];
+        s_v[lpos] = v[j];
       }
+    }
+  }
+  __syncthreads();
+  const int cnt = int(n - base < kItems ? n - base : kItems);
+  for (int i = tid; i < cnt; i += kRadixThreads) {
+    const Key kk = s_k[i];
+    const unsigned int dd = unsigned(kk >> shift) & 255u;
+    const unsigned int dst = s_base[dd] + (unsigned(i) - s_dstart[dd]);
+    if (check_ok((long long)dst < cap, kCheckPairSlot)) {
+      keys_out[dst] = kk;
+      vals_out[dst] = s_v[i];
     }
   }
 }

@@ -252,6 +252,17 @@ def heavy_2048x1360(seed: int = 3000, n: int = 300_000) -> Workload:
                     cholesky_heavy_tail(n, rng), _rgb(n, rng), tgt)
 
 
+def heavy_1024x680(seed: int = 3000, n: int = 75_000) -> Workload:
+    """A quarter of heavy_2048x1360 (half the width and height, a quarter of
+    the Gaussians; the same target lattice, density and size distribution),
+    small enough for profiler captures of the same kernels."""
+    rng = np.random.default_rng(seed)
+    h, w = 680, 1024
+    tgt = target_noise_polygons(h, w, rng, lattice_scale=2048 / 768)
+    return Workload("heavy_1024x680_75k", w, h, SUM, positions_by_gradient(n, tgt, rng),
+                    cholesky_heavy_tail(n, rng), _rgb(n, rng), tgt)
+
+
 def image_768x512_sr(seed: int = 2000, n: int = 50_000) -> Workload:
     """The 768x512 workload with scale-rotation shapes: scales U(0.7,2.5) px,
     rotation U(-pi, pi)."""
@@ -340,6 +351,7 @@ WORKLOADS = {
     "small_64x64_1k": small_64x64,
     "image_768x512_50k": image_768x512,
     "heavy_2048x1360_300k": heavy_2048x1360,
+    "heavy_1024x680_75k": heavy_1024x680,
     "image_768x512_50k_sr": image_768x512_sr,
     "heavy_2048x1360_300k_sr": heavy_2048x1360_sr,
     "composite_768x512_50k": composite_768x512,
