@@ -22,10 +22,14 @@ namespace gs2d {
 namespace {
 
 constexpr int kBwdThreads = 256;  // threads per block; pairs per block round: at most 256 / kSplit
-constexpr int kStageTiles = 8;     // tiles of dL/dC staged at a time
-
+// Tiles of dL/dC staged at a time (kStage): 8 with at most 2048 tiles, where
+// a one-round chunk of up to 256 pairs spans several tiles (with 6, 768x512
+// went 23.4 -> 35.6 us: chunks over more tiles skip the shape sort); 4 on
+// larger images, where a 256-pair chunk spans 2-3 tiles and the smaller
+// footprint leaves the L1 more room (2048x1360: 509.8 -> 500.5 us).
+template <int kStage>
 struct BwdSumSmem {
-  float4 g[kStageTiles][kTilePixels];  // dL/dC of the staged tiles (r, g, b, 0)
+  float4 g[kStage][kTilePixels];  // dL/dC of the staged tiles (r, g, b, 0)
   float4 rec[kBwdThreads][3];          // the chunk's records
   int gid[kBwdThreads];
   int slot[kBwdThreads];               // index of the pair's tile among the chunk's tiles
@@ -60,8 +64,8 @@ __device__ __forceinline__ int block_inclusive_count_256(int flag, int* total, i
 // of 128 < kChunkPairs <= 256 pairs: up to 256 - kChunkPairs of its largest
 // pairs get two threads each, the others one, so that few threads idle).
 constexpr int kHybrid = 3;
-template <bool kAbs, int kSplit>
-__device__ __forceinline__ void bwd_sum_rounds(BwdSumSmem& sm, int* warp_tot, const gs2d_config& c,
+template <bool kAbs, int kSplit, int kStageTiles>
+__device__ __forceinline__ void bwd_sum_rounds(BwdSumSmem<kStageTiles>& sm, int* warp_tot, const gs2d_config& c,
                                                int tiles_x, int n_gauss, long long n,
                                                const Header* __restrict__ hdr,
                                                const unsigned char* __restrict__ ws,
@@ -279,7 +283,7 @@ __device__ __forceinline__ void bwd_sum_rounds(BwdSumSmem& sm, int* warp_tot, co
 //   otherwise:   one thread per pair, 256-pair chunks.  kAbs: also the absgrad sums over the pair's
 // pixels of |t (A dx + B dy)| and |t (B dx + C dy)| (each pixel's share of
 // dL/dmu in absolute value), in a third float4 of the pair's slot.
-template <bool kAbs>
+template <bool kAbs, int kStage>
 __global__ void __launch_bounds__(kBwdThreads, 4)  // 4 per SM: measured best (5 or 6 spill and lose)
 k_render_bwd_sum(gs2d_config c, int tiles_x, int n_gauss, const Header* __restrict__ hdr,
                  const unsigned char* __restrict__ ws, const float4* __restrict__ rec,
@@ -288,20 +292,20 @@ k_render_bwd_sum(gs2d_config c, int tiles_x, int n_gauss, const Header* __restri
                  float4* __restrict__ partials) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  BwdSumSmem& sm = *reinterpret_cast<BwdSumSmem*>(smem_raw);
+  BwdSumSmem<kStage>& sm = *reinterpret_cast<BwdSumSmem<kStage>*>(smem_raw);
   __shared__ int warp_tot[8];
   const unsigned int f = hdr->flags;
   const long long n = (f & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) ? 0
                       : hdr->pairs;
   const long long G = gridDim.x;
   if (n <= G * (kBwdThreads / 2))
-    bwd_sum_rounds<kAbs, 2>(sm, warp_tot, c, tiles_x, n_gauss, n, hdr, ws, rec, rect, sorted_gid,
+    bwd_sum_rounds<kAbs, 2, kStage>(sm, warp_tot, c, tiles_x, n_gauss, n, hdr, ws, rec, rect, sorted_gid,
                             offsets, d_image, partials, kBwdThreads / 2);
   else if (n <= G * kBwdThreads)
-    bwd_sum_rounds<kAbs, kHybrid>(sm, warp_tot, c, tiles_x, n_gauss, n, hdr, ws, rec, rect,
+    bwd_sum_rounds<kAbs, kHybrid, kStage>(sm, warp_tot, c, tiles_x, n_gauss, n, hdr, ws, rec, rect,
                                   sorted_gid, offsets, d_image, partials, int((n + G - 1) / G));
   else
-    bwd_sum_rounds<kAbs, 1>(sm, warp_tot, c, tiles_x, n_gauss, n, hdr, ws, rec, rect, sorted_gid,
+    bwd_sum_rounds<kAbs, 1, kStage>(sm, warp_tot, c, tiles_x, n_gauss, n, hdr, ws, rec, rect, sorted_gid,
                             offsets, d_image, partials, kBwdThreads);
 }
 
@@ -372,8 +376,9 @@ cudaError_t launch_bwd_pairs(const gs2d_config& c, int n, const Layout& L, const
                     reinterpret_cast<float4*>(ws + L.tile_partials),
                     L.count_sort ? reinterpret_cast<const int*>(ws + L.tile_order) : nullptr));
   } else {
-    const size_t smem = sizeof(BwdSumSmem);
-    auto kern = k_render_bwd_sum<kAbs>;
+    const bool wide = T > kCountSortMaxTiles;
+    const size_t smem = wide ? sizeof(BwdSumSmem<4>) : sizeof(BwdSumSmem<8>);
+    auto kern = wide ? k_render_bwd_sum<kAbs, 4> : k_render_bwd_sum<kAbs, 8>;
     GS2D_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
     GS2D_TRY(launch(kern, dim3(4 * sm_count()), dim3(kBwdThreads), smem, s, c, tiles_x(c), n,
                     reinterpret_cast<const Header*>(ws), static_cast<const unsigned char*>(ws), r, rc,
