@@ -9,18 +9,21 @@
 //   k_emit         per block: Gaussian pair offsets, then the (key, Gaussian
 //                  index) pairs of its Gaussians in index order -- key = tile
 //                  id (sum) or (tile id << 32 | depth key) (composite) -- plus
-//                  the digit histograms of every radix pass and the digit
-//                  counts of every 2048-key partition for the first pass.
+//                  the digit counts of every 2048-key partition for the first
+//                  pass.
 //   per radix pass (8-bit digits, least significant first):
-//     k_digit_offsets  per digit: exclusive scan of its partition counts,
-//                      plus the digit's global start -> every partition's
-//                      output offset for that digit;
 //     k_radix_count    (passes after the first) digit counts of every
 //                      partition of the pass's input;
-//     k_radix_scatter  per partition: stable ranks within the partition (lane
-//                      groups by digit from ballots + per-warp counts), the
-//                      keys reordered by digit in shared memory, and the
-//                      scatter from there in runs of consecutive slots.
+//     k_digit_offsets  (more than 128 partitions) per digit: exclusive scan
+//                      of its partition counts and the digit's total;
+//     k_radix_scatter  per partition: each digit's output start (a block
+//                      scan of the digit totals) plus the partition's prefix
+//                      (both summed by the block itself when partitions are
+//                      few), stable
+//                      ranks within the partition (lane groups by digit from
+//                      ballots + per-warp counts), the keys reordered by digit
+//                      in shared memory, and the scatter from there in runs
+//                      of consecutive slots.
 //   k_tile_bounds  [start, end) of every non-empty tile from the places where
 //                  the tile id changes along the sorted keys (empty tiles keep
 //                  the [0, 0) written by k_count_scan).
@@ -145,8 +148,9 @@ __device__ __forceinline__ void finish_block_totals(Header* hdr, long long* __re
 // them per block, so that only one block in kCountSubs takes a turn at the
 // arrival counter: with one block per sub-block, the 7,813 atomics of 2M
 // Gaussians on that one address set the kernel's length); the last block
-// scans them.  Also clears the count tables and the tile ranges for the
-// kernels that follow.
+// scans them.  Also clears the first pass's count table (k_emit adds to it;
+// the later passes' tables are written whole by k_radix_count) and the tile
+// ranges for the kernels that follow.
 constexpr int kCountSubs = 8;
 
 __global__ void __launch_bounds__(kScanThreads)
@@ -432,19 +436,16 @@ __global__ void __launch_bounds__(kScanThreads)
 k_emit(int n, int tiles_x, int passes, long long cap, long long partitions4,
        const int4* __restrict__ rect, const int* __restrict__ count,
        const float4* __restrict__ rec, const long long* __restrict__ block_off,
-       unsigned int* __restrict__ hist, unsigned int* __restrict__ table0,
-       int* __restrict__ offsets, KeyOf<kComposite>* __restrict__ keys,
-       unsigned int* __restrict__ vals) {
+       unsigned int* __restrict__ table0, int* __restrict__ offsets,
+       KeyOf<kComposite>* __restrict__ keys, unsigned int* __restrict__ vals) {
   pdl_enter();
   using Key = KeyOf<kComposite>;
   __shared__ long long s_excl[kScanItems + 1];
   __shared__ int4 s_rect[kScanItems];
   __shared__ unsigned int s_dkey[kComposite ? kScanItems : 1];
-  __shared__ unsigned int s_hist[kMaxPasses][kMaxRadix];
   __shared__ unsigned int s_part[kSpan][kMaxRadix];
   const int tid = threadIdx.x;
   const long long g = (long long)blockIdx.x * kScanItems + tid;
-  for (int k = tid; k < kMaxPasses * kMaxRadix; k += blockDim.x) (&s_hist[0][0])[k] = 0u;
   for (int k = tid; k < kSpan * kMaxRadix; k += blockDim.x) (&s_part[0][0])[k] = 0u;
   const int cnt = (g < n) ? count[g] : 0;
   s_rect[tid] = (g < n) ? rect[g] : make_int4(0, 0, -1, -1);
@@ -478,7 +479,6 @@ k_emit(int n, int tiles_x, int passes, long long cap, long long partitions4,
       key = (Key(tile) << 32) | Key(s_dkey[lo]);
     else
       key = Key(tile);
-    for (int p = 0; p < passes; ++p) atomicAdd(&s_hist[p][unsigned(key >> (8 * p)) & 255u], 1u);
     const long long slot = base + e;
     if (slot < cap) {
       keys[slot] = key;
@@ -494,10 +494,6 @@ k_emit(int n, int tiles_x, int passes, long long cap, long long partitions4,
     }
   }
   __syncthreads();
-  for (int k = tid; k < passes * kMaxRadix; k += blockDim.x) {
-    const unsigned int v = (&s_hist[0][0])[k];
-    if (v) atomicAdd(&hist[k], v);
-  }
   if (passes > 0) {
     for (int k = tid; k < kSpan * kMaxRadix; k += blockDim.x) {
       const unsigned int v = (&s_part[0][0])[k];
@@ -506,21 +502,19 @@ k_emit(int n, int tiles_x, int passes, long long cap, long long partitions4,
   }
 }
 
-// Per digit (one block each): every partition's output offset for the digit
-// = the digit's global start + the counts of the digit in the partitions
-// before it.  Overwrites the counts with the offsets.
+// Per digit (one block each): every used partition's offset for the digit
+// within the digit's run (the counts of the digit in the partitions before
+// it), over the counts it replaces, and the digit's total, to totals[d]
+// (each scatter block scans the totals into the digits' starts: as a
+// last-block tail here the scan cost as much as it saved).
 __global__ void __launch_bounds__(256)
-k_digit_offsets(int pass, long long cap, long long partitions, long long partitions4,
-                const Header* __restrict__ hdr, const unsigned int* __restrict__ hist,
-                unsigned int* __restrict__ table) {
+k_digit_offsets(int pass, long long cap, long long partitions4, const Header* __restrict__ hdr,
+                unsigned int* __restrict__ totals, unsigned int* __restrict__ table) {
   pdl_enter();
   const long long n = usable_pairs(hdr, cap);
   if (n == 0) return;
+  const long long partitions = (n + kPartKeys - 1) / kPartKeys;  // the used ones
   const int d = blockIdx.x, tid = threadIdx.x;
-  // global start of digit d: sum of the histogram below d
-  const unsigned int below = (tid < d) ? hist[pass * kMaxRadix + tid] : 0u;
-  unsigned int dstart;
-  block_exclusive_scan_256<unsigned int>(below, &dstart);
   unsigned int* row = table + (long long)d * partitions4;
   const long long per = (partitions + blockDim.x - 1) / blockDim.x;
   const long long a = (long long)tid * per;
@@ -535,7 +529,8 @@ k_digit_offsets(int pass, long long cap, long long partitions, long long partiti
     for (int j = 0; j < 8; ++j) sum += c8[j];
   }
   unsigned int tot;
-  unsigned int run = dstart + block_exclusive_scan_256<unsigned int>(sum, &tot);
+  unsigned int run = block_exclusive_scan_256<unsigned int>(sum, &tot);
+  if (tid == 0) totals[d] = tot;
   for (long long p0 = a; p0 < b; p0 += 8) {
     unsigned int c8[8];
 #pragma unroll
@@ -549,14 +544,18 @@ k_digit_offsets(int pass, long long cap, long long partitions, long long partiti
   }
 }
 
-// One stable LSD pass over the digit at bits [8 pass, 8 pass + 8).  With
-// own_offsets the table still holds counts and every block derives its
-// offsets itself (digit start + the counts of the partitions before it):
-// cheaper than a separate k_digit_offsets launch when partitions are few.
+// One stable LSD pass over the digit at bits [8 pass, 8 pass + 8).  A
+// digit's output run starts after the runs of the digits below it (a block
+// scan of the digit totals), and the partition's part of it after the
+// digit's keys in the partitions before it.  With own_offsets the table
+// still holds counts and every block sums them itself (the totals and its
+// own prefix): cheaper than a separate k_digit_offsets launch when
+// partitions are few.  Otherwise k_digit_offsets left the prefix in the table
+// and the totals in `totals`.
 template <typename Key, int kPerThread>
 __global__ void __launch_bounds__(kRadixThreads)
 k_radix_scatter(int pass, long long cap, long long partitions4, bool own_offsets,
-                const unsigned int* __restrict__ hist,
+                const unsigned int* __restrict__ totals,
                 const Header* __restrict__ hdr, const unsigned int* __restrict__ table,
                 const Key* __restrict__ keys_in,
                 const unsigned int* __restrict__ vals_in, Key* __restrict__ keys_out,
@@ -574,20 +573,26 @@ k_radix_scatter(int pass, long long cap, long long partitions4, bool own_offsets
   const long long base = part * kItems;
   if (base >= n) return;
   for (int k = tid; k < 8 * kMaxRadix; k += blockDim.x) (&s_whist[0][0])[k] = 0;
-  if (own_offsets) {
-    unsigned int tot;
-    unsigned int b = block_exclusive_scan_256<unsigned int>(hist[pass * kMaxRadix + tid], &tot);
-    const unsigned int* row = table + (long long)tid * partitions4;
-    const uint4* row4 = reinterpret_cast<const uint4*>(row);
-    long long p = 0;
-    for (; p + 4 <= part; p += 4) {
-      const uint4 c = row4[p >> 2];
-      b += c.x + c.y + c.z + c.w;
+  {
+    unsigned int total = 0u, prefix = 0u;  // digit tid: keys in all partitions, in those before this one
+    if (own_offsets) {
+      const long long used = (n + kItems - 1) / kItems;
+      const uint4* row4 = reinterpret_cast<const uint4*>(table + (long long)tid * partitions4);
+      for (long long p = 0; p < used; p += 4) {  // the row is padded to a multiple of 4 (zeros)
+        const uint4 c = row4[p >> 2];
+        const unsigned int cc[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (p + j < part) prefix += cc[j];
+          if (p + j < used) total += cc[j];
+        }
+      }
+    } else {
+      total = totals[tid];
+      prefix = table[(long long)tid * partitions4 + part];
     }
-    for (; p < part; ++p) b += row[p];
-    s_base[tid] = b;
-  } else {
-    s_base[tid] = table[(long long)tid * partitions4 + part];
+    unsigned int all;
+    s_base[tid] = block_exclusive_scan_256<unsigned int>(total, &all) + prefix;
   }
   __syncthreads();
   const int shift = 8 * pass;
@@ -866,13 +871,13 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const ProjectIn* proj,
   if (proj)
     GS2D_TRY(launch_project(c, n, proj->xy, proj->shape, proj->rgb, proj->depth, proj->opacity, rec,
                             rect, count, s));
-  GS2D_TRY(cudaMemsetAsync(ws, 0, kOffScan, s));  // header and histograms
+  GS2D_TRY(cudaMemsetAsync(ws, 0, kOffScan, s));  // header, loss partials and digit totals
   GS2D_TRY(launch(k_count_scan, dim3((blocks + kCountSubs - 1) / kCountSubs), dim3(kScanThreads), 0, s, n, cap, count, hdr, block_off, tables,
-                                               L.passes * table_words,
+                                               L.passes > 0 ? table_words : 0,  // pass 0's counts (atomics)
                                                reinterpret_cast<unsigned int*>(tile_ranges), 2ll * T,
                                                (unsigned long long)keys_final));
   GS2D_TRY(launch(k_emit<kComposite>, dim3(blocks), dim3(kScanThreads), 0, s, n, tiles_x(c), L.passes, cap, L.partitions4, reinterpret_cast<const int4*>(rect), count,
-      reinterpret_cast<const float4*>(rec), block_off, hist, tables, offsets, ka, vals_a));
+      reinterpret_cast<const float4*>(rec), block_off, tables, offsets, ka, vals_a));
   // Up to 128 partitions each scatter block sums its own offsets (at most 128
   // counts per digit); beyond that one k_digit_offsets launch per pass does.
   const bool own = L.partitions <= 128;
@@ -882,9 +887,10 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const ProjectIn* proj,
     if (p > 0)  // pass 0 counts come from k_emit
       GS2D_TRY(launch(k_radix_count<Key>, dim3(int(L.partitions)), dim3(kRadixThreads), 0, s, p, cap, L.partitions4, hdr,
                                                                     even ? ka : kb, table));
+    unsigned int* totals = hist + p * kMaxRadix;  // this pass's digit totals
     if (!own)
-      GS2D_TRY(launch(k_digit_offsets, dim3(kMaxRadix), dim3(256), 0, s, p, cap, L.partitions, L.partitions4, hdr, hist, table));
-    GS2D_TRY(launch(k_radix_scatter<Key, 8>, dim3(int(L.partitions)), dim3(kRadixThreads), 0, s, p, cap, L.partitions4, own, hist, hdr, table, even ? ka : kb, even ? vals_a : vals_b,
+      GS2D_TRY(launch(k_digit_offsets, dim3(kMaxRadix), dim3(256), 0, s, p, cap, L.partitions4, hdr, totals, table));
+    GS2D_TRY(launch(k_radix_scatter<Key, 8>, dim3(int(L.partitions)), dim3(kRadixThreads), 0, s, p, cap, L.partitions4, own, totals, hdr, table, even ? ka : kb, even ? vals_a : vals_b,
         even ? kb : ka, even ? vals_b : vals_a));
   }
   if (cap > 0) {

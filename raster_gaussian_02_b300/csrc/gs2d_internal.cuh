@@ -19,7 +19,7 @@ constexpr int kTilePixels = kTile * kTile;
 // exception, the sorted keys, is located through Header::keys_final.
 //   [0, 256)          Header
 //   [256, 4352)       loss partial sums (kLossMaxBlocks floats)
-//   [4352, 12544)     radix digit histograms [kMaxPasses][kMaxRadix]
+//   [4352, 12544)     radix digit totals [kMaxPasses][kMaxRadix]
 //   then              per-block pair totals, then offsets [ceil(n / kScanItems) + 1] (int64)
 //   then              per-Gaussian pair offsets [n] (int32)
 //   then              background partials [T] x 4 floats (composite)
