@@ -27,10 +27,10 @@ k_project(gs2d_config c, int n, const float* __restrict__ xy, const float* __res
 // emission order) and apply the chain rule to the shape parameters
 // (sum_pair_partials, write_gaussian_grads).
 // kAbs: also the pairs' absgrad sums (third float4 of the slot, .y and .z).
-// Block 0 also sums, in a fixed order, the per-tile background
-// partials (composite, d_bg non-null) and the fused pass's per-block loss
-// partials (loss non-null; the total is divided by m, the number of image
-// values).
+// One extra block, the last, sums no Gaussian: it adds, in a fixed order, the
+// per-tile background partials (composite, d_bg non-null) and the fused
+// pass's per-block loss partials (loss non-null; the total is divided by m,
+// the number of image values).
 constexpr int kWarpSlots = 32;
 
 template <bool kComposite, bool kAbs>
@@ -44,7 +44,8 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
          float* __restrict__ loss, float m, int param, float sc, float* __restrict__ d_xy_abs) {
   pdl_enter();
   constexpr int kStride = (kComposite || kAbs) ? 3 : 2;  // float4 per pair slot
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const bool extra = blockIdx.x == gridDim.x - 1;
+  const int i = extra ? n : blockIdx.x * blockDim.x + threadIdx.x;
   const int lane = threadIdx.x & 31;
   const bool bad = (hdr->flags & (GS2D_FLAG_CAPACITY | GS2D_FLAG_OVERFLOW | GS2D_FLAG_TIMEOUT)) != 0;
   // every per-Gaussian load is issued up front, so one round trip precedes
@@ -113,7 +114,7 @@ k_gather(int n, const float* __restrict__ chol, const float4* __restrict__ rec,
   if (i < n)
     write_gaussian_grads(i, ok, s, ax, ay, A, shp, param, sc, d_xy, d_chol, d_rgb,
                          kComposite ? d_opacity : nullptr, kAbs ? d_xy_abs : nullptr);
-  if ((d_bg || loss) && blockIdx.x == 0) {  // the first block: its extra work overlaps the rest
+  if ((d_bg || loss) && extra) {  // beside the others (done by block 0 after its own sums: 768x512 step 63.6 -> 62.1 us)
     // fixed-order reduction of the per-tile partials
     // Each thread adds entries tid, tid + 256, ... in that order; the loads of
     // kBatch entries are issued before their adds, so one round trip serves
@@ -200,7 +201,7 @@ cudaError_t launch_gather(const gs2d_config& c, int n, const float* chol, const 
   float* d_op = comp ? d_opacity : nullptr;
   float* d_b = comp ? d_bg : nullptr;
   auto go = [&](auto kern) {
-    return launch(kern, dim3(blocks), dim3(256), 0, s, n, chol, r, rc, offsets, partials, hdr, d_xy,
+    return launch(kern, dim3(blocks + 1), dim3(256), 0, s, n, chol, r, rc, offsets, partials, hdr, d_xy,
                   d_chol, d_rgb, d_op, T, tp, d_b, lp, loss_blocks, loss, m, param, render_scale(c),
                   d_xy_abs);
   };

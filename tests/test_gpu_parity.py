@@ -95,6 +95,31 @@ def test_composite_sort_paths_near_the_tile_limit(w, h, n):
     check_lists(g, s)
 
 
+def test_composite_radix_many_partitions():
+    """2752 tiles and about 630K pairs: the composite keys (tile, depth,
+    index; 44 bits) go through six 8-bit radix passes over more than 128
+    partitions of 2048 keys, where every digit's offsets come from the
+    per-partition count tables and the scatter stages each partition in
+    shared memory; the lists must be the oracle's."""
+    wl = synth.random_scene(1024, 680, 100_000, seed=77, mode=synth.COMPOSITE, diag=(0.5, 8.0))
+    g = gpu_run(wl, backward=False)
+    s = oracle_scene(wl)
+    assert g["P"] > 128 * 2048
+    check_projection(g, s)
+    check_lists(g, s)
+
+
+def test_sum_radix_many_partitions_ragged():
+    """Sum mode above 2048 tiles with more than 128 partitions and a last
+    partition that is not full: lists bit-exact."""
+    wl = synth.random_scene(1040, 688, 90_001, seed=78, diag=(0.5, 8.0))
+    g = gpu_run(wl, backward=False)
+    s = oracle_scene(wl)
+    assert g["P"] > 128 * 2048 and g["P"] % 2048 != 0
+    check_projection(g, s)
+    check_lists(g, s)
+
+
 def test_composite_early_termination_dense():
     wl = synth.random_scene(96, 80, 4000, seed=12, mode=synth.COMPOSITE, diag=(1.0, 4.0))
     wl.opacity[:] = 0.95
