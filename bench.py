@@ -858,6 +858,33 @@ def run_gs2d(args):
     e2e_val, _ = aggregate_replicas(e2e_total, k4, world, dev)
     serial_val, _ = aggregate_replicas(sum(serial_ms), k4, world, dev)
 
+    # ---- the selective Adam step (not part of the timed step): the step's
+    # xy, shape and rgb rows with the step's gradients, moments from zero and
+    # the pair counts as the selection; HBM-bound, 28 bytes per updated
+    # element (p, g, m, v read; p, m, v written) plus the counts
+    adam = None
+    if not fwd_only:
+        nG = w.wl.n
+        params = [w.xy.clone(), w.chol.clone(), w.rgb.clone()]
+        grads = [R.d_xy[:nG], R.d_shape[:nG], R.d_rgb[:nG]]
+        moms = [(torch.zeros_like(q), torch.zeros_like(q)) for q in params]
+        cnt = R.count[:nG]
+
+        def adam_all():
+            for q, g, (m1, m2) in zip(params, grads, moms):
+                gs2d.adam_step(q, g, m1, m2, 1, 1e-3, count=cnt, stream=stream)
+        adam_ms = statistics.median(w.timed(w.graph(adam_all, force=True), k3, 5))
+        rows = int((cnt > 0).sum().item())
+        upd = rows * sum(int(q[0].numel()) for q in params)
+        abytes = 28 * upd + 4 * nG * len(params)
+        hbm = float((load_json(PEAKS) or {}).get("hbm_gbs") or 0.0)
+        agbs = abytes / (adam_ms * 1e-3) / 1e9
+        adam = {"ms": adam_ms, "launches": len(params), "rows": nG, "rows_updated": rows,
+                "elements_updated": upd, "bytes": abytes, "gbs": agbs,
+                "hbm_frac": agbs / hbm if hbm else None,
+                "how": "three gs2d_adam_step calls (xy, shape, rgb) as one CUDA graph, L2 flushed before each"}
+        params = grads = moms = cnt = None
+
     # ---- the other workloads (one GPU only): graph-replayed throughput and
     # kernel-time rooflines
     configs = None
@@ -898,6 +925,7 @@ def run_gs2d(args):
             "kernels": kernel_table(kernels, med_step),
             "step_call_ms": calls,
             "phase_ms": phases,
+            "adam": adam,
             "phase_basis": "device time of each call on its own: the call captured 10 times back "
                            "to back in one CUDA graph, median of 20 replays (each after an L2 "
                            "flush) / 10",

@@ -331,6 +331,36 @@ GS2D_API gs2d_status gs2d_merge(const gs2d_config* cfg, int32_t n, const float* 
                                 int32_t* merges_out, void* merge_workspace, gs2d_stream_t stream);
 
 /*
+ * Selective Adam step on one parameter array of n rows (one per Gaussian)
+ * of `width` floats, with the optimizer's two moments in the same row layout
+ * (DrawingWithGaussians README, MLX-specific notes: row-aligned optimizer
+ * state for a selective Adam).  With t = opt->step (this step's number,
+ * from 1) and g an element's gradient, every updated element does
+ *     m = beta1 m + (1 - beta1) g,    v = beta2 v + (1 - beta2) g^2,
+ *     p = p - lr (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps)
+ * in FP32 (the bias corrections 1 - beta^t in double on the host).  With
+ * count non-NULL (the pair counts of gs2d_project) the step is selective:
+ * the rows of Gaussians that touch no tile (count 0) keep their parameters
+ * and both moments.  One kernel per call; the arrays are device memory.
+ *   param, exp_avg, exp_avg_sq [n, width]  in/out
+ *   grad [n, width];  count [n] or NULL
+ * Errors: GS2D_ERR_INVALID_ARG for n < 0, width outside 1..16, a NULL or
+ * unaligned array (count may be NULL), step < 1, lr negative or not
+ * finite, a beta outside [0, 1), eps not > 0 and finite.
+ */
+typedef struct gs2d_adam {
+  float lr;
+  float beta1;    /* 0.9 by convention */
+  float beta2;    /* 0.999 by convention */
+  float eps;      /* 1e-8 by convention */
+  int32_t step;   /* 1 on the first step */
+} gs2d_adam;
+
+GS2D_API gs2d_status gs2d_adam_step(const gs2d_adam* opt, int32_t n, int32_t width, float* param,
+                                    const float* grad, float* exp_avg, float* exp_avg_sq,
+                                    const int32_t* count, gs2d_stream_t stream);
+
+/*
  * The L2 loss of gs2d_loss_l2 for callers that cannot supply a workspace.
  * (This call has no counterpart in the method's pages; it serves callers.)
  * Some callers cannot hand the library device memory beyond the image,

@@ -381,3 +381,36 @@ def step(cfg: Config, xy, chol, rgb, target, depth=None, opacity=None, backgroun
     loss, dimg = loss_l2(fwd["image"], target)
     grads = s.render_bwd(dimg, omp=omp)
     return s, fwd, loss, dimg, grads
+
+
+def adam_step(param, grad, exp_avg, exp_avg_sq, step: int, lr: float, beta1: float = 0.9,
+              beta2: float = 0.999, eps: float = 1e-8, count=None):
+    """One selective Adam step on row-aligned state (DrawingWithGaussians
+    README, MLX-specific notes: the COLMAP trainer carries row-aligned
+    optimizer state for its selective Adam).  The pages name the optimizer
+    and give no formula; this is Adam as Kingma and Ba define it, in the
+    order they state it, in double:
+        m_t = beta1 m_{t-1} + (1 - beta1) g_t
+        v_t = beta2 v_{t-1} + (1 - beta2) g_t^2
+        mhat = m_t / (1 - beta1^t),  vhat = v_t / (1 - beta2^t)
+        p_t = p_{t-1} - lr mhat / (sqrt(vhat) + eps)
+    param, grad, exp_avg, exp_avg_sq: [n, width] (or [n]); count: [n] or
+    None.  Selective: rows with count == 0 keep p, m and v.  Returns new
+    (param, exp_avg, exp_avg_sq) as float64 arrays; the inputs are left as
+    they are."""
+    p = np.array(param, np.float64, copy=True)
+    g = np.asarray(grad, np.float64)
+    m = np.array(exp_avg, np.float64, copy=True)
+    v = np.array(exp_avg_sq, np.float64, copy=True)
+    if not (p.shape == g.shape == m.shape == v.shape):
+        raise ValueError("param, grad and both moments must have one shape")
+    if step < 1:
+        raise ValueError("step counts from 1")
+    rows = np.ones(p.shape[0], bool) if count is None else np.asarray(count)[: p.shape[0]] != 0
+    m_new = beta1 * m + (1.0 - beta1) * g
+    v_new = beta2 * v + (1.0 - beta2) * g * g
+    mhat = m_new / (1.0 - beta1 ** step)
+    vhat = v_new / (1.0 - beta2 ** step)
+    p_new = p - lr * mhat / (np.sqrt(vhat) + eps)
+    sel = rows.reshape((-1,) + (1,) * (p.ndim - 1))
+    return np.where(sel, p_new, p), np.where(sel, m_new, m), np.where(sel, v_new, v)

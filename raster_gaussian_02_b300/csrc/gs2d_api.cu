@@ -205,6 +205,22 @@ size_t gs2d_merge_workspace_size(int32_t n) {
   return merge_workspace_size(n);
 }
 
+gs2d_status gs2d_adam_step(const gs2d_adam* opt, int32_t n, int32_t width, float* param,
+                           const float* grad, float* exp_avg, float* exp_avg_sq, const int32_t* count,
+                           gs2d_stream_t stream) {
+  if (!opt || n < 0 || width < 1 || width > 16) return GS2D_ERR_INVALID_ARG;
+  if (!param || !grad || !exp_avg || !exp_avg_sq) return GS2D_ERR_INVALID_ARG;
+  if (!aligned(param, 4) || !aligned(grad, 4) || !aligned(exp_avg, 4) || !aligned(exp_avg_sq, 4) ||
+      (count && !aligned(count, 4)))
+    return GS2D_ERR_INVALID_ARG;
+  if (opt->step < 1 || !isfinite(opt->lr) || opt->lr < 0.0f) return GS2D_ERR_INVALID_ARG;
+  if (!(opt->beta1 >= 0.0f && opt->beta1 < 1.0f) || !(opt->beta2 >= 0.0f && opt->beta2 < 1.0f))
+    return GS2D_ERR_INVALID_ARG;
+  if (!isfinite(opt->eps) || !(opt->eps > 0.0f)) return GS2D_ERR_INVALID_ARG;
+  return from_cuda(launch_adam(n, width, param, grad, exp_avg, exp_avg_sq, count, opt->lr, opt->beta1,
+                               opt->beta2, opt->eps, opt->step, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 gs2d_status gs2d_merge(const gs2d_config* cfg, int32_t n, const float* xy, const float* shape,
                        const float* rgb, const gs2d_record* rec, const int32_t* count,
                        const int32_t* tile_ranges, const int32_t* sorted_gid, int32_t max_merges,

@@ -499,6 +499,12 @@ cudaError_t launch_render_bwd(const gs2d_config& c, int n, const float* chol,
 // dL/dC = scale (C - target) to d_image and one loss partial per block to
 // loss_partials; returns the number of blocks in *blocks.  order (may be
 // NULL): the tiles in the order their blocks are launched.
+// Selective Adam step (csrc/adam.cu): param, m, v [n, width]; rows with
+// count[row] == 0 untouched when count is non-NULL.
+cudaError_t launch_adam(int n, int width, float* param, const float* grad, float* m, float* v,
+                        const int* count, float lr, float beta1, float beta2, float eps, int step,
+                        cudaStream_t s);
+
 cudaError_t launch_render_fwd_loss(const gs2d_config& c, int n, const gs2d_record* rec, const int* ranges,
                                    const int* sorted_gid, const float* target, float scale,
                                    float* image, float* d_image, float* loss_partials, int* blocks,

@@ -45,6 +45,11 @@ def make_config(width: int, height: int, mode: int = GS2D_MODE_SUM, cutoff_sigma
                        int(param), float(scale))
 
 
+class gs2d_adam(C.Structure):
+    _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
+                ("step", C.c_int32)]
+
+
 class Gs2dError(RuntimeError):
     def __init__(self, status: int, where: str):
         super().__init__(f"{where}: {status_string(status)} (status {status})")
@@ -87,6 +92,8 @@ def lib() -> C.CDLL:
         L.gs2d_merge_workspace_size.restype = C.c_size_t
         L.gs2d_merge.argtypes = [_cfgp, C.c_int32] + [_p] * 7 + [C.c_int32] + [_p] * 5 + [_p]
         L.gs2d_merge.restype = C.c_int
+        L.gs2d_adam_step.argtypes = [C.POINTER(gs2d_adam), C.c_int32, C.c_int32] + [_p] * 5 + [_p]
+        L.gs2d_adam_step.restype = C.c_int
         L.gs2d_loss_l2_noalloc.argtypes = [C.c_int32, C.c_int32] + [_p] * 4 + [_p]
         L.gs2d_loss_l2_noalloc.restype = C.c_int
         L.gs2d_read_status.argtypes = [_p, C.POINTER(C.c_int64), C.POINTER(C.c_uint32), _p]
@@ -238,6 +245,30 @@ def gs2d_merge(cfg, n, xy, shape, rgb, rec, count, tile_ranges, sorted_gid, max_
         _ptr(out_shape, _f32, "out_shape"), _ptr(out_rgb, _f32, "out_rgb"),
         None if merges_out is None else C.byref(merges_out),
         _ptr(merge_workspace, None, "merge_workspace"), _stream(stream))
+
+
+def gs2d_adam_step(opt: gs2d_adam, n, width, param, grad, exp_avg, exp_avg_sq, count=None,
+                   stream=None) -> int:
+    return lib().gs2d_adam_step(
+        C.byref(opt), int(n), int(width), _ptr(param, _f32, "param"), _ptr(grad, _f32, "grad"),
+        _ptr(exp_avg, _f32, "exp_avg"), _ptr(exp_avg_sq, _f32, "exp_avg_sq"),
+        _ptr(count, _i32, "count"), _stream(stream))
+
+
+def adam_step(param, grad, exp_avg, exp_avg_sq, step, lr, beta1=0.9, beta2=0.999, eps=1e-8,
+              count=None, stream=None) -> None:
+    """Selective Adam step in place on a [n, width] parameter tensor and its
+    two moment tensors (rows with count == 0 untouched when count is given)."""
+    n = param.shape[0]
+    width = 1 if param.dim() == 1 else int(param[0].numel())
+    for t, what in ((grad, "grad"), (exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq")):
+        if t.shape != param.shape:
+            raise ValueError(f"{what}: shape {tuple(t.shape)} != param {tuple(param.shape)}")
+    if count is not None and count.numel() < n:
+        raise ValueError("count: fewer entries than parameter rows")
+    opt = gs2d_adam(float(lr), float(beta1), float(beta2), float(eps), int(step))
+    check(gs2d_adam_step(opt, n, width, param, grad, exp_avg, exp_avg_sq, count, stream),
+          "gs2d_adam_step")
 
 
 def gs2d_read_status(workspace, stream=None):

@@ -177,6 +177,18 @@ def test_host_checks_reject_bad_arguments(gs2d):
     assert L.gs2d_merge(C.byref(good), 4, *margs, 1, null, fake, fake, None, fake, null) == INVALID
     assert gs2d.gs2d_merge_workspace_size(-1) == 0
     assert gs2d.gs2d_merge_workspace_size(1000) > gs2d.gs2d_merge_workspace_size(10) > 0
+    # adam: step >= 1, lr >= 0 and finite, betas in [0, 1), eps > 0, width 1..16, arrays non-NULL
+    ok = gs2d.gs2d_adam(0.01, 0.9, 0.999, 1e-8, 1)
+    for o in (gs2d.gs2d_adam(0.01, 0.9, 0.999, 1e-8, 0), gs2d.gs2d_adam(-1.0, 0.9, 0.999, 1e-8, 1),
+              gs2d.gs2d_adam(float("nan"), 0.9, 0.999, 1e-8, 1), gs2d.gs2d_adam(0.01, 1.0, 0.999, 1e-8, 1),
+              gs2d.gs2d_adam(0.01, 0.9, -0.5, 1e-8, 1), gs2d.gs2d_adam(0.01, 0.9, 0.999, 0.0, 1)):
+        assert L.gs2d_adam_step(C.byref(o), 4, 2, fake, fake, fake, fake, null, null) == INVALID
+    assert L.gs2d_adam_step(None, 4, 2, fake, fake, fake, fake, null, null) == INVALID
+    assert L.gs2d_adam_step(C.byref(ok), -1, 2, fake, fake, fake, fake, null, null) == INVALID
+    assert L.gs2d_adam_step(C.byref(ok), 4, 0, fake, fake, fake, fake, null, null) == INVALID
+    assert L.gs2d_adam_step(C.byref(ok), 4, 17, fake, fake, fake, fake, null, null) == INVALID
+    assert L.gs2d_adam_step(C.byref(ok), 4, 2, fake, null, fake, fake, null, null) == INVALID
+    assert L.gs2d_adam_step(C.byref(ok), 4, 2, fake, fake, fake, C.c_void_p(0x10002), null, null) == INVALID
     # read_status
     assert L.gs2d_read_status(None, None, None, None) == INVALID
     assert L.gs2d_read_status(odd, None, None, None) == INVALID
