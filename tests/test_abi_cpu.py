@@ -184,6 +184,7 @@ def test_host_checks_reject_bad_arguments(gs2d):
               gs2d.gs2d_adam(0.01, 0.9, -0.5, 1e-8, 1), gs2d.gs2d_adam(0.01, 0.9, 0.999, 0.0, 1)):
         assert L.gs2d_adam_step(C.byref(o), 4, 2, fake, fake, fake, fake, null, null) == INVALID
     assert L.gs2d_adam_step(None, 4, 2, fake, fake, fake, fake, null, null) == INVALID
+    assert L.gs2d_adam_step(C.byref(ok), 0, 2, fake, fake, fake, fake, null, null) == gs2d.GS2D_OK  # nothing to do
     assert L.gs2d_adam_step(C.byref(ok), -1, 2, fake, fake, fake, fake, null, null) == INVALID
     assert L.gs2d_adam_step(C.byref(ok), 4, 0, fake, fake, fake, fake, null, null) == INVALID
     assert L.gs2d_adam_step(C.byref(ok), 4, 17, fake, fake, fake, fake, null, null) == INVALID
