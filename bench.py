@@ -331,21 +331,26 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ gs2d ---
 
+_COMMENTS = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
 def kernel_source_hash(kernel: str) -> str:
-    """Hash of the sources a kernel is compiled from: the .cu file that
-    defines it and every shared header.  A stored traffic figure is used only
-    while this matches, so editing one kernel voids only its own figures."""
+    """Hash of the sources a kernel is compiled from, comments removed: the
+    .cu file that defines it and every shared header.  A stored traffic
+    figure is used only while this matches, so editing one kernel voids only
+    its own figures, and editing a comment voids none."""
     base = kernel.split("<", 1)[0]
     pat = re.compile(r"__global__[^;{]*?\b" + re.escape(base) + r"\s*\(", re.S)
     h = hashlib.sha256()
     found = False
     for name in sorted(os.listdir(CSRC)):
-        with open(os.path.join(CSRC, name), "rb") as f:
+        with open(os.path.join(CSRC, name)) as f:
             text = f.read()
+        code = _COMMENTS.sub("", text)
         if name.endswith(".cuh"):
-            h.update(name.encode() + text)
-        elif name.endswith(".cu") and pat.search(text.decode()):
-            h.update(name.encode() + text)
+            h.update(name.encode() + code.encode())
+        elif name.endswith(".cu") and pat.search(code):
+            h.update(name.encode() + code.encode())
             found = True
     return h.hexdigest()[:16] if found else ""
 
