@@ -296,8 +296,9 @@ k_tile_scatter(int n, int T, int tiles_x, long long cap, Header* __restrict__ hd
                unsigned int* __restrict__ keys_out, unsigned long long keys_final) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned int s_mask[];  // [T][8]: bit i = local Gaussian i covers t
-  __shared__ long long s_excl[kScanItems + 1];
+  __shared__ int s_excl[kScanItems + 1];  // block-local pair offsets (P < 2^31 here)
   __shared__ int4 s_rect[kScanItems];
+  __shared__ float s_rcpw[kScanItems];   // 1 / rectangle width
   __shared__ unsigned int s_base[kCountSortMaxTiles];  // where the block's part of list t starts
   constexpr int kTilesPer = kCountSortMaxTiles / kScanThreads;  // tiles per thread, consecutive
   const int tid = threadIdx.x;
@@ -327,10 +328,11 @@ k_tile_scatter(int n, int T, int tiles_x, long long cap, Header* __restrict__ hd
     for (int j = 0; j < 4; ++j) before_blocks += v4[j];
   }
   s_rect[tid] = r;
+  s_rcpw[tid] = 1.0f / float(max(r.z - r.x + 1, 1));
   long long total;
   const long long excl = block_exclusive_scan_256<long long>(cnt, &total);  // orders the clears
-  s_excl[tid] = excl;
-  if (tid == 0) s_excl[kScanItems] = total;
+  s_excl[tid] = int(excl);
+  if (tid == 0) s_excl[kScanItems] = int(total);
   long long boff;
   block_exclusive_scan_256<long long>(before_blocks, &boff);
   // tile starts: exclusive scan of the row totals (P fits 32 bits: n <= 2^20, T <= 2^11)
@@ -410,16 +412,21 @@ k_tile_scatter(int n, int T, int tiles_x, long long cap, Header* __restrict__ hd
   }
   __syncthreads();
   if (!ok || P == 0) return;  // P > capacity, overflow, or no pairs
-  for (long long e = tid; e < total; e += blockDim.x) {
+  const int total32 = int(total);
+  for (int e = tid; e < total32; e += blockDim.x) {
     int lo = 0, hi = kScanItems - 1;  // the local Gaussian of pair e (as in k_emit)
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (s_excl[mid] <= e) lo = mid; else hi = mid - 1;
     }
-    const int k = int(e - s_excl[lo]);
+    const int k = e - s_excl[lo];
     const int4 q = s_rect[lo];
     const int rw = q.z - q.x + 1;
-    const int t = (q.y + k / rw) * tiles_x + q.x + k % rw;
+    int qy = int(float(k) * s_rcpw[lo]);  // k / rw as in k_emit
+    int qx = k - qy * rw;
+    if (qx >= rw) { ++qy; qx -= rw; }
+    if (qx < 0) { --qy; qx += rw; }
+    const int t = (q.y + qy) * tiles_x + q.x + qx;
     if (!check_ok(t >= 0 && t < T, kCheckTile)) continue;
     const unsigned int* m = s_mask + t * 8;
     unsigned int rank = __popc(m[lo >> 5] & ((1u << (lo & 31)) - 1u));
@@ -440,20 +447,23 @@ k_emit(int n, int tiles_x, int passes, long long cap, long long partitions4,
        KeyOf<kComposite>* __restrict__ keys, unsigned int* __restrict__ vals) {
   pdl_enter();
   using Key = KeyOf<kComposite>;
-  __shared__ long long s_excl[kScanItems + 1];
+  __shared__ int s_excl[kScanItems + 1];  // block-local pair offsets (below 2^30)
   __shared__ int4 s_rect[kScanItems];
+  __shared__ float s_rcpw[kScanItems];   // 1 / rectangle width
   __shared__ unsigned int s_dkey[kComposite ? kScanItems : 1];
   __shared__ unsigned int s_part[kSpan][kMaxRadix];
   const int tid = threadIdx.x;
   const long long g = (long long)blockIdx.x * kScanItems + tid;
   for (int k = tid; k < kSpan * kMaxRadix; k += blockDim.x) (&s_part[0][0])[k] = 0u;
   const int cnt = (g < n) ? count[g] : 0;
-  s_rect[tid] = (g < n) ? rect[g] : make_int4(0, 0, -1, -1);
+  const int4 myrect = (g < n) ? rect[g] : make_int4(0, 0, -1, -1);
+  s_rect[tid] = myrect;
+  s_rcpw[tid] = 1.0f / float(max(myrect.z - myrect.x + 1, 1));
   if constexpr (kComposite) s_dkey[tid] = (g < n) ? depth_key(rec[3 * g + 2].w) : 0u;
   long long total;
   const long long excl = block_exclusive_scan_256<long long>(cnt, &total);
-  s_excl[tid] = excl;
-  if (tid == 0) s_excl[kScanItems] = total;
+  s_excl[tid] = int(excl);
+  if (tid == 0) s_excl[kScanItems] = int(total);
   const long long base = block_off[blockIdx.x];
   if (g < n) {
     const long long o = base + excl;
@@ -463,16 +473,24 @@ k_emit(int n, int tiles_x, int passes, long long cap, long long partitions4,
   const long long part0 = base / kPartKeys;
   // Pair e of this block belongs to the last local Gaussian whose exclusive
   // offset is <= e (that one has a non-zero count).
-  for (long long e = tid; e < total; e += blockDim.x) {
+  const int total32 = int(total);
+  for (int e = tid; e < total32; e += blockDim.x) {
     int lo = 0, hi = kScanItems - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (s_excl[mid] <= e) lo = mid; else hi = mid - 1;
     }
-    const int k = int(e - s_excl[lo]);
+    const int k = e - s_excl[lo];
     const int4 r = s_rect[lo];
     const int rw = r.z - r.x + 1;
-    const int ty = r.y + k / rw, tx = r.x + k % rw;
+    // k / rw by the rounded reciprocal (k < 2^24, exact in FP32) and one
+    // correction step, in place of an integer division (4096x4096 / 2M:
+    // emission with 64-bit offsets and the division 60.2 us, now 55.6 us)
+    int qy = int(float(k) * s_rcpw[lo]);
+    int qx = k - qy * rw;
+    if (qx >= rw) { ++qy; qx -= rw; }
+    if (qx < 0) { --qy; qx += rw; }
+    const int ty = r.y + qy, tx = r.x + qx;
     const unsigned int tile = unsigned(ty) * unsigned(tiles_x) + unsigned(tx);
     Key key;
     if constexpr (kComposite)
