@@ -590,7 +590,20 @@ k_radix_scatter(int pass, long long cap, long long partitions4, bool own_offsets
   const long long part = blockIdx.x;
   const long long base = part * kItems;
   if (base >= n) return;
-  for (int k = tid; k < 8 * kMaxRadix; k += blockDim.x) (&s_whist[0][0])[k] = 0;
+  // The partition's keys and values are loaded first, so that their round
+  // trip overlaps the digit-offset loads and scan below (4096x4096 / 2M:
+  // both passes 118.4 -> 95.9 us); the digits are formed after the scan.
+  Key k[kPerThread];
+  unsigned int v[kPerThread], d[kPerThread], rank[kPerThread];
+  const long long wbase = base + (long long)warp * (32 * kPerThread);
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const long long idx = wbase + j * 32 + lane;
+    const bool ok = idx < n;
+    k[j] = ok ? keys_in[idx] : Key(0);
+    v[j] = ok ? vals_in[idx] : 0u;
+  }
+  for (int q = tid; q < 8 * kMaxRadix; q += blockDim.x) (&s_whist[0][0])[q] = 0;
   {
     unsigned int total = 0u, prefix = 0u;  // digit tid: keys in all partitions, in those before this one
     if (own_offsets) {
@@ -614,16 +627,10 @@ k_radix_scatter(int pass, long long cap, long long partitions4, bool own_offsets
   }
   __syncthreads();
   const int shift = 8 * pass;
-  Key k[kPerThread];
-  unsigned int v[kPerThread], d[kPerThread], rank[kPerThread];
-  const long long wbase = base + (long long)warp * (32 * kPerThread);
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
     const long long idx = wbase + j * 32 + lane;
-    const bool ok = idx < n;
-    k[j] = ok ? keys_in[idx] : Key(0);
-    v[j] = ok ? vals_in[idx] : 0u;
-    d[j] = ok ? (unsigned(k[j] >> shift) & 255u) : 256u;
+    d[j] = idx < n ? (unsigned(k[j] >> shift) & 255u) : 256u;
   }
   // Stable rank within the warp: item j of lane l precedes item j of lane
   // l+1 and every item j+1.  The lanes sharing a digit come from nine

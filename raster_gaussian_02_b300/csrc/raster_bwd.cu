@@ -85,16 +85,24 @@ __device__ __forceinline__ void bwd_sum_rounds(BwdSumSmem<kStageTiles>& sm, int*
     if (valid && !check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile))
       tile = 0;
     const int prev = (valid && tid > 0) ? int(keys[k - 1]) : -2;
-    int ntiles;
-    const int slot = block_inclusive_count_256(valid && tile != prev, &ntiles, warp_tot) - 1;
-    if (valid && tile != prev) sm.tiles[slot] = tile;
+    // the pair's Gaussian index and record, loaded before the block-wide
+    // count below so that their round trips overlap the key loads and the
+    // count's barriers (768x512: 23.4 -> 21.3 us traced)
     int gid = 0;
-    int key = 255;  // sort key: boxes of the same shape (h, w) side by side, largest first
+    float4 p0 = make_float4(0.f, 0.f, 0.f, 0.f), p1 = p0, p2 = p0;
     if (valid) {
       gid = sorted_gid[k];
       if (!check_ok(gid >= 0 && gid < n_gauss, kCheckGaussian)) gid = 0;
       const float4* r = rec + 3 * size_t(gid);
-      const float4 p0 = r[0], p1 = r[1], p2 = r[2];
+      p0 = r[0];
+      p1 = r[1];
+      p2 = r[2];
+    }
+    int ntiles;
+    const int slot = block_inclusive_count_256(valid && tile != prev, &ntiles, warp_tot) - 1;
+    if (valid && tile != prev) sm.tiles[slot] = tile;
+    int key = 255;  // sort key: boxes of the same shape (h, w) side by side, largest first
+    if (valid) {
       sm.rec[tid][0] = p0;
       sm.rec[tid][1] = p1;
       sm.rec[tid][2] = p2;
