@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kScanThreads)
 k_tile_scatter(int n, int T, int tiles_x, long long cap, Header* __restrict__ hdr,
                const int4* __restrict__ rect, const int* __restrict__ count,
                const long long* __restrict__ block_tot, const unsigned int* __restrict__ H,
-               const unsigned int* __restrict__ R, int2* __restrict__ ranges, int* __restrict__ order,
+               const unsigned int* __restrict__ R, int2* __restrict__ ranges, int4* __restrict__ order,
                int* __restrict__ offsets, int* __restrict__ sorted_gid,
                unsigned int* __restrict__ keys_out, unsigned long long keys_final) {
   pdl_enter();
@@ -407,7 +407,12 @@ k_tile_scatter(int n, int T, int tiles_x, long long cap, Header* __restrict__ hd
 #pragma unroll
     for (int j = 0; j < kTilesPer; ++j) {
       const int u = tid * kTilesPer + j;
-      if (u < T) order[atomicAdd(&s_pos[bk[j]], 1u)] = u;
+      if (u < T) {
+        const int start = int(before + ex[j]);
+        const bool used = ok && v[j];
+        order[atomicAdd(&s_pos[bk[j]], 1u)] =
+            make_int4(u, used ? start : 0, used ? start + int(v[j]) : 0, 0);
+      }
     }
   }
   __syncthreads();
@@ -789,14 +794,14 @@ __global__ void __launch_bounds__(256)
 k_tile_depth_sort(int n, int T, long long cap, const Header* __restrict__ hdr,
                   const int2* __restrict__ ranges, const float4* __restrict__ rec,
                   int* __restrict__ sorted_gid, unsigned long long* __restrict__ temp,
-                  const int* __restrict__ order) {
+                  const int4* __restrict__ order) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned long long s_key[];  // kSegSmem
   const long long P = usable_pairs(hdr, cap);
   if (P == 0) return;
-  const int tile = order[blockIdx.x];  // longest lists first
+  int2 rg;
+  const int tile = tile_of_slot(order, int(blockIdx.x), ranges, &rg);  // longest lists first
   if (!check_ok(tile >= 0 && tile < T, kCheckTile)) return;
-  const int2 rg = ranges[tile];
   const int len = rg.y - rg.x;
   if (len <= 1) return;
   if (!check_ok(rg.x >= 0 && rg.y <= P, kCheckRange)) return;
@@ -879,7 +884,7 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const ProjectIn* proj,
                       hdr, reinterpret_cast<const int4*>(rect), count,
                       static_cast<const long long*>(block_off), static_cast<const unsigned int*>(H),
                       static_cast<const unsigned int*>(R), reinterpret_cast<int2*>(tile_ranges),
-                      reinterpret_cast<int*>(ws + L.tile_order), offsets, sorted_gid,
+                      reinterpret_cast<int4*>(ws + L.tile_order), offsets, sorted_gid,
                       reinterpret_cast<unsigned int*>(ws + L.keys_a), (unsigned long long)L.keys_a));
       if (kComposite) {
         const size_t dsmem = size_t(kSegSmem) * sizeof(unsigned long long);
@@ -888,7 +893,7 @@ cudaError_t launch_binning_t(const gs2d_config& c, int n, const ProjectIn* proj,
         GS2D_TRY(launch(k_tile_depth_sort, dim3(T), dim3(256), dsmem, s, n, T, cap,
                         static_cast<const Header*>(hdr), rg, reinterpret_cast<const float4*>(rec),
                         sorted_gid, reinterpret_cast<unsigned long long*>(ws + L.keys_b),
-                        reinterpret_cast<const int*>(ws + L.tile_order)));
+                        reinterpret_cast<const int4*>(ws + L.tile_order)));
       }
       return cudaGetLastError();
     }

@@ -55,14 +55,15 @@ k_fused_comp(gs2d_config c, int tiles_x, int n, const Header* __restrict__ hdr, 
              const float* __restrict__ bg, const float* __restrict__ target,
              float* __restrict__ image, float4* __restrict__ partials,
              float4* __restrict__ tile_partials, float* __restrict__ loss_partials,
-             const int* __restrict__ order) {
+             const int4* __restrict__ order) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   FusedCompSmem<kAbs>& sm = *reinterpret_cast<FusedCompSmem<kAbs>*>(smem_raw);
   // kCompMaxParts blocks per tile (its parts), longest lists first when known;
   // the parts of one tile have adjacent block indices
   const int part = int(blockIdx.x % kCompMaxParts);
-  const int tile = order ? order[blockIdx.x / kCompMaxParts] : int(blockIdx.x / kCompMaxParts);
+  int2 rg;
+  const int tile = tile_of_slot(order, int(blockIdx.x / kCompMaxParts), ranges, &rg);
   if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile)) return;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -73,7 +74,6 @@ k_fused_comp(gs2d_config c, int tiles_x, int n, const Header* __restrict__ hdr, 
   const bool inside = px < c.width && py < c.height;
   const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
   const long long pairs = hdr->pairs;
-  int2 rg = ranges[tile];
   if (!check_ok(rg.x >= 0 && rg.x <= rg.y && rg.y <= pairs, kCheckRange)) rg = make_int2(0, 0);
   const int len = rg.y - rg.x;
   const int parts = min(kCompMaxParts, max(1, (len + kCompSegLen - 1) / kCompSegLen));
@@ -153,7 +153,7 @@ cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* cho
       return launch(kern, dim3(kCompMaxParts * T), dim3(256), smem, s, c, tiles_x(c), n,
                     reinterpret_cast<const Header*>(ws), scale, r, rc, rg, sorted_gid,
                     offsets, bg, target, image, reinterpret_cast<float4*>(ws + L.partials), tp, lp,
-                    L.count_sort ? reinterpret_cast<const int*>(ws + L.tile_order) : nullptr);
+                    L.count_sort ? reinterpret_cast<const int4*>(ws + L.tile_order) : nullptr);
     };
     if (d_xy_abs)
       GS2D_TRY(go(k_fused_comp<true>, sizeof(FusedCompSmem<true>)));
@@ -165,7 +165,7 @@ cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* cho
   float* d_image = reinterpret_cast<float*>(ws + L.dimage);
   int blocks = 0;
   // the counting sort leaves a longest-first launch order of the tiles
-  const int* order = L.count_sort ? reinterpret_cast<const int*>(ws + L.tile_order) : nullptr;
+  const int4* order = L.count_sort ? reinterpret_cast<const int4*>(ws + L.tile_order) : nullptr;
   GS2D_TRY(launch_render_fwd_loss(c, n, rec, ranges, sorted_gid, target, scale, image, d_image, lp, &blocks,
                                   order, s));
   return launch_render_bwd(c, n, chol, rec, rect, ranges, sorted_gid, nullptr, nullptr, nullptr, d_image,

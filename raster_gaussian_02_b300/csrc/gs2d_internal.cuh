@@ -119,8 +119,8 @@ inline Layout layout_of(const gs2d_config& c, long long n, long long cap) {
   o = align256(o + 8 * size_t(T));
   L.dimage = o;  // fused pass, sum mode: dL/dC [3,H,W]
   if (!comp) o = align256(o + 12 * size_t(c.width) * size_t(c.height));
-  L.tile_order = o;  // counting sort: tiles by descending list length (launch order)
-  o = align256(o + 4 * size_t(T));
+  L.tile_order = o;  // counting sort: (tile, start, end, 0) by descending list length (launch order)
+  o = align256(o + 16 * size_t(T));
   L.tile_hist = o;  // counting sort by tile: [T][blocks] counts, then row totals [T]
   L.count_sort = T <= kCountSortMaxTiles && n <= kCountSortMaxGaussians;
   if (L.count_sort) {
@@ -388,6 +388,21 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// The tile a block takes and that tile's list range.  With the counting
+// sort's launch order (one int4 per slot: tile, start, end, 0; longest lists
+// first) both come from one 16-byte load; without it slot i is tile i and
+// its range is read from the ranges array.
+__device__ __forceinline__ int tile_of_slot(const int4* __restrict__ order, int i,
+                                            const int2* __restrict__ ranges, int2* rg) {
+  if (order) {
+    const int4 o = order[i];
+    *rg = make_int2(o.y, o.z);
+    return o.x;
+  }
+  *rg = ranges[i];
+  return i;
+}
+
 __device__ __forceinline__ void pdl_enter() {
   pdl_wait();
   pdl_trigger();
@@ -508,7 +523,7 @@ cudaError_t launch_adam(int n, int width, float* param, const float* grad, float
 cudaError_t launch_render_fwd_loss(const gs2d_config& c, int n, const gs2d_record* rec, const int* ranges,
                                    const int* sorted_gid, const float* target, float scale,
                                    float* image, float* d_image, float* loss_partials, int* blocks,
-                                   const int* order, cudaStream_t s);
+                                   const int4* order, cudaStream_t s);
 
 cudaError_t launch_render_fused_l2(const gs2d_config& c, int n, const float* chol,
                                    const gs2d_record* rec, const int* rect, const int* ranges,

@@ -331,14 +331,14 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, int n, const Header* __restrict__ 
                   const float* __restrict__ bg, const float* __restrict__ t_final,
                   const int* __restrict__ last, const float* __restrict__ d_image,
                   float4* __restrict__ partials, float4* __restrict__ tile_partials,
-                  const int* __restrict__ order) {
+                  const int4* __restrict__ order) {
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   CompStage<kAbs>& sm = *reinterpret_cast<CompStage<kAbs>*>(smem_raw);
-  const int tile = order ? order[blockIdx.x] : int(blockIdx.x);  // longest lists first when known
+  int2 rg;
+  const int tile = tile_of_slot(order, int(blockIdx.x), ranges, &rg);  // longest lists first when known
   if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile)) return;
   const long long pairs = hdr->pairs;
-  int2 rg = ranges[tile];
   if (!check_ok(rg.x >= 0 && rg.x <= rg.y && rg.y <= pairs, kCheckRange)) rg = make_int2(0, 0);
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -382,7 +382,7 @@ cudaError_t launch_bwd_pairs(const gs2d_config& c, int n, const Layout& L, const
     GS2D_TRY(launch(kern, dim3(T), dim3(kBwdCompThreads), smem, s, c, tiles_x(c), n,
                     reinterpret_cast<const Header*>(ws), r, rc, rg, sorted_gid, offsets, bg, t_final, last, d_image, partials,
                     reinterpret_cast<float4*>(ws + L.tile_partials),
-                    L.count_sort ? reinterpret_cast<const int*>(ws + L.tile_order) : nullptr));
+                    L.count_sort ? reinterpret_cast<const int4*>(ws + L.tile_order) : nullptr));
   } else {
     const bool wide = T > kCountSortMaxTiles;
     const size_t smem = wide ? sizeof(BwdSumSmem<4>) : sizeof(BwdSumSmem<8>);

@@ -28,12 +28,13 @@ k_render_fwd_sum(gs2d_config c, int tiles_x, int n, const float4* __restrict__ r
                  const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
                  float* __restrict__ image, const float* __restrict__ target, float scale,
                  float* __restrict__ d_image, float* __restrict__ loss_partials,
-                 const int* __restrict__ order) {
+                 const int4* __restrict__ order) {
   constexpr int kParts = 8 / kWarps;
   pdl_enter();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SumSmem<kWarps>& sm = *reinterpret_cast<SumSmem<kWarps>*>(smem_raw);
-  const int tile = order ? order[blockIdx.x / kParts] : int(blockIdx.x / kParts);
+  int2 rg;
+  const int tile = tile_of_slot(order, int(blockIdx.x / kParts), ranges, &rg);
   if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile)) return;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -42,7 +43,6 @@ k_render_fwd_sum(gs2d_config c, int tiles_x, int n, const float4* __restrict__ r
   const int by0 = ty * kTile + (sub >> 1) * 4;
   const int px = bx0 + (lane & 7), py = by0 + (lane >> 3);
   const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
-  int2 rg = ranges[tile];
   if (!check_ok(rg.x >= 0 && rg.x <= rg.y, kCheckRange)) rg = make_int2(0, 0);
   const float3 a = sum_tile_forward<kWarps>(sm, rg, bx0, by0, float(px) + 0.5f, float(py) + 0.5f, kk,
                                             n, rec, sorted_gid);
@@ -109,7 +109,7 @@ k_render_fwd_comp(gs2d_config c, int tiles_x, int n, const float4* __restrict__ 
 template <int kWarps, bool kLoss>
 cudaError_t launch_fwd_sum(const gs2d_config& c, int n, const float4* r, const int2* rg, const int* sorted_gid,
                            float* image, const float* target, float scale, float* d_image,
-                           float* loss_partials, const int* order, cudaStream_t s) {
+                           float* loss_partials, const int4* order, cudaStream_t s) {
   const size_t smem = sizeof(SumSmem<kWarps>);
   auto kern = k_render_fwd_sum<kWarps, kLoss>;
   GS2D_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
@@ -149,7 +149,7 @@ cudaError_t launch_render_fwd(const gs2d_config& c, int n, const gs2d_record* re
 cudaError_t launch_render_fwd_loss(const gs2d_config& c, int n, const gs2d_record* rec, const int* ranges,
                                    const int* sorted_gid, const float* target, float scale,
                                    float* image, float* d_image, float* loss_partials, int* blocks,
-                                   const int* order, cudaStream_t s) {
+                                   const int4* order, cudaStream_t s) {
   const int T = num_tiles(c);
   const float4* r = reinterpret_cast<const float4*>(rec);
   const int2* rg = reinterpret_cast<const int2*>(ranges);
