@@ -223,11 +223,19 @@ GS2D_API gs2d_status gs2d_project_bin_and_sort(const gs2d_config* cfg, int32_t n
  *                  otherwise): final transmittance
  *   last[H,W]      out, composite (same): 1 + position within the tile's list
  *                  of the last Gaussian that contributed, 0 if none
+ *   workspace      optional (NULL: tiles in index order): the workspace of
+ *                  the gs2d_bin_and_sort / gs2d_project_bin_and_sort call
+ *                  that wrote tile_ranges and sorted_gid, with the same cfg
+ *                  and n.  With at most 2048 tiles that call also left a
+ *                  launch order there (tiles by descending list length, each
+ *                  with its range), and the blocks then take the longest
+ *                  lists first; the result is the same either way.  Not
+ *                  written.
  */
 GS2D_API gs2d_status gs2d_render_fwd(const gs2d_config* cfg, int32_t n, const gs2d_record* rec,
                             const int32_t* tile_ranges, const int32_t* sorted_gid,
                             const float* background, float* image, float* t_final, int32_t* last,
-                            gs2d_stream_t stream);
+                            const void* workspace, gs2d_stream_t stream);
 
 /*
  * L2 image loss: loss = (1/(3HW)) sum (image - target)^2 and

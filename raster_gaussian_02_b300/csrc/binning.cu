@@ -800,8 +800,8 @@ k_tile_depth_sort(int n, int T, long long cap, const Header* __restrict__ hdr,
   const long long P = usable_pairs(hdr, cap);
   if (P == 0) return;
   int2 rg;
-  const int tile = tile_of_slot(order, int(blockIdx.x), ranges, &rg);  // longest lists first
-  if (!check_ok(tile >= 0 && tile < T, kCheckTile)) return;
+  const int tile = tile_of_slot(order, int(blockIdx.x), ranges, T, &rg);  // longest lists first
+  if (!check_ok(tile >= 0 && tile < T, kCheckTile) || tile < 0) return;
   const int len = rg.y - rg.x;
   if (len <= 1) return;
   if (!check_ok(rg.x >= 0 && rg.y <= P, kCheckRange)) return;

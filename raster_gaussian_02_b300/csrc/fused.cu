@@ -63,8 +63,8 @@ k_fused_comp(gs2d_config c, int tiles_x, int n, const Header* __restrict__ hdr, 
   // the parts of one tile have adjacent block indices
   const int part = int(blockIdx.x % kCompMaxParts);
   int2 rg;
-  const int tile = tile_of_slot(order, int(blockIdx.x / kCompMaxParts), ranges, &rg);
-  if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile)) return;
+  const int tile = tile_of_slot(order, int(blockIdx.x / kCompMaxParts), ranges, tiles_x * ((c.height + kTile - 1) / kTile), &rg);
+  if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile) || tile < 0) return;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bx0 = tx * kTile + (warp & 1) * 8;

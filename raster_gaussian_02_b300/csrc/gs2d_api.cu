@@ -116,8 +116,9 @@ gs2d_status gs2d_project_bin_and_sort(const gs2d_config* cfg, int32_t n, const f
 gs2d_status gs2d_render_fwd(const gs2d_config* cfg, int32_t n, const gs2d_record* rec,
                             const int32_t* tile_ranges, const int32_t* sorted_gid,
                             const float* background, float* image, float* t_final, int32_t* last,
-                            gs2d_stream_t stream) {
+                            const void* workspace, gs2d_stream_t stream) {
   if (!config_ok(cfg) || n < 0) return GS2D_ERR_INVALID_ARG;
+  if (workspace && !aligned(workspace, 16)) return GS2D_ERR_INVALID_ARG;
   if (!tile_ranges || !image || !aligned(tile_ranges, 16) || !aligned(image, 4))
     return GS2D_ERR_INVALID_ARG;
   if (n > 0 && (!rec || !sorted_gid || !aligned(rec, 16) || !aligned(sorted_gid, 4)))
@@ -126,7 +127,8 @@ gs2d_status gs2d_render_fwd(const gs2d_config* cfg, int32_t n, const gs2d_record
       (background && !aligned(background, 4)))
     return GS2D_ERR_INVALID_ARG;
   return from_cuda(launch_render_fwd(*cfg, n, rec, tile_ranges, sorted_gid, background, image, t_final,
-                                     last, reinterpret_cast<cudaStream_t>(stream)));
+                                     last, static_cast<const unsigned char*>(workspace),
+                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gs2d_status gs2d_loss_l2(int32_t height, int32_t width, const float* image, const float* target,

@@ -391,13 +391,15 @@ __device__ __forceinline__ void pdl_trigger() {
 // The tile a block takes and that tile's list range.  With the counting
 // sort's launch order (one int4 per slot: tile, start, end, 0; longest lists
 // first) both come from one 16-byte load; without it slot i is tile i and
-// its range is read from the ranges array.
+// its range is read from the ranges array.  A slot naming no tile of the
+// T (a workspace the binning has not written) gives -1, and the caller's
+// block does nothing.
 __device__ __forceinline__ int tile_of_slot(const int4* __restrict__ order, int i,
-                                            const int2* __restrict__ ranges, int2* rg) {
+                                            const int2* __restrict__ ranges, int T, int2* rg) {
   if (order) {
     const int4 o = order[i];
     *rg = make_int2(o.y, o.z);
-    return o.x;
+    return (o.x >= 0 && o.x < T) ? o.x : -1;
   }
   *rg = ranges[i];
   return i;
@@ -490,7 +492,7 @@ cudaError_t launch_project_binning(const gs2d_config& c, int n, const ProjectIn&
 
 cudaError_t launch_render_fwd(const gs2d_config& c, int n, const gs2d_record* rec, const int* ranges,
                               const int* sorted_gid, const float* bg, float* image, float* t_final,
-                              int* last, cudaStream_t s);
+                              int* last, const unsigned char* ws, cudaStream_t s);
 
 cudaError_t launch_loss_l2(int h, int w, const float* image, const float* target, float* loss,
                            float* d_image, unsigned char* ws, cudaStream_t s);

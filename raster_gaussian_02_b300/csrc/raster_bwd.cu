@@ -336,8 +336,8 @@ k_render_bwd_comp(gs2d_config c, int tiles_x, int n, const Header* __restrict__ 
   extern __shared__ __align__(16) unsigned char smem_raw[];
   CompStage<kAbs>& sm = *reinterpret_cast<CompStage<kAbs>*>(smem_raw);
   int2 rg;
-  const int tile = tile_of_slot(order, int(blockIdx.x), ranges, &rg);  // longest lists first when known
-  if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile)) return;
+  const int tile = tile_of_slot(order, int(blockIdx.x), ranges, tiles_x * ((c.height + kTile - 1) / kTile), &rg);  // longest lists first when known
+  if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile) || tile < 0) return;
   const long long pairs = hdr->pairs;
   if (!check_ok(rg.x >= 0 && rg.x <= rg.y && rg.y <= pairs, kCheckRange)) rg = make_int2(0, 0);
   const int tx = tile % tiles_x, ty = tile / tiles_x;

@@ -34,8 +34,8 @@ k_render_fwd_sum(gs2d_config c, int tiles_x, int n, const float4* __restrict__ r
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SumSmem<kWarps>& sm = *reinterpret_cast<SumSmem<kWarps>*>(smem_raw);
   int2 rg;
-  const int tile = tile_of_slot(order, int(blockIdx.x / kParts), ranges, &rg);
-  if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile)) return;
+  const int tile = tile_of_slot(order, int(blockIdx.x / kParts), ranges, tiles_x * ((c.height + kTile - 1) / kTile), &rg);
+  if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile) || tile < 0) return;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = (blockIdx.x % kParts) * kWarps + warp;  // 8x4 sub-block 0..7 of the tile
@@ -74,10 +74,12 @@ __global__ void __launch_bounds__(256)
 k_render_fwd_comp(gs2d_config c, int tiles_x, int n, const float4* __restrict__ rec,
                   const int2* __restrict__ ranges, const int* __restrict__ sorted_gid,
                   const float* __restrict__ bg, float* __restrict__ image,
-                  float* __restrict__ t_final, int* __restrict__ last) {
+                  float* __restrict__ t_final, int* __restrict__ last, const int4* __restrict__ order) {
   pdl_enter();
   __shared__ CompSmem sm;
-  const int tile = blockIdx.x;
+  int2 rg;
+  const int tile = tile_of_slot(order, int(blockIdx.x), ranges, tiles_x * ((c.height + kTile - 1) / kTile), &rg);  // longest lists first when known
+  if (!check_ok(tile >= 0 && tile < tiles_x * ((c.height + kTile - 1) / kTile), kCheckTile) || tile < 0) return;
   const int tx = tile % tiles_x, ty = tile / tiles_x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bx0 = tx * kTile + (warp & 1) * 8;
@@ -85,7 +87,6 @@ k_render_fwd_comp(gs2d_config c, int tiles_x, int n, const float4* __restrict__ 
   const int px = bx0 + (lane & 7), py = by0 + (lane >> 3);
   const bool inside = px < c.width && py < c.height;
   const float kk = __fmul_rn(c.cutoff_sigma, c.cutoff_sigma);
-  int2 rg = ranges[tile];
   if (!check_ok(rg.x >= 0 && rg.x <= rg.y, kCheckRange)) rg = make_int2(0, 0);
   const CompFwdOut o = comp_tile_forward(sm, c, rg, bx0, by0, float(px) + 0.5f, float(py) + 0.5f,
                                          inside, kk, n, rec, sorted_gid);
@@ -129,19 +130,26 @@ bool half_tile_blocks(int T) { return T <= 2 * 8 * sm_count(); }
 
 cudaError_t launch_render_fwd(const gs2d_config& c, int n, const gs2d_record* rec, const int* ranges,
                               const int* sorted_gid, const float* bg, float* image, float* t_final,
-                              int* last, cudaStream_t s) {
+                              int* last, const unsigned char* ws, cudaStream_t s) {
   const int T = num_tiles(c);
   const float4* r = reinterpret_cast<const float4*>(rec);
   const int2* rg = reinterpret_cast<const int2*>(ranges);
+  // the binning's launch order (counting sort only), when its workspace is given
+  const int4* order = nullptr;
+  if (ws) {
+    const Layout L = layout_of(c, n, 0);
+    if (L.count_sort) order = reinterpret_cast<const int4*>(ws + L.tile_order);
+  }
   if (c.mode == GS2D_MODE_COMPOSITE) {
-    GS2D_TRY(launch(k_render_fwd_comp, dim3(T), dim3(256), 0, s, c, tiles_x(c), n, r, rg, sorted_gid, bg, image, t_final, last));
+    GS2D_TRY(launch(k_render_fwd_comp, dim3(T), dim3(256), 0, s, c, tiles_x(c), n, r, rg, sorted_gid, bg, image,
+                    t_final, last, order));
   } else {
     if (half_tile_blocks(T))
       GS2D_TRY((launch_fwd_sum<4, false>(c, n, r, rg, sorted_gid, image, nullptr, 0.f, nullptr, nullptr,
-                                         nullptr, s)));
+                                         order, s)));
     else
       GS2D_TRY((launch_fwd_sum<8, false>(c, n, r, rg, sorted_gid, image, nullptr, 0.f, nullptr, nullptr,
-                                         nullptr, s)));
+                                         order, s)));
   }
   return cudaGetLastError();
 }

@@ -80,7 +80,7 @@ def lib() -> C.CDLL:
         L.gs2d_project_bin_and_sort.argtypes = ([_cfgp, C.c_int32] + [_p] * 8 +
                                                 [C.c_int64, C.POINTER(C.c_int64)] + [_p] * 3 + [_p])
         L.gs2d_project_bin_and_sort.restype = C.c_int
-        L.gs2d_render_fwd.argtypes = [_cfgp, C.c_int32] + [_p] * 7 + [_p]
+        L.gs2d_render_fwd.argtypes = [_cfgp, C.c_int32] + [_p] * 8 + [_p]
         L.gs2d_render_fwd.restype = C.c_int
         L.gs2d_loss_l2.argtypes = [C.c_int32, C.c_int32] + [_p] * 5 + [_p]
         L.gs2d_loss_l2.restype = C.c_int
@@ -181,13 +181,13 @@ def gs2d_project_bin_and_sort(cfg, n, xy, shape, rgb, depth, opacity, rec, rect,
 
 
 def gs2d_render_fwd(cfg, n, rec, tile_ranges, sorted_gid, background, image, t_final, last,
-                    stream=None) -> int:
+                    workspace=None, stream=None) -> int:
     return lib().gs2d_render_fwd(C.byref(cfg), int(n), _ptr(rec, None, "rec"),
                                  _ptr(tile_ranges, _i32, "tile_ranges"),
                                  _ptr(sorted_gid, _i32, "sorted_gid"),
                                  _ptr(background, _f32, "background"), _ptr(image, _f32, "image"),
                                  _ptr(t_final, _f32, "t_final"), _ptr(last, _i32, "last"),
-                                 _stream(stream))
+                                 _ptr(workspace, None, "workspace"), _stream(stream))
 
 
 def gs2d_loss_l2(height, width, image, target, loss, d_image, workspace, stream=None) -> int:
@@ -434,7 +434,8 @@ class Rasterizer:
     def render_fwd(self, background=None):
         self.background = background
         check(gs2d_render_fwd(self.cfg, self.n, self.rec, self.tile_ranges, self.sorted_gid,
-                              background, self.image, self.t_final, self.last), "gs2d_render_fwd")
+                              background, self.image, self.t_final, self.last, self.workspace),
+              "gs2d_render_fwd")
         return self.image
 
     def loss_l2(self, target):

@@ -134,10 +134,11 @@ def test_host_checks_reject_bad_arguments(gs2d):
     assert pb(C.byref(good), 4, fake, fake, fake, null, null, fake, fake, fake, -1, None, fake, fake, fake, null) == INVALID
     assert pb(C.byref(good), 4, fake, fake, fake, null, null, fake, fake, fake, 10, None, fake, fake, odd, null) == INVALID
     assert pb(C.byref(good), 4, fake, fake, fake, null, null, fake, fake, fake, 10, None, fake, null, fake, null) == INVALID
-    # render_fwd
-    assert L.gs2d_render_fwd(C.byref(good), 4, fake, fake, fake, null, null, null, null, null) == INVALID
-    assert L.gs2d_render_fwd(C.byref(good), 4, odd, fake, fake, null, fake, null, null, null) == INVALID
-    assert L.gs2d_render_fwd(C.byref(bad), 4, fake, fake, fake, null, fake, null, null, null) == INVALID
+    # render_fwd: (rec ranges gid bg image t_final last workspace)
+    assert L.gs2d_render_fwd(C.byref(good), 4, fake, fake, fake, null, null, null, null, null, null) == INVALID
+    assert L.gs2d_render_fwd(C.byref(good), 4, odd, fake, fake, null, fake, null, null, null, null) == INVALID
+    assert L.gs2d_render_fwd(C.byref(bad), 4, fake, fake, fake, null, fake, null, null, null, null) == INVALID
+    assert L.gs2d_render_fwd(C.byref(good), 4, fake, fake, fake, null, fake, null, null, odd, null) == INVALID
     # loss
     assert L.gs2d_loss_l2(0, 64, fake, fake, fake, fake, fake, null) == INVALID
     assert L.gs2d_loss_l2(64, 64, fake, null, fake, fake, fake, null) == INVALID
